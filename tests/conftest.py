@@ -1,0 +1,78 @@
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from linear_attention_rnn_gb300.inputs import Inputs, Workload  # noqa: E402
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+    config.addinivalue_line("markers", "slow: long-running (full-size workloads)")
+
+
+def from_arrays(q, k, v, g, beta, h0=None, dO=None, dhT=None, chunk=128, name="adhoc"):
+    """Build an Inputs from arrays shaped [B,T,H,D] / [B,T,H] / [B,H,dk,dv].
+
+    q, k, v, dO are rounded to bf16 (RNE); callers that need exact values pass
+    values representable in bf16.
+    """
+    q = np.asarray(q, np.float32)
+    k = np.asarray(k, np.float32)
+    v = np.asarray(v, np.float32)
+    B, T, Hk, dk = k.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    wl = Workload(name, B=B, T=T, Hk=Hk, Hv=Hv, dk=dk, dv=dv, chunk=chunk,
+                  h0_std=1.0 if h0 is not None else 0.0, backward=dO is not None)
+    bf = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16)
+    f32 = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x, np.float32))
+    return Inputs(wl, bf(q), bf(k), bf(v), f32(g), f32(beta), f32(h0),
+                  None if dO is None else bf(dO), f32(dhT))
+
+
+def as64(inp, name):
+    """Exact fp64 copy of an input tensor (bf16 and fp32 widen exactly)."""
+    x = getattr(inp, name)
+    return None if x is None else x.detach().cpu().to(torch.float64).numpy()
+
+
+def head(inp, b, j):
+    """fp64 per-head slices (q, k, v, g, beta, h0) of value head j."""
+    grp = inp.wl.Hv // inp.wl.Hk
+    kh = j // grp
+    q, k, v = as64(inp, "q"), as64(inp, "k"), as64(inp, "v")
+    g, beta, h0 = as64(inp, "g"), as64(inp, "beta"), as64(inp, "h0")
+    return (q[b, :, kh], k[b, :, kh], v[b, :, j], g[b, :, j], beta[b, :, j],
+            None if h0 is None else h0[b, j])
+
+
+def relmax(x, ref):
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.max(np.abs(ref))
+    return float(np.max(np.abs(x - ref)) / (den if den > 0 else 1.0))
+
+
+def random_small(B=1, T=40, Hk=1, Hv=1, dk=8, dv=8, seed=0, gate_shift=0.0, h0=True,
+                 bwd=False, unit=True):
+    """Small random inputs with the workload distributions (host numpy)."""
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, T, Hk, dk))
+    k = rng.standard_normal((B, T, Hk, dk))
+    if unit:
+        q /= np.linalg.norm(q, axis=-1, keepdims=True)
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, Hv, dv))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((B, T, Hv))))
+    x = rng.standard_normal((B, T, Hv)) + gate_shift
+    g = -(np.maximum(x, 0) + np.log1p(np.exp(-np.abs(x))))
+    h0a = rng.standard_normal((B, Hv, dk, dv)) * 0.5 if h0 else None
+    dO = rng.standard_normal((B, T, Hv, dv)) if bwd else None
+    dhT = rng.standard_normal((B, Hv, dk, dv)) * 0.3 if bwd else None
+    return from_arrays(q, k, v, g, beta, h0a, dO, dhT)
