@@ -1,0 +1,145 @@
+/*
+ * gdn.h -- C ABI of the chunked Gated DeltaNet (gated delta rule) forward and
+ * backward for NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  Per batch row b and value head j (key head kh = j / (Hv/Hk)),
+ * with the state written transposed, h = S^T of shape d_k x d_v:
+ *     h_t = exp(g_t) (I - beta_t k_t k_t^T) h_{t-1} + beta_t k_t v_t^T,
+ *     o_t = h_t^T q_t,          h_{-1} = h0,  hT = h_{T-1}.
+ * It is evaluated in chunks of `chunk` tokens through the WY/UT form: per chunk
+ * the UT inverse T = (I + S)^-1 of S = tril(diag(beta) (K K^T * decay), -1)
+ * (blockwise doubling ladder), w = T diag(beta exp(G)) K, u = T diag(beta) V,
+ * the inter-chunk step h' = (exp(g_last) I - k_g^T w) h + k_g^T u = A h + B,
+ * and the masked intra-chunk output.  Sources (pages' titles and sections):
+ *   - the inter-chunk step as an affine map h' = A h + B and the composition
+ *     law (A2,B2) o (A1,B1) = (A2 A1, A2 B1 + B2): issue "GatedDeltaNet does
+ *     not support ici_context_parallelism", section "The recurrence is affine,
+ *     so it can be parallelized";
+ *   - the two-pass scan (fold each stretch of chunks into one (A, B), exclusive
+ *     prefix, replay from the incoming state): PR "Shard the GatedDeltaNet
+ *     sequence under ici_context_parallelism", description;
+ *   - the ladder inverse, its analytic backward dS = -(T^T dT T^T) (strictly
+ *     lower), the reverse chunk walk of the backward and initial/final state
+ *     as first-class inputs/outputs: PR "Fuse the Gated Delta Net inter-chunk
+ *     scan into a Pallas TPU kernel", section "Changes".
+ *
+ * Conventions for every entry point:
+ *   - Pointers are device pointers (cudaMalloc'd, or any memory the device can
+ *     address), contiguous, 16-byte aligned.  bf16 tensors are passed as
+ *     void* to raw IEEE bfloat16 data.  The caller owns all memory; the
+ *     library allocates nothing, keeps no state between calls and never
+ *     synchronises the stream.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work
+ *     is enqueued on it asynchronously; outputs are valid once it has run.
+ *   - Layouts: q, k [B, T, Hk, d_k]; v, o, dO, dv [B, T, Hv, d_v];
+ *     g, beta, dg, dbeta [B, T, Hv]; h0, hT, dhT, dh0 [B, Hv, d_k, d_v];
+ *     dq, dk [B, T, Hk, d_k].
+ *   - Return value: GDN_OK, or a negative gdn_status.  Argument errors are
+ *     detected on the host before anything is enqueued, so a failed call has
+ *     no effect.  GDN_ERR_CUDA reports a launch failure (cudaGetLastError).
+ *   - Supported sizes in this version: d_k = d_v = 128, chunk = 128, any
+ *     T >= 0 (a ragged last chunk is zero-padded with g = 0, beta = 0, which
+ *     leaves the state unchanged), Hv a multiple of Hk.
+ *   - Workspace: the caller passes `ws` of at least the size the matching
+ *     *_workspace_bytes call returns for the same arguments (256-byte aligned).
+ *     Its contents on entry do not matter.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_ARG = -1,        /* null required pointer, misalignment, Hv % Hk != 0, negative size */
+  GDN_ERR_SHAPE = -2,      /* unsupported d_k, d_v or chunk */
+  GDN_ERR_WORKSPACE = -3,  /* workspace missing or smaller than required */
+  GDN_ERR_CUDA = -4,       /* a kernel launch failed */
+  GDN_ERR_TIMEOUT = -5,    /* reserved: a bounded in-kernel wait gave up */
+  GDN_ERR_UNSUPPORTED = -6 /* device is not sm_103 / sm_100 class */
+} gdn_status;
+
+/* Human-readable text of a status code (static storage, never NULL). */
+const char* gdn_strerror(int status);
+
+/* Number of chunk segments the forward/backward use when n_segments == 0. */
+int gdn_default_segments(int B, int T, int Hv, int chunk);
+
+/*
+ * Workspace bytes of gdn_chunk_fwd / gdn_chunk_bwd for these arguments
+ * (n_segments as it will be passed, 0 = automatic).  Returns 0 for invalid
+ * sizes.
+ */
+size_t gdn_fwd_workspace_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk,
+                               int n_segments);
+size_t gdn_bwd_workspace_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk,
+                               int n_segments);
+
+/*
+ * Forward.  Reads q, k, v (bf16), g, beta (fp32, g is the per-token log-gate,
+ * exp(g) the decay), h0 (fp32, NULL = zero state); writes o (bf16) and hT
+ * (fp32, NULL = not written).
+ * n_segments: 1 = one sequential walk over the chunks per (b, value head);
+ * S > 1 = the two-pass segment scan with S segments of whole chunks (segment
+ * s holds chunks [floor(sN/S), floor((s+1)N/S)) of the N chunks); 0 = the
+ * library's choice (gdn_default_segments).  Results agree across segment
+ * counts up to rounding.
+ */
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                  const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                  int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
+                  size_t ws_bytes, void* stream);
+
+/*
+ * Backward of gdn_chunk_fwd.  Takes the forward's inputs plus the output
+ * cotangent dO (bf16, required) and the final-state cotangent dhT (fp32,
+ * NULL = zero).  Writes dq, dk (bf16, summed over the value heads that share
+ * each key head), dv (bf16), dg, dbeta (fp32) and dh0 (fp32, NULL = not
+ * written).  The forward states are recomputed (nothing is saved from the
+ * forward call).  n_segments as for the forward (it segments the reverse walk
+ * of the state cotangent and the recomputation of the states).
+ */
+int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                  const float* beta, const float* h0, const void* dO, const float* dhT,
+                  void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0, int B,
+                  int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
+                  size_t ws_bytes, void* stream);
+
+/*
+ * Inclusive prefix of affine maps along n, per batch row:
+ *   (A_out[i], B_out[i]) = (A_i, B_i) o (A_{i-1}, B_{i-1}) o ... o (A_0, B_0)
+ * with (A2, B2) o (A1, B1) = (A2 A1, A2 B1 + B2), i.e. A_out[i] h + B_out[i] is
+ * h pushed through maps 0..i in order.  This is the prefix the pages take over
+ * the gathered per-device pairs (PR "Shard the GatedDeltaNet sequence ...",
+ * description; issue "GatedDeltaNet does not support ...", composition law).
+ * A, A_out: fp32 [batch, n, d_k, d_k]; B, B_out: fp32 [batch, n, d_k, d_v];
+ * row-major.  The exclusive prefix and its application to an initial state
+ * are the caller's.  Sizes: d_k = 128, d_v a multiple of 16 up to 128.
+ * Out-of-place only (outputs must not overlap inputs).
+ */
+int gdn_affine_compose(const float* A, const float* B, float* A_out, float* B_out, int batch,
+                       int n, int d_k, int d_v, void* stream);
+
+/*
+ * Debug export of the per-chunk UT quantities, for tests.  For every
+ * (b, value head j, chunk c), in [B, Hv, N, ...] order with N = ceil(T/chunk):
+ *   S_out [.., chunk, chunk] fp32  S = tril(diag(beta) (K K^T * decay), -1)
+ *   T_out [.., chunk, chunk] fp32  T = (I + S)^-1 (the device's ladder)
+ *   w_out [.., chunk, d_k]   bf16  w = T diag(beta exp(G)) K
+ *   u_out [.., chunk, d_v]   bf16  u = T diag(beta) V
+ * Any output may be NULL.  Rows of a ragged last chunk beyond T are the
+ * zero-padding rows.  Uses no workspace.
+ */
+int gdn_debug_ut(const void* k, const void* v, const float* g,
+                 const float* beta, float* S_out, float* T_out, void* w_out, void* u_out,
+                 int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,414 @@
+// gdn_api.cu -- the extern "C" boundary declared in include/gdn.h: argument
+// validation (on the host, before anything is enqueued), workspace layout,
+// and the launch sequence of each operation on the caller's stream.
+#include <stdint.h>
+#include <string.h>
+
+#include "gdn.h"
+#include "gdn_kernels.cuh"
+
+using namespace gdn;
+
+namespace {
+
+constexpr size_t ALIGN = 256;
+inline size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Dims {
+  int B, T, Hk, Hv, NC, S;
+  long BH() const { return (long)B * Hv; }
+};
+
+int check_dims(int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int n_segments) {
+  if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || n_segments < 0) return GDN_ERR_ARG;
+  if (Hv % Hk != 0) return GDN_ERR_ARG;
+  if (dk != HD || dv != HD || chunk != CH) return GDN_ERR_SHAPE;
+  return GDN_OK;
+}
+
+Dims make_dims(int B, int T, int Hk, int Hv, int n_segments) {
+  Dims d;
+  d.B = B;
+  d.T = T;
+  d.Hk = Hk;
+  d.Hv = Hv;
+  d.NC = (T + CH - 1) / CH;
+  int S = n_segments == 0 ? gdn_default_segments(B, T, Hv, CH) : n_segments;
+  if (S > d.NC) S = d.NC;
+  if (S < 1) S = 1;
+  d.S = S;
+  return d;
+}
+
+// Workspace layout.  Forward: w, u, P per chunk; with segments also the
+// per-segment (A, B) pairs and entering states.  Backward adds T (bf16), the
+// bf16 entering states, Delta, the state cotangents, dDelta and the fp32
+// per-value-head dq/dk.
+struct Layout {
+  size_t W, U, P, Tb, pairA, pairB, hin, states, delta, dstates, ddelta, dqp, dkp, total;
+};
+
+Layout layout(const Dims& d, bool bwd) {
+  Layout L;
+  memset(&L, 0, sizeof L);
+  const size_t chunks = (size_t)d.BH() * d.NC;
+  const size_t tile = (size_t)CH * HD * sizeof(bf16);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += up(bytes);
+    return o;
+  };
+  L.W = take(chunks * tile);
+  L.U = take(chunks * tile);
+  L.P = take(chunks * tile);
+  if (d.S > 1) {
+    const size_t pair = (size_t)d.BH() * d.S * HD * HD * sizeof(float);
+    L.pairA = take(pair);
+    L.pairB = take(pair);
+    L.hin = take(pair);
+  }
+  if (bwd) {
+    L.Tb = take(chunks * tile);
+    L.states = take(chunks * tile);
+    L.delta = take(chunks * tile);
+    L.dstates = take(chunks * tile);
+    L.ddelta = take(chunks * tile);
+    const size_t part = (size_t)d.B * d.T * d.Hv * HD * sizeof(float);
+    L.dqp = take(part);
+    L.dkp = take(part);
+  }
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+// Forward states: prep has run; walk (with segments: fold, cross, replay).
+int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, const void* k,
+                      const float* g, const float* h0, void* o, float* hT, bf16* states,
+                      bf16* delta, cudaStream_t s) {
+  WalkFwdArgs w;
+  memset(&w, 0, sizeof w);
+  w.W = at<bf16>(ws, Lw.W);
+  w.U = at<bf16>(ws, Lw.U);
+  w.P = at<bf16>(ws, Lw.P);
+  w.q = static_cast<const bf16*>(q);
+  w.k = static_cast<const bf16*>(k);
+  w.g = g;
+  w.B = d.B;
+  w.T = d.T;
+  w.Hk = d.Hk;
+  w.Hv = d.Hv;
+  w.NC = d.NC;
+  w.S = d.S;
+  w.o = static_cast<bf16*>(o);
+  w.hT = hT;
+  w.states = states;
+  w.delta = delta;
+  if (d.S == 1) {
+    w.hstart = h0;
+    w.hstart_bh_stride = (long)HD * HD;
+    w.hstart_seg_stride = 0;
+    return cuda_status(launch_walk_fwd(w, 0, s));
+  }
+  WalkFwdArgs f = w;
+  f.pairA = at<float>(ws, Lw.pairA);
+  f.pairB = at<float>(ws, Lw.pairB);
+  f.o = nullptr;
+  f.hT = nullptr;
+  f.states = nullptr;
+  f.delta = nullptr;
+  int rc = cuda_status(launch_walk_fwd(f, 1, s));
+  if (rc) return rc;
+  AffineWalkArgs x;
+  memset(&x, 0, sizeof x);
+  x.A = f.pairA;
+  x.Bv = f.pairB;
+  x.init = h0;
+  x.outB = at<float>(ws, Lw.hin);
+  x.batch = (int)d.BH();
+  x.n = d.S;
+  x.dv = HD;
+  x.with_A = 0;
+  x.exclusive = 1;
+  x.reverse = 0;
+  rc = cuda_status(launch_affine_walk(x, s));
+  if (rc) return rc;
+  w.hstart = at<float>(ws, Lw.hin);
+  w.hstart_bh_stride = (long)d.S * HD * HD;
+  w.hstart_seg_stride = (long)HD * HD;
+  return cuda_status(launch_walk_fwd(w, 0, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_strerror(int status) {
+  switch (status) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_ARG: return "invalid argument (null pointer, misalignment, negative size or Hv % Hk != 0)";
+    case GDN_ERR_SHAPE: return "unsupported shape (this version needs d_k = d_v = 128 and chunk = 128)";
+    case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+    case GDN_ERR_CUDA: return "CUDA launch failed";
+    case GDN_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+    case GDN_ERR_UNSUPPORTED: return "unsupported device";
+    default: return "unknown status";
+  }
+}
+
+int gdn_default_segments(int B, int T, int Hv, int chunk) {
+  if (chunk <= 0 || T <= 0) return 1;
+  const int NC = (T + chunk - 1) / chunk;
+  (void)B;
+  (void)Hv;
+  if (NC <= 64) return 1;
+  int S = NC / 32;
+  if (S > 64) S = 64;
+  return S < 2 ? 2 : S;
+}
+
+size_t gdn_fwd_workspace_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk,
+                               int n_segments) {
+  if (check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments) != GDN_OK) return 0;
+  return layout(make_dims(B, T, Hk, Hv, n_segments), false).total;
+}
+
+size_t gdn_bwd_workspace_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk,
+                               int n_segments) {
+  if (check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments) != GDN_OK) return 0;
+  return layout(make_dims(B, T, Hk, Hv, n_segments), true).total;
+}
+
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const float* h0, void* o, float* hT, int B, int T, int Hk, int Hv, int d_k,
+                  int d_v, int chunk, int n_segments, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
+  if (rc) return rc;
+  const long tokens = (long)B * T;
+  if (tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, h0, o, hT, ws};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Dims d = make_dims(B, T, Hk, Hv, n_segments);
+  if (B == 0) return GDN_OK;
+  if (T == 0) {  // no tokens: the final state is the initial state
+    if (!hT) return GDN_OK;
+    const size_t bytes = (size_t)B * Hv * HD * HD * sizeof(float);
+    return cuda_status(h0 ? cudaMemcpyAsync(hT, h0, bytes, cudaMemcpyDeviceToDevice, s)
+                          : cudaMemsetAsync(hT, 0, bytes, s));
+  }
+  const Layout L = layout(d, false);
+  if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+
+  PrepArgs p;
+  memset(&p, 0, sizeof p);
+  p.q = static_cast<const bf16*>(q);
+  p.k = static_cast<const bf16*>(k);
+  p.v = static_cast<const bf16*>(v);
+  p.g = g;
+  p.beta = beta;
+  p.W = at<bf16>(ws, L.W);
+  p.U = at<bf16>(ws, L.U);
+  p.P = at<bf16>(ws, L.P);
+  p.B = B;
+  p.T = T;
+  p.Hk = Hk;
+  p.Hv = Hv;
+  p.NC = d.NC;
+  rc = cuda_status(launch_prep(p, s));
+  if (rc) return rc;
+  return run_forward_walks(d, L, ws, q, k, g, h0, o, hT, nullptr, nullptr, s);
+}
+
+int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const float* h0, const void* dO, const float* dhT, void* dq, void* dk, void* dv,
+                  float* dg, float* dbeta, float* dh0, int B, int T, int Hk, int Hv, int d_k,
+                  int d_v, int chunk, int n_segments, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
+  if (rc) return rc;
+  const long tokens = (long)B * T;
+  if (tokens > 0 && (!q || !k || !v || !g || !beta || !dO || !dq || !dk || !dv || !dg || !dbeta))
+    return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, h0, dO, dhT, dq, dk, dv, dg, dbeta, dh0, ws};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Dims d = make_dims(B, T, Hk, Hv, n_segments);
+  if (B == 0) return GDN_OK;
+  if (T == 0) {  // dh0 = dhT
+    if (!dh0) return GDN_OK;
+    const size_t bytes = (size_t)B * Hv * HD * HD * sizeof(float);
+    return cuda_status(dhT ? cudaMemcpyAsync(dh0, dhT, bytes, cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(dh0, 0, bytes, s));
+  }
+  const Layout L = layout(d, true);
+  if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+
+  // 1. per-chunk UT quantities (w, u, P, T)
+  PrepArgs p;
+  memset(&p, 0, sizeof p);
+  p.q = static_cast<const bf16*>(q);
+  p.k = static_cast<const bf16*>(k);
+  p.v = static_cast<const bf16*>(v);
+  p.g = g;
+  p.beta = beta;
+  p.W = at<bf16>(ws, L.W);
+  p.U = at<bf16>(ws, L.U);
+  p.P = at<bf16>(ws, L.P);
+  p.Tb = at<bf16>(ws, L.Tb);
+  p.B = B;
+  p.T = T;
+  p.Hk = Hk;
+  p.Hv = Hv;
+  p.NC = d.NC;
+  rc = cuda_status(launch_prep(p, s));
+  if (rc) return rc;
+  // 2. recompute the state entering every chunk, and Delta
+  rc = run_forward_walks(d, L, ws, q, k, g, h0, nullptr, nullptr, at<bf16>(ws, L.states),
+                         at<bf16>(ws, L.delta), s);
+  if (rc) return rc;
+  // 3. reverse walk of the state cotangent
+  WalkBwdArgs w;
+  memset(&w, 0, sizeof w);
+  w.W = at<bf16>(ws, L.W);
+  w.P = at<bf16>(ws, L.P);
+  w.q = static_cast<const bf16*>(q);
+  w.k = static_cast<const bf16*>(k);
+  w.dO = static_cast<const bf16*>(dO);
+  w.g = g;
+  w.B = B;
+  w.T = T;
+  w.Hk = Hk;
+  w.Hv = Hv;
+  w.NC = d.NC;
+  w.S = d.S;
+  w.dh0 = dh0;
+  w.dstates = at<bf16>(ws, L.dstates);
+  w.ddelta = at<bf16>(ws, L.ddelta);
+  if (d.S == 1) {
+    w.hstart = dhT;
+    w.hstart_bh_stride = (long)HD * HD;
+    w.hstart_seg_stride = 0;
+    rc = cuda_status(launch_walk_bwd(w, 0, s));
+  } else {
+    WalkBwdArgs f = w;
+    f.pairA = at<float>(ws, L.pairA);
+    f.pairB = at<float>(ws, L.pairB);
+    f.dh0 = nullptr;
+    rc = cuda_status(launch_walk_bwd(f, 1, s));
+    if (rc) return rc;
+    AffineWalkArgs x;
+    memset(&x, 0, sizeof x);
+    x.A = f.pairA;
+    x.Bv = f.pairB;
+    x.init = dhT;
+    x.outB = at<float>(ws, L.hin);
+    x.batch = (int)d.BH();
+    x.n = d.S;
+    x.dv = HD;
+    x.with_A = 0;
+    x.exclusive = 1;
+    x.reverse = 1;
+    rc = cuda_status(launch_affine_walk(x, s));
+    if (rc) return rc;
+    w.hstart = at<float>(ws, L.hin);
+    w.hstart_bh_stride = (long)d.S * HD * HD;
+    w.hstart_seg_stride = (long)HD * HD;
+    rc = cuda_status(launch_walk_bwd(w, 0, s));
+  }
+  if (rc) return rc;
+  // 4. chunk-parallel gradients, then the key-head sums of dq and dk
+  GradArgs ga;
+  memset(&ga, 0, sizeof ga);
+  ga.q = static_cast<const bf16*>(q);
+  ga.k = static_cast<const bf16*>(k);
+  ga.v = static_cast<const bf16*>(v);
+  ga.g = g;
+  ga.beta = beta;
+  ga.dO = static_cast<const bf16*>(dO);
+  ga.Tb = at<bf16>(ws, L.Tb);
+  ga.states = at<bf16>(ws, L.states);
+  ga.dstates = at<bf16>(ws, L.dstates);
+  ga.delta = at<bf16>(ws, L.delta);
+  ga.ddelta = at<bf16>(ws, L.ddelta);
+  ga.dq_part = at<float>(ws, L.dqp);
+  ga.dk_part = at<float>(ws, L.dkp);
+  ga.dv = static_cast<bf16*>(dv);
+  ga.dg = dg;
+  ga.dbeta = dbeta;
+  ga.B = B;
+  ga.T = T;
+  ga.Hk = Hk;
+  ga.Hv = Hv;
+  ga.NC = d.NC;
+  rc = cuda_status(launch_grads(ga, s));
+  if (rc) return rc;
+  return cuda_status(launch_reduce_dqdk(ga.dq_part, ga.dk_part, static_cast<bf16*>(dq),
+                                        static_cast<bf16*>(dk), tokens, Hk, Hv, s));
+}
+
+int gdn_affine_compose(const float* A, const float* B, float* A_out, float* B_out, int batch,
+                       int n, int d_k, int d_v, void* stream) {
+  if (batch < 0 || n < 0) return GDN_ERR_ARG;
+  if (d_k != HD || d_v <= 0 || d_v > HD || d_v % 16 != 0) return GDN_ERR_SHAPE;
+  if ((long)batch * n == 0) return GDN_OK;
+  if (!A || !B || !A_out || !B_out) return GDN_ERR_ARG;
+  const void* ptrs[] = {A, B, A_out, B_out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return GDN_ERR_ARG;
+  AffineWalkArgs x;
+  memset(&x, 0, sizeof x);
+  x.A = A;
+  x.Bv = B;
+  x.init = nullptr;
+  x.outA = A_out;
+  x.outB = B_out;
+  x.batch = batch;
+  x.n = n;
+  x.dv = d_v;
+  x.with_A = 1;
+  x.exclusive = 0;
+  x.reverse = 0;
+  return cuda_status(launch_affine_walk(x, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_debug_ut(const void* k, const void* v, const float* g, const float* beta, float* S_out,
+                 float* T_out, void* w_out, void* u_out, int B, int T, int Hk, int Hv, int d_k,
+                 int d_v, int chunk, void* stream) {
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, 1);
+  if (rc) return rc;
+  if ((long)B * T == 0) return GDN_OK;
+  if (!k || !v || !g || !beta) return GDN_ERR_ARG;
+  const void* ptrs[] = {k, v, g, beta, S_out, T_out, w_out, u_out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_ARG;
+  PrepArgs p;
+  memset(&p, 0, sizeof p);
+  p.q = static_cast<const bf16*>(k);  // unused: P is not requested
+  p.k = static_cast<const bf16*>(k);
+  p.v = static_cast<const bf16*>(v);
+  p.g = g;
+  p.beta = beta;
+  p.W = static_cast<bf16*>(w_out);
+  p.U = static_cast<bf16*>(u_out);
+  p.S_dbg = S_out;
+  p.T_dbg = T_out;
+  p.B = B;
+  p.T = T;
+  p.Hk = Hk;
+  p.Hv = Hv;
+  p.NC = (T + CH - 1) / CH;
+  return cuda_status(launch_prep(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

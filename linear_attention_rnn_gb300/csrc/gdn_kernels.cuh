@@ -1,0 +1,115 @@
+// gdn_kernels.cuh -- argument blocks and launchers of the gated-delta-rule kernels
+// (internal to the library; the public boundary is include/gdn.h).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+// Per-chunk UT/WY preparation: one CTA per (chunk, value head, batch row).
+struct PrepArgs {
+  const bf16* q;
+  const bf16* k;
+  const bf16* v;
+  const float* g;
+  const float* beta;
+  bf16* W;       // [BH][NC][CH][HD]  w = T diag(beta gamma) K      (nullable)
+  bf16* U;       // [BH][NC][CH][HD]  u = T diag(beta) V            (nullable)
+  bf16* P;       // [BH][NC][CH][CH]  (Q K^T) * decay, incl. diag   (nullable)
+  bf16* Tb;      // [BH][NC][CH][CH]  T in bf16 (backward)           (nullable)
+  float* S_dbg;  // [BH][NC][CH][CH]  fp32 S  (debug export)        (nullable)
+  float* T_dbg;  // [BH][NC][CH][CH]  fp32 T  (debug export)        (nullable)
+  int B, T, Hk, Hv, NC;
+};
+
+// Sequential forward walk over the chunks of one segment for one
+// (state-column slice, segment, batch*value head).
+struct WalkFwdArgs {
+  const bf16* W;
+  const bf16* U;
+  const bf16* P;
+  const bf16* q;
+  const bf16* k;
+  const float* g;
+  const float* hstart;     // entering state of each segment, fp32 (nullable = 0)
+  long hstart_seg_stride;  // elements between consecutive segments' states
+  long hstart_bh_stride;   // elements between consecutive (b, j)
+  bf16* o;                 // [B,T,Hv,HD] (nullable)
+  float* hT;               // [BH][HD][HD] written by the last segment (nullable)
+  bf16* states;            // [BH][NC][HD][HD] bf16 entering state of every chunk (nullable)
+  bf16* delta;             // [BH][NC][CH][HD] bf16 Delta of every chunk (nullable)
+  float* pairA;            // fold output [BH][S][HD][HD]
+  float* pairB;            // fold output [BH][S][HD][HD]
+  int B, T, Hk, Hv, NC, S;
+};
+
+// Sequential backward walk (state cotangent) over the chunks of one segment.
+struct WalkBwdArgs {
+  const bf16* W;
+  const bf16* P;
+  const bf16* q;
+  const bf16* k;
+  const bf16* dO;
+  const float* g;
+  const float* hstart;     // cotangent of the state leaving each segment (nullable = 0)
+  long hstart_seg_stride;
+  long hstart_bh_stride;
+  float* dh0;              // [BH][HD][HD] written by segment 0 (nullable)
+  bf16* dstates;           // [BH][NC][HD][HD] bf16 cotangent of the state leaving every chunk
+  bf16* ddelta;            // [BH][NC][CH][HD] bf16 dDelta of every chunk
+  float* pairA;            // fold output
+  float* pairB;
+  int B, T, Hk, Hv, NC, S;
+};
+
+// Sequential affine walk X <- A_i X (+ B_i) over i (segment prefix / compose).
+struct AffineWalkArgs {
+  const float* A;      // [batch][n][HD][HD]
+  const float* Bv;     // [batch][n][HD][dv] (nullable = 0)
+  const float* init;   // [batch][HD][dv] initial B-part columns (nullable = 0)
+  float* outA;         // inclusive mode: [batch][n][HD][HD]
+  float* outB;         // [batch][n][HD][dv]
+  int batch, n, dv;
+  int with_A;          // 1: state is [A | B] starting from [I | 0] (compose)
+  int exclusive;       // 1: write the state entering map i (else after it)
+  int reverse;         // 1: walk i = n-1 .. 0
+};
+
+// Chunk-parallel gradients, one CTA per (chunk, value head, batch row).
+struct GradArgs {
+  const bf16* q;
+  const bf16* k;
+  const bf16* v;
+  const float* g;
+  const float* beta;
+  const bf16* dO;
+  const bf16* Tb;       // [BH][NC][CH][CH]
+  const bf16* states;   // [BH][NC][HD][HD]  h entering chunk
+  const bf16* dstates;  // [BH][NC][HD][HD]  cotangent of h leaving chunk
+  const bf16* delta;    // [BH][NC][CH][HD]
+  const bf16* ddelta;   // [BH][NC][CH][HD]
+  float* dq_part;       // [B,T,Hv,HD] fp32 per value head
+  float* dk_part;       // [B,T,Hv,HD]
+  bf16* dv;             // [B,T,Hv,HD]
+  float* dg;            // [B,T,Hv]
+  float* dbeta;         // [B,T,Hv]
+  int B, T, Hk, Hv, NC;
+};
+
+size_t prep_smem_bytes();
+size_t walk_fwd_smem_bytes(int fold);
+size_t walk_bwd_smem_bytes(int fold);
+size_t affine_walk_smem_bytes();
+size_t grad_smem_bytes();
+
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_walk_fwd(const WalkFwdArgs& a, int fold, cudaStream_t s);
+cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int fold, cudaStream_t s);
+cudaError_t launch_affine_walk(const AffineWalkArgs& a, cudaStream_t s);
+cudaError_t launch_grads(const GradArgs& a, cudaStream_t s);
+cudaError_t launch_reduce_dqdk(const float* dq_part, const float* dk_part, bf16* dq, bf16* dk,
+                               long tokens, int Hk, int Hv, cudaStream_t s);
+
+}  // namespace gdn

@@ -76,3 +76,36 @@ def random_small(B=1, T=40, Hk=1, Hv=1, dk=8, dv=8, seed=0, gate_shift=0.0, h0=T
     dO = rng.standard_normal((B, T, Hv, dv)) if bwd else None
     dhT = rng.standard_normal((B, Hv, dk, dv)) * 0.3 if bwd else None
     return from_arrays(q, k, v, g, beta, h0a, dO, dhT)
+
+
+# --------------------------------------------------------------------- GPU side
+@pytest.fixture(scope="session")
+def gdn_lib():
+    """The built C-ABI library (GPU tests only)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import linear_attention_rnn_gb300 as gdn
+    gdn.build()
+    gdn.lib()
+    return gdn
+
+
+def key_head_slice(inp, b, kh):
+    """Inputs restricted to batch row b, key head kh and its value heads
+    (host tensors) -- what the oracle needs to check those heads exactly."""
+    wl = inp.wl
+    grp = wl.Hv // wl.Hk
+    j0 = kh * grp
+    cut = lambda x, lo, n: None if x is None else x[b:b + 1, :, lo:lo + n].contiguous().cpu()
+    cut_s = lambda x: None if x is None else x[b:b + 1, j0:j0 + grp].contiguous().cpu()
+    sub = Inputs(wl.replace(B=1, Hk=1, Hv=grp), cut(inp.q, kh, 1), cut(inp.k, kh, 1),
+                 cut(inp.v, j0, grp), cut(inp.g, j0, grp), cut(inp.beta, j0, grp),
+                 cut_s(inp.h0), cut(inp.dO, j0, grp) if inp.dO is not None else None,
+                 cut_s(inp.dhT))
+    return sub, j0, grp
+
+
+def assert_rel(x, ref, tol, what):
+    err = relmax(x, ref)
+    assert err <= tol, f"{what}: max|x - ref| / max|ref| = {err:.3e} > {tol:.1e}"
+    return err

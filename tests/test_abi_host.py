@@ -1,0 +1,106 @@
+"""C-ABI library: builds, loads, exports every declared symbol, and rejects bad
+arguments on the host (before any CUDA call) -- no GPU needed."""
+import ctypes
+
+import pytest
+
+import linear_attention_rnn_gb300 as gdn
+
+
+@pytest.fixture(scope="module")
+def L():
+    gdn.build()
+    return gdn.lib()
+
+
+def test_exports_every_declared_function(L):
+    names = gdn.header_functions()
+    assert {"gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_affine_compose", "gdn_debug_ut",
+            "gdn_strerror", "gdn_fwd_workspace_bytes", "gdn_bwd_workspace_bytes",
+            "gdn_default_segments"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_strerror_covers_codes(L):
+    for code in range(-6, 1):
+        assert L.gdn_strerror(code)
+    assert L.gdn_strerror(-99) == b"unknown status"
+
+
+P = ctypes.c_void_p
+FAKE = P(1 << 20)          # aligned, never dereferenced (validation fails first)
+MISAL = P((1 << 20) + 2)
+
+
+def _fwd(L, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, o=FAKE, hT=None,
+         B=1, T=256, Hk=2, Hv=4, dk=128, dv=128, chunk=128, S=0, ws=FAKE, ws_bytes=0):
+    return L.gdn_chunk_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hk, Hv, dk, dv, chunk, S, ws,
+                           ws_bytes, None)
+
+
+def test_fwd_argument_errors(L):
+    assert _fwd(L, dk=64) == -2
+    assert _fwd(L, dv=96) == -2
+    assert _fwd(L, chunk=64) == -2
+    assert _fwd(L, Hk=3, Hv=4) == -1
+    assert _fwd(L, T=-1) == -1
+    assert _fwd(L, S=-2) == -1
+    assert _fwd(L, q=None) == -1
+    assert _fwd(L, o=None) == -1
+    assert _fwd(L, k=MISAL) == -1
+    assert _fwd(L, ws_bytes=10) == -3          # too small
+    assert _fwd(L, ws=None, ws_bytes=1 << 40) == -3
+    assert _fwd(L, B=0) == 0                   # nothing to do
+    assert _fwd(L, q=None, k=None, v=None, g=None, beta=None, o=None, T=0) == 0  # T=0, no hT
+
+
+def test_bwd_argument_errors(L):
+    args = [FAKE] * 5 + [None, FAKE, None] + [FAKE] * 5 + [None]
+    ok = dict(B=1, T=256, Hk=2, Hv=4, dk=128, dv=128, chunk=128, S=0)
+
+    def call(a, **kw):
+        d = dict(ok, **kw)
+        return L.gdn_chunk_bwd(*a, d["B"], d["T"], d["Hk"], d["Hv"], d["dk"], d["dv"],
+                               d["chunk"], d["S"], FAKE, 16, None)
+    assert call(args, dk=256) == -2
+    assert call(args, Hv=5) == -1
+    bad = list(args)
+    bad[6] = None  # dO
+    assert call(bad) == -1
+    assert call(args) == -3  # workspace of 16 bytes
+
+
+def test_compose_argument_errors(L):
+    assert L.gdn_affine_compose(FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 128, None) == -2
+    assert L.gdn_affine_compose(FAKE, FAKE, FAKE, FAKE, 1, 4, 128, 20, None) == -2
+    assert L.gdn_affine_compose(None, FAKE, FAKE, FAKE, 1, 4, 128, 128, None) == -1
+    assert L.gdn_affine_compose(FAKE, MISAL, FAKE, FAKE, 1, 4, 128, 128, None) == -1
+    assert L.gdn_affine_compose(None, None, None, None, 0, 4, 128, 128, None) == 0
+
+
+def test_workspace_sizes(L):
+    f = gdn.fwd_workspace_bytes
+    b = gdn.bwd_workspace_bytes
+    assert f(1, 4096, 16, 32, 64) == 0  # unsupported d_k
+    w1 = f(1, 4096, 16, 32, n_segments=1)
+    # w, u and P: three bf16 128x128 tiles per (chunk, value head)
+    assert w1 >= 3 * 32 * 32 * 128 * 128 * 2
+    assert f(1, 4096, 16, 32, n_segments=4) > w1  # per-segment (A, B) and entering states
+    assert b(1, 4096, 16, 32, n_segments=1) > w1
+    assert f(2, 1000, 2, 4) > 0
+
+
+def test_default_segments(L):
+    assert gdn.default_segments(1, 4096, 32) == 1
+    assert gdn.default_segments(1, 0, 32) == 1
+    s = gdn.default_segments(1, 262144, 32)
+    assert 2 <= s <= 64
+    assert gdn.default_segments(1, 1 << 20, 32) == 64
+
+
+def test_binding_validates_before_calling():
+    import torch
+    q = torch.zeros(1, 8, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gdn.chunk_fwd(q, q, q, torch.zeros(1, 8, 1), torch.zeros(1, 8, 1))  # CPU tensors

@@ -1,0 +1,207 @@
+"""GPU parity of the forward path against the fp64 oracle (through the C ABI).
+
+Tolerances: max|o - o_ref| <= 2e-2 max|o_ref| and max|hT - hT_ref| <= 1e-2
+max|hT_ref| for bf16 inputs with an fp32 state; ladder residual
+max|(I + S) T - I| <= 1e-4 with the oracle's S and the device's T.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import chunked
+from linear_attention_rnn_gb300.inputs import WORKLOADS, make_host
+from conftest import as64, assert_rel, from_arrays, head, key_head_slice, random_small
+
+pytestmark = pytest.mark.gpu
+
+O_TOL, H_TOL, RES_TOL = 2e-2, 1e-2, 1e-4
+
+
+def _cuda(inp):
+    return inp.to("cuda")
+
+
+def _check_fwd(gdn, inp, n_segments=0, heads=None):
+    d = _cuda(inp)
+    o, hT = gdn.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=n_segments)
+    torch.cuda.synchronize()
+    o = o.float().cpu().numpy()
+    hT = hT.cpu().numpy()
+    heads = heads or [(b, j) for b in range(inp.wl.B) for j in range(inp.wl.Hv)]
+    ro, rh = oracle.fwd(inp, heads=heads)
+    eo = max(assert_rel(o[b, :, j], ro[i], O_TOL, f"o[{b},{j}]") for i, (b, j) in enumerate(heads))
+    eh = max(assert_rel(hT[b, j], rh[i], H_TOL, f"hT[{b},{j}]") for i, (b, j) in enumerate(heads))
+    return eo, eh
+
+
+def test_tiny_workload(gdn_lib):
+    inp = make_host(WORKLOADS["tiny_t1024"])
+    _check_fwd(gdn_lib, inp)
+
+
+def test_layer_workload_all_heads(gdn_lib):
+    inp = make_host(WORKLOADS["layer_t4096"], backward=False)
+    _check_fwd(gdn_lib, inp)
+
+
+@pytest.mark.parametrize("T", [1, 5, 127, 128, 129, 300, 1000])
+def test_ragged_lengths(gdn_lib, T):
+    inp = make_host(WORKLOADS["tiny_t1024"].replace(T=T, Hk=2, Hv=4, h0_std=0.1, seed=T))
+    _check_fwd(gdn_lib, inp)
+
+
+@pytest.mark.parametrize("Hk,Hv", [(1, 1), (1, 4), (3, 6), (4, 4)])
+def test_head_groupings(gdn_lib, Hk, Hv):
+    inp = make_host(WORKLOADS["tiny_t1024"].replace(T=384, B=2, Hk=Hk, Hv=Hv, h0_std=0.1, seed=3))
+    _check_fwd(gdn_lib, inp)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 16])
+def test_segment_counts_slow_decay(gdn_lib, S):
+    """Slow decay (g ~ -0.05 per token) so the incoming state of every
+    segment matters; results must not depend on the segment count."""
+    inp = make_host(WORKLOADS["tiny_t1024"].replace(T=2048 + 77, Hk=1, Hv=2, gate_shift=-3.0,
+                                                   h0_std=0.5, seed=11))
+    _check_fwd(gdn_lib, inp, n_segments=S)
+
+
+def test_near_zero_decay_segments(gdn_lib):
+    """g ~ -0.002 per token: the per-chunk maps A are far from zero, so the
+    segment prefix carries real mass across segments."""
+    inp = make_host(WORKLOADS["tiny_t1024"].replace(T=4096, Hk=1, Hv=2, gate_shift=-6.0,
+                                                   h0_std=1.0, seed=12))
+    for S in (1, 5, 32):
+        _check_fwd(gdn_lib, inp, n_segments=S)
+
+
+def test_beta_zero_closed_form(gdn_lib):
+    """beta = 0: hT = exp(sum g) h0 exactly in the rule; the device matches."""
+    inp = make_host(WORKLOADS["tiny_t1024"].replace(T=300, Hk=1, Hv=2, gate_shift=-5.0,
+                                                   h0_std=1.0, seed=13))
+    inp.beta.zero_()
+    d = _cuda(inp)
+    o, hT = gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    G = np.cumsum(as64(inp, "g")[0], axis=0)  # [T, Hv]
+    for j in range(2):
+        ref = np.exp(G[-1, j]) * as64(inp, "h0")[0, j]
+        assert_rel(hT[0, j].cpu().numpy(), ref, 1e-5, "hT beta=0")
+
+
+def test_empty_sequence(gdn_lib):
+    inp = make_host(WORKLOADS["tiny_t1024"].replace(T=0, Hk=1, Hv=2, h0_std=1.0))
+    d = _cuda(inp)
+    o, hT = gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0)
+    assert o.numel() == 0
+    assert torch.equal(hT.cpu(), inp.h0)
+    o, hT = gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, None)
+    assert torch.count_nonzero(hT) == 0
+
+
+def test_no_final_state_requested(gdn_lib):
+    inp = make_host(WORKLOADS["tiny_t1024"].replace(T=256, Hk=1, Hv=1))
+    d = _cuda(inp)
+    o, hT = gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, None, want_hT=False)
+    assert hT is None
+    ro, _ = oracle.fwd(inp)
+    assert_rel(o[0, :, 0].float().cpu().numpy(), ro[0], O_TOL, "o")
+
+
+# ---------------------------------------------------------------- UT / ladder
+@pytest.mark.parametrize("name", ["tiny_t1024", "layer_t4096"])
+def test_ut_intermediates_and_ladder_residual(gdn_lib, name):
+    wl = WORKLOADS[name]
+    inp = make_host(wl, backward=False)
+    d = _cuda(inp)
+    S, T, w, u = gdn_lib.debug_ut(d.k, d.v, d.g, d.beta)
+    torch.cuda.synchronize()
+    S, T, w, u = (x.float().cpu().numpy() for x in (S, T, w, u))
+    heads = [(0, 0), (0, wl.Hv - 1)] if wl.Hv > 2 else [(0, j) for j in range(wl.Hv)]
+    I = np.eye(128)
+    worst = 0.0
+    for b, j in heads:
+        q, k, v, g, beta, _ = head(inp, b, j)
+        for c in range(wl.T // 128):
+            sl = slice(c * 128, (c + 1) * 128)
+            it = chunked.chunk_intermediates(q[sl], k[sl], v[sl], g[sl], beta[sl])
+            # fp32 gates: G reaches ~ -170 over a chunk here, so G_r - G_s keeps
+            # ~1e-5 relative accuracy after cancellation (fp32 cumsum)
+            assert_rel(S[b, j, c], it["S"], 1e-4, f"S[{b},{j},{c}]")
+            res = np.max(np.abs((I + it["S"]) @ T[b, j, c].astype(np.float64) - I))
+            worst = max(worst, res)
+            assert res <= RES_TOL, f"ladder residual {res:.2e} at {(b, j, c)}"
+            assert_rel(w[b, j, c], it["w"], 1e-2, "w")
+            assert_rel(u[b, j, c], it["u"], 1e-2, "u")
+    assert worst <= RES_TOL
+
+
+@pytest.mark.parametrize("kind", ["all_ones", "gaussian_unnormalised"])
+def test_ladder_stress_inputs(gdn_lib, kind):
+    """The page's stress cases for the inversion.  all-ones: keys all equal
+    (K K^T = 1), beta = 1, g = 0 gives S = strictly-lower ones, whose inverse
+    is I minus the subdiagonal.  Unnormalised Gaussian keys give large S;
+    judged relative to forward substitution."""
+    T = 128
+    if kind == "all_ones":
+        k = np.zeros((1, T, 1, 128))
+        k[..., 0] = 1.0
+        beta = np.ones((1, T, 1))
+        g = np.zeros((1, T, 1))
+    else:
+        rng = np.random.default_rng(21)
+        k = rng.standard_normal((1, T, 1, 128)) * 0.25
+        beta = 1 / (1 + np.exp(-rng.standard_normal((1, T, 1))))
+        g = -0.01 * np.ones((1, T, 1))
+    inp = from_arrays(k, k, np.zeros((1, T, 1, 128)), g, beta)
+    d = _cuda(inp)
+    S, Tm, _, _ = gdn_lib.debug_ut(d.k, d.v, d.g, d.beta)
+    Tm = Tm[0, 0, 0].cpu().numpy().astype(np.float64)
+    q, kk, v, gg, bb, _ = head(inp, 0, 0)
+    it = chunked.chunk_intermediates(q, kk, v, gg, bb)
+    ref = chunked.ut_forward_substitution(it["S"])
+    if kind == "all_ones":
+        assert np.array_equal(ref, np.eye(T) - np.eye(T, k=-1))
+        assert np.max(np.abs(Tm - ref)) <= 1e-6
+    else:
+        assert_rel(Tm, ref, 1e-3, "T (unnormalised Gaussian keys)")
+
+
+# ----------------------------------------------------------------- compose
+def test_affine_compose_matches_oracle(gdn_lib):
+    rng = np.random.default_rng(5)
+    batch, n = 3, 9
+    A = (rng.standard_normal((batch, n, 128, 128)) / np.sqrt(128) * 0.9).astype(np.float32)
+    B = rng.standard_normal((batch, n, 128, 128)).astype(np.float32)
+    Ao, Bo = gdn_lib.affine_compose(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda())
+    Ao, Bo = Ao.cpu().numpy(), Bo.cpu().numpy()
+    for r in range(batch):
+        rA, rB = chunked.inclusive_prefix(list(A[r].astype(np.float64)), list(B[r].astype(np.float64)))
+        for i in range(n):
+            assert_rel(Ao[r, i], rA[i], 1e-4, f"A_out[{r},{i}]")
+            assert_rel(Bo[r, i], rB[i], 1e-4, f"B_out[{r},{i}]")
+
+
+def test_affine_compose_narrow_values(gdn_lib):
+    rng = np.random.default_rng(6)
+    A = (rng.standard_normal((2, 5, 128, 128)) / np.sqrt(128)).astype(np.float32)
+    B = rng.standard_normal((2, 5, 128, 48)).astype(np.float32)
+    Ao, Bo = gdn_lib.affine_compose(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda())
+    for r in range(2):
+        rA, rB = chunked.inclusive_prefix(list(A[r].astype(np.float64)), list(B[r].astype(np.float64)))
+        assert_rel(Bo[r].cpu().numpy(), np.array(rB), 1e-4, "B_out (d_v = 48)")
+        assert_rel(Ao[r].cpu().numpy(), np.array(rA), 1e-4, "A_out (d_v = 48)")
+
+
+def test_segment_negative_control_on_device_states(gdn_lib):
+    """Dropping the incoming state of later segments is detectable: the
+    device's segmented result matches the oracle, the oracle's dropped-state
+    replay does not."""
+    inp = make_host(WORKLOADS["tiny_t1024"].replace(T=1024, Hk=1, Hv=1, gate_shift=-6.0,
+                                                   h0_std=1.0, seed=14))
+    d = _cuda(inp)
+    o, _ = gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=4)
+    ro, _ = oracle.fwd(inp)
+    bad, _, _ = chunked.head_fwd_segmented(*head(inp, 0, 0), 128, 4, drop_incoming=True)
+    dev = o[0, :, 0].float().cpu().numpy()
+    assert_rel(dev, ro[0], O_TOL, "segmented o")
+    assert np.max(np.abs(bad - ro[0])) > O_TOL * np.max(np.abs(ro[0]))
