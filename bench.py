@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked Gated DeltaNet forward + backward on GB300.
+
+Metric: GDN chunk fwd+bwd tokens/s at T=4096, Hv=32, d=128 (one Qwen3-Next-
+shaped GDN layer: B=1, 16 key heads shared by 32 value heads, chunk 128,
+h0 ~ N(0, 0.1^2), g = -softplus(N(0,1) + 1), cotangents dO ~ N(0,1),
+dhT ~ N(0, 0.1^2)), and the fraction of the binding roofline.
+
+A step is one forward (o, hT) plus one backward (dq, dk, dv, dg, dbeta,
+dh0) over one batch.  Inputs are resident in HBM; L2 is flushed (a 512 MiB
+write) before every timed step, outside the step's events.  Each rank runs
+the same per-GPU workload (weak scaling, no collective on the data path).
+
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+# per-unit algorithmic work of the path (2 m n k per product, triangular
+# operands at their nonzero size; K K^T and Q K^T once per key head)
+FLOP_PER_CHUNK_KHEAD = 4_194_304          # K K^T + Q K^T (both triangular)
+FLOP_LADDER = 1_398_016                   # sum_b 2 b^2 C for b = 1..64
+FLOP_TRI = 2_113_536                      # lower-triangular 128x128 times 128x128
+FLOP_FULL = 4_194_304                     # 128x128x128
+FLOPS = {  # per (chunk, value head), per kernel
+    "prep": FLOP_LADDER + 2 * FLOP_TRI,   # + FLOP_PER_CHUNK_KHEAD per (chunk, key head)
+    "walk": 3 * FLOP_FULL + FLOP_TRI,     # w h, k_g^T Delta, Q h, P Delta
+    "walk_states": 2 * FLOP_FULL,         # w h, k_g^T Delta
+    "walk_bwd": 3 * FLOP_FULL + FLOP_TRI,  # K dh', Q^T dO, w^T dDelta, P^T dO
+    "grads": 3 * FLOP_FULL + 9 * FLOP_TRI,
+    "reduce": 0,
+}
+FWD_KERNELS = ["prep", "walk"]
+BWD_KERNELS = ["prep", "walk_states", "walk_bwd", "grads", "reduce"]
+FWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk"]
+BWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk_states", "fold_bwd", "prefix_bwd",
+                   "walk_bwd", "grads", "reduce"]
+KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<false>", "walk_states": "k_walk_fwd<false>",
+                 "walk_bwd": "k_walk_bwd<false>", "grads": "k_grads", "reduce": "k_reduce_dqdk",
+                 "fold": "k_walk_fwd<true>", "prefix": "k_affine_walk",
+                 "fold_bwd": "k_walk_bwd<true>", "prefix_bwd": "k_affine_walk"}
+# DRAM traffic per launch from the committed ncu capture of the same kernels
+# (profiles/*), keyed by kernel; None until captured for the current code.
+NCU_TRAFFIC = {}
+
+
+def algorithmic(wl):
+    """Algorithmic bytes and FLOPs of the forward and backward at workload wl."""
+    B, T, Hk, Hv, dk, dv = wl.B, wl.T, wl.Hk, wl.Hv, wl.dk, wl.dv
+    NC = (T + wl.chunk - 1) // wl.chunk
+    qk = 2 * B * T * Hk * dk * 2
+    vv = B * T * Hv * dv * 2
+    gb = 2 * B * T * Hv * 4
+    st = B * Hv * dk * dv * 4
+    fwd_bytes = qk + vv + gb + st + vv + st            # read q k v g beta h0, write o hT
+    bwd_bytes = qk + vv + gb + st + vv + st + qk + vv + gb + st  # + dO dhT; dq dk dv dg dbeta dh0
+    units, kunits = B * Hv * NC, B * Hk * NC
+    fwd_flops = kunits * FLOP_PER_CHUNK_KHEAD + units * (FLOPS["prep"] + FLOPS["walk"])
+    bwd_flops = (kunits * FLOP_PER_CHUNK_KHEAD + units * (FLOPS["prep"] + FLOPS["walk_states"]
+                 + FLOPS["walk_bwd"] + FLOPS["grads"]))
+    return dict(fwd_bytes=fwd_bytes, bwd_bytes=bwd_bytes, fwd_flops=fwd_flops,
+                bwd_flops=bwd_flops, units=units, kunits=kunits)
+
+
+def kernel_flops(name, alg):
+    f = FLOPS.get(name)
+    if f is None:
+        return None
+    extra = alg["kunits"] * FLOP_PER_CHUNK_KHEAD if name == "prep" else 0
+    return alg["units"] * f + extra
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            mp = json.load(f)
+        return dict(hbm=float(mp["hbm_gbs"]), bf16=float(mp["bf16_tflops"]),
+                    bf16_sustained=float(mp.get("bf16_tflops_sustained", mp["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples with host timestamps."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "50"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "timed window"
+        if not win:  # timed region shorter than the sampling period: nearest samples
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            win = [p for _, p in near]
+            note = "nearest samples to a short timed window"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(win), "window": note}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import linear_attention_rnn_gb300 as gdn
+    from linear_attention_rnn_gb300.inputs import WORKLOADS, make_host
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gdn.build()
+    wl = WORKLOADS[args.workload].replace(backward=True)
+    nseg = args.n_segments if args.n_segments > 0 else gdn.default_segments(wl.B, wl.T, wl.Hv)
+    host = make_host(wl)
+    d = host.to(dev)
+    ws_f = torch.empty(gdn.fwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
+                       dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
+                       dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    fk = FWD_KERNELS if nseg == 1 else FWD_KERNELS_SEG
+    bk = BWD_KERNELS if nseg == 1 else BWD_KERNELS_SEG
+
+    def mk_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record()
+        return evs
+
+    K, W = args.steps, args.warmup
+    starts = mk_events(K)
+    fev = [mk_events(len(fk)) for _ in range(K)]
+    bev = [mk_events(len(bk)) for _ in range(K)]
+    torch.cuda.synchronize()
+
+    def step(i=None):
+        o, hT = gdn.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=nseg, workspace=ws_f,
+                              events=None if i is None else fev[i])
+        gr = gdn.chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.dO, d.dhT, n_segments=nseg,
+                           workspace=ws_b, events=None if i is None else bev[i])
+        return o, hT, gr
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    # warm-up: at least W steps and at least ~1 s of device work
+    t_w = time.time()
+    n_w = 0
+    while n_w < W or time.time() - t_w < args.min_warmup_s:
+        flush.zero_()
+        step()
+        n_w += 1
+        if n_w % 50 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(2_000_000)  # head start for the host's launches
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record()
+        step(i)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.stop()
+
+    step_ms = [starts[i].elapsed_time(bev[i][-1]) for i in range(K)]
+    fwd_ms = [starts[i].elapsed_time(fev[i][-1]) for i in range(K)]
+    bwd_ms = [fev[i][-1].elapsed_time(bev[i][-1]) for i in range(K)]
+    kern = {}
+    for name_list, evl, first in ((fk, fev, starts), (bk, bev, [f[-1] for f in fev])):
+        for kidx, name in enumerate(name_list):
+            key = name if name_list is fk else name + ("_b" if name in ("prep", "fold", "prefix") else "")
+            ts = []
+            for i in range(K):
+                a = first[i] if kidx == 0 else evl[i][kidx - 1]
+                ts.append(a.elapsed_time(evl[i][kidx]))
+            kern[key] = sum(ts) / K
+    total_ms = sum(step_ms)
+
+    # e2e through the same public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, gdn, wl, host, dev, nseg)
+
+    local = dict(total_ms=total_ms, tokens=wl.tokens * K)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if rank != 0:
+        return None
+    alg = algorithmic(wl)
+    pk = peaks()
+    mean_step = total_ms / K
+    value = world * wl.tokens * K / (total_ms / 1e3)
+    fwd_mean = statistics.mean(fwd_ms)
+    bwd_mean = statistics.mean(bwd_ms)
+
+    def path(bytes_, flops, ms):
+        t_hbm = bytes_ / (pk["hbm"] * 1e9) * 1e3
+        t_tc = flops / (pk["bf16"] * 1e12) * 1e3
+        t_roof = max(t_hbm, t_tc)
+        return {"ms": round(ms, 5), "roof_ms": round(t_roof, 5),
+                "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": round(t_roof / ms, 4),
+                "algorithmic_bytes": bytes_, "algorithmic_flops": flops}
+
+    kernels = {}
+    for name, ms in kern.items():
+        base = name[:-2] if name.endswith("_b") else name
+        fl = kernel_flops(base, alg)
+        kernels[name] = {"symbol": KERNEL_SYMBOL.get(base, base), "ms": round(ms, 5),
+                         "share": round(ms / mean_step, 4)}
+        if fl:
+            kernels[name]["tflops"] = round(fl / (ms * 1e-3) / 1e12, 2)
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    dbase = dom[:-2] if dom.endswith("_b") else dom
+    dfl = kernel_flops(dbase, alg) or 0
+    dms = kernels[dom]["ms"]
+    achieved = dfl / (dms * 1e-3) / 1e12 if dfl else 0.0
+    peak = pk["bf16"]
+    traffic = NCU_TRAFFIC.get(dom)
+    clocks = sampler.summary(t0, t1)
+    out = {
+        "metric": "GDN chunk fwd+bwd tokens/s (T=4096, H_v=32, d=128) and % of roofline",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": n_w,
+        "ms_per_step": round(mean_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{wl.name} fwd+bwd: B={wl.B} T={wl.T} Hk={wl.Hk} Hv={wl.Hv} "
+                               f"dk=dv={wl.dk} chunk={wl.chunk} segments={nseg}",
+                   "l2": "flushed (512 MiB write) before every timed step",
+                   "parallelism": f"replicas x{world} (independent problems)"},
+        "roofline": {"kernel": KERNEL_SYMBOL.get(dbase, dbase), "bound": "tensor",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"bf16 burst, {pk['source']}"},
+        "path_roofline": {"fwd": path(alg["fwd_bytes"], alg["fwd_flops"], fwd_mean),
+                          "bwd": path(alg["bwd_bytes"], alg["bwd_flops"], bwd_mean),
+                          "step": path(alg["fwd_bytes"] + alg["bwd_bytes"],
+                                       alg["fwd_flops"] + alg["bwd_flops"], mean_step),
+                          "peaks": {"hbm_gbs": pk["hbm"], "bf16_tflops": pk["bf16"],
+                                    "source": pk["source"]}},
+        "kernels": kernels,
+        "fwd_tokens_per_s": round(wl.tokens / (fwd_mean * 1e-3), 1),
+        "bwd_tokens_per_s": round(wl.tokens / (bwd_mean * 1e-3), 1),
+        "gpu_launches": K * (len(fk) + len(bk)),
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        out["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, host)
+    return out
+
+
+def run_e2e(args, gdn, wl, host, dev, nseg):
+    """Same step through the public API with pinned host buffers: H2D of the
+    step's inputs, forward + backward, D2H of every result, all timed."""
+    import torch
+    names_in = ["q", "k", "v", "g", "beta", "h0", "dO", "dhT"]
+    hin = {n: getattr(host, n).pin_memory() for n in names_in}
+    din = {n: torch.empty_like(hin[n], device=dev) for n in names_in}
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    outs_h = None
+    ws_f = torch.empty(gdn.fwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
+                       dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
+                       dtype=torch.uint8, device=dev)
+
+    def one():
+        nonlocal outs_h
+        for n in names_in:
+            din[n].copy_(hin[n], non_blocking=True)
+        o, hT = gdn.chunk_fwd(din["q"], din["k"], din["v"], din["g"], din["beta"], din["h0"],
+                              n_segments=nseg, workspace=ws_f)
+        gr = gdn.chunk_bwd(din["q"], din["k"], din["v"], din["g"], din["beta"], din["h0"],
+                           din["dO"], din["dhT"], n_segments=nseg, workspace=ws_b)
+        outs = [o, hT, *gr]
+        if outs_h is None:
+            outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        for hb, t in zip(outs_h, outs):
+            hb.copy_(t, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    K = args.steps
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        one()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    return {"value": round(wl.tokens * K / (ms * 1e-3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / K, 5)}
+
+
+# ---------------------------------------------------------------- oracle arm
+def oracle_step(host, key_heads):
+    """fp64 oracle forward + backward on the value heads of `key_heads`."""
+    import oracle
+    wl = host.wl
+    grp = wl.Hv // wl.Hk
+    heads = [(b, kh * grp + r) for b in range(wl.B) for kh in key_heads for r in range(grp)]
+    oracle.fwd(host, heads=heads)
+    oracle.bwd(host, heads=heads)
+
+
+def cpu_baseline(wl, host):
+    import oracle
+    t = time.time()
+    oracle_step(host, list(range(wl.Hk)))
+    dt = time.time() - t
+    return {"value": round(wl.tokens / dt, 2), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"one full {wl.name} fwd+bwd step (all {wl.Hv} value heads), fp64, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    from linear_attention_rnn_gb300.inputs import WORKLOADS, make_host
+    wl = WORKLOADS[args.workload].replace(backward=True)
+    host = make_host(wl)
+    oracle.build()
+    # size each step so that warm-up + timed steps stay within ~2-3 minutes
+    t = time.time()
+    oracle_step(host, [0])
+    per_kh = time.time() - t
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n_kh = max(1, min(wl.Hk, int(budget / max(per_kh, 1e-3))))
+    kh = list(range(n_kh))
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_step(host, kh)
+    t = time.time()
+    for _ in range(args.steps):
+        oracle_step(host, kh)
+    dt = time.time() - t
+    frac = n_kh / wl.Hk
+    value = wl.tokens * frac * args.steps / dt
+    sample = (f"{n_kh} of {wl.Hk} key heads ({n_kh * wl.Hv // wl.Hk} of {wl.Hv} value heads) "
+              f"of {wl.name} fwd+bwd per step, fp64; tokens scaled by that fraction")
+    return {
+        "impl": "reference",
+        "metric": "GDN chunk fwd+bwd tokens/s (T=4096, H_v=32, d=128) and % of roofline",
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3 / frac, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{wl.name} fwd+bwd: B={wl.B} T={wl.T} Hk={wl.Hk} Hv={wl.Hv} "
+                               f"dk=dv={wl.dk} chunk={wl.chunk}",
+                   "l2": "n/a (host)", "parallelism": "host cores"},
+        "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "sample": sample,
+                         "value": round(value, 2)},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="layer_t4096")
+    ap.add_argument("--n-segments", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+                    help="keep warming up until this much wall time has passed")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only; other ranks exit at once
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend="nccl")
+    try:
+        out = run_ours(args, rank, world, local_rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -110,6 +110,30 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   size_t ws_bytes, void* stream);
 
 /*
+ * Timing variants of gdn_chunk_fwd / gdn_chunk_bwd: identical results, plus
+ * cudaEventRecord(events[i], stream) right after the library's i-th kernel
+ * launch, for i < n_events (NULL entries are skipped).  The events are the
+ * caller's (cudaEvent_t handles created by the caller).  Launch order:
+ *   forward,  n_segments = 1:  prep, walk
+ *   forward,  n_segments > 1:  prep, fold, segment prefix, walk
+ *   backward, n_segments = 1:  prep, forward walk, reverse walk, gradients, dq/dk sum
+ *   backward, n_segments > 1:  prep, fold, prefix, forward walk, reverse fold,
+ *                              reverse prefix, reverse walk, gradients, dq/dk sum
+ * With T == 0 or B == 0 no kernel is launched and no event is recorded.
+ * Pages: none (instrumentation of the same operations).
+ */
+int gdn_chunk_fwd_timed(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                        int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
+                        size_t ws_bytes, void* stream, void* const* events, int n_events);
+int gdn_chunk_bwd_timed(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const float* h0, const void* dO, const float* dhT,
+                        void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0, int B,
+                        int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments,
+                        void* ws, size_t ws_bytes, void* stream, void* const* events,
+                        int n_events);
+
+/*
  * Inclusive prefix of affine maps along n, per batch row:
  *   (A_out[i], B_out[i]) = (A_i, B_i) o (A_{i-1}, B_{i-1}) o ... o (A_0, B_0)
  * with (A2, B2) o (A1, B1) = (A2 A1, A2 B1 + B2), i.e. A_out[i] h + B_out[i] is

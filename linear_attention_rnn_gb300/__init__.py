@@ -68,6 +68,10 @@ def lib():
         L.gdn_chunk_fwd.restype = I
         L.gdn_chunk_bwd.argtypes = [P] * 14 + [I] * 8 + [P, Z, P]
         L.gdn_chunk_bwd.restype = I
+        L.gdn_chunk_fwd_timed.argtypes = [P] * 8 + [I] * 8 + [P, Z, P, P, I]
+        L.gdn_chunk_fwd_timed.restype = I
+        L.gdn_chunk_bwd_timed.argtypes = [P] * 14 + [I] * 8 + [P, Z, P, P, I]
+        L.gdn_chunk_bwd_timed.restype = I
         L.gdn_affine_compose.argtypes = [P] * 4 + [I] * 4 + [P]
         L.gdn_affine_compose.restype = I
         L.gdn_debug_ut.argtypes = [P] * 8 + [I] * 7 + [P]
@@ -122,6 +126,13 @@ def bwd_workspace_bytes(B, T, Hk, Hv, dk=128, dv=128, chunk=128, n_segments=0) -
     return int(lib().gdn_bwd_workspace_bytes(B, T, Hk, Hv, dk, dv, chunk, n_segments))
 
 
+def _events(events):
+    """ctypes array of raw cudaEvent_t handles of torch.cuda.Event objects
+    (each must have been recorded once, so that it exists)."""
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    return arr, len(events)
+
+
 def _workspace(nbytes, device, ws):
     if ws is not None:
         if ws.numel() * ws.element_size() < nbytes:
@@ -131,9 +142,10 @@ def _workspace(nbytes, device, ws):
 
 
 def chunk_fwd(q, k, v, g, beta, h0=None, *, chunk: int = 128, n_segments: int = 0,
-              want_hT: bool = True, o=None, hT=None, workspace=None
+              want_hT: bool = True, o=None, hT=None, workspace=None, events=None
               ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Forward of the chunked gated delta rule.  Returns (o, hT)."""
+    """Forward of the chunked gated delta rule.  Returns (o, hT).
+    events: optional torch.cuda.Event list recorded after each kernel launch."""
     B, T, Hk, Hv, dk, dv = _dims(q, k, v, g, beta)
     dev = q.device
     _check(h0, "h0", torch.float32, (B, Hv, dk, dv))
@@ -144,18 +156,22 @@ def chunk_fwd(q, k, v, g, beta, h0=None, *, chunk: int = 128, n_segments: int = 
         hT = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=dev)
     nbytes = fwd_workspace_bytes(B, T, Hk, Hv, dk, dv, chunk, n_segments)
     ws = _workspace(nbytes, dev, workspace)
-    rc = lib().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
-                             _ptr(hT), B, T, Hk, Hv, dk, dv, chunk, n_segments, _ptr(ws),
-                             ws.numel(), _stream(dev))
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(hT), B, T,
+            Hk, Hv, dk, dv, chunk, n_segments, _ptr(ws), ws.numel(), _stream(dev)]
+    if events:
+        rc = lib().gdn_chunk_fwd_timed(*args, *_events(events))
+    else:
+        rc = lib().gdn_chunk_fwd(*args)
     if rc != GDN_OK:
         raise GDNError(rc, "gdn_chunk_fwd")
     return o, hT
 
 
 def chunk_bwd(q, k, v, g, beta, h0, dO, dhT=None, *, chunk: int = 128, n_segments: int = 0,
-              want_dh0: bool = True, workspace=None):
+              want_dh0: bool = True, workspace=None, events=None):
     """Backward of the chunked gated delta rule.
-    Returns (dq, dk, dv, dg, dbeta, dh0)."""
+    Returns (dq, dk, dv, dg, dbeta, dh0).
+    events: optional torch.cuda.Event list recorded after each kernel launch."""
     B, T, Hk, Hv, dk, dv = _dims(q, k, v, g, beta)
     dev = q.device
     _check(h0, "h0", torch.float32, (B, Hv, dk, dv))
@@ -169,10 +185,13 @@ def chunk_bwd(q, k, v, g, beta, h0, dO, dhT=None, *, chunk: int = 128, n_segment
     dh0 = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=dev) if want_dh0 else None
     nbytes = bwd_workspace_bytes(B, T, Hk, Hv, dk, dv, chunk, n_segments)
     ws = _workspace(nbytes, dev, workspace)
-    rc = lib().gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(dO),
-                             _ptr(dhT), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(db),
-                             _ptr(dh0), B, T, Hk, Hv, dk, dv, chunk, n_segments, _ptr(ws),
-                             ws.numel(), _stream(dev))
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(dO), _ptr(dhT),
+            _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(db), _ptr(dh0), B, T, Hk, Hv, dk, dv,
+            chunk, n_segments, _ptr(ws), ws.numel(), _stream(dev)]
+    if events:
+        rc = lib().gdn_chunk_bwd_timed(*args, *_events(events))
+    else:
+        rc = lib().gdn_chunk_bwd(*args)
     if rc != GDN_OK:
         raise GDNError(rc, "gdn_chunk_bwd")
     return dq, dk_, dv_, dg, db, dh0

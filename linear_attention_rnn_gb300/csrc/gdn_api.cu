@@ -91,10 +91,27 @@ T* at(void* ws, size_t off) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
 
+// Records the caller's events after each launch (timing variants only).
+struct Marks {
+  void* const* ev;
+  int n;
+  int i;
+  cudaStream_t s;
+  int rec() {
+    if (ev && i < n && ev[i]) {
+      cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+      ++i;
+      return cuda_status(e);
+    }
+    ++i;
+    return GDN_OK;
+  }
+};
+
 // Forward states: prep has run; walk (with segments: fold, cross, replay).
 int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, const void* k,
                       const float* g, const float* h0, void* o, float* hT, bf16* states,
-                      bf16* delta, cudaStream_t s) {
+                      bf16* delta, cudaStream_t s, Marks& mk) {
   WalkFwdArgs w;
   memset(&w, 0, sizeof w);
   w.W = at<bf16>(ws, Lw.W);
@@ -117,7 +134,8 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
     w.hstart = h0;
     w.hstart_bh_stride = (long)HD * HD;
     w.hstart_seg_stride = 0;
-    return cuda_status(launch_walk_fwd(w, 0, s));
+    int r = cuda_status(launch_walk_fwd(w, 0, s));
+    return r ? r : mk.rec();
   }
   WalkFwdArgs f = w;
   f.pairA = at<float>(ws, Lw.pairA);
@@ -127,7 +145,7 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
   f.states = nullptr;
   f.delta = nullptr;
   int rc = cuda_status(launch_walk_fwd(f, 1, s));
-  if (rc) return rc;
+  if (rc || (rc = mk.rec())) return rc;
   AffineWalkArgs x;
   memset(&x, 0, sizeof x);
   x.A = f.pairA;
@@ -141,11 +159,12 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
   x.exclusive = 1;
   x.reverse = 0;
   rc = cuda_status(launch_affine_walk(x, s));
-  if (rc) return rc;
+  if (rc || (rc = mk.rec())) return rc;
   w.hstart = at<float>(ws, Lw.hin);
   w.hstart_bh_stride = (long)d.S * HD * HD;
   w.hstart_seg_stride = (long)HD * HD;
-  return cuda_status(launch_walk_fwd(w, 0, s));
+  rc = cuda_status(launch_walk_fwd(w, 0, s));
+  return rc ? rc : mk.rec();
 }
 
 }  // namespace
@@ -188,9 +207,10 @@ size_t gdn_bwd_workspace_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, i
   return layout(make_dims(B, T, Hk, Hv, n_segments), true).total;
 }
 
-int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                  const float* h0, void* o, float* hT, int B, int T, int Hk, int Hv, int d_k,
-                  int d_v, int chunk, int n_segments, void* ws, size_t ws_bytes, void* stream) {
+static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
+                    const float* beta, const float* h0, void* o, float* hT, int B, int T, int Hk,
+                    int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
+                    size_t ws_bytes, void* stream, void* const* events, int n_events) {
   int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
   if (rc) return rc;
   const long tokens = (long)B * T;
@@ -209,6 +229,7 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
   }
   const Layout L = layout(d, false);
   if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  Marks mk = {events, n_events, 0, s};
 
   PrepArgs p;
   memset(&p, 0, sizeof p);
@@ -226,14 +247,15 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
   p.Hv = Hv;
   p.NC = d.NC;
   rc = cuda_status(launch_prep(p, s));
-  if (rc) return rc;
-  return run_forward_walks(d, L, ws, q, k, g, h0, o, hT, nullptr, nullptr, s);
+  if (rc || (rc = mk.rec())) return rc;
+  return run_forward_walks(d, L, ws, q, k, g, h0, o, hT, nullptr, nullptr, s, mk);
 }
 
-int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                  const float* h0, const void* dO, const float* dhT, void* dq, void* dk, void* dv,
-                  float* dg, float* dbeta, float* dh0, int B, int T, int Hk, int Hv, int d_k,
-                  int d_v, int chunk, int n_segments, void* ws, size_t ws_bytes, void* stream) {
+static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
+                    const float* beta, const float* h0, const void* dO, const float* dhT,
+                    void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0, int B,
+                    int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
+                    size_t ws_bytes, void* stream, void* const* events, int n_events) {
   int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
   if (rc) return rc;
   const long tokens = (long)B * T;
@@ -253,6 +275,7 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
   }
   const Layout L = layout(d, true);
   if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  Marks mk = {events, n_events, 0, s};
 
   // 1. per-chunk UT quantities (w, u, P, T)
   PrepArgs p;
@@ -272,10 +295,10 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
   p.Hv = Hv;
   p.NC = d.NC;
   rc = cuda_status(launch_prep(p, s));
-  if (rc) return rc;
+  if (rc || (rc = mk.rec())) return rc;
   // 2. recompute the state entering every chunk, and Delta
   rc = run_forward_walks(d, L, ws, q, k, g, h0, nullptr, nullptr, at<bf16>(ws, L.states),
-                         at<bf16>(ws, L.delta), s);
+                         at<bf16>(ws, L.delta), s, mk);
   if (rc) return rc;
   // 3. reverse walk of the state cotangent
   WalkBwdArgs w;
@@ -300,13 +323,14 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
     w.hstart_bh_stride = (long)HD * HD;
     w.hstart_seg_stride = 0;
     rc = cuda_status(launch_walk_bwd(w, 0, s));
+    if (!rc) rc = mk.rec();
   } else {
     WalkBwdArgs f = w;
     f.pairA = at<float>(ws, L.pairA);
     f.pairB = at<float>(ws, L.pairB);
     f.dh0 = nullptr;
     rc = cuda_status(launch_walk_bwd(f, 1, s));
-    if (rc) return rc;
+    if (rc || (rc = mk.rec())) return rc;
     AffineWalkArgs x;
     memset(&x, 0, sizeof x);
     x.A = f.pairA;
@@ -320,11 +344,12 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
     x.exclusive = 1;
     x.reverse = 1;
     rc = cuda_status(launch_affine_walk(x, s));
-    if (rc) return rc;
+    if (rc || (rc = mk.rec())) return rc;
     w.hstart = at<float>(ws, L.hin);
     w.hstart_bh_stride = (long)d.S * HD * HD;
     w.hstart_seg_stride = (long)HD * HD;
     rc = cuda_status(launch_walk_bwd(w, 0, s));
+    if (!rc) rc = mk.rec();
   }
   if (rc) return rc;
   // 4. chunk-parallel gradients, then the key-head sums of dq and dk
@@ -352,9 +377,43 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
   ga.Hv = Hv;
   ga.NC = d.NC;
   rc = cuda_status(launch_grads(ga, s));
-  if (rc) return rc;
-  return cuda_status(launch_reduce_dqdk(ga.dq_part, ga.dk_part, static_cast<bf16*>(dq),
-                                        static_cast<bf16*>(dk), tokens, Hk, Hv, s));
+  if (rc || (rc = mk.rec())) return rc;
+  rc = cuda_status(launch_reduce_dqdk(ga.dq_part, ga.dk_part, static_cast<bf16*>(dq),
+                                      static_cast<bf16*>(dk), tokens, Hk, Hv, s));
+  return rc ? rc : mk.rec();
+}
+
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const float* h0, void* o, float* hT, int B, int T, int Hk, int Hv, int d_k,
+                  int d_v, int chunk, int n_segments, void* ws, size_t ws_bytes, void* stream) {
+  return fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, Hk, Hv, d_k, d_v, chunk, n_segments, ws,
+                  ws_bytes, stream, nullptr, 0);
+}
+
+int gdn_chunk_fwd_timed(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                        int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
+                        size_t ws_bytes, void* stream, void* const* events, int n_events) {
+  return fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, Hk, Hv, d_k, d_v, chunk, n_segments, ws,
+                  ws_bytes, stream, events, n_events);
+}
+
+int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const float* h0, const void* dO, const float* dhT, void* dq, void* dk, void* dv,
+                  float* dg, float* dbeta, float* dh0, int B, int T, int Hk, int Hv, int d_k,
+                  int d_v, int chunk, int n_segments, void* ws, size_t ws_bytes, void* stream) {
+  return bwd_impl(q, k, v, g, beta, h0, dO, dhT, dq, dk, dv, dg, dbeta, dh0, B, T, Hk, Hv, d_k,
+                  d_v, chunk, n_segments, ws, ws_bytes, stream, nullptr, 0);
+}
+
+int gdn_chunk_bwd_timed(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const float* h0, const void* dO, const float* dhT,
+                        void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0, int B,
+                        int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments,
+                        void* ws, size_t ws_bytes, void* stream, void* const* events,
+                        int n_events) {
+  return bwd_impl(q, k, v, g, beta, h0, dO, dhT, dq, dk, dv, dg, dbeta, dh0, B, T, Hk, Hv, d_k,
+                  d_v, chunk, n_segments, ws, ws_bytes, stream, events, n_events);
 }
 
 int gdn_affine_compose(const float* A, const float* B, float* A_out, float* B_out, int batch,
