@@ -110,6 +110,37 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   size_t ws_bytes, void* stream);
 
 /*
+ * Forward that allocates nothing and takes no workspace.  The pages have no
+ * counterpart of this entry point; it exists for callers that may not
+ * allocate device memory at call time and cannot lend a scratch buffer:
+ * services that plan and lock all their device memory up front (where an
+ * allocation could fail, fragment the plan, or stall the device while it
+ * synchronises), and plug-ins whose host framework owns every byte of device
+ * memory.  It computes exactly what gdn_chunk_fwd computes with
+ * n_segments = 1 (same arguments otherwise, same results).
+ *
+ * Scratch: a fixed array inside the library's device image, sized for
+ * GDN_NOALLOC_MAX_UNITS (batch x value head x chunk) units, i.e. the call
+ * needs B * Hv * ceil(T / chunk) <= GDN_NOALLOC_MAX_UNITS (24 MiB of scratch);
+ * larger problems are refused with GDN_ERR_WORKSPACE before anything is
+ * enqueued.  Every GPU that loads the library keeps that array until the
+ * process exits.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.
+ * Sharing: all calls on a device use the same array, and its contents persist
+ * from call to call.  Nothing in it needs to start at zero (each call writes
+ * every scratch byte it reads before reading it), but calls whose executions
+ * overlap on the GPU (different streams, or several host threads without
+ * ordering) race on the array and may return wrong results: order them.
+ * Never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+#define GDN_NOALLOC_MAX_UNITS 256
+int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                          const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                          int Hk, int Hv, int d_k, int d_v, int chunk, void* stream);
+
+/*
  * Timing variants of gdn_chunk_fwd / gdn_chunk_bwd: identical results, plus
  * cudaEventRecord(events[i], stream) right after the library's i-th kernel
  * launch, for i < n_events (NULL entries are skipped).  The events are the

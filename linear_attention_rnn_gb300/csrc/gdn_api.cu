@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "gdn.h"
 #include "gdn_kernels.cuh"
 
@@ -471,3 +473,58 @@ int gdn_debug_ut(const void* k, const void* v, const float* g, const float* beta
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward without any allocation.
+//
+// Some callers cannot hand this library a workspace and must not trigger an
+// allocation: code that runs after a service has planned and locked all of
+// its device memory (a cudaMalloc there could fail, fragment the plan, or
+// stall every stream on the device while it synchronises), or hosts whose
+// device memory belongs entirely to another framework that exposes no
+// scratch buffer to plug-ins.  For them the forward below keeps its scratch
+// (w, u and the masked Q K^T of every chunk) in one fixed array that lives in
+// this library's device image.  Every GPU that loads the library holds the
+// array until the process exits, which is why it is kept to a modest size.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)GDN_NOALLOC_MAX_UNITS * 3 * CH * HD * sizeof(bf16);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The name of a
+// __device__ array in host code is only a host-side stand-in, so the address
+// is looked up once per device, with that device current, and cached.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                                     const float* beta, const float* h0, void* o, float* hT,
+                                     int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk,
+                                     void* stream) {
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, 1);
+  if (rc) return rc;
+  const long units = (long)B * Hv * ((T + CH - 1) / CH);
+  if (units > GDN_NOALLOC_MAX_UNITS) return GDN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (units > 0 && (rc = noalloc_scratch(&scratch))) return rc;
+  return fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, Hk, Hv, d_k, d_v, chunk, 1, scratch,
+                  kNoAllocScratchBytes, stream, nullptr, 0);
+}
