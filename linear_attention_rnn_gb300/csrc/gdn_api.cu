@@ -49,7 +49,7 @@ Dims make_dims(int B, int T, int Hk, int Hv, int n_segments) {
 // bf16 entering states, Delta, the state cotangents, dDelta and the fp32
 // per-value-head dq/dk.
 struct Layout {
-  size_t W, U, P, Tb, pairA, pairB, hin, states, delta, dstates, ddelta, dqp, dkp, total;
+  size_t status, W, U, P, Tb, pairA, pairB, hin, states, delta, dstates, ddelta, dqp, dkp, total;
 };
 
 Layout layout(const Dims& d, bool bwd) {
@@ -63,6 +63,7 @@ Layout layout(const Dims& d, bool bwd) {
     off += up(bytes);
     return o;
   };
+  L.status = take(sizeof(int));  // bit 0 set by a kernel whose bounded wait gave up
   L.W = take(chunks * tile);
   L.U = take(chunks * tile);
   L.P = take(chunks * tile);
@@ -132,6 +133,7 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
   w.hT = hT;
   w.states = states;
   w.delta = delta;
+  w.status = at<int>(ws, Lw.status);
   if (d.S == 1) {
     w.hstart = h0;
     w.hstart_bh_stride = (long)HD * HD;
@@ -243,6 +245,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   p.W = at<bf16>(ws, L.W);
   p.U = at<bf16>(ws, L.U);
   p.P = at<bf16>(ws, L.P);
+  p.status = at<int>(ws, L.status);
   p.B = B;
   p.T = T;
   p.Hk = Hk;
@@ -291,6 +294,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   p.U = at<bf16>(ws, L.U);
   p.P = at<bf16>(ws, L.P);
   p.Tb = at<bf16>(ws, L.Tb);
+  p.status = at<int>(ws, L.status);
   p.B = B;
   p.T = T;
   p.Hk = Hk;
@@ -488,7 +492,10 @@ int gdn_debug_ut(const void* k, const void* v, const float* g, const float* beta
 // array until the process exits, which is why it is kept to a modest size.
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = (size_t)GDN_NOALLOC_MAX_UNITS * 3 * CH * HD * sizeof(bf16);
+// one status word, then w, u and P of every unit (the forward workspace of
+// gdn_chunk_fwd with one segment)
+constexpr size_t kNoAllocScratchBytes =
+    256 + (size_t)GDN_NOALLOC_MAX_UNITS * 3 * CH * HD * sizeof(bf16) + 3 * 256;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

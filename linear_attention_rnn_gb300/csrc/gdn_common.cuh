@@ -130,6 +130,57 @@ __device__ __forceinline__ void slice_load_async(bf16* s, const bf16* g, long gs
   }
 }
 
+// ---- XOR-swizzled [rows x 128] bf16 tiles (256-byte rows, no padding) ----------
+// The 16-byte chunk j of row r sits at chunk position j ^ (r & 7), so the 8 row
+// addresses of every ldmatrix phase fall in 8 distinct bank groups.
+__device__ __forceinline__ const bf16* swz(const bf16* base, int r, int j) {
+  return base + r * HD + ((j ^ (r & 7)) << 3);
+}
+__device__ __forceinline__ bf16* swz(bf16* base, int r, int j) {
+  return base + r * HD + ((j ^ (r & 7)) << 3);
+}
+__device__ __forceinline__ void lda_rm_s(uint32_t (&a)[4], const bf16* base, int m0, int k0,
+                                         int lane) {
+  ldsm_x4(a, swz(base, m0 + (lane & 15), (k0 >> 3) + (lane >> 4)));
+}
+__device__ __forceinline__ void lda_tr_s(uint32_t (&a)[4], const bf16* base, int m0, int k0,
+                                         int lane) {
+  const int i = lane >> 3, r = lane & 7;
+  ldsm_x4_t(a, swz(base, k0 + ((i >> 1) << 3) + r, (m0 >> 3) + (i & 1)));
+}
+__device__ __forceinline__ void ldb_kn_s(uint32_t (&b)[4], const bf16* base, int k0, int n0,
+                                         int lane) {
+  ldsm_x4_t(b, swz(base, k0 + (lane & 15), (n0 >> 3) + (lane >> 4)));
+}
+__device__ __forceinline__ void ldb_nk_s(uint32_t (&b)[4], const bf16* base, int k0, int n0,
+                                         int lane) {
+  const int i = lane >> 3, r = lane & 7;
+  ldsm_x4(b, swz(base, n0 + ((i >> 1) << 3) + r, (k0 >> 3) + (i & 1)));
+}
+// rows [0, rows) of a [128 x 128] global tile (row stride gstride) into a
+// swizzled shared tile; rows past `rows` are zero-filled
+__device__ __forceinline__ void tile_load_async_s(bf16* s, const bf16* g, long gstride, int rows,
+                                                  int tid, int nthreads) {
+  for (int idx = tid; idx < CH * 16; idx += nthreads) {
+    const int r = idx >> 4, j = idx & 15;
+    const bool ok = r < rows;
+    cp_async16(swz(s, r, j), g + (ok ? (long)r * gstride + j * 8 : 0), ok);
+  }
+}
+// cp.async.wait_group with a run-time count (0..7)
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
+  }
+}
+
 // Inclusive prefix sum over the 128 values held 4-per-lane by one warp
 // (lane l holds rows 4l..4l+3 in v[0..3]).
 __device__ __forceinline__ void warp_cumsum128(float (&v)[4], int lane) {

@@ -21,6 +21,7 @@ struct PrepArgs {
   bf16* Tb;      // [BH][NC][CH][CH]  T in bf16 (backward)           (nullable)
   float* S_dbg;  // [BH][NC][CH][CH]  fp32 S  (debug export)        (nullable)
   float* T_dbg;  // [BH][NC][CH][CH]  fp32 T  (debug export)        (nullable)
+  int* status;   // bit 0 set if a bounded wait gave up (nullable)
   int B, T, Hk, Hv, NC;
 };
 
@@ -42,6 +43,7 @@ struct WalkFwdArgs {
   bf16* delta;             // [BH][NC][CH][HD] bf16 Delta of every chunk (nullable)
   float* pairA;            // fold output [BH][S][HD][HD]
   float* pairB;            // fold output [BH][S][HD][HD]
+  int* status;             // bit 0 set if a bounded wait gave up (nullable)
   int B, T, Hk, Hv, NC, S;
 };
 

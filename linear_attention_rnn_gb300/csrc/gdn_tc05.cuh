@@ -1,0 +1,134 @@
+// gdn_tc05.cuh -- 5th-generation tensor-core (tcgen05) helpers for sm_103a.
+//
+// Operands live in shared memory in the K-major, 128-byte-swizzled canonical
+// layout: a [rows x 128] bf16 tile is stored as two 64-column halves, each
+// rows x 128 B, and within a half the 16-byte chunk j of row r sits at chunk
+// position j ^ (r % 8).  A matrix descriptor points at one half (plus 32 B per
+// 16-element k step); the stride between 8-row groups is 1024 B.  The
+// accumulator lives in tensor memory (TMEM): for M = 128, row m of D is TMEM
+// lane m and column n is TMEM column base + n (fp32).
+#pragma once
+#include <stdint.h>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace tc {
+
+// byte offset of element (r, c) in a [rows x 128] bf16 K-major SW128 tile
+__device__ __forceinline__ uint32_t sw128(int r, int c, int rows) {
+  const int half = c >> 6, cc = c & 63;
+  return (uint32_t)(half * rows * 128 + r * 128 + ((((cc >> 3) ^ (r & 7))) << 4) + ((cc & 7) << 1));
+}
+// byte offset of the 16-byte chunk j (columns 8j..8j+7) of row r
+__device__ __forceinline__ uint32_t sw128_chunk(int r, int j, int rows) {
+  const int half = j >> 3;
+  return (uint32_t)(half * rows * 128 + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+}
+
+// shared-memory matrix descriptor: start address, LBO (unused for swizzled
+// K-major), SBO = 1024 B, descriptor version 1, 128-byte swizzle
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// instruction descriptor: kind::f16, A = B = bf16 (K-major), D = fp32
+__device__ __forceinline__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
+                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+
+// D[128 x N] (+)= A[128 x 128] * B[N x 128]^T, both K-major SW128 tiles
+// (A with 128 rows, B with N rows); issued by one thread.
+__device__ __forceinline__ void gemm_k128(uint32_t tmem_d, uint32_t a_smem, uint32_t b_smem,
+                                          int N, bool accumulate_first) {
+  const uint32_t idesc = (N == 128) ? idesc_bf16(128, 128) : idesc_bf16(128, N);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t koff = (uint32_t)(k & 3) * 32u;
+    const uint64_t da = desc_sw128(a_smem + (uint32_t)(k >> 2) * 128u * 128u + koff);
+    const uint64_t db = desc_sw128(b_smem + (uint32_t)(k >> 2) * (uint32_t)N * 128u + koff);
+    mma(tmem_d, da, db, idesc, (k > 0 || accumulate_first) ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void commit(uint64_t* mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(mbar))
+               : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// make generic-proxy shared-memory writes visible to the tensor core (async proxy)
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32(w%4)..+31)
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---- mbarriers --------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Waits for the phase with the given parity to complete; gives up after a
+// bounded number of polls and returns false (the caller records an error).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  for (int it = 0; it < (1 << 24); ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+}  // namespace tc
+}  // namespace gdn

@@ -10,6 +10,9 @@
 // an affine map of dh' with matrix A_c^T, so it segments exactly like the
 // forward (the transposed maps compose in reverse order).  Each CTA owns a
 // 32-column slice of dh (columns are independent) in fp32 registers.
+// The chunk tiles stream, in the order they are consumed (K, P, then Q, w),
+// through a ring of swizzled 32 KiB shared buffers, each requested about a
+// chunk before it is needed; the CTA's dO columns are double-buffered.
 //
 // Modes:
 //   WALK (fold = 0): from the cotangent leaving the segment, store for every
@@ -25,12 +28,11 @@ namespace gdn {
 
 namespace {
 
+constexpr int NSLOT_MAX = 5;
+
 struct WalkBwdSmem {
-  bf16 K[CH * LDB];
-  bf16 P[CH * LDB];
-  bf16 Q[CH * LDB];
-  bf16 W[CH * LDB];
-  bf16 dO[CH * LDS_];
+  bf16 slot[NSLOT_MAX][CH * HD];  // swizzled 128 x 128 tiles
+  bf16 dO[2][CH * LDS_];
   bf16 dOg[CH * LDS_];
   bf16 X[HD * LDS_];
   bf16 Yn[CH * LDS_];
@@ -63,6 +65,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
   const int cbeg = (int)((long)seg * a.NC / a.S), cend = (int)((long)(seg + 1) * a.NC / a.S);
   const bool partA = FOLD && slice < 4;  // Abar columns: no dO terms
   const bool withO = !partA;
+  const int TPC = withO ? 4 : 2;  // tiles per chunk: K, P, Q, w  (or K, w)
+  const int NSLOT = withO ? 5 : 4;
+  const int ntiles = (cend - cbeg) * TPC;
   const int col0 = (slice & 3) * SL;
   const int m0 = warp * 16;
   const int r0 = m0 + g4, r1 = r0 + 8;
@@ -98,21 +103,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
 
   auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
   auto tok = [&](int c) { return (long)b * a.T + (long)c * CH; };
-  auto issue_G1 = [&](int c) {  // K, P, dO of chunk c
-    if (c >= cbeg) {
-      tile_load_async(sm.K, a.k + (tok(c) * a.Hk + kh) * HD, tokstride, rows_of(c), tid);
-      if (withO) {
-        tile_load_async(sm.P, a.P + (bh * a.NC + c) * CH * CH, CH, CH, tid);
-        slice_load_async(sm.dO, a.dO + (tok(c) * a.Hv + j) * HD + col0, (long)a.Hv * HD,
-                         rows_of(c), tid);
+  // request tile i of the reverse sequence (always commits one cp.async group)
+  auto issue = [&](int i) {
+    if (i < ntiles) {
+      const int ci = i / TPC, t = i % TPC;
+      const int c = cend - 1 - ci;
+      const long cid = bh * a.NC + c;
+      bf16* dst = sm.slot[i % NSLOT];
+      const int kind = withO ? t : (t == 0 ? 0 : 3);  // 0 K, 1 P, 2 Q, 3 w
+      if (kind == 0) {
+        tile_load_async_s(dst, a.k + (tok(c) * a.Hk + kh) * HD, tokstride, rows_of(c), tid, NTHREADS);
+        if (withO)
+          slice_load_async(sm.dO[ci & 1], a.dO + (tok(c) * a.Hv + j) * HD + col0, (long)a.Hv * HD,
+                           rows_of(c), tid);
+      } else if (kind == 1) {
+        tile_load_async_s(dst, a.P + cid * CH * CH, CH, CH, tid, NTHREADS);
+      } else if (kind == 2) {
+        tile_load_async_s(dst, a.q + (tok(c) * a.Hk + kh) * HD, tokstride, rows_of(c), tid, NTHREADS);
+      } else {
+        tile_load_async_s(dst, a.W + cid * CH * HD, HD, CH, tid, NTHREADS);
       }
-    }
-    cp_async_commit();
-  };
-  auto issue_G2 = [&](int c) {  // Q, W of chunk c
-    if (c >= cbeg) {
-      if (withO) tile_load_async(sm.Q, a.q + (tok(c) * a.Hk + kh) * HD, tokstride, rows_of(c), tid);
-      tile_load_async(sm.W, a.W + (bh * a.NC + c) * CH * HD, HD, CH, tid);
     }
     cp_async_commit();
   };
@@ -124,8 +134,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
     }
   };
 
-  issue_G1(cend - 1);
-  issue_G2(cend - 1);
+  for (int i = 0; i < NSLOT; ++i) issue(i);
   float gnext[4];
   if (warp == 0) {
     float v[4];
@@ -135,9 +144,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
   }
 
   for (int c = cend - 1; c >= cbeg; --c) {
+    const int ci = cend - 1 - c;
     const int par = c & 1;
-    cp_async_wait<1>();
-    __syncthreads();  // K, P, dO of chunk c and its gates are ready
+    const int tk = ci * TPC;  // index of this chunk's K tile
+    const bf16* sK = sm.slot[tk % NSLOT];
+    const bf16* sP = sm.slot[(tk + 1) % NSLOT];
+    const bf16* sQ = sm.slot[(tk + 2) % NSLOT];
+    const bf16* sW = sm.slot[(tk + (withO ? 3 : 1)) % NSLOT];
+    const bf16* sdO = sm.dO[ci & 1];
+    cp_async_wait_n(3);  // K (and P, dO) of chunk c ready
     // bf16 image of dh' (B operand), its export, and gamma * dO
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -154,6 +169,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
         *reinterpret_cast<uint32_t*>(st + (long)r1 * HD + col) = pack_bf16(x[nt][2], x[nt][3]);
       }
     }
+    __syncthreads();  // dO landed for every thread's copy, gates and the dh' image visible
     if (withO) {
       // 128 rows x 32 cols: 2 rows of 8 columns per thread
 #pragma unroll
@@ -161,7 +177,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
         const int idx = tid + i * NTHREADS;
         const int r = idx >> 2, c8 = (idx & 3) << 3;
         const float gm = sm.gamma[par][r];
-        uint4 raw = *reinterpret_cast<const uint4*>(sm.dO + r * LDS_ + c8);
+        uint4 raw = *reinterpret_cast<const uint4*>(sdO + r * LDS_ + c8);
         uint32_t* w = reinterpret_cast<uint32_t*>(&raw);
 #pragma unroll
         for (int q2 = 0; q2 < 4; ++q2) {
@@ -171,7 +187,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
         *reinterpret_cast<uint4*>(sm.dOg + r * LDS_ + c8) = raw;
       }
     }
-    __syncthreads();
 
     // ---- Y = dDelta = diag(ef) K dh' + P^T dO ---------------------------------
     float y[4][4];
@@ -180,7 +195,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       uint32_t af[4], bb[4];
-      lda_rm(af, sm.K, LDB, m0, ks * 16, lane);
+      lda_rm_s(af, sK, m0, ks * 16, lane);
       ldb_kn(bb, sm.X, LDS_, ks * 16, 0, lane);
       mma16816(y[0], af, bb[0], bb[1]);
       mma16816(y[1], af, bb[2], bb[3]);
@@ -203,11 +218,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
       for (int ks = 0; ks < 8; ++ks) {
         if (ks >= warp) {  // P^T is upper triangular
           uint32_t af[4], bb[4];
-          lda_tr(af, sm.P, LDB, m0, ks * 16, lane);
-          ldb_kn(bb, sm.dO, LDS_, ks * 16, 0, lane);
+          lda_tr_s(af, sP, m0, ks * 16, lane);
+          ldb_kn(bb, sdO, LDS_, ks * 16, 0, lane);
           mma16816(y[0], af, bb[0], bb[1]);
           mma16816(y[1], af, bb[2], bb[3]);
-          ldb_kn(bb, sm.dO, LDS_, ks * 16, 16, lane);
+          ldb_kn(bb, sdO, LDS_, ks * 16, 16, lane);
           mma16816(y[2], af, bb[0], bb[1]);
           mma16816(y[3], af, bb[2], bb[3]);
         }
@@ -224,10 +239,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
         *reinterpret_cast<uint32_t*>(dd + (long)r1 * HD) = pack_bf16(y[nt][2], y[nt][3]);
       }
     }
-    __syncthreads();  // K, P, dO consumed; Yn complete
-    issue_G1(c - 1);
-    cp_async_wait<1>();
-    __syncthreads();  // Q, W of chunk c ready
+    // NSLOT + tk groups requested; Q and w are tiles tk+2, tk+3 (or w = tk+1)
+    cp_async_wait_n(withO ? 1 : 2);
+    __syncthreads();  // K, P consumed; Yn, dOg complete; Q, w visible
+    issue(tk + NSLOT);
+    if (withO) issue(tk + 1 + NSLOT);
 
     // ---- dh = gamma_C dh' + Q^T (gamma dO) + W^T (-Y) -----------------------------
     {
@@ -240,7 +256,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           uint32_t af[4], bb[4];
-          lda_tr(af, sm.Q, LDB, m0, ks * 16, lane);
+          lda_tr_s(af, sQ, m0, ks * 16, lane);
           ldb_kn(bb, sm.dOg, LDS_, ks * 16, 0, lane);
           mma16816(x[0], af, bb[0], bb[1]);
           mma16816(x[1], af, bb[2], bb[3]);
@@ -252,7 +268,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         uint32_t af[4], bb[4];
-        lda_tr(af, sm.W, LDB, m0, ks * 16, lane);
+        lda_tr_s(af, sW, m0, ks * 16, lane);
         ldb_kn(bb, sm.Yn, LDS_, ks * 16, 0, lane);
         mma16816(x[0], af, bb[0], bb[1]);
         mma16816(x[1], af, bb[2], bb[3]);
@@ -261,8 +277,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
         mma16816(x[3], af, bb[2], bb[3]);
       }
     }
-    __syncthreads();  // Q, W, dOg, X, Yn consumed
-    issue_G2(c - 1);
+    __syncthreads();  // Q, w, dOg, X, Yn consumed
+    if (withO) {
+      issue(tk + 2 + NSLOT);
+      issue(tk + 3 + NSLOT);
+    } else {
+      issue(tk + 1 + NSLOT);
+    }
     if (warp == 0 && c - 1 >= cbeg) {
       chunk_gates_b(gnext, sm.gamma[par ^ 1], sm.ef[par ^ 1], &sm.gC[par ^ 1], lane);
       load_g(c - 2, gnext);
