@@ -324,6 +324,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   w.dh0 = dh0;
   w.dstates = at<bf16>(ws, L.dstates);
   w.ddelta = at<bf16>(ws, L.ddelta);
+  w.status = at<int>(ws, L.status);
   if (d.S == 1) {
     w.hstart = dhT;
     w.hstart_bh_stride = (long)HD * HD;

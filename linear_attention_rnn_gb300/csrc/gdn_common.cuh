@@ -181,6 +181,70 @@ __device__ __forceinline__ void cp_async_wait_n(int n) {
   }
 }
 
+// ---- bulk async copies completing on transaction-count mbarriers ---------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Waits for the phase of the given parity; gives up after a bounded number of
+// polls and returns false.
+__device__ __forceinline__ bool mbar_wait_parity(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  for (int it = 0; it < (1 << 22); ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Rows [0, rows) of a [128 x 128] bf16 global tile (row stride gstride) into
+// a padded shared tile, one 256-byte bulk copy per row, issued by the 32
+// lanes of one warp; rows past `rows` are cleared with ordinary stores (the
+// caller orders them with a CTA barrier).  Completes rows * 256 bytes on bar.
+__device__ __forceinline__ void tile_bulk_rows(bf16* s, const bf16* g, long gstride, int rows,
+                                               uint64_t* bar, int lane) {
+  for (int r = lane; r < CH; r += 32) {
+    if (r < rows) {
+      bulk_g2s(s + r * LDB, g + (long)r * gstride, HD * sizeof(bf16), bar);
+    } else {
+#pragma unroll
+      for (int c8 = 0; c8 < HD; c8 += 8) *reinterpret_cast<uint4*>(s + r * LDB + c8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+// Same for a [128 x 32] column slice (64-byte rows) into a padded slice tile.
+__device__ __forceinline__ void slice_bulk_rows(bf16* s, const bf16* g, long gstride, int rows,
+                                                uint64_t* bar, int lane) {
+  for (int r = lane; r < CH; r += 32) {
+    if (r < rows) {
+      bulk_g2s(s + r * LDS_, g + (long)r * gstride, SL * sizeof(bf16), bar);
+    } else {
+#pragma unroll
+      for (int c8 = 0; c8 < SL; c8 += 8) *reinterpret_cast<uint4*>(s + r * LDS_ + c8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
 // Inclusive prefix sum over the 128 values held 4-per-lane by one warp
 // (lane l holds rows 4l..4l+3 in v[0..3]).
 __device__ __forceinline__ void warp_cumsum128(float (&v)[4], int lane) {

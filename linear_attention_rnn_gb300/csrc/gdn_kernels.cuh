@@ -63,6 +63,7 @@ struct WalkBwdArgs {
   bf16* ddelta;            // [BH][NC][CH][HD] bf16 dDelta of every chunk
   float* pairA;            // fold output
   float* pairB;
+  int* status;             // bit 0 set if a bounded wait gave up (nullable)
   int B, T, Hk, Hv, NC, S;
 };
 

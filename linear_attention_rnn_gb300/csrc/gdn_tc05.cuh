@@ -132,3 +132,55 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 
 }  // namespace tc
 }  // namespace gdn
+
+namespace gdn {
+namespace tc {
+
+// ---- TMA tiled loads (tensor maps live in kernel parameter space) ---------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int x, int y, int z, int w,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// shared-memory descriptor of an MN-major SW128 operand: the tile holds
+// 64-element MN atoms of 128-byte rows along K; LBO is the distance between
+// MN atoms, SBO the distance between 8-row K groups (1024 B)
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t mn_atom_stride) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(mn_atom_stride >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// D[128 x N] (+)= A * B^T where A (M = 128, K = 128) is stored MN-major as a
+// [128 (K) rows x 128 (M)] SW128 tile and B is a K-major [N x 128] SW128 tile
+__device__ __forceinline__ void gemm_amn_k128(uint32_t tmem_d, uint32_t a_smem, uint32_t b_smem,
+                                              int N, bool accumulate_first) {
+  const uint32_t idesc = idesc_bf16(128, N) | (1u << 15);  // A is MN-major
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint64_t da = desc_sw128_mn(a_smem + (uint32_t)k * 2048u, 128u * 128u);
+    const uint32_t koff = (uint32_t)(k & 3) * 32u;
+    const uint64_t db = desc_sw128(b_smem + (uint32_t)(k >> 2) * (uint32_t)N * 128u + koff);
+    mma(tmem_d, da, db, idesc, (k > 0 || accumulate_first) ? 1u : 0u);
+  }
+}
+
+}  // namespace tc
+}  // namespace gdn

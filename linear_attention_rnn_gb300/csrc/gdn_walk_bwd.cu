@@ -11,8 +11,9 @@
 // forward (the transposed maps compose in reverse order).  Each CTA owns a
 // 32-column slice of dh (columns are independent) in fp32 registers.
 // The chunk tiles stream, in the order they are consumed (K, P, then Q, w),
-// through a ring of swizzled 32 KiB shared buffers, each requested about a
-// chunk before it is needed; the CTA's dO columns are double-buffered.
+// through a ring of padded shared buffers, each requested with cp.async
+// (one commit group per tile) about a chunk before it is needed; the CTA's dO
+// columns are double-buffered.
 //
 // Modes:
 //   WALK (fold = 0): from the cotangent leaving the segment, store for every
@@ -31,7 +32,7 @@ namespace {
 constexpr int NSLOT_MAX = 5;
 
 struct WalkBwdSmem {
-  bf16 slot[NSLOT_MAX][CH * HD];  // swizzled 128 x 128 tiles
+  bf16 slot[NSLOT_MAX][CH * LDB];  // padded 128 x 128 tiles
   bf16 dO[2][CH * LDS_];
   bf16 dOg[CH * LDS_];
   bf16 X[HD * LDS_];
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
 
   auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
   auto tok = [&](int c) { return (long)b * a.T + (long)c * CH; };
-  // request tile i of the reverse sequence (always commits one cp.async group)
+  // request tile i of the reverse sequence (every thread; one commit group per tile)
   auto issue = [&](int i) {
     if (i < ntiles) {
       const int ci = i / TPC, t = i % TPC;
@@ -112,16 +113,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
       bf16* dst = sm.slot[i % NSLOT];
       const int kind = withO ? t : (t == 0 ? 0 : 3);  // 0 K, 1 P, 2 Q, 3 w
       if (kind == 0) {
-        tile_load_async_s(dst, a.k + (tok(c) * a.Hk + kh) * HD, tokstride, rows_of(c), tid, NTHREADS);
+        tile_load_async(dst, a.k + (tok(c) * a.Hk + kh) * HD, tokstride, rows_of(c), tid);
         if (withO)
           slice_load_async(sm.dO[ci & 1], a.dO + (tok(c) * a.Hv + j) * HD + col0, (long)a.Hv * HD,
                            rows_of(c), tid);
       } else if (kind == 1) {
-        tile_load_async_s(dst, a.P + cid * CH * CH, CH, CH, tid, NTHREADS);
+        tile_load_async(dst, a.P + cid * CH * CH, CH, CH, tid);
       } else if (kind == 2) {
-        tile_load_async_s(dst, a.q + (tok(c) * a.Hk + kh) * HD, tokstride, rows_of(c), tid, NTHREADS);
+        tile_load_async(dst, a.q + (tok(c) * a.Hk + kh) * HD, tokstride, rows_of(c), tid);
       } else {
-        tile_load_async_s(dst, a.W + cid * CH * HD, HD, CH, tid, NTHREADS);
+        tile_load_async(dst, a.W + cid * CH * HD, HD, CH, tid);
       }
     }
     cp_async_commit();
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
     const bf16* sQ = sm.slot[(tk + 2) % NSLOT];
     const bf16* sW = sm.slot[(tk + (withO ? 3 : 1)) % NSLOT];
     const bf16* sdO = sm.dO[ci & 1];
-    cp_async_wait_n(3);  // K (and P, dO) of chunk c ready
+    cp_async_wait_n(3);  // K, dO (and P): NSLOT + tk groups committed
     // bf16 image of dh' (B operand), its export, and gamma * dO
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       uint32_t af[4], bb[4];
-      lda_rm_s(af, sK, m0, ks * 16, lane);
+      lda_rm(af, sK, LDB, m0, ks * 16, lane);
       ldb_kn(bb, sm.X, LDS_, ks * 16, 0, lane);
       mma16816(y[0], af, bb[0], bb[1]);
       mma16816(y[1], af, bb[2], bb[3]);
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
       for (int ks = 0; ks < 8; ++ks) {
         if (ks >= warp) {  // P^T is upper triangular
           uint32_t af[4], bb[4];
-          lda_tr_s(af, sP, m0, ks * 16, lane);
+          lda_tr(af, sP, LDB, m0, ks * 16, lane);
           ldb_kn(bb, sdO, LDS_, ks * 16, 0, lane);
           mma16816(y[0], af, bb[0], bb[1]);
           mma16816(y[1], af, bb[2], bb[3]);
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
         *reinterpret_cast<uint32_t*>(dd + (long)r1 * HD) = pack_bf16(y[nt][2], y[nt][3]);
       }
     }
-    // NSLOT + tk groups requested; Q and w are tiles tk+2, tk+3 (or w = tk+1)
+    // NSLOT + tk groups committed; Q and w are tiles tk+2, tk+3 (or w = tk+1)
     cp_async_wait_n(withO ? 1 : 2);
     __syncthreads();  // K, P consumed; Yn, dOg complete; Q, w visible
     issue(tk + NSLOT);
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           uint32_t af[4], bb[4];
-          lda_tr_s(af, sQ, m0, ks * 16, lane);
+          lda_tr(af, sQ, LDB, m0, ks * 16, lane);
           ldb_kn(bb, sm.dOg, LDS_, ks * 16, 0, lane);
           mma16816(x[0], af, bb[0], bb[1]);
           mma16816(x[1], af, bb[2], bb[3]);
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         uint32_t af[4], bb[4];
-        lda_tr_s(af, sW, m0, ks * 16, lane);
+        lda_tr(af, sW, LDB, m0, ks * 16, lane);
         ldb_kn(bb, sm.Yn, LDS_, ks * 16, 0, lane);
         mma16816(x[0], af, bb[0], bb[1]);
         mma16816(x[1], af, bb[2], bb[3]);

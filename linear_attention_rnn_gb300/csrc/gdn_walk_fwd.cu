@@ -12,13 +12,14 @@
 // registers; its bf16 image in shared memory is the B operand of the next
 // chunk's w h and Q h.
 //
-// The chunk tiles stream through a ring of NSLOT swizzled 32 KiB shared
-// buffers in the order they are consumed (w, K, then Q, P when the output is
-// produced).  Tile i goes to slot i % NSLOT and is requested (cp.async) as soon
-// as tile i - NSLOT has been consumed, so every tile is in flight for about a
-// chunk before it is needed and the sequential chain does not wait on memory.
-// u (the CTA's own 32 columns) is double-buffered by chunk parity and travels
-// with the w tile of its chunk.
+// The chunk tiles stream through a ring of NSLOT padded shared buffers in the
+// order they are consumed (w, K, then Q, P when the output is produced).  Tile
+// i goes to slot i % NSLOT and is requested as soon as tile i - NSLOT has been
+// consumed, so every tile is in flight for about a chunk before it is needed.
+// A tile is requested with cp.async (16 bytes per thread and copy, one commit
+// group per tile, so "tile i has landed" is a group count); u (the CTA's own
+// 32 columns) is double-buffered by chunk parity and travels with its chunk's
+// w tile.
 //
 // Modes:
 //   RECUR (fold = 0): walk from the segment's entering state, write O (if o
@@ -38,7 +39,7 @@ namespace {
 constexpr int NSLOT_MAX = 5;
 
 struct WalkFwdSmem {
-  bf16 slot[NSLOT_MAX][CH * HD];  // swizzled 128 x 128 tiles
+  bf16 slot[NSLOT_MAX][CH * LDB];  // padded 128 x 128 tiles
   bf16 U[2][CH * LDS_];
   bf16 H[HD * LDS_];
   bf16 D[CH * LDS_];
@@ -83,23 +84,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_fwd(WalkFwdArgs a) {
   if (cbeg >= cend) return;
 
   auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
-  // request tile i (always commits exactly one cp.async group)
+  // request tile i (every thread; always commits exactly one cp.async group)
   auto issue = [&](int i) {
     if (i < ntiles) {
       const int c = cbeg + i / TPC, t = i % TPC;
       const long cid = bh * a.NC + c;
       bf16* dst = sm.slot[i % NSLOT];
       if (t == 0) {
-        tile_load_async_s(dst, a.W + cid * CH * HD, HD, CH, tid, NTHREADS);
+        tile_load_async(dst, a.W + cid * CH * HD, HD, CH, tid);
         if (!partA) slice_load_async(sm.U[c & 1], a.U + cid * CH * HD + col0, HD, CH, tid);
       } else if (t == 1) {
-        tile_load_async_s(dst, a.k + (((long)b * a.T + (long)c * CH) * a.Hk + kh) * HD, tokstride,
-                          rows_of(c), tid, NTHREADS);
+        tile_load_async(dst, a.k + (((long)b * a.T + (long)c * CH) * a.Hk + kh) * HD, tokstride,
+                        rows_of(c), tid);
       } else if (t == 2) {
-        tile_load_async_s(dst, a.q + (((long)b * a.T + (long)c * CH) * a.Hk + kh) * HD, tokstride,
-                          rows_of(c), tid, NTHREADS);
+        tile_load_async(dst, a.q + (((long)b * a.T + (long)c * CH) * a.Hk + kh) * HD, tokstride,
+                        rows_of(c), tid);
       } else {
-        tile_load_async_s(dst, a.P + cid * CH * CH, CH, CH, tid, NTHREADS);
+        tile_load_async(dst, a.P + cid * CH * CH, CH, CH, tid);
       }
     }
     cp_async_commit();
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_fwd(WalkFwdArgs a) {
     const bf16* sW = sm.slot[tw % NSLOT];
     const bf16* sK = sm.slot[(tw + 1) % NSLOT];
     const bf16* sU = sm.U[c & 1];
-    // tiles <= tw + 1 are needed now; NSLOT + tw have been requested
+    // tiles <= tw + 1 (w, u, K) are needed; NSLOT + tw groups have been committed
     cp_async_wait_n(NSLOT - 2);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {  // bf16 image of the entering state
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_fwd(WalkFwdArgs a) {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       uint32_t af[4], bb[4];
-      lda_rm_s(af, sW, m0, ks * 16, lane);
+      lda_rm(af, sW, LDB, m0, ks * 16, lane);
       ldb_kn(bb, sm.H, LDS_, ks * 16, 0, lane);
       mma16816(x[0], af, bb[0], bb[1]);
       mma16816(x[1], af, bb[2], bb[3]);
@@ -228,7 +229,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_fwd(WalkFwdArgs a) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         uint32_t af[4], bb[4];
-        lda_tr_s(af, sK, m0, ks * 16, lane);
+        lda_tr(af, sK, LDB, m0, ks * 16, lane);
         ldb_kn(bb, sm.Dg, LDS_, ks * 16, 0, lane);
         mma16816(h[0], af, bb[0], bb[1]);
         mma16816(h[1], af, bb[2], bb[3]);
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_fwd(WalkFwdArgs a) {
     if (withO) {
       const bf16* sQ = sm.slot[(tw + 2) % NSLOT];
       const bf16* sP = sm.slot[(tw + 3) % NSLOT];
-      cp_async_wait_n(NSLOT - 3);  // Q, P (tiles tw+2, tw+3) ready; NSLOT + tw + 1 requested
+      cp_async_wait_n(NSLOT - 3);  // Q, P (tiles tw+2, tw+3); NSLOT + tw + 1 committed
       __syncthreads();             // K consumed
       issue(tw + 1 + NSLOT);
       float o[4][4];
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_fwd(WalkFwdArgs a) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         uint32_t af[4], bb[4];
-        lda_rm_s(af, sQ, m0, ks * 16, lane);
+        lda_rm(af, sQ, LDB, m0, ks * 16, lane);
         ldb_kn(bb, sm.H, LDS_, ks * 16, 0, lane);
         mma16816(o[0], af, bb[0], bb[1]);
         mma16816(o[1], af, bb[2], bb[3]);
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_walk_fwd(WalkFwdArgs a) {
       for (int ks = 0; ks < 8; ++ks) {
         if (ks <= warp) {  // P is lower triangular
           uint32_t af[4], bb[4];
-          lda_rm_s(af, sP, m0, ks * 16, lane);
+          lda_rm(af, sP, LDB, m0, ks * 16, lane);
           ldb_kn(bb, sm.D, LDS_, ks * 16, 0, lane);
           mma16816(o[0], af, bb[0], bb[1]);
           mma16816(o[1], af, bb[2], bb[3]);
