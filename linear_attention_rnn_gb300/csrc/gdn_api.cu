@@ -8,6 +8,7 @@
 
 #include "gdn.h"
 #include "gdn_kernels.cuh"
+#include "gdn_tmap.cuh"
 
 using namespace gdn;
 
@@ -134,11 +135,18 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
   w.states = states;
   w.delta = delta;
   w.status = at<int>(ws, Lw.status);
+  WalkFwdMaps mp;
+  const uint64_t wrows = (uint64_t)d.BH() * d.NC * CH;
+  if (!tmap_heads(&mp.k, k, d.B, d.T, d.Hk, HD) || !tmap_heads(&mp.q, q, d.B, d.T, d.Hk, HD) ||
+      !tmap_2d(&mp.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
+      !tmap_2d(&mp.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true) ||
+      !tmap_2d(&mp.U, w.U, HD, wrows, HD * sizeof(bf16), SL, CH, false))
+    return GDN_ERR_CUDA;
   if (d.S == 1) {
     w.hstart = h0;
     w.hstart_bh_stride = (long)HD * HD;
     w.hstart_seg_stride = 0;
-    int r = cuda_status(launch_walk_fwd(w, 0, s));
+    int r = cuda_status(launch_walk_fwd(w, mp, 0, s));
     return r ? r : mk.rec();
   }
   WalkFwdArgs f = w;
@@ -148,7 +156,7 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
   f.hT = nullptr;
   f.states = nullptr;
   f.delta = nullptr;
-  int rc = cuda_status(launch_walk_fwd(f, 1, s));
+  int rc = cuda_status(launch_walk_fwd(f, mp, 1, s));
   if (rc || (rc = mk.rec())) return rc;
   AffineWalkArgs x;
   memset(&x, 0, sizeof x);
@@ -167,7 +175,7 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
   w.hstart = at<float>(ws, Lw.hin);
   w.hstart_bh_stride = (long)d.S * HD * HD;
   w.hstart_seg_stride = (long)HD * HD;
-  rc = cuda_status(launch_walk_fwd(w, 0, s));
+  rc = cuda_status(launch_walk_fwd(w, mp, 0, s));
   return rc ? rc : mk.rec();
 }
 

@@ -1,6 +1,7 @@
 // gdn_kernels.cuh -- argument blocks and launchers of the gated-delta-rule kernels
 // (internal to the library; the public boundary is include/gdn.h).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 
@@ -45,6 +46,13 @@ struct WalkFwdArgs {
   float* pairB;            // fold output [BH][S][HD][HD]
   int* status;             // bit 0 set if a bounded wait gave up (nullable)
   int B, T, Hk, Hv, NC, S;
+};
+
+// TMA tensor maps of the forward walk: K and Q over [B, T, Hk, 128] (boxes of
+// 64 columns x 128 tokens, 128-byte swizzle), w and P over the workspace rows
+// (same boxes), u over the workspace rows (32 columns x 128 rows, no swizzle).
+struct WalkFwdMaps {
+  CUtensorMap k, q, W, P, U;
 };
 
 // Sequential backward walk (state cotangent) over the chunks of one segment.
@@ -108,7 +116,7 @@ size_t affine_walk_smem_bytes();
 size_t grad_smem_bytes();
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
-cudaError_t launch_walk_fwd(const WalkFwdArgs& a, int fold, cudaStream_t s);
+cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold, cudaStream_t s);
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int fold, cudaStream_t s);
 cudaError_t launch_affine_walk(const AffineWalkArgs& a, cudaStream_t s);
 cudaError_t launch_grads(const GradArgs& a, cudaStream_t s);

@@ -6,20 +6,20 @@
 // with k_g = diag(exp(G_last - G)) K, and the masked intra-chunk output
 //     O = diag(gamma) Q h + P Delta,      P = (Q K^T) * decay (diagonal included).
 //
-// The state h (128 x 128 fp32) never leaves the SM while a segment is walked:
-// each CTA owns a 32-column slice of h (the matrices of the step act on h from
-// the left only, so columns evolve independently), kept in mma accumulator
-// registers; its bf16 image in shared memory is the B operand of the next
-// chunk's w h and Q h.
-//
-// The chunk tiles stream through a ring of NSLOT padded shared buffers in the
-// order they are consumed (w, K, then Q, P when the output is produced).  Tile
-// i goes to slot i % NSLOT and is requested as soon as tile i - NSLOT has been
-// consumed, so every tile is in flight for about a chunk before it is needed.
-// A tile is requested with cp.async (16 bytes per thread and copy, one commit
-// group per tile, so "tile i has landed" is a group count); u (the CTA's own
-// 32 columns) is double-buffered by chunk parity and travels with its chunk's
-// w tile.
+// One CTA walks a 32-column slice of one head's state (columns of h evolve
+// independently: every matrix of the step acts on h from the left).  Thread r
+// (of 128) owns row r: row r of the state slice in fp32 registers for the
+// whole segment, and TMEM lane r of every product.  Per chunk the products
+//     X  = w h            (A = w, K-major)
+//     H' = K^T (ef Delta) (A = the K tile read MN-major: no transpose pass)
+//     O1 = Q h,  O2 = P Delta
+// are tcgen05 MMAs (M = 128, N = 32, K = 128) issued by one thread into tensor
+// memory; their B operands (h^T, Delta^T, (ef Delta)^T: 32 x 128 bf16) are
+// written column by column by the 128 threads in the 128-byte-swizzled
+// K-major layout.  The chunk tiles (w, K, Q, P) arrive by TMA into a ring of
+// 32 KiB slots, each requested about a chunk before it is needed; u (this
+// CTA's 32 columns) arrives by TMA into a double buffer with its chunk's w.
+// Waits are bounded; one that gives up sets bit 0 of the status word.
 //
 // Modes:
 //   RECUR (fold = 0): walk from the segment's entering state, write O (if o
@@ -31,312 +31,308 @@
 //     from [I | 0]; the A columns take no u term.  CTAs 0-3 hold A's column
 //     slices, 4-7 hold B's.
 #include "gdn_kernels.cuh"
+#include "gdn_tc05.cuh"
 
 namespace gdn {
 
 namespace {
 
-constexpr int NSLOT_MAX = 5;
+constexpr int NT = 128;                        // threads: one per chunk row / state row
+constexpr int NSLOT = 5;                       // tile ring
+constexpr uint32_t TILE_BYTES = CH * HD * 2;   // 32 KiB
+constexpr uint32_t BT_BYTES = SL * HD * 2;     // 8 KiB: a [32 x 128] B-operand tile
+constexpr uint32_t USL_BYTES = CH * SL * 2;    // 8 KiB: u slice
 
-struct WalkFwdSmem {
-  bf16 slot[NSLOT_MAX][CH * LDB];  // padded 128 x 128 tiles
-  bf16 U[2][CH * LDS_];
-  bf16 H[HD * LDS_];
-  bf16 D[CH * LDS_];
-  bf16 Dg[CH * LDS_];
-  float gamma[2][CH];
-  float ef[2][CH];
-  float gC[2];
+struct WalkSmem {
+  unsigned char slot[NSLOT][TILE_BYTES];
+  unsigned char Ht[2][BT_BYTES];
+  unsigned char Dt[BT_BYTES];
+  unsigned char Dgt[BT_BYTES];
+  bf16 U[2][CH * SL];
+  float gsum[4];
+  uint64_t full[NSLOT];
+  uint64_t barX, barH, barO1, barO2;
+  uint32_t tmem;
 };
 
-// Gates of one chunk from the 128 log-gates held 4 per lane by warp 0.
-__device__ __forceinline__ void chunk_gates(float (&v)[4], float* gamma, float* ef, float* gC,
-                                            int lane) {
-  warp_cumsum128(v, lane);
-  const float Glast = __shfl_sync(0xffffffffu, v[3], 31);
+// Column k of a [32 x 128] K-major SW128 B tile from 32 fp32 values (rows n).
+__device__ __forceinline__ void write_bt_column(unsigned char* tile, int k, const float (&v)[32]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    gamma[lane * 4 + i] = expf(v[i]);
-    ef[lane * 4 + i] = expf(Glast - v[i]);
+  for (int n = 0; n < 32; ++n)
+    *reinterpret_cast<bf16*>(tile + tc::sw128(n, k, 32)) = __float2bfloat16_rn(v[n]);
+}
+
+__device__ __forceinline__ void store_row_bf16(bf16* dst, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 o;
+    o.x = pack_bf16(v[8 * q], v[8 * q + 1]);
+    o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(dst + 8 * q) = o;
   }
-  if (lane == 0) *gC = expf(Glast);
 }
 
 template <bool FOLD>
-__global__ void __launch_bounds__(NTHREADS, 1) k_walk_fwd(WalkFwdArgs a) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  WalkFwdSmem& sm = *reinterpret_cast<WalkFwdSmem*>(smem_raw);
+__global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_constant__ WalkFwdMaps mp) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  WalkSmem& sm = *reinterpret_cast<WalkSmem*>(base);
   const int slice = blockIdx.x, seg = blockIdx.y, bhi = blockIdx.z;
   const int b = bhi / a.Hv, j = bhi % a.Hv, kh = j / (a.Hv / a.Hk);
   const long bh = bhi;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g4 = lane >> 2, t4 = lane & 3;
+  const int r = tid;  // chunk row / state row owned by this thread
   const int cbeg = (int)((long)seg * a.NC / a.S), cend = (int)((long)(seg + 1) * a.NC / a.S);
   const bool partA = FOLD && slice < 4;  // A columns: no u term
   const bool withO = !FOLD && a.o != nullptr;
-  const int TPC = withO ? 4 : 2;                 // tiles per chunk: w, K (, Q, P)
-  const int NSLOT = withO ? 5 : 4;
+  const int TPC = withO ? 4 : 2;  // tiles per chunk: w, K (, Q, P)
+  // ring depth: 5 slots with the output, 4 without; either way the w tile of
+  // chunk c + 2 (which brings u into the buffer of chunk c) is requested only
+  // after chunk c has read its u
+  const int NS = withO ? NSLOT : 4;
   const int ntiles = (cend - cbeg) * TPC;
   const int col0 = (slice & 3) * SL;
-  const int m0 = warp * 16;
-  const int r0 = m0 + g4, r1 = r0 + 8;
-  const long tokstride = (long)a.Hk * HD;
   if (cbeg >= cend) return;
-
   auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
-  // request tile i (every thread; always commits exactly one cp.async group)
+
+  if (tid == 0) {
+    for (int k = 0; k < NSLOT; ++k) tc::mbar_init(&sm.full[k], 1);
+    tc::mbar_init(&sm.barX, 1);
+    tc::mbar_init(&sm.barH, 1);
+    tc::mbar_init(&sm.barO1, 1);
+    tc::mbar_init(&sm.barO2, 1);
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) tc::alloc(&sm.tmem, 128);
+
+  // request tile i (thread 0); tiles of chunk c in order: w (+u), K, Q, P
   auto issue = [&](int i) {
-    if (i < ntiles) {
-      const int c = cbeg + i / TPC, t = i % TPC;
-      const long cid = bh * a.NC + c;
-      bf16* dst = sm.slot[i % NSLOT];
-      if (t == 0) {
-        tile_load_async(dst, a.W + cid * CH * HD, HD, CH, tid);
-        if (!partA) slice_load_async(sm.U[c & 1], a.U + cid * CH * HD + col0, HD, CH, tid);
-      } else if (t == 1) {
-        tile_load_async(dst, a.k + (((long)b * a.T + (long)c * CH) * a.Hk + kh) * HD, tokstride,
-                        rows_of(c), tid);
-      } else if (t == 2) {
-        tile_load_async(dst, a.q + (((long)b * a.T + (long)c * CH) * a.Hk + kh) * HD, tokstride,
-                        rows_of(c), tid);
-      } else {
-        tile_load_async(dst, a.P + cid * CH * CH, CH, CH, tid);
-      }
+    if (i >= ntiles) return;
+    const int c = cbeg + i / TPC, t = i % TPC;
+    const long cid = bh * a.NC + c;
+    unsigned char* dst = sm.slot[i % NS];
+    uint64_t* bar = &sm.full[i % NS];
+    const bool withU = (t == 0) && !partA;
+    tc::arrive_expect_tx(bar, TILE_BYTES + (withU ? USL_BYTES : 0u));
+    if (t == 0 || t == 3) {
+      const CUtensorMap* m = (t == 0) ? &mp.W : &mp.P;
+      tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
+      tc::tma_load_2d(dst + TILE_BYTES / 2, m, 64, (int)(cid * CH), bar);
+      if (withU) tc::tma_load_2d(sm.U[c & 1], &mp.U, col0, (int)(cid * CH), bar);
+    } else {
+      const CUtensorMap* m = (t == 1) ? &mp.k : &mp.q;
+      tc::tma_load_4d(dst, m, 0, kh, c * CH, b, bar);
+      tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
     }
-    cp_async_commit();
   };
-  auto load_g = [&](int c, float (&v)[4]) {
+  bool ok = true;
+  auto wait_tile = [&](int i) { ok = tc::mbar_wait(&sm.full[i % NS], (i / NS) & 1) && ok; };
+  auto load_g = [&](int c) {
+    return (c < cend && r < rows_of(c)) ? a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j] : 0.f;
+  };
+  // chunk-local cumsum of the gate: warp scan, warp totals through smem (a CTA
+  // barrier separates scan_part from finish_gates)
+  auto scan_part = [&](float gv) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = lane * 4 + i;
-      v[i] = (c < cend && r < rows_of(c)) ? a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j] : 0.f;
+    for (int off = 1; off < 32; off <<= 1) {
+      const float o = __shfl_up_sync(0xffffffffu, gv, off);
+      if (lane >= off) gv += o;
     }
+    if (lane == 31) sm.gsum[warp] = gv;
+    return gv;
+  };
+  float gam_r = 0.f, ef_r = 0.f, gC = 0.f;  // gates of the current chunk for this row
+  auto finish_gates = [&](float part) {
+    float off = 0.f, tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float s = sm.gsum[w];
+      off += (w < warp) ? s : 0.f;
+      tot += s;
+    }
+    const float G = part + off;
+    gam_r = expf(G);
+    ef_r = expf(tot - G);
+    gC = expf(tot);
   };
 
-  // state slice: rows r0, r1 of h; columns col0 + 8 nt + 2 t4 + {0,1}
-  float h[4][4];
+  // state row r, columns col0..col0+31
+  float h[32];
   if (FOLD) {
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = col0 + nt * 8 + 2 * t4 + e;
-        h[nt][e] = (partA && r0 == col) ? 1.f : 0.f;
-        h[nt][2 + e] = (partA && r1 == col) ? 1.f : 0.f;
-      }
+    for (int n = 0; n < 32; ++n) h[n] = (partA && r == col0 + n) ? 1.f : 0.f;
   } else {
     const float* hs = a.hstart ? a.hstart + bh * a.hstart_bh_stride + seg * a.hstart_seg_stride : nullptr;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = col0 + nt * 8 + 2 * t4;
-      float2 x0 = make_float2(0.f, 0.f), x1 = x0;
-      if (hs) {
-        x0 = *reinterpret_cast<const float2*>(hs + r0 * HD + col);
-        x1 = *reinterpret_cast<const float2*>(hs + r1 * HD + col);
-      }
-      h[nt][0] = x0.x;
-      h[nt][1] = x0.y;
-      h[nt][2] = x1.x;
-      h[nt][3] = x1.y;
+    for (int q = 0; q < 8; ++q) {
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (hs) x = *reinterpret_cast<const float4*>(hs + (long)r * HD + col0 + 4 * q);
+      h[4 * q] = x.x;
+      h[4 * q + 1] = x.y;
+      h[4 * q + 2] = x.z;
+      h[4 * q + 3] = x.w;
     }
   }
-
-  for (int i = 0; i < NSLOT; ++i) issue(i);
-  float gnext[4];
-  if (warp == 0) {
-    float v[4];
-    load_g(cbeg, v);
-    chunk_gates(v, sm.gamma[cbeg & 1], sm.ef[cbeg & 1], &sm.gC[cbeg & 1], lane);
-    load_g(cbeg + 1, gnext);
-  }
+  write_bt_column(sm.Ht[0], r, h);
+  float part = scan_part(load_g(cbeg));
+  float gnext = load_g(cbeg + 1);
+  tc::fence_proxy_async();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  finish_gates(part);
+  const uint32_t tmem = sm.tmem;
+  const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
+  if (tid == 0)
+    for (int i = 0; i < NS; ++i) issue(i);
 
   for (int c = cbeg; c < cend; ++c) {
     const int ci = c - cbeg;
-    const int par = c & 1;
-    const int tw = ci * TPC;  // index of this chunk's w tile
-    const bf16* sW = sm.slot[tw % NSLOT];
-    const bf16* sK = sm.slot[(tw + 1) % NSLOT];
-    const bf16* sU = sm.U[c & 1];
-    // tiles <= tw + 1 (w, u, K) are needed; NSLOT + tw groups have been committed
-    cp_async_wait_n(NSLOT - 2);
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {  // bf16 image of the entering state
-      const int col = nt * 8 + 2 * t4;
-      *reinterpret_cast<uint32_t*>(sm.H + r0 * LDS_ + col) = pack_bf16(h[nt][0], h[nt][1]);
-      *reinterpret_cast<uint32_t*>(sm.H + r1 * LDS_ + col) = pack_bf16(h[nt][2], h[nt][3]);
-    }
-    if (!FOLD && a.states) {
-      bf16* st = a.states + ((bh * a.NC + c) * HD) * HD + col0;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int col = nt * 8 + 2 * t4;
-        *reinterpret_cast<uint32_t*>(st + (long)r0 * HD + col) = pack_bf16(h[nt][0], h[nt][1]);
-        *reinterpret_cast<uint32_t*>(st + (long)r1 * HD + col) = pack_bf16(h[nt][2], h[nt][3]);
+    const int cur = ci & 1;
+    const uint32_t par = (uint32_t)(ci & 1);
+    const int tw = ci * TPC;
+    unsigned char* sW = sm.slot[tw % NS];
+    unsigned char* sK = sm.slot[(tw + 1) % NS];
+    unsigned char* sQ = sm.slot[(tw + 2) % NS];
+    unsigned char* sP = sm.slot[(tw + 3) % NS];
+    const int L = rows_of(c);
+
+    if (!FOLD && a.states) store_row_bf16(a.states + ((bh * a.NC + c) * HD + r) * HD + col0, h);
+    // ---- X = w h  (and O1 = Q h) ----------------------------------------------------
+    if (tid == 0) {
+      wait_tile(tw);
+      tc::fence_after();
+      tc::gemm_k128(tmem + 0, smem_u32(sW), smem_u32(sm.Ht[cur]), 32, false);
+      tc::commit(&sm.barX);
+      if (withO) {
+        wait_tile(tw + 2);
+        tc::fence_after();
+        tc::gemm_k128(tmem + 64, smem_u32(sQ), smem_u32(sm.Ht[cur]), 32, false);
+        tc::commit(&sm.barO1);
       }
     }
-    __syncthreads();  // w, K, u of chunk c, the state image and the gates are ready
-
-    // ---- X = w h;  Delta = u - X -----------------------------------------------
-    float x[4][4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) x[q][0] = x[q][1] = x[q][2] = x[q][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t af[4], bb[4];
-      lda_rm(af, sW, LDB, m0, ks * 16, lane);
-      ldb_kn(bb, sm.H, LDS_, ks * 16, 0, lane);
-      mma16816(x[0], af, bb[0], bb[1]);
-      mma16816(x[1], af, bb[2], bb[3]);
-      ldb_kn(bb, sm.H, LDS_, ks * 16, 16, lane);
-      mma16816(x[2], af, bb[0], bb[1]);
-      mma16816(x[3], af, bb[2], bb[3]);
-    }
+    wait_tile(tw);  // u of chunk c
+    ok = tc::mbar_wait(&sm.barX, par) && ok;
+    tc::fence_after();
     {
-      const float e0 = sm.ef[par][r0], e1 = sm.ef[par][r1];
+      float x[32];
+      tc::ld32(tl + 0, x);
+      if (!partA) {
+        const bf16* ur = sm.U[c & 1] + r * SL;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int col = nt * 8 + 2 * t4;
-        float2 u0 = make_float2(0.f, 0.f), u1 = u0;
-        if (!partA) {
-          u0 = unpack_bf16(*reinterpret_cast<const uint32_t*>(sU + r0 * LDS_ + col));
-          u1 = unpack_bf16(*reinterpret_cast<const uint32_t*>(sU + r1 * LDS_ + col));
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(ur + 8 * q);
+          const float2 f0 = unpack_bf16(w4.x), f1 = unpack_bf16(w4.y), f2 = unpack_bf16(w4.z),
+                       f3 = unpack_bf16(w4.w);
+          x[8 * q] = f0.x - x[8 * q];
+          x[8 * q + 1] = f0.y - x[8 * q + 1];
+          x[8 * q + 2] = f1.x - x[8 * q + 2];
+          x[8 * q + 3] = f1.y - x[8 * q + 3];
+          x[8 * q + 4] = f2.x - x[8 * q + 4];
+          x[8 * q + 5] = f2.y - x[8 * q + 5];
+          x[8 * q + 6] = f3.x - x[8 * q + 6];
+          x[8 * q + 7] = f3.y - x[8 * q + 7];
         }
-        const float d00 = u0.x - x[nt][0], d01 = u0.y - x[nt][1];
-        const float d10 = u1.x - x[nt][2], d11 = u1.y - x[nt][3];
-        if (withO) {
-          *reinterpret_cast<uint32_t*>(sm.D + r0 * LDS_ + col) = pack_bf16(d00, d01);
-          *reinterpret_cast<uint32_t*>(sm.D + r1 * LDS_ + col) = pack_bf16(d10, d11);
-        }
-        if (!FOLD && a.delta) {
-          bf16* dd = a.delta + ((bh * a.NC + c) * CH) * HD + col0 + col;
-          *reinterpret_cast<uint32_t*>(dd + (long)r0 * HD) = pack_bf16(d00, d01);
-          *reinterpret_cast<uint32_t*>(dd + (long)r1 * HD) = pack_bf16(d10, d11);
-        }
-        *reinterpret_cast<uint32_t*>(sm.Dg + r0 * LDS_ + col) = pack_bf16(e0 * d00, e0 * d01);
-        *reinterpret_cast<uint32_t*>(sm.Dg + r1 * LDS_ + col) = pack_bf16(e1 * d10, e1 * d11);
+      } else {
+#pragma unroll
+        for (int n = 0; n < 32; ++n) x[n] = -x[n];
+      }
+      // x is Delta
+      if (withO) write_bt_column(sm.Dt, r, x);
+      if (!FOLD && a.delta) store_row_bf16(a.delta + ((bh * a.NC + c) * CH + r) * HD + col0, x);
+#pragma unroll
+      for (int n = 0; n < 32; ++n) x[n] *= ef_r;
+      write_bt_column(sm.Dgt, r, x);
+    }
+    tc::fence_proxy_async();
+    tc::fence_before();
+    __syncthreads();  // Delta^T, (ef Delta)^T complete; u read
+    tc::fence_after();
+    if (tid == 0) issue(tw + NS);  // into w's slot (X done) and the u buffer (read)
+
+    // ---- H' = K^T (ef Delta)  (and O2 = P Delta) -----------------------------------
+    if (tid == 0) {
+      wait_tile(tw + 1);
+      tc::fence_after();
+      tc::gemm_amn_k128(tmem + 32, smem_u32(sK), smem_u32(sm.Dgt), 32, false);
+      tc::commit(&sm.barH);
+      if (withO) {
+        wait_tile(tw + 3);
+        tc::fence_after();
+        tc::gemm_k128(tmem + 96, smem_u32(sP), smem_u32(sm.Dt), 32, false);
+        tc::commit(&sm.barO2);
       }
     }
-    __syncthreads();  // w and u consumed; D, Dg complete
-    issue(tw + NSLOT);
-
-    // ---- h' = exp(g_last) h + K^T (ef * Delta) ---------------------------------
+    part = scan_part(gnext);  // gates of chunk c + 1 (totals read after the next barrier)
+    gnext = load_g(c + 2);
+    ok = tc::mbar_wait(&sm.barH, par) && ok;
+    tc::fence_after();
     {
-      const float gC = sm.gC[par];
+      float hh[32];
+      tc::ld32(tl + 32, hh);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) h[nt][e] *= gC;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t af[4], bb[4];
-        lda_tr(af, sK, LDB, m0, ks * 16, lane);
-        ldb_kn(bb, sm.Dg, LDS_, ks * 16, 0, lane);
-        mma16816(h[0], af, bb[0], bb[1]);
-        mma16816(h[1], af, bb[2], bb[3]);
-        ldb_kn(bb, sm.Dg, LDS_, ks * 16, 16, lane);
-        mma16816(h[2], af, bb[0], bb[1]);
-        mma16816(h[3], af, bb[2], bb[3]);
-      }
+      for (int n = 0; n < 32; ++n) h[n] = gC * h[n] + hh[n];
+      write_bt_column(sm.Ht[cur ^ 1], r, h);
     }
-
     if (withO) {
-      const bf16* sQ = sm.slot[(tw + 2) % NSLOT];
-      const bf16* sP = sm.slot[(tw + 3) % NSLOT];
-      cp_async_wait_n(NSLOT - 3);  // Q, P (tiles tw+2, tw+3); NSLOT + tw + 1 committed
-      __syncthreads();             // K consumed
-      issue(tw + 1 + NSLOT);
-      float o[4][4];
+      ok = tc::mbar_wait(&sm.barO1, par) && ok;
+      ok = tc::mbar_wait(&sm.barO2, par) && ok;
+      tc::fence_after();
+      float o1[32], o2[32];
+      tc::ld32(tl + 64, o1);
+      tc::ld32(tl + 96, o2);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) o[q][0] = o[q][1] = o[q][2] = o[q][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t af[4], bb[4];
-        lda_rm(af, sQ, LDB, m0, ks * 16, lane);
-        ldb_kn(bb, sm.H, LDS_, ks * 16, 0, lane);
-        mma16816(o[0], af, bb[0], bb[1]);
-        mma16816(o[1], af, bb[2], bb[3]);
-        ldb_kn(bb, sm.H, LDS_, ks * 16, 16, lane);
-        mma16816(o[2], af, bb[0], bb[1]);
-        mma16816(o[3], af, bb[2], bb[3]);
-      }
-      const float gm0 = sm.gamma[par][r0], gm1 = sm.gamma[par][r1];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        o[nt][0] *= gm0;
-        o[nt][1] *= gm0;
-        o[nt][2] *= gm1;
-        o[nt][3] *= gm1;
-      }
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if (ks <= warp) {  // P is lower triangular
-          uint32_t af[4], bb[4];
-          lda_rm(af, sP, LDB, m0, ks * 16, lane);
-          ldb_kn(bb, sm.D, LDS_, ks * 16, 0, lane);
-          mma16816(o[0], af, bb[0], bb[1]);
-          mma16816(o[1], af, bb[2], bb[3]);
-          ldb_kn(bb, sm.D, LDS_, ks * 16, 16, lane);
-          mma16816(o[2], af, bb[0], bb[1]);
-          mma16816(o[3], af, bb[2], bb[3]);
-        }
-      }
-      const int L = rows_of(c);
-      bf16* ob = a.o + (((long)b * a.T + (long)c * CH) * a.Hv + j) * HD + col0;
-      const long os = (long)a.Hv * HD;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int col = nt * 8 + 2 * t4;
-        if (r0 < L) *reinterpret_cast<uint32_t*>(ob + r0 * os + col) = pack_bf16(o[nt][0], o[nt][1]);
-        if (r1 < L) *reinterpret_cast<uint32_t*>(ob + r1 * os + col) = pack_bf16(o[nt][2], o[nt][3]);
-      }
-      __syncthreads();  // Q, P, D and the state image consumed
-      issue(tw + 2 + NSLOT);
-      issue(tw + 3 + NSLOT);
-    } else {
-      __syncthreads();  // K, Dg and the state image consumed
-      issue(tw + 1 + NSLOT);
+      for (int n = 0; n < 32; ++n) o1[n] = gam_r * o1[n] + o2[n];
+      if (r < L) store_row_bf16(a.o + (((long)b * a.T + (long)c * CH + r) * a.Hv + j) * HD + col0, o1);
     }
-    if (warp == 0 && c + 1 < cend) {
-      chunk_gates(gnext, sm.gamma[par ^ 1], sm.ef[par ^ 1], &sm.gC[par ^ 1], lane);
-      load_g(c + 2, gnext);
+    tc::fence_proxy_async();
+    tc::fence_before();
+    __syncthreads();  // next state image complete; this chunk's products all read
+    tc::fence_after();
+    finish_gates(part);
+    if (tid == 0) {
+      issue(tw + 1 + NS);  // K's slot (H' done)
+      if (withO) {
+        issue(tw + 2 + NS);  // Q's slot (O1 done)
+        issue(tw + 3 + NS);  // P's slot (O2 done)
+      }
     }
   }
-  cp_async_wait<0>();
 
   if (FOLD) {
-    float* dst = (partA ? a.pairA : a.pairB) + (bh * a.S + seg) * HD * HD + col0;
+    float* dst = (partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = nt * 8 + 2 * t4;
-      *reinterpret_cast<float2*>(dst + r0 * HD + col) = make_float2(h[nt][0], h[nt][1]);
-      *reinterpret_cast<float2*>(dst + r1 * HD + col) = make_float2(h[nt][2], h[nt][3]);
-    }
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
   } else if (a.hT && seg == a.S - 1) {
-    float* dst = a.hT + bh * HD * HD + col0;
+    float* dst = a.hT + (bh * HD + r) * HD + col0;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = nt * 8 + 2 * t4;
-      *reinterpret_cast<float2*>(dst + r0 * HD + col) = make_float2(h[nt][0], h[nt][1]);
-      *reinterpret_cast<float2*>(dst + r1 * HD + col) = make_float2(h[nt][2], h[nt][3]);
-    }
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
   }
+  if (!ok && a.status && lane == 0) atomicOr(a.status, 1);
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, 128);
 }
 
 template <bool FOLD>
-cudaError_t launch_one(const WalkFwdArgs& a, cudaStream_t s) {
-  const size_t smem = sizeof(WalkFwdSmem);
+cudaError_t launch_one(const WalkFwdArgs& a, const WalkFwdMaps& m, cudaStream_t s) {
+  const size_t smem = sizeof(WalkSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(k_walk_fwd<FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_walk_fwd<FOLD><<<dim3(FOLD ? 8 : HD / SL, a.S, a.B * a.Hv), NTHREADS, smem, s>>>(a);
+  k_walk_fwd<FOLD><<<dim3(FOLD ? 8 : HD / SL, a.S, a.B * a.Hv), NT, smem, s>>>(a, m);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t walk_fwd_smem_bytes(int) { return sizeof(WalkFwdSmem); }
+size_t walk_fwd_smem_bytes(int) { return sizeof(WalkSmem) + 1024; }
 
-cudaError_t launch_walk_fwd(const WalkFwdArgs& a, int fold, cudaStream_t s) {
-  return fold ? launch_one<true>(a, s) : launch_one<false>(a, s);
+cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold, cudaStream_t s) {
+  return fold ? launch_one<true>(a, m, s) : launch_one<false>(a, m, s);
 }
 
 }  // namespace gdn
