@@ -7,19 +7,23 @@
 //     O = diag(gamma) Q h + P Delta,      P = (Q K^T) * decay (diagonal included).
 //
 // One CTA walks a 32-column slice of one head's state (columns of h evolve
-// independently: every matrix of the step acts on h from the left).  Thread r
-// (of 128) owns row r: row r of the state slice in fp32 registers for the
-// whole segment, and TMEM lane r of every product.  Per chunk the products
+// independently: every matrix of the step acts on h from the left).  Compute
+// thread r (of 128) owns row r: row r of the state slice in fp32 registers for
+// the whole segment, and TMEM lane r of every product.  Per chunk the products
 //     X  = w h            (A = w, K-major)
 //     H' = K^T (ef Delta) (A = the K tile read MN-major: no transpose pass)
 //     O1 = Q h,  O2 = P Delta
-// are tcgen05 MMAs (M = 128, N = 32, K = 128) issued by one thread into tensor
-// memory; their B operands (h^T, Delta^T, (ef Delta)^T: 32 x 128 bf16) are
-// written column by column by the 128 threads in the 128-byte-swizzled
-// K-major layout.  The chunk tiles (w, K, Q, P) arrive by TMA into a ring of
-// 32 KiB slots, each requested about a chunk before it is needed; u (this
-// CTA's 32 columns) arrives by TMA into a double buffer with its chunk's w.
-// Waits are bounded; one that gives up sets bit 0 of the status word.
+// are tcgen05 MMAs (M = 128, N = 32, K = 128) into tensor memory.  Their B
+// operands (h^T, Delta^T, (ef Delta)^T, 32 x 128 bf16) are written column by
+// column by the compute threads in the 128-byte-swizzled K-major layout.
+//
+// A fifth warp issues everything asynchronous: the MMAs (as soon as their
+// operands are signalled ready on mbarriers by the compute threads) and the
+// TMA loads of the chunk tiles into a ring of six 32 KiB slots (w, Q, K, P in
+// the order the MMAs consume them; each slot is refilled as soon as the MMA
+// that read it has completed) and of u.  The compute threads never wait on
+// memory issue, only on MMA completion.  Every wait is bounded; one that
+// gives up sets bit 0 of the status word.
 //
 // Modes:
 //   RECUR (fold = 0): walk from the segment's entering state, write O (if o
@@ -37,21 +41,22 @@ namespace gdn {
 
 namespace {
 
-constexpr int NT = 128;                        // threads: one per chunk row / state row
-constexpr int NSLOT = 5;                       // tile ring
+constexpr int NC_THREADS = 128;                // compute threads: one per chunk row / state row
+constexpr int NT = NC_THREADS + 32;            // + the issuer warp
+constexpr int NSLOT = 6;                       // tile ring
 constexpr uint32_t TILE_BYTES = CH * HD * 2;   // 32 KiB
 constexpr uint32_t BT_BYTES = SL * HD * 2;     // 8 KiB: a [32 x 128] B-operand tile
 constexpr uint32_t USL_BYTES = CH * SL * 2;    // 8 KiB: u slice
 
 struct WalkSmem {
   unsigned char slot[NSLOT][TILE_BYTES];
-  unsigned char Ht[2][BT_BYTES];
+  unsigned char Ht[BT_BYTES];
   unsigned char Dt[BT_BYTES];
   unsigned char Dgt[BT_BYTES];
-  bf16 U[2][CH * SL];
-  float gsum[4];
+  bf16 U[CH * SL];
+  float gsum[2][4];
   uint64_t full[NSLOT];
-  uint64_t barX, barH, barO1, barO2;
+  uint64_t ufull, barX, barO1, barH, barO2, barDg, barD, barHt;
   uint32_t tmem;
 };
 
@@ -74,6 +79,10 @@ __device__ __forceinline__ void store_row_bf16(bf16* dst, const float (&v)[32]) 
   }
 }
 
+__device__ __forceinline__ void arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 template <bool FOLD>
 __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_constant__ WalkFwdMaps mp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -83,144 +92,182 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
   const int b = bhi / a.Hv, j = bhi % a.Hv, kh = j / (a.Hv / a.Hk);
   const long bh = bhi;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = tid;  // chunk row / state row owned by this thread
   const int cbeg = (int)((long)seg * a.NC / a.S), cend = (int)((long)(seg + 1) * a.NC / a.S);
   const bool partA = FOLD && slice < 4;  // A columns: no u term
   const bool withO = !FOLD && a.o != nullptr;
-  const int TPC = withO ? 4 : 2;  // tiles per chunk: w, K (, Q, P)
-  // ring depth: 5 slots with the output, 4 without; either way the w tile of
-  // chunk c + 2 (which brings u into the buffer of chunk c) is requested only
-  // after chunk c has read its u
-  const int NS = withO ? NSLOT : 4;
+  const int TPC = withO ? 4 : 2;  // tiles per chunk: w, (Q,) K (, P)
   const int ntiles = (cend - cbeg) * TPC;
   const int col0 = (slice & 3) * SL;
   if (cbeg >= cend) return;
   auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
+  // tile sequence of a chunk: w, Q, K, P (with output) or w, K
+  auto tile_of = [&](int kind) { return withO ? kind : (kind == 0 ? 0 : 1); };  // kind: 0 w, 1 Q, 2 K, 3 P
 
   if (tid == 0) {
     for (int k = 0; k < NSLOT; ++k) tc::mbar_init(&sm.full[k], 1);
+    tc::mbar_init(&sm.ufull, 1);
     tc::mbar_init(&sm.barX, 1);
-    tc::mbar_init(&sm.barH, 1);
     tc::mbar_init(&sm.barO1, 1);
+    tc::mbar_init(&sm.barH, 1);
     tc::mbar_init(&sm.barO2, 1);
+    tc::mbar_init(&sm.barDg, NC_THREADS);
+    tc::mbar_init(&sm.barD, NC_THREADS);
+    tc::mbar_init(&sm.barHt, NC_THREADS);
     tc::mbar_fence_init();
   }
-  if (warp == 0) tc::alloc(&sm.tmem, 128);
-
-  // request tile i (thread 0); tiles of chunk c in order: w (+u), K, Q, P
-  auto issue = [&](int i) {
-    if (i >= ntiles) return;
-    const int c = cbeg + i / TPC, t = i % TPC;
-    const long cid = bh * a.NC + c;
-    unsigned char* dst = sm.slot[i % NS];
-    uint64_t* bar = &sm.full[i % NS];
-    const bool withU = (t == 0) && !partA;
-    tc::arrive_expect_tx(bar, TILE_BYTES + (withU ? USL_BYTES : 0u));
-    if (t == 0 || t == 3) {
-      const CUtensorMap* m = (t == 0) ? &mp.W : &mp.P;
-      tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
-      tc::tma_load_2d(dst + TILE_BYTES / 2, m, 64, (int)(cid * CH), bar);
-      if (withU) tc::tma_load_2d(sm.U[c & 1], &mp.U, col0, (int)(cid * CH), bar);
-    } else {
-      const CUtensorMap* m = (t == 1) ? &mp.k : &mp.q;
-      tc::tma_load_4d(dst, m, 0, kh, c * CH, b, bar);
-      tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
-    }
-  };
+  if (warp == 0) tc::alloc(&sm.tmem, 256);
   bool ok = true;
-  auto wait_tile = [&](int i) { ok = tc::mbar_wait(&sm.full[i % NS], (i / NS) & 1) && ok; };
+
+  // state row r = tid (compute threads), columns col0..col0+31
+  const int r = tid;
+  float h[32];
+  float gnext = 0.f, part = 0.f;
+  float gam_r = 0.f, ef_r = 0.f, gC = 0.f;
   auto load_g = [&](int c) {
     return (c < cend && r < rows_of(c)) ? a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j] : 0.f;
   };
-  // chunk-local cumsum of the gate: warp scan, warp totals through smem (a CTA
-  // barrier separates scan_part from finish_gates)
-  auto scan_part = [&](float gv) {
+  // gate totals of chunk index i (from the segment start) go to gsum[i & 1]:
+  // a warp may post the totals of chunk i + 1 while another still reads those of i
+  auto scan_part = [&](float gv, int i) {  // warp-inclusive scan; warp totals to smem
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const float o = __shfl_up_sync(0xffffffffu, gv, off);
       if (lane >= off) gv += o;
     }
-    if (lane == 31) sm.gsum[warp] = gv;
+    if (lane == 31) sm.gsum[i & 1][warp] = gv;
     return gv;
   };
-  float gam_r = 0.f, ef_r = 0.f, gC = 0.f;  // gates of the current chunk for this row
-  auto finish_gates = [&](float part) {
+  auto finish_gates = [&](float p, int i) {  // after a barrier over the compute threads
     float off = 0.f, tot = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const float s = sm.gsum[w];
+      const float s = sm.gsum[i & 1][w];
       off += (w < warp) ? s : 0.f;
       tot += s;
     }
-    const float G = part + off;
+    const float G = p + off;
     gam_r = expf(G);
     ef_r = expf(tot - G);
     gC = expf(tot);
   };
-
-  // state row r, columns col0..col0+31
-  float h[32];
-  if (FOLD) {
+  if (warp < 4) {
+    if (FOLD) {
 #pragma unroll
-    for (int n = 0; n < 32; ++n) h[n] = (partA && r == col0 + n) ? 1.f : 0.f;
-  } else {
-    const float* hs = a.hstart ? a.hstart + bh * a.hstart_bh_stride + seg * a.hstart_seg_stride : nullptr;
+      for (int n = 0; n < 32; ++n) h[n] = (partA && r == col0 + n) ? 1.f : 0.f;
+    } else {
+      const float* hs = a.hstart ? a.hstart + bh * a.hstart_bh_stride + seg * a.hstart_seg_stride : nullptr;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (hs) x = *reinterpret_cast<const float4*>(hs + (long)r * HD + col0 + 4 * q);
-      h[4 * q] = x.x;
-      h[4 * q + 1] = x.y;
-      h[4 * q + 2] = x.z;
-      h[4 * q + 3] = x.w;
+      for (int q = 0; q < 8; ++q) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (hs) x = *reinterpret_cast<const float4*>(hs + (long)r * HD + col0 + 4 * q);
+        h[4 * q] = x.x;
+        h[4 * q + 1] = x.y;
+        h[4 * q + 2] = x.z;
+        h[4 * q + 3] = x.w;
+      }
     }
+    write_bt_column(sm.Ht, r, h);
+    part = scan_part(load_g(cbeg), 0);
+    gnext = load_g(cbeg + 1);
   }
-  write_bt_column(sm.Ht[0], r, h);
-  float part = scan_part(load_g(cbeg));
-  float gnext = load_g(cbeg + 1);
   tc::fence_proxy_async();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  finish_gates(part);
+  // TMEM columns: X = w h at 0, H' at 32, P Delta at 96; Q h alternates between
+  // 64 and 128 (it is read after the next chunk's Q h may have been issued)
   const uint32_t tmem = sm.tmem;
-  const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
-  if (tid == 0)
-    for (int i = 0; i < NS; ++i) issue(i);
+  auto o1_col = [](int ci) { return (ci & 1) ? 128u : 64u; };
 
-  for (int c = cbeg; c < cend; ++c) {
-    const int ci = c - cbeg;
-    const int cur = ci & 1;
-    const uint32_t par = (uint32_t)(ci & 1);
-    const int tw = ci * TPC;
-    unsigned char* sW = sm.slot[tw % NS];
-    unsigned char* sK = sm.slot[(tw + 1) % NS];
-    unsigned char* sQ = sm.slot[(tw + 2) % NS];
-    unsigned char* sP = sm.slot[(tw + 3) % NS];
-    const int L = rows_of(c);
-
-    if (!FOLD && a.states) store_row_bf16(a.states + ((bh * a.NC + c) * HD + r) * HD + col0, h);
-    // ---- X = w h  (and O1 = Q h) ----------------------------------------------------
-    if (tid == 0) {
-      wait_tile(tw);
-      tc::fence_after();
-      tc::gemm_k128(tmem + 0, smem_u32(sW), smem_u32(sm.Ht[cur]), 32, false);
-      tc::commit(&sm.barX);
-      if (withO) {
-        wait_tile(tw + 2);
+  if (warp == 4) {
+    // ================================================================= issuer
+    if (lane == 0) {
+      auto issue = [&](int i) {  // TMA request of tile i into slot i % NSLOT
+        if (i >= ntiles) return;
+        const int c = cbeg + i / TPC, t = i % TPC;
+        const int kind = withO ? t : (t == 0 ? 0 : 2);
+        const long cid = bh * a.NC + c;
+        unsigned char* dst = sm.slot[i % NSLOT];
+        uint64_t* bar = &sm.full[i % NSLOT];
+        tc::arrive_expect_tx(bar, TILE_BYTES);
+        if (kind == 0 || kind == 3) {
+          const CUtensorMap* m = (kind == 0) ? &mp.W : &mp.P;
+          tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
+          tc::tma_load_2d(dst + TILE_BYTES / 2, m, 64, (int)(cid * CH), bar);
+        } else {
+          const CUtensorMap* m = (kind == 1) ? &mp.q : &mp.k;
+          tc::tma_load_4d(dst, m, 0, kh, c * CH, b, bar);
+          tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
+        }
+      };
+      auto issue_u = [&](int c) {
+        if (partA || c >= cend) return;
+        tc::arrive_expect_tx(&sm.ufull, USL_BYTES);
+        tc::tma_load_2d(sm.U, &mp.U, col0, (int)((bh * a.NC + c) * CH), &sm.ufull);
+      };
+      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NSLOT], (i / NSLOT) & 1); };
+      auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NSLOT]); };
+      for (int i = 0; i < NSLOT; ++i) issue(i);
+      issue_u(cbeg);
+      for (int c = cbeg; c < cend; ++c) {
+        const int ci = c - cbeg;
+        const uint32_t par = (uint32_t)(ci & 1);
+        const int t0 = ci * TPC;
+        const int iW = t0, iQ = t0 + 1, iK = t0 + tile_of(2), iP = t0 + 3;
+        if (ci > 0) ok = ok && tc::mbar_wait(&sm.barHt, par ^ 1);  // state image of chunk c
+        wait_tile(iW);
         tc::fence_after();
-        tc::gemm_k128(tmem + 64, smem_u32(sQ), smem_u32(sm.Ht[cur]), 32, false);
-        tc::commit(&sm.barO1);
+        tc::gemm_k128(tmem + 0, slot_of(iW), smem_u32(sm.Ht), 32, false);
+        tc::commit(&sm.barX);
+        if (withO) {
+          wait_tile(iQ);
+          tc::fence_after();
+          tc::gemm_k128(tmem + o1_col(ci), slot_of(iQ), smem_u32(sm.Ht), 32, false);
+          tc::commit(&sm.barO1);
+        }
+        ok = ok && tc::mbar_wait(&sm.barX, par);
+        issue(iW + NSLOT);  // w consumed
+        ok = ok && tc::mbar_wait(&sm.barDg, par);  // (ef Delta)^T written; u read
+        issue_u(c + 1);
+        wait_tile(iK);
+        tc::fence_after();
+        tc::gemm_amn_k128(tmem + 32, slot_of(iK), smem_u32(sm.Dgt), 32, false);
+        tc::commit(&sm.barH);
+        if (withO) {
+          ok = ok && tc::mbar_wait(&sm.barD, par);  // Delta^T written
+          wait_tile(iP);
+          tc::fence_after();
+          tc::gemm_k128(tmem + 96, slot_of(iP), smem_u32(sm.Dt), 32, false);
+          tc::commit(&sm.barO2);
+          ok = ok && tc::mbar_wait(&sm.barO1, par);
+          issue(iQ + NSLOT);  // Q consumed
+        }
+        ok = ok && tc::mbar_wait(&sm.barH, par);
+        issue(iK + NSLOT);  // K consumed
+        if (withO) {
+          ok = ok && tc::mbar_wait(&sm.barO2, par);
+          issue(iP + NSLOT);  // P consumed
+        }
       }
     }
-    wait_tile(tw);  // u of chunk c
-    ok = tc::mbar_wait(&sm.barX, par) && ok;
-    tc::fence_after();
-    {
+  } else {
+    // ========================================================== compute threads
+    finish_gates(part, 0);
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
+    for (int c = cbeg; c < cend; ++c) {
+      const int ci = c - cbeg;
+      const uint32_t par = (uint32_t)(ci & 1);
+      const int L = rows_of(c);
+      if (!FOLD && a.states) store_row_bf16(a.states + ((bh * a.NC + c) * HD + r) * HD + col0, h);
+
+      // ---- Delta = u - X -------------------------------------------------------
+      ok = ok && tc::mbar_wait(&sm.barX, par);
+      tc::fence_after();
       float x[32];
       tc::ld32(tl + 0, x);
       if (!partA) {
-        const bf16* ur = sm.U[c & 1] + r * SL;
+        ok = ok && tc::mbar_wait(&sm.ufull, par);
+        const bf16* ur = sm.U + r * SL;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint4 w4 = *reinterpret_cast<const uint4*>(ur + 8 * q);
@@ -239,83 +286,67 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
 #pragma unroll
         for (int n = 0; n < 32; ++n) x[n] = -x[n];
       }
-      // x is Delta
-      if (withO) write_bt_column(sm.Dt, r, x);
-      if (!FOLD && a.delta) store_row_bf16(a.delta + ((bh * a.NC + c) * CH + r) * HD + col0, x);
+      float xg[32];
 #pragma unroll
-      for (int n = 0; n < 32; ++n) x[n] *= ef_r;
-      write_bt_column(sm.Dgt, r, x);
-    }
-    tc::fence_proxy_async();
-    tc::fence_before();
-    __syncthreads();  // Delta^T, (ef Delta)^T complete; u read
-    tc::fence_after();
-    if (tid == 0) issue(tw + NS);  // into w's slot (X done) and the u buffer (read)
-
-    // ---- H' = K^T (ef Delta)  (and O2 = P Delta) -----------------------------------
-    if (tid == 0) {
-      wait_tile(tw + 1);
-      tc::fence_after();
-      tc::gemm_amn_k128(tmem + 32, smem_u32(sK), smem_u32(sm.Dgt), 32, false);
-      tc::commit(&sm.barH);
+      for (int n = 0; n < 32; ++n) xg[n] = x[n] * ef_r;
+      write_bt_column(sm.Dgt, r, xg);  // operand of the state update: first
+      tc::fence_proxy_async();
+      tc::fence_before();
+      arrive(&sm.barDg);
       if (withO) {
-        wait_tile(tw + 3);
-        tc::fence_after();
-        tc::gemm_k128(tmem + 96, smem_u32(sP), smem_u32(sm.Dt), 32, false);
-        tc::commit(&sm.barO2);
+        write_bt_column(sm.Dt, r, x);
+        tc::fence_proxy_async();
+        tc::fence_before();
+        arrive(&sm.barD);
       }
-    }
-    part = scan_part(gnext);  // gates of chunk c + 1 (totals read after the next barrier)
-    gnext = load_g(c + 2);
-    ok = tc::mbar_wait(&sm.barH, par) && ok;
-    tc::fence_after();
-    {
+      if (!FOLD && a.delta) store_row_bf16(a.delta + ((bh * a.NC + c) * CH + r) * HD + col0, x);
+      part = scan_part(gnext, ci + 1);  // gates of chunk c + 1
+      gnext = load_g(c + 2);
+
+      // ---- h' = gamma_C h + H' ---------------------------------------------------
+      ok = ok && tc::mbar_wait(&sm.barH, par);
+      tc::fence_after();
       float hh[32];
       tc::ld32(tl + 32, hh);
 #pragma unroll
       for (int n = 0; n < 32; ++n) h[n] = gC * h[n] + hh[n];
-      write_bt_column(sm.Ht[cur ^ 1], r, h);
-    }
-    if (withO) {
-      ok = tc::mbar_wait(&sm.barO1, par) && ok;
-      ok = tc::mbar_wait(&sm.barO2, par) && ok;
-      tc::fence_after();
-      float o1[32], o2[32];
-      tc::ld32(tl + 64, o1);
-      tc::ld32(tl + 96, o2);
+      // Q h has been read by the tensor core before the state image is replaced
+      if (withO) ok = ok && tc::mbar_wait(&sm.barO1, par);
+      write_bt_column(sm.Ht, r, h);
+      tc::fence_proxy_async();
+      tc::fence_before();
+      arrive(&sm.barHt);
+      if (withO) {  // output epilogue overlaps the next chunk's first product
+        ok = ok && tc::mbar_wait(&sm.barO2, par);
+        tc::fence_after();
+        float o1[32], o2[32];
+        tc::ld32(tl + o1_col(ci), o1);
+        tc::ld32(tl + 96, o2);
+        if (r < L) {
 #pragma unroll
-      for (int n = 0; n < 32; ++n) o1[n] = gam_r * o1[n] + o2[n];
-      if (r < L) store_row_bf16(a.o + (((long)b * a.T + (long)c * CH + r) * a.Hv + j) * HD + col0, o1);
-    }
-    tc::fence_proxy_async();
-    tc::fence_before();
-    __syncthreads();  // next state image complete; this chunk's products all read
-    tc::fence_after();
-    finish_gates(part);
-    if (tid == 0) {
-      issue(tw + 1 + NS);  // K's slot (H' done)
-      if (withO) {
-        issue(tw + 2 + NS);  // Q's slot (O1 done)
-        issue(tw + 3 + NS);  // P's slot (O2 done)
+          for (int n = 0; n < 32; ++n) o1[n] = gam_r * o1[n] + o2[n];
+          store_row_bf16(a.o + (((long)b * a.T + (long)c * CH + r) * a.Hv + j) * HD + col0, o1);
+        }
       }
+      asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");  // gate totals of chunk c + 1
+      finish_gates(part, ci + 1);
+    }
+    if (FOLD) {
+      float* dst = (partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+    } else if (a.hT && seg == a.S - 1) {
+      float* dst = a.hT + (bh * HD + r) * HD + col0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
     }
   }
-
-  if (FOLD) {
-    float* dst = (partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-  } else if (a.hT && seg == a.S - 1) {
-    float* dst = a.hT + (bh * HD + r) * HD + col0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-  }
-  if (!ok && a.status && lane == 0) atomicOr(a.status, 1);
+  if (!ok && a.status) atomicOr(a.status, 1);
   tc::fence_before();
   __syncthreads();
-  if (warp == 0) tc::dealloc(tmem, 128);
+  if (warp == 0) tc::dealloc(tmem, 256);
 }
 
 template <bool FOLD>
