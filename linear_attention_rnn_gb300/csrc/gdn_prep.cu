@@ -7,192 +7,101 @@
 //   gates  G = chunk-local cumsum of g, gamma = exp(G)               (per value head)
 //   S = tril(diag(beta) (K K^T * M), -1),  M_rs = exp(G_r - G_s) for s <= r,
 //       the exponent masked before exp so nothing overflows
-//   P = (Q K^T) * M, diagonal included                               (for the output)
+//   P = (Q K^T) * M, diagonal included (same exponentials as S)      (for the output)
 //   T = (I + S)^-1 by the blockwise doubling ladder
-//   w = T diag(beta gamma) K,  u = T diag(beta) V                     tcgen05 products
+//   u = T' V and w = T' (diag(gamma) K) with T' = T diag(beta)        tcgen05 products
 // The ladder ("Fuse the Gated Delta Net inter-chunk scan into a Pallas TPU
 // kernel", section "Changes", triangular inversion kernel): with X the inverse
 // of I + S on its diagonal blocks of size b, the inverse on blocks of size 2b
 // is X - X S_l X, S_l the lower-left b x b block of each 2b x 2b diagonal
 // block.  The 16 x 16 diagonal blocks are inverted exactly in fp32 by forward
-// substitution (one warp per block; the ladder's levels b = 1..8 in one exact
-// step) and the levels b = 16, 32, 64 run on the tensor cores with two-term
-// bf16 operand splitting (hi*hi + hi*lo + lo*hi, fp32 accumulate), keeping T
-// at fp32-like accuracy.  At level b the only new block is the lower-left one,
-// -X_D S_C X_A, computed as Y = S_C X_A, then -X_D Y.
-// w and u take T rounded to bf16 after the column scaling, as tensor-core
-// operands; they are bf16 outputs themselves.
+// substitution (the ladder's levels b = 1..8 in one exact step) and the levels
+// b = 16, 32, 64 run on the tensor cores.
+//
+// Precision: S and T are held as pairs of bf16 tiles (x = hi + lo, hi =
+// bf16(x), lo = bf16(x - hi): about 16 significant bits), so every ladder
+// operand is a plain ldmatrix load; a product is hi*hi + hi*lo + lo*hi with
+// fp32 accumulation.  The zero blocks of the triangular factors are skipped.
+// T' and diag(gamma) K are rounded to bf16 as tensor-core operands; w and u
+// are bf16 outputs themselves.
+//
+// Operands arrive by TMA in the 128-byte-swizzled layout: K and Q serve
+// K K^T and Q K^T as K-major operands, and K (scaled) and V serve w and u as
+// MN-major B operands, so nothing is transposed in shared memory.  V of the
+// next value head is requested while the current one is processed (the Q
+// buffer takes the odd heads once Q K^T has completed).
 #include "gdn_kernels.cuh"
 #include "gdn_tc05.cuh"
+#include "gdn_tmap.cuh"
 
 namespace gdn {
 
 namespace {
 
-constexpr int LDF = HD + 4;  // fp32 row stride of the S/T tile (float4 rows, 16-byte aligned)
-constexpr int LDY = 64 + 4;  // fp32 row stride of the ladder scratch
+constexpr uint32_t TILE = CH * HD * 2;  // 32 KiB bf16 tile
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct PrepSmem {
-  bf16 Q[CH * HD];   // SW128 [s][d]: Q, then V^T of the current value head ([v][s])
-  bf16 K[CH * HD];   // SW128 [s][d]
-  bf16 Kt[CH * HD];  // SW128 [d][s]
-  bf16 Tp[CH * HD];  // SW128: raw V staging, then T' = T diag(scale) (A operand of w, u)
-  float F[CH * LDF];  // S, overwritten in place by T
-  float Y[64 * LDY];
-  float Gl[CH], beta[CH], gamma[CH], bg[CH];
-  uint64_t bar;
+  unsigned char Q[TILE];   // SW128 [s][d]: Q; after Q K^T, V of the odd value heads
+  unsigned char K[TILE];   // SW128 [s][d]
+  unsigned char V[TILE];   // SW128 [s][v]: V of the even value heads
+  unsigned char Kg[TILE];  // SW128 [s][d]: diag(gamma) K of the current value head
+  unsigned char Tp[TILE];  // SW128 [r][s]: T diag(beta); during the inverse its scratch
+  bf16 Fh[CH * CH];        // S, overwritten in place by T: high parts (XOR-swizzled rows)
+  bf16 Fl[CH * CH];        // low parts
+  float Gl[CH], beta[CH], gamma[CH];
+  uint64_t barKQ, barV[2], barM;
   uint32_t tmem;
-  int err;
+};
+// scratch of the inverse inside Tp
+constexpr uint32_t Y_HI = 0, Y_LO = 8192, SD = 16384;  // Y: [64][64] bf16 pair; Sd: [8][16][16] fp32
+
+struct PrepMaps {
+  CUtensorMap q, k, v;
 };
 
-// rows [0, rows) of a [128 x 128] bf16 global tile (row stride gstride) into a
-// K-major SW128 shared tile; rows past `rows` are zero-filled
-__device__ __forceinline__ void load_sw128_async(bf16* s, const bf16* g, long gstride, int rows,
-                                                 int tid) {
-  unsigned char* sb = reinterpret_cast<unsigned char*>(s);
+// [rows][64] bf16 tile with 128-byte rows, 16-byte chunk j of row r at j ^ (r & 7)
+__device__ __forceinline__ bf16* swz64(bf16* base, int r, int j) {
+  return base + r * 64 + ((j ^ (r & 7)) << 3);
+}
+
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  split_bf16(x0, x1, hi, lo);
+}
+// eight fp32 values -> hi and lo 16-byte chunks
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
+  split2(v[0], v[1], hi.x, lo.x);
+  split2(v[2], v[3], hi.y, lo.y);
+  split2(v[4], v[5], hi.z, lo.z);
+  split2(v[6], v[7], hi.w, lo.w);
+}
+__device__ __forceinline__ void join8(const uint4& hi, const uint4& lo, float* v) {
+  const uint32_t h[4] = {hi.x, hi.y, hi.z, hi.w}, l[4] = {lo.x, lo.y, lo.z, lo.w};
 #pragma unroll
-  for (int i = 0; i < (CH * 16) / NTHREADS; ++i) {
-    const int idx = tid + i * NTHREADS;
-    const int r = idx >> 4, j = idx & 15;
-    const bool ok = r < rows;
-    cp_async16(sb + tc::sw128_chunk(r, j, CH), g + (ok ? (long)r * gstride + j * 8 : 0), ok);
+  for (int i = 0; i < 4; ++i) {
+    const float2 a = unpack_bf16(h[i]), b = unpack_bf16(l[i]);
+    v[2 * i] = a.x + b.x;
+    v[2 * i + 1] = a.y + b.y;
   }
 }
 
-// dst[c][r] = src[r][c] for two [128 x 128] K-major SW128 tiles; one 8 x 8 block per thread
-__device__ __forceinline__ void transpose_sw128(const bf16* src, bf16* dst, int tid) {
-  const unsigned char* sb = reinterpret_cast<const unsigned char*>(src);
-  unsigned char* db = reinterpret_cast<unsigned char*>(dst);
-  const int br = tid >> 4, bc = tid & 15;  // source rows 8br.., source columns 8bc..
-  uint32_t in[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 u = *reinterpret_cast<const uint4*>(sb + tc::sw128_chunk(8 * br + i, bc, CH));
-    in[i][0] = u.x;
-    in[i][1] = u.y;
-    in[i][2] = u.z;
-    in[i][3] = u.w;
-  }
-  // element (i, c) of the block: half (c & 1) of word in[i][c >> 1]
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint32_t w[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const uint32_t lo = in[2 * p][c >> 1], hi = in[2 * p + 1][c >> 1];
-      w[p] = (c & 1) ? __byte_perm(lo, hi, 0x7632) : __byte_perm(lo, hi, 0x5410);
-    }
-    *reinterpret_cast<uint4*>(db + tc::sw128_chunk(8 * bc + c, br, CH)) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
+// d += A B for a 16 x 16 A and two 8-column B tiles, each operand a hi + lo pair
+__device__ __forceinline__ void mma_pair(float (&d0)[4], float (&d1)[4], const uint32_t (&ah)[4],
+                                         const uint32_t (&al)[4], const uint32_t (&bh)[4],
+                                         const uint32_t (&bl)[4]) {
+  mma16816(d0, ah, bh[0], bh[1]);
+  mma16816(d0, ah, bl[0], bl[1]);
+  mma16816(d0, al, bh[0], bh[1]);
+  mma16816(d1, ah, bh[2], bh[3]);
+  mma16816(d1, ah, bl[2], bl[3]);
+  mma16816(d1, al, bh[2], bh[3]);
 }
 
-// 16x16 fp32 block (row-major, stride lda) times 16x8 fp32 block ([k][n],
-// stride ldb), fp32-accurate via two-term bf16 splitting.
-__device__ __forceinline__ void mma_split(float (&d)[4], const float* pa, int lda,
-                                          const float* pb, int ldb, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  const float2 x0 = *reinterpret_cast<const float2*>(pa + g * lda + 2 * t);
-  const float2 x1 = *reinterpret_cast<const float2*>(pa + (g + 8) * lda + 2 * t);
-  const float2 x2 = *reinterpret_cast<const float2*>(pa + g * lda + 2 * t + 8);
-  const float2 x3 = *reinterpret_cast<const float2*>(pa + (g + 8) * lda + 2 * t + 8);
-  uint32_t ah[4], al[4];
-  split_bf16(x0.x, x0.y, ah[0], al[0]);
-  split_bf16(x1.x, x1.y, ah[1], al[1]);
-  split_bf16(x2.x, x2.y, ah[2], al[2]);
-  split_bf16(x3.x, x3.y, ah[3], al[3]);
-  uint32_t bh0, bl0, bh1, bl1;
-  split_bf16(pb[(2 * t) * ldb + g], pb[(2 * t + 1) * ldb + g], bh0, bl0);
-  split_bf16(pb[(2 * t + 8) * ldb + g], pb[(2 * t + 9) * ldb + g], bh1, bl1);
-  mma16816(d, ah, bh0, bh1);
-  mma16816(d, ah, bl0, bl1);
-  mma16816(d, al, bh0, bh1);
+// B fragments (k0..k0+15, n0..n0+15) of a row-major [k][n] [64 x 64] tile
+__device__ __forceinline__ void ldb_kn_64(uint32_t (&b)[4], bf16* base, int k0, int n0, int lane) {
+  ldsm_x4_t(b, swz64(base, k0 + (lane & 15), (n0 >> 3) + (lane >> 4)));
 }
 
-// T = (I + S)^-1 in place in F (all threads of the CTA).
-__device__ __forceinline__ void ut_inverse(PrepSmem& sm, int warp, int lane) {
-  const int g4 = lane >> 2, t4 = lane & 3;
-  // (1) exact forward substitution of the 16x16 diagonal block of this warp;
-  //     lane j (< 16) carries column j of the block in t[]
-  {
-    const int base = 16 * warp;
-    const int jl = lane & 15;
-    float t[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float* srow = &sm.F[(base + i) * LDF + base];
-      float x = (jl == i) ? 1.f : 0.f;
-#pragma unroll
-      for (int s = 0; s < i; ++s) x -= srow[s] * t[s];
-      t[i] = x;
-    }
-    __syncwarp();
-    if (lane < 16) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) sm.F[(base + i) * LDF + base + lane] = t[i];
-    }
-  }
-  __syncthreads();
-  // (2) ladder levels b = 16, 32, 64 on the lower-left blocks
-  for (int bs = 16; bs < CH; bs *= 2) {
-    const int tiles_m = bs / 16, tiles_n = bs / 8;
-    const int per_pair = tiles_m * tiles_n;
-    const int ntiles = (CH / (2 * bs)) * per_pair;
-    for (int tile = warp; tile < ntiles; tile += 8) {
-      const int p = tile / per_pair, rem = tile % per_pair;
-      const int tm = rem / tiles_n, tn = rem % tiles_n;
-      const int s0 = p * 2 * bs;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int k0 = 0; k0 < bs; k0 += 16)
-        mma_split(d, &sm.F[(s0 + bs + 16 * tm) * LDF + s0 + k0], LDF,
-                  &sm.F[(s0 + k0) * LDF + s0 + 8 * tn], LDF, lane);
-      float* y0 = &sm.Y[(p * bs + 16 * tm + g4) * LDY + 8 * tn + 2 * t4];
-      y0[0] = d[0];
-      y0[1] = d[1];
-      y0[8 * LDY] = d[2];
-      y0[8 * LDY + 1] = d[3];
-    }
-    __syncthreads();
-    for (int tile = warp; tile < ntiles; tile += 8) {
-      const int p = tile / per_pair, rem = tile % per_pair;
-      const int tm = rem / tiles_n, tn = rem % tiles_n;
-      const int s0 = p * 2 * bs;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int k0 = 0; k0 < bs; k0 += 16)
-        mma_split(d, &sm.F[(s0 + bs + 16 * tm) * LDF + s0 + bs + k0], LDF,
-                  &sm.Y[(p * bs + k0) * LDY + 8 * tn], LDY, lane);
-      float* o0 = &sm.F[(s0 + bs + 16 * tm + g4) * LDF + s0 + 8 * tn + 2 * t4];
-      o0[0] = -d[0];
-      o0[1] = -d[1];
-      o0[8 * LDF] = -d[2];
-      o0[8 * LDF + 1] = -d[3];
-    }
-    __syncthreads();
-  }
-}
-
-// T' = T diag(scale) rounded to bf16 into the SW128 tile Tp.
-__device__ __forceinline__ void build_tprime(PrepSmem& sm, const float* scale, int tid) {
-  unsigned char* tb = reinterpret_cast<unsigned char*>(sm.Tp);
-#pragma unroll
-  for (int i = 0; i < (CH * 16) / NTHREADS; ++i) {
-    const int idx = tid + i * NTHREADS;
-    const int r = idx >> 4, j = idx & 15;
-    const float4 a = *reinterpret_cast<const float4*>(&sm.F[r * LDF + 8 * j]);
-    const float4 b = *reinterpret_cast<const float4*>(&sm.F[r * LDF + 8 * j + 4]);
-    const float4 sa = *reinterpret_cast<const float4*>(&scale[8 * j]);
-    const float4 sb = *reinterpret_cast<const float4*>(&scale[8 * j + 4]);
-    uint4 o;
-    o.x = pack_bf16(a.x * sa.x, a.y * sa.y);
-    o.y = pack_bf16(a.z * sa.z, a.w * sa.w);
-    o.z = pack_bf16(b.x * sb.x, b.y * sb.y);
-    o.w = pack_bf16(b.z * sb.z, b.w * sb.w);
-    *reinterpret_cast<uint4*>(tb + tc::sw128_chunk(r, j, CH)) = o;
-  }
-}
-
-// 64 columns (half hh) of this thread's TMEM row -> bf16 in global memory:
-// columns 0..31 to dst0, 32..63 to dst1
 __device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, bf16* dst0, bf16* dst1) {
 #pragma unroll
   for (int cb = 0; cb < 64; cb += 32) {
@@ -211,7 +120,99 @@ __device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, bf16* dst0, bf1
   }
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a) {
+// element (r, c) of a [128 x 128] XOR-swizzled bf16 tile
+__device__ __forceinline__ bf16* fel(bf16* base, int r, int c) { return swz(base, r, c >> 3) + (c & 7); }
+
+// the two halves of a 16 x 16 accumulator pair (rows r, r + 8; columns
+// 2t4.. of n-tile h) -> hi/lo 32-bit words at element pointers given per row
+__device__ __forceinline__ void store_split(bf16* hi0, bf16* lo0, bf16* hi1, bf16* lo1,
+                                            const float (&d)[4], float sign) {
+  uint32_t h, l;
+  split2(sign * d[0], sign * d[1], h, l);
+  *reinterpret_cast<uint32_t*>(hi0) = h;
+  *reinterpret_cast<uint32_t*>(lo0) = l;
+  split2(sign * d[2], sign * d[3], h, l);
+  *reinterpret_cast<uint32_t*>(hi1) = h;
+  *reinterpret_cast<uint32_t*>(lo1) = l;
+}
+
+// T = (I + S)^-1 in place in (Fh, Fl); the fp32 diagonal 16 x 16 blocks of S
+// are in the Sd scratch.  All threads of the CTA.
+__device__ __forceinline__ void ut_inverse(PrepSmem& sm, int warp, int lane) {
+  bf16* Yh = reinterpret_cast<bf16*>(sm.Tp + Y_HI);
+  bf16* Yl = reinterpret_cast<bf16*>(sm.Tp + Y_LO);
+  const float* Sd = reinterpret_cast<const float*>(sm.Tp + SD);
+  const int g4 = lane >> 2, t4 = lane & 3;
+  // (1) exact forward substitution of diagonal block `warp`: lane j (mod 16)
+  //     carries column j; lanes 0-15 store the high parts, 16-31 the low parts
+  {
+    const float* blk = Sd + warp * 256;
+    const int jl = lane & 15;
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float x = (jl == i) ? 1.f : 0.f;
+#pragma unroll
+      for (int s = 0; s < i; ++s) x -= blk[i * 16 + s] * t[s];
+      t[i] = x;
+    }
+    bf16* F = lane < 16 ? sm.Fh : sm.Fl;
+    const int c = 16 * warp + jl;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const bf16 hb = __float2bfloat16_rn(t[i]);
+      *fel(F, 16 * warp + i, c) = lane < 16 ? hb : __float2bfloat16_rn(t[i] - __bfloat162float(hb));
+    }
+  }
+  __syncthreads();
+  // (2) levels b = 16, 32, 64: for every 2b block pair p (rows s0 = 2bp..),
+  //     Y = S_C X_A, then T_C = -X_D Y, in 16 x 16 output tiles
+  for (int bs = 16; bs < CH; bs *= 2) {
+    const int nb = bs >> 4, per = nb * nb;
+    const int ntiles = (CH / (2 * bs)) * per;
+    for (int t = warp; t < ntiles; t += 8) {
+      const int p = t / per, tm = (t % per) / nb, tn = t % nb;
+      const int s0 = 2 * bs * p;
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kb = tn; kb < nb; ++kb) {  // X_A is lower triangular
+        uint32_t ah[4], al[4], bh[4], bl[4];
+        lda_rm_s(ah, sm.Fh, s0 + bs + 16 * tm, s0 + 16 * kb, lane);
+        lda_rm_s(al, sm.Fl, s0 + bs + 16 * tm, s0 + 16 * kb, lane);
+        ldb_kn_s(bh, sm.Fh, s0 + 16 * kb, s0 + 16 * tn, lane);
+        ldb_kn_s(bl, sm.Fl, s0 + 16 * kb, s0 + 16 * tn, lane);
+        mma_pair(d0, d1, ah, al, bh, bl);
+      }
+      const int yr = p * bs + 16 * tm + g4;
+      store_split(swz64(Yh, yr, 2 * tn) + 2 * t4, swz64(Yl, yr, 2 * tn) + 2 * t4,
+                  swz64(Yh, yr + 8, 2 * tn) + 2 * t4, swz64(Yl, yr + 8, 2 * tn) + 2 * t4, d0, 1.f);
+      store_split(swz64(Yh, yr, 2 * tn + 1) + 2 * t4, swz64(Yl, yr, 2 * tn + 1) + 2 * t4,
+                  swz64(Yh, yr + 8, 2 * tn + 1) + 2 * t4, swz64(Yl, yr + 8, 2 * tn + 1) + 2 * t4, d1,
+                  1.f);
+    }
+    __syncthreads();
+    for (int t = warp; t < ntiles; t += 8) {
+      const int p = t / per, tm = (t % per) / nb, tn = t % nb;
+      const int s0 = 2 * bs * p;
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kb = 0; kb <= tm; ++kb) {  // X_D is lower triangular
+        uint32_t ah[4], al[4], bh[4], bl[4];
+        lda_rm_s(ah, sm.Fh, s0 + bs + 16 * tm, s0 + bs + 16 * kb, lane);
+        lda_rm_s(al, sm.Fl, s0 + bs + 16 * tm, s0 + bs + 16 * kb, lane);
+        ldb_kn_64(bh, Yh, p * bs + 16 * kb, 16 * tn, lane);
+        ldb_kn_64(bl, Yl, p * bs + 16 * kb, 16 * tn, lane);
+        mma_pair(d0, d1, ah, al, bh, bl);
+      }
+      const int fr = s0 + bs + 16 * tm + g4, fc = s0 + 16 * tn + 2 * t4;
+      store_split(fel(sm.Fh, fr, fc), fel(sm.Fl, fr, fc), fel(sm.Fh, fr + 8, fc), fel(sm.Fl, fr + 8, fc),
+                  d0, -1.f);
+      store_split(fel(sm.Fh, fr, fc + 8), fel(sm.Fl, fr, fc + 8), fel(sm.Fh, fr + 8, fc + 8),
+                  fel(sm.Fl, fr + 8, fc + 8), d1, -1.f);
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_constant__ PrepMaps mp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   PrepSmem& sm = *reinterpret_cast<PrepSmem*>(base);
@@ -220,65 +221,64 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a) {
   const int group = a.Hv / a.Hk;
   const int t0 = c * CH;
   const int L = min(CH, a.T - t0);
-  const long tokstride = (long)a.Hk * HD;
-  const bf16* kgl = a.k + (((long)b * a.T + t0) * a.Hk + kh) * HD;
-  const bf16* qgl = a.q + (((long)b * a.T + t0) * a.Hk + kh) * HD;
-  const bool needP = a.P != nullptr;
-  const bool needU = a.U != nullptr;
+  const bool needP = a.P != nullptr, needU = a.U != nullptr, needW = a.W != nullptr;
   // TMEM row of this thread in the epilogues: lane quarter of the warp, column half
   const int quarter = warp & 3, hh = warp >> 2;
   const int row = 32 * quarter + lane;
-  const long tileP = (long)CH * CH;  // w, u and P tiles: [128][128] row-major
-  const int ldP = CH;
+  const long tile = (long)CH * CH;  // w, u and P tiles: [128][128] row-major in global memory
 
-  load_sw128_async(sm.K, kgl, tokstride, L, tid);
-  if (needP) load_sw128_async(sm.Q, qgl, tokstride, L, tid);
-  cp_async_commit();
-  if (warp == 0) tc::alloc(&sm.tmem, 512);
+  // V of value head kh * group + jj into buffer jj % 2 (thread 0)
+  auto load_v = [&](int jj) {
+    unsigned char* dst = (jj & 1) ? sm.Q : sm.V;
+    uint64_t* bar = &sm.barV[jj & 1];
+    tc::arrive_expect_tx(bar, TILE);
+    tc::tma_load_4d(dst, &mp.v, 0, kh * group + jj, t0, b, bar);
+    tc::tma_load_4d(dst + TILE / 2, &mp.v, 64, kh * group + jj, t0, b, bar);
+  };
   if (tid == 0) {
-    tc::mbar_init(&sm.bar, 1);
+    tc::mbar_init(&sm.barKQ, 1);
+    tc::mbar_init(&sm.barV[0], 1);
+    tc::mbar_init(&sm.barV[1], 1);
+    tc::mbar_init(&sm.barM, 1);
     tc::mbar_fence_init();
-    sm.err = 0;
+    tc::arrive_expect_tx(&sm.barKQ, needP ? 2 * TILE : TILE);
+    tc::tma_load_4d(sm.K, &mp.k, 0, kh, t0, b, &sm.barKQ);
+    tc::tma_load_4d(sm.K + TILE / 2, &mp.k, 64, kh, t0, b, &sm.barKQ);
+    if (needP) {
+      tc::tma_load_4d(sm.Q, &mp.q, 0, kh, t0, b, &sm.barKQ);
+      tc::tma_load_4d(sm.Q + TILE / 2, &mp.q, 64, kh, t0, b, &sm.barKQ);
+    }
+    if (needU) {
+      load_v(0);
+      if (group > 1 && !needP) load_v(1);  // the Q buffer is not needed
+    }
   }
-  cp_async_wait<0>();
-  __syncthreads();
-  transpose_sw128(sm.K, sm.Kt, tid);
-  tc::fence_proxy_async();
+  if (warp == 0) tc::alloc(&sm.tmem, 512);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tmem = sm.tmem;
+  const uint32_t tmem = sm.tmem;  // columns: K K^T 0, Q K^T 128, w 256, u 384
   const uint32_t tlane = tmem + ((uint32_t)(32 * quarter) << 16);
+  bool ok = true;
   if (tid == 0) {
+    ok = tc::mbar_wait(&sm.barKQ, 0);
+    tc::fence_after();
     tc::gemm_k128(tmem + 0, smem_u32(sm.K), smem_u32(sm.K), 128, false);
     if (needP) tc::gemm_k128(tmem + 128, smem_u32(sm.Q), smem_u32(sm.K), 128, false);
-    tc::commit(&sm.bar);
+    tc::commit(&sm.barM);
   }
-  uint32_t phase = 0;
-  bool ok = true;
+  uint32_t mphase = 0;
 
-  for (int jj = 0; jj < group && ok; ++jj) {
+  for (int jj = 0; jj < group; ++jj) {
     const int j = kh * group + jj;
     const long bh = (long)b * a.Hv + j;
     const long chunk_id = bh * a.NC + c;
-    // V_j (raw rows) into the T' buffer; gates of value head j
-    if (needU) {
-      load_sw128_async(sm.Tp, a.v + (((long)b * a.T + t0) * a.Hv + j) * HD, (long)a.Hv * HD, L, tid);
-    }
-    cp_async_commit();
-    float gv = 0.f;
+    // ---- gates of value head j --------------------------------------------------
     if (tid < CH) {
       const long idx = ((long)b * a.T + t0 + tid) * a.Hv + j;
-      gv = tid < L ? a.g[idx] : 0.f;
+      sm.Gl[tid] = tid < L ? a.g[idx] : 0.f;
       sm.beta[tid] = tid < L ? a.beta[idx] : 0.f;
     }
-    if (jj == 0) {  // K K^T and Q K^T are done (they read Q, which V^T overwrites)
-      ok = tc::mbar_wait(&sm.bar, phase);
-      phase ^= 1;
-    }
-    tc::fence_after();
-    __syncthreads();
-    if (tid < CH) sm.Gl[tid] = gv;
     __syncthreads();
     if (warp == 0) {
       float v[4];
@@ -287,132 +287,173 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a) {
       warp_cumsum128(v, lane);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int r = lane * 4 + i;
-        const float gm = expf(v[i]);
-        sm.Gl[r] = v[i] * LOG2E;
-        sm.gamma[r] = gm;
-        sm.bg[r] = sm.beta[r] * gm;
+        sm.Gl[lane * 4 + i] = v[i] * LOG2E;
+        sm.gamma[lane * 4 + i] = expf(v[i]);
       }
     }
-    cp_async_wait<0>();
+    if (jj == 0) {  // K K^T, Q K^T complete; K readable
+      ok = ok && tc::mbar_wait(&sm.barKQ, 0);
+      ok = ok && tc::mbar_wait(&sm.barM, mphase);
+      mphase ^= 1;
+      tc::fence_after();
+    }
+    if (tid == 0 && needU) {  // prefetch V of the next value head into the free buffer
+      if (jj == 0) {
+        if (group > 1 && needP) load_v(1);  // Q K^T has read Q
+      } else if (jj + 1 < group) {
+        load_v(jj + 1);  // its buffer held V of head jj - 1, whose u is complete
+      }
+    }
     __syncthreads();
-    if (needU) transpose_sw128(sm.Tp, sm.Q, tid);  // V^T: [v][s]
 
-    // ---- S (fp32, into F) and P (bf16, to global) from K K^T and Q K^T -------
+    // ---- diag(gamma) K ----------------------------------------------------------------
+#pragma unroll
+    for (int i = 0; i < (CH * 16) / NTHREADS; ++i) {
+      const int idx = tid + i * NTHREADS;
+      const int r = idx >> 4, jc = idx & 15;
+      const uint32_t off = tc::sw128_chunk(r, jc, CH);
+      const uint4 x = *reinterpret_cast<const uint4*>(sm.K + off);
+      const float gm = sm.gamma[r];
+      const float2 x0 = unpack_bf16(x.x), x1 = unpack_bf16(x.y), x2 = unpack_bf16(x.z), x3 = unpack_bf16(x.w);
+      uint4 o;
+      o.x = pack_bf16(gm * x0.x, gm * x0.y);
+      o.y = pack_bf16(gm * x1.x, gm * x1.y);
+      o.z = pack_bf16(gm * x2.x, gm * x2.y);
+      o.w = pack_bf16(gm * x3.x, gm * x3.y);
+      *reinterpret_cast<uint4*>(sm.Kg + off) = o;
+    }
+
+    // ---- S (hi/lo into F, fp32 diagonal blocks into Sd) and P (to global) ----------
     {
       const float Glr = sm.Gl[row], br = sm.beta[row];
-      const bool upper = (64 * hh) >= (32 * quarter + 32);  // block entirely above the diagonal
+      float* Sd = reinterpret_cast<float*>(sm.Tp + SD);
+      bf16* prow = needP ? a.P + chunk_id * tile + (long)row * CH : nullptr;
 #pragma unroll
-      for (int cb = 0; cb < 64; cb += 32) {
+      for (int cb = 0; cb < 64; cb += 16) {
         const int c0 = 64 * hh + cb;
-        float v[32];
-        if (!upper) {
-          tc::ld32(tlane + c0, v);
+        float sv[16], pv[16];
+        if (c0 <= 32 * quarter + 31) {  // warp-uniform: the block reaches the diagonal
+          float kk[16];
+          tc::ld16(tlane + c0, kk);
+          if (needP) tc::ld16(tlane + 128 + c0, pv);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             const int s = c0 + i;
-            v[i] = (s < row) ? br * v[i] * exp2f(Glr - sm.Gl[s]) : 0.f;
+            const float m = (s <= row) ? exp2f(Glr - sm.Gl[s]) : 0.f;
+            sv[i] = (s < row) ? br * kk[i] * m : 0.f;
+            pv[i] = needP ? pv[i] * m : 0.f;
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          for (int i = 0; i < 16; ++i) sv[i] = pv[i] = 0.f;
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4*>(&sm.F[row * LDF + c0 + 4 * q]) =
-              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      }
-      if (needP) {
-        bf16* prow = a.P + chunk_id * tileP + (long)row * ldP + 64 * hh;
+        for (int q = 0; q < 2; ++q) {
+          uint4 hi, lo;
+          split8(sv + 8 * q, hi, lo);
+          *reinterpret_cast<uint4*>(swz(sm.Fh, row, (c0 >> 3) + q)) = hi;
+          *reinterpret_cast<uint4*>(swz(sm.Fl, row, (c0 >> 3) + q)) = lo;
+        }
+        if (((row >> 4) << 4) == c0) {  // this row's diagonal block, kept in fp32
+          float* sd = Sd + (row >> 4) * 256 + (row & 15) * 16;
 #pragma unroll
-        for (int cb = 0; cb < 64; cb += 32) {
-          const int c0 = 64 * hh + cb;
-          float v[32];
-          if (!upper) {
-            tc::ld32(tlane + 128 + c0, v);
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(sd + 4 * q) = make_float4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
+        }
+        if (needP) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int s = c0 + i;
-              v[i] = (s <= row) ? v[i] * exp2f(Glr - sm.Gl[s]) : 0.f;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 2; ++q) {
             uint4 o;
-            o.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
-            o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-            o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-            o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-            *reinterpret_cast<uint4*>(prow + cb + 8 * q) = o;
+            o.x = pack_bf16(pv[8 * q + 0], pv[8 * q + 1]);
+            o.y = pack_bf16(pv[8 * q + 2], pv[8 * q + 3]);
+            o.z = pack_bf16(pv[8 * q + 4], pv[8 * q + 5]);
+            o.w = pack_bf16(pv[8 * q + 6], pv[8 * q + 7]);
+            *reinterpret_cast<uint4*>(prow + c0 + 8 * q) = o;
           }
         }
       }
     }
+    tc::fence_proxy_async();  // diag(gamma) K is read by the tensor core
     __syncthreads();
+    auto export_f32 = [&](float* dst) {
+      for (int i = tid; i < CH * 16; i += NTHREADS) {
+        const int r = i >> 4, jc = i & 15;
+        float v[8];
+        join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
+        *reinterpret_cast<float4*>(dst + r * CH + 8 * jc) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(dst + r * CH + 8 * jc + 4) = make_float4(v[4], v[5], v[6], v[7]);
+      }
+    };
     if (a.S_dbg) {
-      float* dst = a.S_dbg + chunk_id * CH * CH;
-      for (int i = tid; i < CH * CH; i += NTHREADS) dst[i] = sm.F[(i >> 7) * LDF + (i & 127)];
+      export_f32(a.S_dbg + chunk_id * tile);
       __syncthreads();
     }
 
     // ---- T = (I + S)^-1 -------------------------------------------------------------
     ut_inverse(sm, warp, lane);
-    if (a.T_dbg) {
-      float* dst = a.T_dbg + chunk_id * CH * CH;
-      for (int i = tid; i < CH * CH; i += NTHREADS) dst[i] = sm.F[(i >> 7) * LDF + (i & 127)];
-    }
+    if (a.T_dbg) export_f32(a.T_dbg + chunk_id * tile);
     if (a.Tb) {
-      bf16* dst = a.Tb + chunk_id * CH * CH;
-      for (int i = tid; i < CH * CH / 2; i += NTHREADS) {
-        const int r = (2 * i) >> 7, cc = (2 * i) & 127;
-        *reinterpret_cast<uint32_t*>(dst + 2 * i) = pack_bf16(sm.F[r * LDF + cc], sm.F[r * LDF + cc + 1]);
+      bf16* dst = a.Tb + chunk_id * tile;
+      for (int i = tid; i < CH * 16; i += NTHREADS) {
+        const int r = i >> 4, jc = i & 15;
+        float v[8];
+        join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
+        uint4 o;
+        o.x = pack_bf16(v[0], v[1]);
+        o.y = pack_bf16(v[2], v[3]);
+        o.z = pack_bf16(v[4], v[5]);
+        o.w = pack_bf16(v[6], v[7]);
+        *reinterpret_cast<uint4*>(dst + r * CH + 8 * jc) = o;
       }
     }
-    // ---- w = T diag(beta gamma) K --------------------------------------------------
-    if (a.W) {
-      build_tprime(sm, sm.bg, tid);
-      tc::fence_proxy_async();
-      tc::fence_before();
-      __syncthreads();
-      tc::fence_after();
-      if (tid == 0) {
-        tc::gemm_k128(tmem + 256, smem_u32(sm.Tp), smem_u32(sm.Kt), 128, false);
-        tc::commit(&sm.bar);
+    // ---- T' = T diag(beta) (bf16, K-major SW128) --------------------------------------
+#pragma unroll
+    for (int i = 0; i < (CH * 16) / NTHREADS; ++i) {
+      const int idx = tid + i * NTHREADS;
+      const int r = idx >> 4, jc = idx & 15;
+      float v[8];
+      join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
+      const float4 b0 = *reinterpret_cast<const float4*>(&sm.beta[8 * jc]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&sm.beta[8 * jc + 4]);
+      uint4 o;
+      o.x = pack_bf16(v[0] * b0.x, v[1] * b0.y);
+      o.y = pack_bf16(v[2] * b0.z, v[3] * b0.w);
+      o.z = pack_bf16(v[4] * b1.x, v[5] * b1.y);
+      o.w = pack_bf16(v[6] * b1.z, v[7] * b1.w);
+      *reinterpret_cast<uint4*>(sm.Tp + tc::sw128_chunk(r, jc, CH)) = o;
+    }
+    tc::fence_proxy_async();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    // ---- u = T' V,  w = T' diag(gamma) K ------------------------------------------------
+    if (tid == 0) {
+      if (needU) {
+        ok = ok && tc::mbar_wait(&sm.barV[jj & 1], (uint32_t)((jj >> 1) & 1));
+        tc::fence_after();
+        tc::gemm_bmn_k128(tmem + 384, smem_u32(sm.Tp), smem_u32((jj & 1) ? sm.Q : sm.V), false);
       }
-      ok = ok && tc::mbar_wait(&sm.bar, phase);
-      phase ^= 1;
+      if (needW) tc::gemm_bmn_k128(tmem + 256, smem_u32(sm.Tp), smem_u32(sm.Kg), false);
+      if (needU || needW) tc::commit(&sm.barM);
+    }
+    if (needU || needW) {
+      ok = ok && tc::mbar_wait(&sm.barM, mphase);
+      mphase ^= 1;
       tc::fence_after();
-      bf16* wrow = a.W + chunk_id * tileP + (long)row * ldP + 64 * hh;
+    }
+    if (needW) {
+      bf16* wrow = a.W + chunk_id * tile + (long)row * CH + 64 * hh;
       tmem_row_to_bf16(tlane + 256 + 64 * hh, wrow, wrow + 32);
-      tc::fence_before();
-      __syncthreads();  // the w product has finished reading T'
-      tc::fence_after();
     }
-    // ---- u = T diag(beta) V ----------------------------------------------------------
     if (needU) {
-      build_tprime(sm, sm.beta, tid);
-      tc::fence_proxy_async();
-      tc::fence_before();
-      __syncthreads();
-      tc::fence_after();
-      if (tid == 0) {
-        tc::gemm_k128(tmem + 384, smem_u32(sm.Tp), smem_u32(sm.Q), 128, false);
-        tc::commit(&sm.bar);
-      }
-      ok = ok && tc::mbar_wait(&sm.bar, phase);
-      phase ^= 1;
-      tc::fence_after();
-      bf16* urow = a.U + chunk_id * CH * HD + (long)row * HD + 64 * hh;
+      bf16* urow = a.U + chunk_id * tile + (long)row * HD + 64 * hh;
       tmem_row_to_bf16(tlane + 384 + 64 * hh, urow, urow + 32);
     }
     tc::fence_before();
-    __syncthreads();  // T', V^T and F are free for the next value head
+    __syncthreads();  // TMEM w/u, Tp, Kg, F and the gate vectors are free for the next value head
     tc::fence_after();
   }
-  if (!ok && a.status && lane == 0) atomicOr(a.status, 1);
+  if (!ok && a.status) atomicOr(a.status, 1);
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, 512);
@@ -423,11 +464,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a) {
 size_t prep_smem_bytes() { return sizeof(PrepSmem) + 1024; }
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
+  PrepMaps mp;
+  memset(&mp, 0, sizeof mp);
+  if (!tmap_heads(&mp.k, a.k, a.B, a.T, a.Hk, HD)) return cudaErrorInvalidValue;
+  if (a.P && !tmap_heads(&mp.q, a.q, a.B, a.T, a.Hk, HD)) return cudaErrorInvalidValue;
+  if (a.U && !tmap_heads(&mp.v, a.v, a.B, a.T, a.Hv, HD)) return cudaErrorInvalidValue;
   const size_t smem = prep_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.NC, a.Hk, a.B);
-  k_prep<<<grid, NTHREADS, smem, s>>>(a);
+  k_prep<<<grid, NTHREADS, smem, s>>>(a, mp);
   return cudaGetLastError();
 }
 

@@ -106,6 +106,21 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // ---- mbarriers --------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
@@ -178,6 +193,22 @@ __device__ __forceinline__ void gemm_amn_k128(uint32_t tmem_d, uint32_t a_smem, 
     const uint64_t da = desc_sw128_mn(a_smem + (uint32_t)k * 2048u, 128u * 128u);
     const uint32_t koff = (uint32_t)(k & 3) * 32u;
     const uint64_t db = desc_sw128(b_smem + (uint32_t)(k >> 2) * (uint32_t)N * 128u + koff);
+    mma(tmem_d, da, db, idesc, (k > 0 || accumulate_first) ? 1u : 0u);
+  }
+}
+
+// D[128 x 128] (+)= A * B where A is a K-major [128 x 128] SW128 tile and B
+// (K = 128 rows, N = 128 columns) is stored MN-major: the [K rows x N] SW128
+// tile as a tiled load of a row-major [K][N] matrix lands it (two 64-column
+// atoms 16 KiB apart, 128-byte rows along K)
+__device__ __forceinline__ void gemm_bmn_k128(uint32_t tmem_d, uint32_t a_smem, uint32_t b_smem,
+                                              bool accumulate_first) {
+  const uint32_t idesc = idesc_bf16(128, 128) | (1u << 16);  // B is MN-major
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t koff = (uint32_t)(k & 3) * 32u;
+    const uint64_t da = desc_sw128(a_smem + (uint32_t)(k >> 2) * 128u * 128u + koff);
+    const uint64_t db = desc_sw128_mn(b_smem + (uint32_t)k * 2048u, 128u * 128u);
     mma(tmem_d, da, db, idesc, (k > 0 || accumulate_first) ? 1u : 0u);
   }
 }
