@@ -39,15 +39,14 @@ FLOPS = {  # per (chunk, value head), per kernel
     "walk_states": 2 * FLOP_FULL,         # w h, k_g^T Delta
     "walk_bwd": 3 * FLOP_FULL + FLOP_TRI,  # K dh', Q^T dO, w^T dDelta, P^T dO
     "grads": 3 * FLOP_FULL + 9 * FLOP_TRI,
-    "reduce": 0,
 }
 FWD_KERNELS = ["prep", "walk"]
-BWD_KERNELS = ["prep", "walk_states", "walk_bwd", "grads", "reduce"]
+BWD_KERNELS = ["prep", "walk_states", "walk_bwd", "grads"]
 FWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk"]
 BWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk_states", "fold_bwd", "prefix_bwd",
-                   "walk_bwd", "grads", "reduce"]
+                   "walk_bwd", "grads"]
 KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<false>", "walk_states": "k_walk_fwd<false>",
-                 "walk_bwd": "k_walk_bwd<false>", "grads": "k_grads", "reduce": "k_reduce_dqdk",
+                 "walk_bwd": "k_walk_bwd<false>", "grads": "k_grads",
                  "fold": "k_walk_fwd<true>", "prefix": "k_affine_walk",
                  "fold_bwd": "k_walk_bwd<true>", "prefix_bwd": "k_affine_walk"}
 # DRAM traffic per launch from the committed ncu capture of the same kernels

@@ -50,7 +50,7 @@ Dims make_dims(int B, int T, int Hk, int Hv, int n_segments) {
 // bf16 entering states, Delta, the state cotangents, dDelta and the fp32
 // per-value-head dq/dk.
 struct Layout {
-  size_t status, W, U, P, Tb, pairA, pairB, hin, states, delta, dstates, ddelta, dqp, dkp, total;
+  size_t status, W, U, P, Tb, pairA, pairB, hin, states, delta, dstates, ddelta, total;
 };
 
 Layout layout(const Dims& d, bool bwd) {
@@ -80,9 +80,6 @@ Layout layout(const Dims& d, bool bwd) {
     L.delta = take(chunks * tile);
     L.dstates = take(chunks * tile);
     L.ddelta = take(chunks * tile);
-    const size_t part = (size_t)d.B * d.T * d.Hv * HD * sizeof(float);
-    L.dqp = take(part);
-    L.dkp = take(part);
   }
   L.total = off;
   return L;
@@ -367,7 +364,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
     if (!rc) rc = mk.rec();
   }
   if (rc) return rc;
-  // 4. chunk-parallel gradients, then the key-head sums of dq and dk
+  // 4. chunk-parallel gradients (dq and dk summed over the value heads of each key head)
   GradArgs ga;
   memset(&ga, 0, sizeof ga);
   ga.q = static_cast<const bf16*>(q);
@@ -381,8 +378,9 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   ga.dstates = at<bf16>(ws, L.dstates);
   ga.delta = at<bf16>(ws, L.delta);
   ga.ddelta = at<bf16>(ws, L.ddelta);
-  ga.dq_part = at<float>(ws, L.dqp);
-  ga.dk_part = at<float>(ws, L.dkp);
+  ga.dq = static_cast<bf16*>(dq);
+  ga.dk = static_cast<bf16*>(dk);
+  ga.status = at<int>(ws, L.status);
   ga.dv = static_cast<bf16*>(dv);
   ga.dg = dg;
   ga.dbeta = dbeta;
@@ -392,9 +390,6 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   ga.Hv = Hv;
   ga.NC = d.NC;
   rc = cuda_status(launch_grads(ga, s));
-  if (rc || (rc = mk.rec())) return rc;
-  rc = cuda_status(launch_reduce_dqdk(ga.dq_part, ga.dk_part, static_cast<bf16*>(dq),
-                                      static_cast<bf16*>(dk), tokens, Hk, Hv, s));
   return rc ? rc : mk.rec();
 }
 

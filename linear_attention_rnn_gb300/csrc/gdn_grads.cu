@@ -1,9 +1,10 @@
 // gdn_grads.cu -- chunk-parallel gradients of the chunked gated delta rule.
 //
-// One CTA per (chunk c, value head j, batch row b), given the chunk's entering
-// state h, the cotangent dh' of the state it leaves, Delta = u - w h and
-// dDelta = P^T dO + k_g dh' (both stored by the two walks), and T.  Writing
-// dV' = T^T dDelta, each line below reverses one line of the chunk forward:
+// One CTA per (chunk c, key head, batch row b) serves the value heads j that
+// share the key head, given for each the chunk's entering state h, the
+// cotangent dh' of the state it leaves, Delta = u - w h and dDelta = P^T dO +
+// k_g dh' (both stored by the two walks), and T.  Writing dV' = T^T dDelta,
+// each line below reverses one line of the chunk forward:
 //   u = T diag(beta) V        ->  dV = diag(beta) dV',  dbeta += rowsum(dV' * V)
 //   w = T diag(beta gamma) K  ->  dK += -diag(beta gamma) dV' h^T, d(beta gamma) from it
 //   T = (I + S)^-1            ->  dS = -(T^T dT T^T), strictly lower
@@ -16,567 +17,505 @@
 // in the equal form dS = -dV' Delta^T: with dU = dDelta and dW = -dDelta h^T,
 // dT = dDelta ((I+S) Delta)^T because (I+S) u = diag(beta) V and
 // (I+S) w = diag(beta gamma) K, and T^T ... (I+S)^T T^T = I.
-// dq and dk are written per value head in fp32; a second kernel sums the
-// value heads of each key head.
+//
+// Every product is a 128 x 128 x 128 tcgen05 MMA into tensor memory (TMEM):
+// dK and dQ of the key head accumulate there over its value heads (512
+// columns: dK, dQ, and two scratch products), so dq and dk leave the CTA once,
+// in bf16.  The row-scaled terms (-diag(beta gamma) dV' h^T, diag(ef) Delta
+// dh'^T, diag(gamma) dO h^T) are formed by the epilogue threads from scratch
+// products and written into the accumulators with tcgen05.st; the plain
+// products (dKK K, dKK^T K, dQK^T Q, dQK K) then accumulate onto them.
+// Epilogue thread (row r, half hh) owns TMEM lane r, columns 64 hh .. 64 hh + 63.
+// Operands are SW128 tiles: the stored tiles arrive by TMA, dV', dKK and dQK
+// are written by the epilogues, and each product reads its tiles K-major or
+// MN-major as the product needs (no transposes).
 #include "gdn_kernels.cuh"
+#include "gdn_tc05.cuh"
+#include "gdn_tmap.cuh"
 
 namespace gdn {
 
 namespace {
 
-constexpr int TILE = CH * LDB;
+constexpr uint32_t TILE = CH * HD * 2;
+constexpr float LOG2E = 1.4426950408889634f;
 
 struct GradSmem {
-  bf16 t[6][TILE];
-  float G[CH], gamma[CH], ef[CH], beta[CH], bg[CH];
-  float dbeta[CH], dbg[CH], d_ef[CH], rowX[CH], dgamO[CH];
-  float colX[8][CH];
+  unsigned char K[TILE], Q[TILE];  // SW128 [s][d] of the key head
+  unsigned char W1[TILE];          // T; dV'; dKK
+  unsigned char W2[TILE];          // dDelta; dh'; dO
+  unsigned char W3[TILE];          // h
+  unsigned char W4[TILE];          // Delta; dQK
+  float Gl[CH], gam[CH], ef[CH], beta[CH];
+  float colX[CH], dbeta[CH], dbg[CH], d_ef[CH], rowX[CH], dgamO[CH];
   float red[8];
+  uint64_t barKQ, barT, barDD, barH, barDl, barDH, barDO, barM;
+  uint32_t tmem;
 };
 
-__device__ __forceinline__ float quad_sum(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 1);
-  v += __shfl_xor_sync(0xffffffffu, v, 2);
-  return v;
-}
-// sum over the 8 row-groups g of a warp (lanes with equal t4)
-__device__ __forceinline__ float rows_sum(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 4);
-  v += __shfl_xor_sync(0xffffffffu, v, 8);
-  v += __shfl_xor_sync(0xffffffffu, v, 16);
-  return v;
-}
+// TMEM columns
+constexpr uint32_t C_DK = 0, C_DQ = 128, C_A = 256, C_B = 384;
 
-__device__ __forceinline__ void zero16(float (&acc)[16][4]) {
+// Column sums over the 32 lanes of a warp: lane l holds 32 values of its own
+// row; on return lane l holds the sum of column l (a reduce-scatter butterfly).
+__device__ __forceinline__ float colsum32(float (&x)[32], int lane) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-}
-
-// acc[16 x 128] += A[rows m0..] (row-major tile) * B, B given as [n][k] tile
-// (i.e. the product A X^T for row-major X), over k-steps [ks0, ks1).
-__device__ __forceinline__ void gemm_rm_nk(float (&acc)[16][4], const bf16* A, const bf16* Bnk,
-                                           int m0, int ks0, int ks1, int lane) {
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    if (ks < ks0 || ks >= ks1) continue;
-    uint32_t af[4];
-    lda_rm(af, A, LDB, m0, ks * 16, lane);
-#pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      uint32_t bb[4];
-      ldb_nk(bb, Bnk, LDB, ks * 16, np * 16, lane);
-      mma16816(acc[2 * np], af, bb[0], bb[1]);
-      mma16816(acc[2 * np + 1], af, bb[2], bb[3]);
+    for (int i = 0; i < w; ++i) {
+      const float send = up ? x[i] : x[i + w];
+      const float keep = up ? x[i + w] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
     }
   }
+  return x[0];
 }
-// acc += A * B with A row-major and B row-major [k][n].
-__device__ __forceinline__ void gemm_rm_kn(float (&acc)[16][4], const bf16* A, const bf16* Bkn,
-                                           int m0, int ks0, int ks1, int lane) {
+
+// 32 bf16 values (four 16-byte chunks) of row r, columns c0.., of a K-major SW128 tile
+__device__ __forceinline__ void row32_load(const unsigned char* tile, int r, int c0, float (&v)[32]) {
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    if (ks < ks0 || ks >= ks1) continue;
-    uint32_t af[4];
-    lda_rm(af, A, LDB, m0, ks * 16, lane);
-#pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      uint32_t bb[4];
-      ldb_kn(bb, Bkn, LDB, ks * 16, np * 16, lane);
-      mma16816(acc[2 * np], af, bb[0], bb[1]);
-      mma16816(acc[2 * np + 1], af, bb[2], bb[3]);
-    }
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + tc::sw128_chunk(r, (c0 >> 3) + q, CH));
+    const float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y), c = unpack_bf16(u.z), d = unpack_bf16(u.w);
+    v[8 * q + 0] = a.x;
+    v[8 * q + 1] = a.y;
+    v[8 * q + 2] = b.x;
+    v[8 * q + 3] = b.y;
+    v[8 * q + 4] = c.x;
+    v[8 * q + 5] = c.y;
+    v[8 * q + 6] = d.x;
+    v[8 * q + 7] = d.y;
   }
 }
-// acc += A^T * B with A stored row-major (so A^T is read transposed) and B row-major [k][n].
-__device__ __forceinline__ void gemm_tr_kn(float (&acc)[16][4], const bf16* At, const bf16* Bkn,
-                                           int m0, int ks0, int ks1, int lane) {
+__device__ __forceinline__ void row32_store(unsigned char* tile, int r, int c0, const float (&v)[32]) {
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    if (ks < ks0 || ks >= ks1) continue;
-    uint32_t af[4];
-    lda_tr(af, At, LDB, m0, ks * 16, lane);
+  for (int q = 0; q < 4; ++q) {
+    uint4 o;
+    o.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+    o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(tile + tc::sw128_chunk(r, (c0 >> 3) + q, CH)) = o;
+  }
+}
+__device__ __forceinline__ void global32_store(bf16* dst, const float (&v)[32], float scale) {
 #pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      uint32_t bb[4];
-      ldb_kn(bb, Bkn, LDB, ks * 16, np * 16, lane);
-      mma16816(acc[2 * np], af, bb[0], bb[1]);
-      mma16816(acc[2 * np + 1], af, bb[2], bb[3]);
-    }
+  for (int q = 0; q < 4; ++q) {
+    uint4 o;
+    o.x = pack_bf16(scale * v[8 * q + 0], scale * v[8 * q + 1]);
+    o.y = pack_bf16(scale * v[8 * q + 2], scale * v[8 * q + 3]);
+    o.z = pack_bf16(scale * v[8 * q + 4], scale * v[8 * q + 5]);
+    o.w = pack_bf16(scale * v[8 * q + 6], scale * v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(dst + 8 * q) = o;
   }
 }
 
-__device__ __forceinline__ float2 ld_bf2(const bf16* p) {
-  return unpack_bf16(*reinterpret_cast<const uint32_t*>(p));
-}
+struct GradMaps {
+  CUtensorMap k, q, dO, Tb, ddelta, states, delta, dstates;
+};
 
-__global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  GradSmem& sm = *reinterpret_cast<GradSmem*>(smem_raw);
-  bf16* t0 = sm.t[0];
-  bf16* t1 = sm.t[1];
-  bf16* t2 = sm.t[2];
-  bf16* t3 = sm.t[3];
-  bf16* t4 = sm.t[4];
-  bf16* t5 = sm.t[5];
-  const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+__global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_constant__ GradMaps mp) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  GradSmem& sm = *reinterpret_cast<GradSmem*>(base);
+  const int c = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g4 = lane >> 2, q4 = lane & 3;
-  const int kh = j / (a.Hv / a.Hk);
-  const int tk0 = c * CH;
-  const int L = min(CH, a.T - tk0);
-  const long bh = (long)b * a.Hv + j;
-  const long cid = bh * a.NC + c;
-  const long tokq = ((long)b * a.T + tk0) * a.Hk + kh;  // row 0 of the q/k tile
-  const long tokv = ((long)b * a.T + tk0) * a.Hv + j;   // row 0 of the v/dO tile
-  const int m0 = warp * 16;
-  const int r0 = m0 + g4, r1 = r0 + 8;
+  const int group = a.Hv / a.Hk;
+  const int t0 = c * CH;
+  const int L = min(CH, a.T - t0);
+  const int quarter = warp & 3, hh = warp >> 2;
+  const int row = 32 * quarter + lane;
+  const long tokq = ((long)b * a.T + t0) * a.Hk + kh;  // row 0 of the q/k tile
 
-  // group A: T, dDelta.  group B: h, Delta, K.
-  tile_load_async(t0, a.Tb + cid * CH * CH, CH, CH, tid);
-  tile_load_async(t1, a.ddelta + cid * CH * HD, HD, CH, tid);
-  cp_async_commit();
-  tile_load_async(t3, a.states + cid * HD * HD, HD, HD, tid);
-  tile_load_async(t4, a.delta + cid * CH * HD, HD, CH, tid);
-  tile_load_async(t5, a.k + tokq * HD, (long)a.Hk * HD, L, tid);
-  cp_async_commit();
-  if (tid < CH) {
-    const long idx = tokv + (long)tid * a.Hv;
-    sm.beta[tid] = tid < L ? a.beta[idx] : 0.f;
-    sm.G[tid] = tid < L ? a.g[idx] : 0.f;
-    sm.dbeta[tid] = 0.f;
-    sm.rowX[tid] = 0.f;
+  auto cid_of = [&](int jj) { return ((long)b * a.Hv + kh * group + jj) * a.NC + c; };
+  auto load2d = [&](unsigned char* dst, const CUtensorMap* m, long cid, uint64_t* bar) {
+    tc::arrive_expect_tx(bar, TILE);
+    tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
+    tc::tma_load_2d(dst + TILE / 2, m, 64, (int)(cid * CH), bar);
+  };
+  auto load4d = [&](unsigned char* dst, const CUtensorMap* m, int head, uint64_t* bar) {
+    tc::tma_load_4d(dst, m, 0, head, t0, b, bar);
+    tc::tma_load_4d(dst + TILE / 2, m, 64, head, t0, b, bar);
+  };
+  if (tid == 0) {
+    tc::mbar_init(&sm.barKQ, 1);
+    tc::mbar_init(&sm.barT, 1);
+    tc::mbar_init(&sm.barDD, 1);
+    tc::mbar_init(&sm.barH, 1);
+    tc::mbar_init(&sm.barDl, 1);
+    tc::mbar_init(&sm.barDH, 1);
+    tc::mbar_init(&sm.barDO, 1);
+    tc::mbar_init(&sm.barM, 1);
+    tc::mbar_fence_init();
+    tc::arrive_expect_tx(&sm.barKQ, 2 * TILE);
+    load4d(sm.K, &mp.k, kh, &sm.barKQ);
+    load4d(sm.Q, &mp.q, kh, &sm.barKQ);
+    const long cid0 = cid_of(0);
+    load2d(sm.W1, &mp.Tb, cid0, &sm.barT);
+    load2d(sm.W2, &mp.ddelta, cid0, &sm.barDD);
+    load2d(sm.W3, &mp.states, cid0, &sm.barH);
+    load2d(sm.W4, &mp.delta, cid0, &sm.barDl);
   }
-  for (int i = tid; i < 8 * CH; i += NTHREADS) (&sm.colX[0][0])[i] = 0.f;
+  if (warp == 0) tc::alloc(&sm.tmem, 512);
+  tc::fence_before();
   __syncthreads();
-  if (warp == 0) {
-    float v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = sm.G[lane * 4 + i];
-    warp_cumsum128(v, lane);
-    const float Glast = __shfl_sync(0xffffffffu, v[3], 31);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = lane * 4 + i;
-      sm.G[r] = v[i];
-      sm.gamma[r] = expf(v[i]);
-      sm.ef[r] = expf(Glast - v[i]);
-      sm.bg[r] = sm.beta[r] * sm.gamma[r];
+  tc::fence_after();
+  const uint32_t tmem = sm.tmem;
+  const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16) + 64u * hh;  // lane row, column half
+  bool ok = true;
+  uint32_t mc = 0;  // completed-commit count of barM seen by this thread
+  auto wait_mma = [&]() {
+    ok = ok && tc::mbar_wait(&sm.barM, mc & 1);
+    ++mc;
+    tc::fence_after();
+  };
+  auto sync_operands = [&]() {  // epilogue-written operand tiles -> tensor core
+    tc::fence_proxy_async();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+  };
+  if (tid == 0) ok = tc::mbar_wait(&sm.barKQ, 0);
+  ok = ok && tc::mbar_wait(&sm.barKQ, 0);  // K and Q rows are read by the epilogues too
+
+  for (int jj = 0; jj < group; ++jj) {
+    const int j = kh * group + jj;
+    const long cid = cid_of(jj);
+    const long tokv = ((long)b * a.T + t0) * a.Hv + j;  // row 0 of the v/dO tile
+    const uint32_t par = (uint32_t)(jj & 1);
+    // ---- gates of value head j; per-row sums cleared ----------------------------
+    if (tid < CH) {
+      const long idx = tokv + (long)tid * a.Hv;
+      sm.Gl[tid] = tid < L ? a.g[idx] : 0.f;
+      sm.beta[tid] = tid < L ? a.beta[idx] : 0.f;
+      sm.colX[tid] = sm.dbeta[tid] = sm.dbg[tid] = sm.d_ef[tid] = sm.rowX[tid] = sm.dgamO[tid] = 0.f;
     }
+    if (tid == 0) {  // S1: dV' = T^T dDelta (both tiles read MN-major)
+      ok = ok && tc::mbar_wait(&sm.barT, par);
+      ok = ok && tc::mbar_wait(&sm.barDD, par);
+      tc::fence_after();
+      tc::gemm128(tmem + C_A, smem_u32(sm.W1), true, smem_u32(sm.W2), true, false);
+      tc::commit(&sm.barM);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = sm.Gl[lane * 4 + i];
+      warp_cumsum128(v, lane);
+      const float Glast = __shfl_sync(0xffffffffu, v[3], 31);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane * 4 + i;
+        sm.Gl[r] = v[i] * LOG2E;
+        sm.gam[r] = expf(v[i]);
+        sm.ef[r] = expf(Glast - v[i]);
+      }
+    }
+    __syncthreads();
+    const float Glr = sm.Gl[row], br = sm.beta[row], gr = sm.gam[row], efr = sm.ef[row];
+    const float bgr = br * gr;
+    float p_db = 0.f, p_dbg = 0.f, p_def = 0.f, p_rowx = 0.f, p_dgam = 0.f;
+
+    // ---- E1: dv = diag(beta) dV';  dbeta += rowsum(dV' V);  dV' -> W1 ----------------
+    wait_mma();
+    if (tid == 0) load2d(sm.W2, &mp.dstates, cid, &sm.barDH);  // dDelta has been read
+#pragma unroll
+    for (int cb = 0; cb < 64; cb += 32) {
+      const int c0 = 64 * hh + cb;
+      float x[32];
+      tc::ld32(tl + C_A + cb, x);
+      if (row < L) {
+        const long off = (tokv + (long)row * a.Hv) * HD + c0;
+        global32_store(a.dv + off, x, br);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 u = *reinterpret_cast<const uint4*>(a.v + off + 8 * q);
+          const float2 v0 = unpack_bf16(u.x), v1 = unpack_bf16(u.y), v2 = unpack_bf16(u.z), v3 = unpack_bf16(u.w);
+          p_db += x[8 * q] * v0.x + x[8 * q + 1] * v0.y + x[8 * q + 2] * v1.x + x[8 * q + 3] * v1.y +
+                  x[8 * q + 4] * v2.x + x[8 * q + 5] * v2.y + x[8 * q + 6] * v3.x + x[8 * q + 7] * v3.y;
+        }
+      }
+      row32_store(sm.W1, row, c0, x);
+    }
+    sync_operands();
+
+    // ---- S2: dV' h^T -> A;  S5: Delta dh'^T -> B --------------------------------------
+    if (tid == 0) {
+      ok = ok && tc::mbar_wait(&sm.barH, par);
+      ok = ok && tc::mbar_wait(&sm.barDl, par);
+      ok = ok && tc::mbar_wait(&sm.barDH, par);
+      tc::fence_after();
+      tc::gemm128(tmem + C_A, smem_u32(sm.W1), false, smem_u32(sm.W3), false, false);
+      tc::gemm128(tmem + C_B, smem_u32(sm.W4), false, smem_u32(sm.W2), false, false);
+      tc::commit(&sm.barM);
+    }
+    {  // <dh', h>: elementwise over two tiles of the same layout
+      ok = ok && tc::mbar_wait(&sm.barDH, par);
+      ok = ok && tc::mbar_wait(&sm.barH, par);
+      float d = 0.f;
+#pragma unroll
+      for (int i = 0; i < (int)(TILE / 16) / NTHREADS; ++i) {
+        const uint32_t off = (uint32_t)(tid + i * NTHREADS) * 16u;
+        const uint4 x = *reinterpret_cast<const uint4*>(sm.W2 + off);
+        const uint4 y = *reinterpret_cast<const uint4*>(sm.W3 + off);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 p = unpack_bf16(xs[e]), q = unpack_bf16(ys[e]);
+          d += p.x * q.x + p.y * q.y;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      if (lane == 0) sm.red[warp] = d;
+    }
+
+    // ---- E2: dK (+)= -diag(beta gamma) dV' h^T + diag(ef) Delta dh'^T ---------------------
+    wait_mma();
+#pragma unroll
+    for (int cb = 0; cb < 64; cb += 32) {
+      const int c0 = 64 * hh + cb;
+      float kv[32], x[32], acc[32];
+      row32_load(sm.K, row, c0, kv);
+      if (jj > 0) {
+        tc::ld32(tl + C_DK + cb, acc);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+      }
+      tc::ld32(tl + C_A + cb, x);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        p_dbg -= x[i] * kv[i];
+        acc[i] -= bgr * x[i];
+      }
+      tc::ld32(tl + C_B + cb, x);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        p_def += x[i] * kv[i];
+        acc[i] += efr * x[i];
+      }
+      tc::st32(tl + C_DK + cb, acc);
+    }
+    tc::wait_st();
+    tc::fence_before();
+    __syncthreads();  // also: every thread is done with dh' (W2)
+    tc::fence_after();
+
+    // ---- S3: ds = dV' Delta^T -> A;  K K^T -> B ----------------------------------------
+    if (tid == 0) {
+      tc::arrive_expect_tx(&sm.barDO, TILE);
+      load4d(sm.W2, &mp.dO, j, &sm.barDO);
+      tc::gemm128(tmem + C_A, smem_u32(sm.W1), false, smem_u32(sm.W4), false, false);
+      tc::gemm128(tmem + C_B, smem_u32(sm.K), false, smem_u32(sm.K), false, false);
+      tc::commit(&sm.barM);
+    }
+    // ---- E3: dKK = -(ds * M) diag-row(beta), strictly lower -> W1; dbeta, rowX, colX -----
+    wait_mma();
+#pragma unroll
+    for (int cb = 0; cb < 64; cb += 32) {
+      const int c0 = 64 * hh + cb;
+      float out[32];
+      if (c0 <= 32 * quarter + 31) {  // warp-uniform: the block reaches the diagonal
+        float ds[32], kk[32];
+        tc::ld32(tl + C_A + cb, ds);
+        tc::ld32(tl + C_B + cb, kk);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int s = c0 + i;
+          const bool lower = s < row;
+          const float M = lower ? exp2f(Glr - sm.Gl[s]) : 0.f;
+          const float dS = lower ? -ds[i] : 0.f;
+          p_db += dS * kk[i] * M;
+          const float dkk = dS * br * M;
+          out[i] = dkk;
+          ds[i] = dkk * kk[i];
+          p_rowx += ds[i];
+        }
+        const float cs = colsum32(ds, lane);
+        atomicAdd(&sm.colX[c0 + lane], cs);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) out[i] = 0.f;
+      }
+      row32_store(sm.W1, row, c0, out);
+    }
+    sync_operands();
+
+    // ---- S4: dK += dKK K + dKK^T K;  S6: dP = dO Delta^T -> A;  Q K^T -> B -------------
+    if (tid == 0) {
+      tc::gemm128(tmem + C_DK, smem_u32(sm.W1), false, smem_u32(sm.K), true, true);
+      tc::gemm128(tmem + C_DK, smem_u32(sm.W1), true, smem_u32(sm.K), true, true);
+      ok = ok && tc::mbar_wait(&sm.barDO, par);
+      tc::fence_after();
+      tc::gemm128(tmem + C_A, smem_u32(sm.W2), false, smem_u32(sm.W4), false, false);
+      tc::gemm128(tmem + C_B, smem_u32(sm.Q), false, smem_u32(sm.K), false, false);
+      tc::commit(&sm.barM);
+    }
+    // ---- E4: dQK = dP * M (diagonal included) -> W4; rowX, colX --------------------------
+    wait_mma();
+#pragma unroll
+    for (int cb = 0; cb < 64; cb += 32) {
+      const int c0 = 64 * hh + cb;
+      float out[32];
+      if (c0 <= 32 * quarter + 31) {
+        float dp[32], qk[32];
+        tc::ld32(tl + C_A + cb, dp);
+        tc::ld32(tl + C_B + cb, qk);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int s = c0 + i;
+          const float M = (s <= row) ? exp2f(Glr - sm.Gl[s]) : 0.f;
+          const float d = dp[i] * M;
+          out[i] = d;
+          dp[i] = d * qk[i];
+          p_rowx += dp[i];
+        }
+        const float cs = colsum32(dp, lane);
+        atomicAdd(&sm.colX[c0 + lane], cs);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) out[i] = 0.f;
+      }
+      row32_store(sm.W4, row, c0, out);
+    }
+    sync_operands();
+
+    // ---- S7: dK += dQK^T Q;  S8: dO h^T -> A -------------------------------------------
+    if (tid == 0) {
+      tc::gemm128(tmem + C_DK, smem_u32(sm.W4), true, smem_u32(sm.Q), true, true);
+      tc::gemm128(tmem + C_A, smem_u32(sm.W2), false, smem_u32(sm.W3), false, false);
+      tc::commit(&sm.barM);
+    }
+    // ---- E5: dgamma_O = rowsum(Q * (dO h^T));  dQ (+)= diag(gamma) dO h^T ------------------
+    wait_mma();
+    if (tid == 0 && jj + 1 < group) {  // next value head: its T, dDelta, h (tiles consumed)
+      const long nc = cid_of(jj + 1);
+      load2d(sm.W1, &mp.Tb, nc, &sm.barT);
+      load2d(sm.W2, &mp.ddelta, nc, &sm.barDD);
+      load2d(sm.W3, &mp.states, nc, &sm.barH);
+    }
+#pragma unroll
+    for (int cb = 0; cb < 64; cb += 32) {
+      const int c0 = 64 * hh + cb;
+      float qv[32], x[32], acc[32];
+      row32_load(sm.Q, row, c0, qv);
+      tc::ld32(tl + C_A + cb, x);
+      if (jj > 0) {
+        tc::ld32(tl + C_DQ + cb, acc);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        p_dgam += x[i] * qv[i];
+        acc[i] += gr * x[i];
+      }
+      tc::st32(tl + C_DQ + cb, acc);
+    }
+    tc::wait_st();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    // ---- S8b: dQ += dQK K ----------------------------------------------------------------
+    if (tid == 0) {
+      tc::gemm128(tmem + C_DQ, smem_u32(sm.W4), false, smem_u32(sm.K), true, true);
+      tc::commit(&sm.barM);
+    }
+    atomicAdd(&sm.dbeta[row], p_db);
+    atomicAdd(&sm.dbg[row], p_dbg);
+    atomicAdd(&sm.d_ef[row], p_def);
+    atomicAdd(&sm.rowX[row], p_rowx);
+    atomicAdd(&sm.dgamO[row], p_dgam);
+    wait_mma();
+    if (tid == 0 && jj + 1 < group) load2d(sm.W4, &mp.delta, cid_of(jj + 1), &sm.barDl);
+    __syncthreads();
+
+    // ---- gate cotangents of value head j ----------------------------------------------
+    if (warp == 0) {
+      float dgC = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) dgC += sm.red[w];
+      float sum_def = 0.f;
+      float dG[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane * 4 + i;
+        const float de = sm.d_ef[r] * sm.ef[r];
+        sum_def += de;
+        const float dgam = sm.dgamO[r] + sm.beta[r] * sm.dbg[r];
+        dG[i] = sm.gam[r] * dgam + sm.rowX[r] - sm.colX[r] - de;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum_def += __shfl_xor_sync(0xffffffffu, sum_def, off);
+      if (lane == 31) dG[3] += sm.gam[CH - 1] * dgC + sum_def;  // row C-1: gamma_C = gamma[C-1]
+      // reverse inclusive cumsum over the 128 rows: dg_s = sum_{r >= s} dG_r
+      const float tot = dG[0] + dG[1] + dG[2] + dG[3];
+      float incl = tot;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_down_sync(0xffffffffu, incl, off);
+        if (lane + off < 32) incl += o;
+      }
+      float run = incl - tot;  // sum over lanes > lane
+      float dg[4];
+#pragma unroll
+      for (int i = 3; i >= 0; --i) {
+        run += dG[i];
+        dg[i] = run;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane * 4 + i;
+        if (r < L) {
+          a.dg[tokv + (long)r * a.Hv] = dg[i];
+          a.dbeta[tokv + (long)r * a.Hv] = sm.dbeta[r] + sm.gam[r] * sm.dbg[r];
+        }
+      }
+    }
+    __syncthreads();
   }
-  cp_async_wait<1>();
+
+  // ---- dq, dk of the key head ----------------------------------------------------------
+#pragma unroll
+  for (int cb = 0; cb < 64; cb += 32) {
+    const int c0 = 64 * hh + cb;
+    const long off = (tokq + (long)row * a.Hk) * HD + c0;
+    float x[32];
+    tc::ld32(tl + C_DQ + cb, x);
+    if (row < L) global32_store(a.dq + off, x, 1.f);
+    tc::ld32(tl + C_DK + cb, x);
+    if (row < L) global32_store(a.dk + off, x, 1.f);
+  }
+  if (!ok && a.status) atomicOr(a.status, 1);
+  tc::fence_before();
   __syncthreads();
-
-  float acc[16][4], tmp[16][4];
-
-  // ---- S1: dV' = T^T dDelta;  dv = beta dV';  dbeta += rowsum(dV' V) ---------
-  zero16(tmp);
-  gemm_tr_kn(tmp, t0, t1, m0, warp, 8, lane);  // T^T upper triangular: k >= m
-  {
-    const float b0 = sm.beta[r0], b1 = sm.beta[r1];
-    float s0 = 0.f, s1 = 0.f;
-    const bf16* vrow0 = a.v + (tokv + (long)r0 * a.Hv) * HD;
-    const bf16* vrow1 = a.v + (tokv + (long)r1 * a.Hv) * HD;
-    bf16* dv0 = a.dv + (tokv + (long)r0 * a.Hv) * HD;
-    bf16* dv1 = a.dv + (tokv + (long)r1 * a.Hv) * HD;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int col = nt * 8 + 2 * q4;
-      if (r0 < L) {
-        const float2 vv = ld_bf2(vrow0 + col);
-        s0 += tmp[nt][0] * vv.x + tmp[nt][1] * vv.y;
-        *reinterpret_cast<uint32_t*>(dv0 + col) = pack_bf16(b0 * tmp[nt][0], b0 * tmp[nt][1]);
-      }
-      if (r1 < L) {
-        const float2 vv = ld_bf2(vrow1 + col);
-        s1 += tmp[nt][2] * vv.x + tmp[nt][3] * vv.y;
-        *reinterpret_cast<uint32_t*>(dv1 + col) = pack_bf16(b1 * tmp[nt][2], b1 * tmp[nt][3]);
-      }
-      *reinterpret_cast<uint32_t*>(t2 + r0 * LDB + col) = pack_bf16(tmp[nt][0], tmp[nt][1]);
-      *reinterpret_cast<uint32_t*>(t2 + r1 * LDB + col) = pack_bf16(tmp[nt][2], tmp[nt][3]);
-    }
-    s0 = quad_sum(s0);
-    s1 = quad_sum(s1);
-    if (q4 == 0) {
-      sm.dbeta[r0] += s0;
-      sm.dbeta[r1] += s1;
-    }
-  }
-  __syncthreads();  // T, dDelta consumed; dV' complete
-  // group C: dh' -> t1
-  tile_load_async(t1, a.dstates + cid * HD * HD, HD, HD, tid);
-  cp_async_commit();
-  cp_async_wait<1>();
-  __syncthreads();  // h, Delta, K ready
-
-  // ---- S2: dK = -diag(beta gamma) dV' h^T;  dbg = rowsum(-(dV' h^T) K) --------
-  zero16(tmp);
-  gemm_rm_nk(tmp, t2, t3, m0, 0, 8, lane);
-  {
-    const float c0 = -sm.bg[r0], c1 = -sm.bg[r1];
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int col = nt * 8 + 2 * q4;
-      const float2 k0 = ld_bf2(t5 + r0 * LDB + col), k1 = ld_bf2(t5 + r1 * LDB + col);
-      s0 -= tmp[nt][0] * k0.x + tmp[nt][1] * k0.y;
-      s1 -= tmp[nt][2] * k1.x + tmp[nt][3] * k1.y;
-      acc[nt][0] = c0 * tmp[nt][0];
-      acc[nt][1] = c0 * tmp[nt][1];
-      acc[nt][2] = c1 * tmp[nt][2];
-      acc[nt][3] = c1 * tmp[nt][3];
-    }
-    s0 = quad_sum(s0);
-    s1 = quad_sum(s1);
-    if (q4 == 0) {
-      sm.dbg[r0] = s0;
-      sm.dbg[r1] = s1;
-    }
-  }
-  cp_async_wait<0>();
-  __syncthreads();  // dh' ready
-
-  // ---- S5: dK += diag(ef) Delta dh'^T;  d_ef = rowsum((Delta dh'^T) K);  <dh', h>
-  zero16(tmp);
-  gemm_rm_nk(tmp, t4, t1, m0, 0, 8, lane);
-  {
-    const float e0 = sm.ef[r0], e1 = sm.ef[r1];
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int col = nt * 8 + 2 * q4;
-      const float2 k0 = ld_bf2(t5 + r0 * LDB + col), k1 = ld_bf2(t5 + r1 * LDB + col);
-      s0 += tmp[nt][0] * k0.x + tmp[nt][1] * k0.y;
-      s1 += tmp[nt][2] * k1.x + tmp[nt][3] * k1.y;
-      acc[nt][0] += e0 * tmp[nt][0];
-      acc[nt][1] += e0 * tmp[nt][1];
-      acc[nt][2] += e1 * tmp[nt][2];
-      acc[nt][3] += e1 * tmp[nt][3];
-    }
-    s0 = quad_sum(s0);
-    s1 = quad_sum(s1);
-    if (q4 == 0) {
-      sm.d_ef[r0] = s0;
-      sm.d_ef[r1] = s1;
-    }
-    // <dh', h>: 128 x 128 elements, 64 per thread
-    float d = 0.f;
-    for (int i = tid; i < HD * HD / 2; i += NTHREADS) {
-      const int r = (2 * i) >> 7, cc = (2 * i) & 127;
-      const float2 x = ld_bf2(t1 + r * LDB + cc), y = ld_bf2(t3 + r * LDB + cc);
-      d += x.x * y.x + x.y * y.y;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-    if (lane == 0) sm.red[warp] = d;
-  }
-  __syncthreads();  // dh' consumed
-  // group E: dO -> t1
-  tile_load_async(t1, a.dO + tokv * HD, (long)a.Hv * HD, L, tid);
-  cp_async_commit();
-
-  // ---- S3: dS = -dV' Delta^T (strict lower);  KK;  dKK -> t0 --------------------
-  {
-    const float G0 = sm.G[r0], G1 = sm.G[r1], b0 = sm.beta[r0], b1 = sm.beta[r1];
-    float db0 = 0.f, db1 = 0.f, x0 = 0.f, x1 = 0.f;
-#pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      if (np > warp) continue;
-      float ds[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float kk[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t af[4], bb[4];
-        lda_rm(af, t2, LDB, m0, ks * 16, lane);
-        ldb_nk(bb, t4, LDB, ks * 16, np * 16, lane);
-        mma16816(ds[0], af, bb[0], bb[1]);
-        mma16816(ds[1], af, bb[2], bb[3]);
-        lda_rm(af, t5, LDB, m0, ks * 16, lane);
-        ldb_nk(bb, t5, LDB, ks * 16, np * 16, lane);
-        mma16816(kk[0], af, bb[0], bb[1]);
-        mma16816(kk[1], af, bb[2], bb[3]);
-      }
-      float cs[2][2];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int s = np * 16 + h2 * 8 + 2 * q4 + e;
-          const float Gs = sm.G[s];
-          const float M0 = (s < r0) ? expf(G0 - Gs) : 0.f;
-          const float M1 = (s < r1) ? expf(G1 - Gs) : 0.f;
-          const float dS0 = -ds[h2][e] * (s < r0 ? 1.f : 0.f);
-          const float dS1 = -ds[h2][2 + e] * (s < r1 ? 1.f : 0.f);
-          const float KK0 = kk[h2][e], KK1 = kk[h2][2 + e];
-          db0 += dS0 * KK0 * M0;
-          db1 += dS1 * KK1 * M1;
-          const float dkk0 = dS0 * b0 * M0, dkk1 = dS1 * b1 * M1;
-          ds[h2][e] = dkk0;
-          ds[h2][2 + e] = dkk1;
-          const float X0 = dkk0 * KK0, X1 = dkk1 * KK1;
-          x0 += X0;
-          x1 += X1;
-          cs[h2][e] = X0 + X1;
-        }
-      }
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int col = np * 16 + h2 * 8 + 2 * q4;
-        *reinterpret_cast<uint32_t*>(t0 + r0 * LDB + col) = pack_bf16(ds[h2][0], ds[h2][1]);
-        *reinterpret_cast<uint32_t*>(t0 + r1 * LDB + col) = pack_bf16(ds[h2][2], ds[h2][3]);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float v = rows_sum(cs[h2][e]);
-          if (g4 == 0) sm.colX[warp][col + e] += v;
-        }
-      }
-    }
-    // zero the strictly-upper tiles of dKK this warp did not write
-#pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      if (np <= warp) continue;
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int col = np * 16 + h2 * 8 + 2 * q4;
-        *reinterpret_cast<uint32_t*>(t0 + r0 * LDB + col) = 0u;
-        *reinterpret_cast<uint32_t*>(t0 + r1 * LDB + col) = 0u;
-      }
-    }
-    db0 = quad_sum(db0);
-    db1 = quad_sum(db1);
-    x0 = quad_sum(x0);
-    x1 = quad_sum(x1);
-    if (q4 == 0) {
-      sm.dbeta[r0] += db0;
-      sm.dbeta[r1] += db1;
-      sm.rowX[r0] += x0;
-      sm.rowX[r1] += x1;
-    }
-  }
-  __syncthreads();  // dV' consumed (t2 free); dKK complete
-  // group D: Q -> t2
-  tile_load_async(t2, a.q + tokq * HD, (long)a.Hk * HD, L, tid);
-  cp_async_commit();
-
-  // ---- S4: dK += dKK K + dKK^T K ----------------------------------------------
-  gemm_rm_kn(acc, t0, t5, m0, 0, warp + 1, lane);
-  gemm_tr_kn(acc, t0, t5, m0, warp, 8, lane);
-  cp_async_wait<0>();
-  __syncthreads();  // Q and dO ready; dKK consumed
-
-  // ---- S6: dP = dO Delta^T;  QK;  dQK = dP * M (lower incl.) -> t0 ---------------
-  {
-    const float G0 = sm.G[r0], G1 = sm.G[r1];
-    float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      if (np > warp) continue;
-      float dp[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float qk[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t af[4], bb[4];
-        lda_rm(af, t1, LDB, m0, ks * 16, lane);
-        ldb_nk(bb, t4, LDB, ks * 16, np * 16, lane);
-        mma16816(dp[0], af, bb[0], bb[1]);
-        mma16816(dp[1], af, bb[2], bb[3]);
-        lda_rm(af, t2, LDB, m0, ks * 16, lane);
-        ldb_nk(bb, t5, LDB, ks * 16, np * 16, lane);
-        mma16816(qk[0], af, bb[0], bb[1]);
-        mma16816(qk[1], af, bb[2], bb[3]);
-      }
-      float cs[2][2];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int s = np * 16 + h2 * 8 + 2 * q4 + e;
-          const float Gs = sm.G[s];
-          const float M0 = (s <= r0) ? expf(G0 - Gs) : 0.f;
-          const float M1 = (s <= r1) ? expf(G1 - Gs) : 0.f;
-          const float d0 = dp[h2][e] * M0, d1 = dp[h2][2 + e] * M1;
-          dp[h2][e] = d0;
-          dp[h2][2 + e] = d1;
-          const float X0 = d0 * qk[h2][e], X1 = d1 * qk[h2][2 + e];
-          x0 += X0;
-          x1 += X1;
-          cs[h2][e] = X0 + X1;
-        }
-      }
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int col = np * 16 + h2 * 8 + 2 * q4;
-        *reinterpret_cast<uint32_t*>(t0 + r0 * LDB + col) = pack_bf16(dp[h2][0], dp[h2][1]);
-        *reinterpret_cast<uint32_t*>(t0 + r1 * LDB + col) = pack_bf16(dp[h2][2], dp[h2][3]);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float v = rows_sum(cs[h2][e]);
-          if (g4 == 0) sm.colX[warp][col + e] += v;
-        }
-      }
-    }
-#pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      if (np <= warp) continue;
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int col = np * 16 + h2 * 8 + 2 * q4;
-        *reinterpret_cast<uint32_t*>(t0 + r0 * LDB + col) = 0u;
-        *reinterpret_cast<uint32_t*>(t0 + r1 * LDB + col) = 0u;
-      }
-    }
-    x0 = quad_sum(x0);
-    x1 = quad_sum(x1);
-    if (q4 == 0) {
-      sm.rowX[r0] += x0;
-      sm.rowX[r1] += x1;
-    }
-  }
-  __syncthreads();  // dQK complete
-
-  // ---- S7: dK += dQK^T Q  -> dk (per value head, fp32) ---------------------------
-  gemm_tr_kn(acc, t0, t2, m0, warp, 8, lane);
-  {
-    float* d0 = a.dk_part + (tokv + (long)r0 * a.Hv) * HD;
-    float* d1 = a.dk_part + (tokv + (long)r1 * a.Hv) * HD;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int col = nt * 8 + 2 * q4;
-      if (r0 < L) *reinterpret_cast<float2*>(d0 + col) = make_float2(acc[nt][0], acc[nt][1]);
-      if (r1 < L) *reinterpret_cast<float2*>(d1 + col) = make_float2(acc[nt][2], acc[nt][3]);
-    }
-  }
-
-  // ---- S8: dQ = diag(gamma) dO h^T + dQK K;  dgamma_O = rowsum(Q * (dO h^T)) ---
-  zero16(acc);
-  gemm_rm_nk(acc, t1, t3, m0, 0, 8, lane);
-  {
-    const float gm0 = sm.gamma[r0], gm1 = sm.gamma[r1];
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int col = nt * 8 + 2 * q4;
-      const float2 q0 = ld_bf2(t2 + r0 * LDB + col), q1 = ld_bf2(t2 + r1 * LDB + col);
-      s0 += acc[nt][0] * q0.x + acc[nt][1] * q0.y;
-      s1 += acc[nt][2] * q1.x + acc[nt][3] * q1.y;
-      acc[nt][0] *= gm0;
-      acc[nt][1] *= gm0;
-      acc[nt][2] *= gm1;
-      acc[nt][3] *= gm1;
-    }
-    s0 = quad_sum(s0);
-    s1 = quad_sum(s1);
-    if (q4 == 0) {
-      sm.dgamO[r0] = s0;
-      sm.dgamO[r1] = s1;
-    }
-  }
-  gemm_rm_kn(acc, t0, t5, m0, 0, warp + 1, lane);
-  {
-    float* d0 = a.dq_part + (tokv + (long)r0 * a.Hv) * HD;
-    float* d1 = a.dq_part + (tokv + (long)r1 * a.Hv) * HD;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int col = nt * 8 + 2 * q4;
-      if (r0 < L) *reinterpret_cast<float2*>(d0 + col) = make_float2(acc[nt][0], acc[nt][1]);
-      if (r1 < L) *reinterpret_cast<float2*>(d1 + col) = make_float2(acc[nt][2], acc[nt][3]);
-    }
-  }
-  __syncthreads();  // all row/column vectors complete
-
-  // ---- S9: gate cotangents -------------------------------------------------------
-  if (warp == 0) {
-    float dgC = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) dgC += sm.red[w];
-    float sum_def = 0.f;
-    float dG[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = lane * 4 + i;
-      float col = 0.f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) col += sm.colX[w][r];
-      const float de = sm.d_ef[r] * sm.ef[r];
-      sum_def += de;
-      const float dgam = sm.dgamO[r] + sm.beta[r] * sm.dbg[r];
-      dG[i] = sm.gamma[r] * dgam + sm.rowX[r] - col - de;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum_def += __shfl_xor_sync(0xffffffffu, sum_def, off);
-    if (lane == 31) dG[3] += sm.gamma[CH - 1] * dgC + sum_def;  // row C-1: gamma_C = gamma[C-1]
-    // reverse inclusive cumsum over the 128 rows: dg_s = sum_{r >= s} dG_r
-    float tot = dG[0] + dG[1] + dG[2] + dG[3];
-    float incl = tot;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float o = __shfl_down_sync(0xffffffffu, incl, off);
-      if (lane + off < 32) incl += o;
-    }
-    float run = incl - tot;  // sum over lanes > lane
-    float dg[4];
-#pragma unroll
-    for (int i = 3; i >= 0; --i) {
-      run += dG[i];
-      dg[i] = run;
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = lane * 4 + i;
-      if (r < L) {
-        a.dg[tokv + (long)r * a.Hv] = dg[i];
-        a.dbeta[tokv + (long)r * a.Hv] = sm.dbeta[r] + sm.gamma[r] * sm.dbg[r];
-      }
-    }
-  }
-}
-
-__global__ void k_reduce_dqdk(const float* __restrict__ dqp, const float* __restrict__ dkp,
-                              bf16* __restrict__ dq, bf16* __restrict__ dk, long tokens, int Hk,
-                              int Hv) {
-  const int group = Hv / Hk;
-  const long n4 = tokens * Hk * (HD / 4);
-  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x) {
-    const long tk = i / (Hk * (HD / 4));
-    const int rem = (int)(i % (Hk * (HD / 4)));
-    const int kh = rem / (HD / 4), c4 = (rem % (HD / 4)) * 4;
-    float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
-    for (int r = 0; r < group; ++r) {
-      const long src = (tk * Hv + kh * group + r) * HD + c4;
-      const float4 x = *reinterpret_cast<const float4*>(dqp + src);
-      const float4 y = *reinterpret_cast<const float4*>(dkp + src);
-      sq.x += x.x; sq.y += x.y; sq.z += x.z; sq.w += x.w;
-      sk.x += y.x; sk.y += y.y; sk.z += y.z; sk.w += y.w;
-    }
-    const long dst = (tk * Hk + kh) * HD + c4;
-    uint2 oq, ok;
-    oq.x = pack_bf16(sq.x, sq.y);
-    oq.y = pack_bf16(sq.z, sq.w);
-    ok.x = pack_bf16(sk.x, sk.y);
-    ok.y = pack_bf16(sk.z, sk.w);
-    *reinterpret_cast<uint2*>(dq + dst) = oq;
-    *reinterpret_cast<uint2*>(dk + dst) = ok;
-  }
+  if (warp == 0) tc::dealloc(tmem, 512);
 }
 
 }  // namespace
 
-size_t grad_smem_bytes() { return sizeof(GradSmem); }
+size_t grad_smem_bytes() { return sizeof(GradSmem) + 1024; }
 
 cudaError_t launch_grads(const GradArgs& a, cudaStream_t s) {
-  const size_t smem = sizeof(GradSmem);
+  GradMaps mp;
+  memset(&mp, 0, sizeof mp);
+  const uint64_t rows = (uint64_t)a.B * a.Hv * a.NC * CH;
+  bool ok = tmap_heads(&mp.k, a.k, a.B, a.T, a.Hk, HD) && tmap_heads(&mp.q, a.q, a.B, a.T, a.Hk, HD) &&
+            tmap_heads(&mp.dO, a.dO, a.B, a.T, a.Hv, HD);
+  ok = ok && tmap_2d(&mp.Tb, a.Tb, CH, rows, CH * 2, 64, CH, true);
+  ok = ok && tmap_2d(&mp.ddelta, a.ddelta, HD, rows, HD * 2, 64, CH, true);
+  ok = ok && tmap_2d(&mp.states, a.states, HD, rows, HD * 2, 64, CH, true);
+  ok = ok && tmap_2d(&mp.delta, a.delta, HD, rows, HD * 2, 64, CH, true);
+  ok = ok && tmap_2d(&mp.dstates, a.dstates, HD, rows, HD * 2, 64, CH, true);
+  if (!ok) return cudaErrorInvalidValue;
+  const size_t smem = grad_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_grads<<<dim3(a.NC, a.Hv, a.B), NTHREADS, smem, s>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_reduce_dqdk(const float* dq_part, const float* dk_part, bf16* dq, bf16* dk,
-                               long tokens, int Hk, int Hv, cudaStream_t s) {
-  const long n4 = tokens * Hk * (HD / 4);
-  if (n4 == 0) return cudaSuccess;
-  long blocks = (n4 + 255) / 256;
-  if (blocks > 152L * 16) blocks = 152L * 16;
-  k_reduce_dqdk<<<(int)blocks, 256, 0, s>>>(dq_part, dk_part, dq, dk, tokens, Hk, Hv);
+  k_grads<<<dim3(a.NC, a.Hk, a.B), NTHREADS, smem, s>>>(a, mp);
   return cudaGetLastError();
 }
 

@@ -101,11 +101,12 @@ struct GradArgs {
   const bf16* dstates;  // [BH][NC][HD][HD]  cotangent of h leaving chunk
   const bf16* delta;    // [BH][NC][CH][HD]
   const bf16* ddelta;   // [BH][NC][CH][HD]
-  float* dq_part;       // [B,T,Hv,HD] fp32 per value head
-  float* dk_part;       // [B,T,Hv,HD]
+  bf16* dq;             // [B,T,Hk,HD]
+  bf16* dk;             // [B,T,Hk,HD]
   bf16* dv;             // [B,T,Hv,HD]
   float* dg;            // [B,T,Hv]
   float* dbeta;         // [B,T,Hv]
+  int* status;          // bit 0 set if a bounded wait gave up (nullable)
   int B, T, Hk, Hv, NC;
 };
 
@@ -120,7 +121,5 @@ cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int fold, cudaStream_t s);
 cudaError_t launch_affine_walk(const AffineWalkArgs& a, cudaStream_t s);
 cudaError_t launch_grads(const GradArgs& a, cudaStream_t s);
-cudaError_t launch_reduce_dqdk(const float* dq_part, const float* dk_part, bf16* dq, bf16* dk,
-                               long tokens, int Hk, int Hv, cudaStream_t s);
 
 }  // namespace gdn

@@ -213,5 +213,41 @@ __device__ __forceinline__ void gemm_bmn_k128(uint32_t tmem_d, uint32_t a_smem, 
   }
 }
 
+// 32 fp32 columns into this thread's TMEM lane (complete after wait_st)
+__device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[128 x 128] (+)= A B^T-style product of two 128 x 128 SW128 operands, each
+// either K-major (rows = M or N, 128-byte rows along K) or MN-major (rows =
+// K, 128-byte rows along M or N: a row-major [K][M] matrix as a tiled load
+// lands it)
+__device__ __forceinline__ void gemm128(uint32_t tmem_d, uint32_t a_smem, bool a_mn, uint32_t b_smem,
+                                        bool b_mn, bool accumulate_first) {
+  const uint32_t idesc = idesc_bf16(128, 128) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t kmaj = (uint32_t)(k >> 2) * 128u * 128u + (uint32_t)(k & 3) * 32u;
+    const uint64_t da = a_mn ? desc_sw128_mn(a_smem + (uint32_t)k * 2048u, 128u * 128u) : desc_sw128(a_smem + kmaj);
+    const uint64_t db = b_mn ? desc_sw128_mn(b_smem + (uint32_t)k * 2048u, 128u * 128u) : desc_sw128(b_smem + kmaj);
+    mma(tmem_d, da, db, idesc, (k > 0 || accumulate_first) ? 1u : 0u);
+  }
+}
+
 }  // namespace tc
 }  // namespace gdn
