@@ -330,18 +330,26 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   w.dstates = at<bf16>(ws, L.dstates);
   w.ddelta = at<bf16>(ws, L.ddelta);
   w.status = at<int>(ws, L.status);
+  WalkBwdMaps bm;
+  {
+    const uint64_t wrows = (uint64_t)d.BH() * d.NC * CH;
+    if (!tmap_heads(&bm.k, k, d.B, d.T, d.Hk, HD) || !tmap_heads(&bm.q, q, d.B, d.T, d.Hk, HD) ||
+        !tmap_2d(&bm.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
+        !tmap_2d(&bm.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true))
+      return GDN_ERR_CUDA;
+  }
   if (d.S == 1) {
     w.hstart = dhT;
     w.hstart_bh_stride = (long)HD * HD;
     w.hstart_seg_stride = 0;
-    rc = cuda_status(launch_walk_bwd(w, 0, s));
+    rc = cuda_status(launch_walk_bwd(w, bm, 0, s));
     if (!rc) rc = mk.rec();
   } else {
     WalkBwdArgs f = w;
     f.pairA = at<float>(ws, L.pairA);
     f.pairB = at<float>(ws, L.pairB);
     f.dh0 = nullptr;
-    rc = cuda_status(launch_walk_bwd(f, 1, s));
+    rc = cuda_status(launch_walk_bwd(f, bm, 1, s));
     if (rc || (rc = mk.rec())) return rc;
     AffineWalkArgs x;
     memset(&x, 0, sizeof x);
@@ -360,7 +368,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
     w.hstart = at<float>(ws, L.hin);
     w.hstart_bh_stride = (long)d.S * HD * HD;
     w.hstart_seg_stride = (long)HD * HD;
-    rc = cuda_status(launch_walk_bwd(w, 0, s));
+    rc = cuda_status(launch_walk_bwd(w, bm, 0, s));
     if (!rc) rc = mk.rec();
   }
   if (rc) return rc;

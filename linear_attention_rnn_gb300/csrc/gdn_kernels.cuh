@@ -75,6 +75,12 @@ struct WalkBwdArgs {
   int B, T, Hk, Hv, NC, S;
 };
 
+// Tensor maps of the backward walk's tiles: k and q as for the forward walk,
+// w and P over the workspace rows (64 columns x 128 rows, 128-byte swizzle).
+struct WalkBwdMaps {
+  CUtensorMap k, q, W, P;
+};
+
 // Sequential affine walk X <- A_i X (+ B_i) over i (segment prefix / compose).
 struct AffineWalkArgs {
   const float* A;      // [batch][n][HD][HD]
@@ -118,7 +124,7 @@ size_t grad_smem_bytes();
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold, cudaStream_t s);
-cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int fold, cudaStream_t s);
+cudaError_t launch_walk_bwd(const WalkBwdArgs& a, const WalkBwdMaps& m, int fold, cudaStream_t s);
 cudaError_t launch_affine_walk(const AffineWalkArgs& a, cudaStream_t s);
 cudaError_t launch_grads(const GradArgs& a, cudaStream_t s);
 

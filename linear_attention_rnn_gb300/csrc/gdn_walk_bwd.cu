@@ -1,19 +1,30 @@
 // gdn_walk_bwd.cu -- reverse walk of the state cotangent over the chunks of a segment.
 //
 // The backward "walks the chunks in reverse" ("Fuse the Gated Delta Net
-// inter-chunk scan into a Pallas TPU kernel", section "Changes").  With dh the
+// inter-chunk scan into a Pallas TPU kernel", section "Changes").  With dh' the
 // cotangent of the state leaving chunk c, the chunk forward
 //     Delta = u - w h,  O = diag(gamma) Q h + P Delta,  h' = gamma_C h + k_g^T Delta
 // gives
-//     dDelta = P^T dO + k_g dh'                          (= Y below)
-//     dh     = gamma_C dh' + Q^T diag(gamma) dO - w^T dDelta,
+//     Y = dDelta = diag(ef) K dh' + P^T dO
+//     dh = gamma_C dh' + Q^T diag(gamma) dO - w^T Y,
 // an affine map of dh' with matrix A_c^T, so it segments exactly like the
-// forward (the transposed maps compose in reverse order).  Each CTA owns a
-// 32-column slice of dh (columns are independent) in fp32 registers.
-// The chunk tiles stream, in the order they are consumed (K, P, then Q, w),
-// through a ring of padded shared buffers, each requested with cp.async
-// (one commit group per tile) about a chunk before it is needed; the CTA's dO
-// columns are double-buffered.
+// forward (the transposed maps compose in reverse order).
+//
+// One CTA walks a 32-column slice of dh (columns are independent).  Compute
+// thread r (of 128) owns row r of the slice in fp32 registers and TMEM lane r
+// of every product.  Per chunk the tcgen05 products (M = 128, N = 32, K = 128)
+//     K dh'            (A = K, K-major)
+//     P^T dO           (A = the P tile read MN-major)
+//     Q^T (gamma dO)   (A = the Q tile read MN-major), then += w^T (-Y) on top
+//                      (A = the w tile read MN-major)
+// take B operands written column by column by the compute threads (dh'^T,
+// dO^T, (gamma dO)^T, (-Y)^T, 32 x 128 bf16, 128-byte-swizzled K-major).  The
+// two dO products do not depend on dh', so they run ahead of the chain
+// dh' -> Y -> dh.  A fifth warp issues the MMAs once their operands are
+// signalled ready, and the TMA loads of the chunk tiles (P, Q, K, w in the
+// order consumed) into a ring of six 32 KiB slots, refilling each as soon as
+// the MMA that read it completes.  Every wait is bounded; one that gives up
+// sets bit 0 of the status word.
 //
 // Modes:
 //   WALK (fold = 0): from the cotangent leaving the segment, store for every
@@ -24,310 +35,335 @@
 //     the cotangent leaving the segment to the one entering it:
 //     dh_in = Abar dh_out + Bbar.
 #include "gdn_kernels.cuh"
+#include "gdn_tc05.cuh"
 
 namespace gdn {
 
 namespace {
 
-constexpr int NSLOT_MAX = 5;
+constexpr int NC_THREADS = 128;               // compute threads
+constexpr int NT = NC_THREADS + 32;           // + the issuer warp
+constexpr int NSLOT = 6;
+constexpr uint32_t TILE_BYTES = CH * HD * 2;  // 32 KiB
+constexpr uint32_t BT_BYTES = SL * HD * 2;    // 8 KiB: a [32 x 128] B-operand tile
 
 struct WalkBwdSmem {
-  bf16 slot[NSLOT_MAX][CH * LDB];  // padded 128 x 128 tiles
-  bf16 dO[2][CH * LDS_];
-  bf16 dOg[CH * LDS_];
-  bf16 X[HD * LDS_];
-  bf16 Yn[CH * LDS_];
-  float gamma[2][CH];
-  float ef[2][CH];
-  float gC[2];
+  unsigned char slot[NSLOT][TILE_BYTES];
+  unsigned char Xt[BT_BYTES];   // dh'^T
+  unsigned char Yt[BT_BYTES];   // (-Y)^T
+  unsigned char Ot[BT_BYTES];   // dO^T (this slice)
+  unsigned char Ogt[BT_BYTES];  // (diag(gamma) dO)^T
+  float gsum[2][4];
+  uint64_t full[NSLOT];
+  uint64_t barO, barXt, barYt, barPQ, barY, barH;
+  uint32_t tmem;
 };
 
-__device__ __forceinline__ void chunk_gates_b(float (&v)[4], float* gamma, float* ef, float* gC,
-                                              int lane) {
-  warp_cumsum128(v, lane);
-  const float Glast = __shfl_sync(0xffffffffu, v[3], 31);
+// TMEM columns: K dh' at 0, P^T dO at 32; Q^T (gamma dO) - w^T Y alternates 64 / 96
+constexpr uint32_t C_Y = 0, C_P = 32;
+__device__ __forceinline__ uint32_t c_q(int ci) { return (ci & 1) ? 96u : 64u; }
+
+__device__ __forceinline__ void write_bt_column(unsigned char* tile, int k, const float (&v)[32]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    gamma[lane * 4 + i] = expf(v[i]);
-    ef[lane * 4 + i] = expf(Glast - v[i]);
+  for (int n = 0; n < 32; ++n)
+    *reinterpret_cast<bf16*>(tile + tc::sw128(n, k, 32)) = __float2bfloat16_rn(v[n]);
+}
+__device__ __forceinline__ void store_row_bf16(bf16* dst, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 o;
+    o.x = pack_bf16(v[8 * q], v[8 * q + 1]);
+    o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(dst + 8 * q) = o;
   }
-  if (lane == 0) *gC = expf(Glast);
+}
+__device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+__device__ __forceinline__ void arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 template <bool FOLD>
-__global__ void __launch_bounds__(NTHREADS, 1) k_walk_bwd(WalkBwdArgs a) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  WalkBwdSmem& sm = *reinterpret_cast<WalkBwdSmem*>(smem_raw);
+__global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_constant__ WalkBwdMaps mp) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  WalkBwdSmem& sm = *reinterpret_cast<WalkBwdSmem*>(base);
   const int slice = blockIdx.x, seg = blockIdx.y, bhi = blockIdx.z;
   const int b = bhi / a.Hv, j = bhi % a.Hv, kh = j / (a.Hv / a.Hk);
   const long bh = bhi;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g4 = lane >> 2, t4 = lane & 3;
   const int cbeg = (int)((long)seg * a.NC / a.S), cend = (int)((long)(seg + 1) * a.NC / a.S);
   const bool partA = FOLD && slice < 4;  // Abar columns: no dO terms
   const bool withO = !partA;
-  const int TPC = withO ? 4 : 2;  // tiles per chunk: K, P, Q, w  (or K, w)
-  const int NSLOT = withO ? 5 : 4;
-  const int ntiles = (cend - cbeg) * TPC;
+  const int TPC = withO ? 4 : 2;  // tiles per chunk: P, Q, K, w (or K, w)
+  const int n = cend - cbeg;
+  const int ntiles = n * TPC;
   const int col0 = (slice & 3) * SL;
-  const int m0 = warp * 16;
-  const int r0 = m0 + g4, r1 = r0 + 8;
-  const long tokstride = (long)a.Hk * HD;
-  if (cbeg >= cend) return;
-
-  float x[4][4];
-  if (FOLD) {
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = col0 + nt * 8 + 2 * t4 + e;
-        x[nt][e] = (partA && r0 == col) ? 1.f : 0.f;
-        x[nt][2 + e] = (partA && r1 == col) ? 1.f : 0.f;
-      }
-  } else {
-    const float* hs = a.hstart ? a.hstart + bh * a.hstart_bh_stride + seg * a.hstart_seg_stride : nullptr;
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = col0 + nt * 8 + 2 * t4;
-      float2 x0 = make_float2(0.f, 0.f), x1 = x0;
-      if (hs) {
-        x0 = *reinterpret_cast<const float2*>(hs + r0 * HD + col);
-        x1 = *reinterpret_cast<const float2*>(hs + r1 * HD + col);
-      }
-      x[nt][0] = x0.x;
-      x[nt][1] = x0.y;
-      x[nt][2] = x1.x;
-      x[nt][3] = x1.y;
-    }
-  }
-
+  if (n <= 0) return;
+  auto chunk_of = [&](int ci) { return cend - 1 - ci; };  // walk order
   auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
-  auto tok = [&](int c) { return (long)b * a.T + (long)c * CH; };
-  // request tile i of the reverse sequence (every thread; one commit group per tile)
-  auto issue = [&](int i) {
-    if (i < ntiles) {
-      const int ci = i / TPC, t = i % TPC;
-      const int c = cend - 1 - ci;
-      const long cid = bh * a.NC + c;
-      bf16* dst = sm.slot[i % NSLOT];
-      const int kind = withO ? t : (t == 0 ? 0 : 3);  // 0 K, 1 P, 2 Q, 3 w
-      if (kind == 0) {
-        tile_load_async(dst, a.k + (tok(c) * a.Hk + kh) * HD, tokstride, rows_of(c), tid);
-        if (withO)
-          slice_load_async(sm.dO[ci & 1], a.dO + (tok(c) * a.Hv + j) * HD + col0, (long)a.Hv * HD,
-                           rows_of(c), tid);
-      } else if (kind == 1) {
-        tile_load_async(dst, a.P + cid * CH * CH, CH, CH, tid);
-      } else if (kind == 2) {
-        tile_load_async(dst, a.q + (tok(c) * a.Hk + kh) * HD, tokstride, rows_of(c), tid);
-      } else {
-        tile_load_async(dst, a.W + cid * CH * HD, HD, CH, tid);
-      }
-    }
-    cp_async_commit();
-  };
-  auto load_g = [&](int c, float (&v)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = lane * 4 + i;
-      v[i] = (c >= cbeg && r < rows_of(c)) ? a.g[(tok(c) + r) * a.Hv + j] : 0.f;
-    }
-  };
 
-  for (int i = 0; i < NSLOT; ++i) issue(i);
-  float gnext[4];
-  if (warp == 0) {
-    float v[4];
-    load_g(cend - 1, v);
-    chunk_gates_b(v, sm.gamma[(cend - 1) & 1], sm.ef[(cend - 1) & 1], &sm.gC[(cend - 1) & 1], lane);
-    load_g(cend - 2, gnext);
+  if (tid == 0) {
+    for (int k = 0; k < NSLOT; ++k) tc::mbar_init(&sm.full[k], 1);
+    tc::mbar_init(&sm.barO, NC_THREADS);
+    tc::mbar_init(&sm.barXt, NC_THREADS);
+    tc::mbar_init(&sm.barYt, NC_THREADS);
+    tc::mbar_init(&sm.barPQ, 1);
+    tc::mbar_init(&sm.barY, 1);
+    tc::mbar_init(&sm.barH, 1);
+    tc::mbar_fence_init();
   }
+  if (warp == 0) tc::alloc(&sm.tmem, 128);
+  bool ok = true;
 
-  for (int c = cend - 1; c >= cbeg; --c) {
-    const int ci = cend - 1 - c;
-    const int par = c & 1;
-    const int tk = ci * TPC;  // index of this chunk's K tile
-    const bf16* sK = sm.slot[tk % NSLOT];
-    const bf16* sP = sm.slot[(tk + 1) % NSLOT];
-    const bf16* sQ = sm.slot[(tk + 2) % NSLOT];
-    const bf16* sW = sm.slot[(tk + (withO ? 3 : 1)) % NSLOT];
-    const bf16* sdO = sm.dO[ci & 1];
-    cp_async_wait_n(3);  // K, dO (and P): NSLOT + tk groups committed
-    // bf16 image of dh' (B operand), its export, and gamma * dO
+  const int r = tid;  // compute threads: row r of the slice / of the chunk
+  float x[32];
+  float gnext = 0.f, part = 0.f;
+  float gam_r = 0.f, ef_r = 0.f, gC = 0.f;
+  uint4 don[4];  // dO row r of the next chunk's images (this slice's 32 columns)
+  auto load_g = [&](int ci) {
+    if (ci >= n) return 0.f;
+    const int c = chunk_of(ci);
+    return r < rows_of(c) ? a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j] : 0.f;
+  };
+  auto load_do = [&](int ci) {
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = nt * 8 + 2 * t4;
-      *reinterpret_cast<uint32_t*>(sm.X + r0 * LDS_ + col) = pack_bf16(x[nt][0], x[nt][1]);
-      *reinterpret_cast<uint32_t*>(sm.X + r1 * LDS_ + col) = pack_bf16(x[nt][2], x[nt][3]);
+    for (int q = 0; q < 4; ++q) don[q] = make_uint4(0u, 0u, 0u, 0u);
+    if (!withO || ci >= n) return;
+    const int c = chunk_of(ci);
+    if (r < rows_of(c)) {
+      const bf16* src = a.dO + (((long)b * a.T + (long)c * CH + r) * a.Hv + j) * HD + col0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) don[q] = *reinterpret_cast<const uint4*>(src + 8 * q);
     }
-    if (!FOLD) {
-      bf16* st = a.dstates + ((bh * a.NC + c) * HD) * HD + col0;
+  };
+  // dO^T and (gamma dO)^T images of the chunk whose dO rows are in don
+  auto write_do_images = [&]() {
+    float d[32], dg[32];
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int col = nt * 8 + 2 * t4;
-        *reinterpret_cast<uint32_t*>(st + (long)r0 * HD + col) = pack_bf16(x[nt][0], x[nt][1]);
-        *reinterpret_cast<uint32_t*>(st + (long)r1 * HD + col) = pack_bf16(x[nt][2], x[nt][3]);
-      }
-    }
-    __syncthreads();  // dO landed for every thread's copy, gates and the dh' image visible
-    if (withO) {
-      // 128 rows x 32 cols: 2 rows of 8 columns per thread
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t w4[4] = {don[q].x, don[q].y, don[q].z, don[q].w};
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int idx = tid + i * NTHREADS;
-        const int r = idx >> 2, c8 = (idx & 3) << 3;
-        const float gm = sm.gamma[par][r];
-        uint4 raw = *reinterpret_cast<const uint4*>(sdO + r * LDS_ + c8);
-        uint32_t* w = reinterpret_cast<uint32_t*>(&raw);
-#pragma unroll
-        for (int q2 = 0; q2 < 4; ++q2) {
-          float2 f = unpack_bf16(w[q2]);
-          w[q2] = pack_bf16(gm * f.x, gm * f.y);
-        }
-        *reinterpret_cast<uint4*>(sm.dOg + r * LDS_ + c8) = raw;
-      }
-    }
-
-    // ---- Y = dDelta = diag(ef) K dh' + P^T dO ---------------------------------
-    float y[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) y[i][0] = y[i][1] = y[i][2] = y[i][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t af[4], bb[4];
-      lda_rm(af, sK, LDB, m0, ks * 16, lane);
-      ldb_kn(bb, sm.X, LDS_, ks * 16, 0, lane);
-      mma16816(y[0], af, bb[0], bb[1]);
-      mma16816(y[1], af, bb[2], bb[3]);
-      ldb_kn(bb, sm.X, LDS_, ks * 16, 16, lane);
-      mma16816(y[2], af, bb[0], bb[1]);
-      mma16816(y[3], af, bb[2], bb[3]);
-    }
-    {
-      const float e0 = sm.ef[par][r0], e1 = sm.ef[par][r1];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        y[nt][0] *= e0;
-        y[nt][1] *= e0;
-        y[nt][2] *= e1;
-        y[nt][3] *= e1;
-      }
-    }
-    if (withO) {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if (ks >= warp) {  // P^T is upper triangular
-          uint32_t af[4], bb[4];
-          lda_tr(af, sP, LDB, m0, ks * 16, lane);
-          ldb_kn(bb, sdO, LDS_, ks * 16, 0, lane);
-          mma16816(y[0], af, bb[0], bb[1]);
-          mma16816(y[1], af, bb[2], bb[3]);
-          ldb_kn(bb, sdO, LDS_, ks * 16, 16, lane);
-          mma16816(y[2], af, bb[0], bb[1]);
-          mma16816(y[3], af, bb[2], bb[3]);
-        }
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16(w4[e]);
+        d[8 * q + 2 * e] = f.x;
+        d[8 * q + 2 * e + 1] = f.y;
       }
     }
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = nt * 8 + 2 * t4;
-      *reinterpret_cast<uint32_t*>(sm.Yn + r0 * LDS_ + col) = pack_bf16(-y[nt][0], -y[nt][1]);
-      *reinterpret_cast<uint32_t*>(sm.Yn + r1 * LDS_ + col) = pack_bf16(-y[nt][2], -y[nt][3]);
-      if (!FOLD) {
-        bf16* dd = a.ddelta + ((bh * a.NC + c) * CH) * HD + col0 + col;
-        *reinterpret_cast<uint32_t*>(dd + (long)r0 * HD) = pack_bf16(y[nt][0], y[nt][1]);
-        *reinterpret_cast<uint32_t*>(dd + (long)r1 * HD) = pack_bf16(y[nt][2], y[nt][3]);
-      }
+    for (int i = 0; i < 32; ++i) dg[i] = gam_r * d[i];
+    write_bt_column(sm.Ot, r, d);
+    write_bt_column(sm.Ogt, r, dg);
+  };
+  auto scan_part = [&](float gv, int i) {  // warp-inclusive scan; warp totals to gsum[i & 1]
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float o = __shfl_up_sync(0xffffffffu, gv, off);
+      if (lane >= off) gv += o;
     }
-    // NSLOT + tk groups committed; Q and w are tiles tk+2, tk+3 (or w = tk+1)
-    cp_async_wait_n(withO ? 1 : 2);
-    __syncthreads();  // K, P consumed; Yn, dOg complete; Q, w visible
-    issue(tk + NSLOT);
-    if (withO) issue(tk + 1 + NSLOT);
-
-    // ---- dh = gamma_C dh' + Q^T (gamma dO) + W^T (-Y) -----------------------------
-    {
-      const float gC = sm.gC[par];
+    if (lane == 31) sm.gsum[i & 1][warp] = gv;
+    return gv;
+  };
+  auto finish_gates = [&](float p, int i) {  // after a barrier over the compute threads
+    float off = 0.f, tot = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[nt][e] *= gC;
-      if (withO) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint32_t af[4], bb[4];
-          lda_tr(af, sQ, LDB, m0, ks * 16, lane);
-          ldb_kn(bb, sm.dOg, LDS_, ks * 16, 0, lane);
-          mma16816(x[0], af, bb[0], bb[1]);
-          mma16816(x[1], af, bb[2], bb[3]);
-          ldb_kn(bb, sm.dOg, LDS_, ks * 16, 16, lane);
-          mma16816(x[2], af, bb[0], bb[1]);
-          mma16816(x[3], af, bb[2], bb[3]);
-        }
-      }
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t af[4], bb[4];
-        lda_tr(af, sW, LDB, m0, ks * 16, lane);
-        ldb_kn(bb, sm.Yn, LDS_, ks * 16, 0, lane);
-        mma16816(x[0], af, bb[0], bb[1]);
-        mma16816(x[1], af, bb[2], bb[3]);
-        ldb_kn(bb, sm.Yn, LDS_, ks * 16, 16, lane);
-        mma16816(x[2], af, bb[0], bb[1]);
-        mma16816(x[3], af, bb[2], bb[3]);
-      }
+    for (int w = 0; w < 4; ++w) {
+      const float s = sm.gsum[i & 1][w];
+      off += (w < warp) ? s : 0.f;
+      tot += s;
     }
-    __syncthreads();  // Q, w, dOg, X, Yn consumed
-    if (withO) {
-      issue(tk + 2 + NSLOT);
-      issue(tk + 3 + NSLOT);
+    const float G = p + off;
+    gam_r = expf(G);
+    ef_r = expf(tot - G);
+    gC = expf(tot);
+  };
+  if (warp < 4) {
+    if (FOLD) {
+#pragma unroll
+      for (int q = 0; q < 32; ++q) x[q] = (partA && r == col0 + q) ? 1.f : 0.f;
     } else {
-      issue(tk + 1 + NSLOT);
+      const float* hs = a.hstart ? a.hstart + bh * a.hstart_bh_stride + seg * a.hstart_seg_stride : nullptr;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (hs) v = *reinterpret_cast<const float4*>(hs + (long)r * HD + col0 + 4 * q);
+        x[4 * q] = v.x;
+        x[4 * q + 1] = v.y;
+        x[4 * q + 2] = v.z;
+        x[4 * q + 3] = v.w;
+      }
     }
-    if (warp == 0 && c - 1 >= cbeg) {
-      chunk_gates_b(gnext, sm.gamma[par ^ 1], sm.ef[par ^ 1], &sm.gC[par ^ 1], lane);
-      load_g(c - 2, gnext);
-    }
+    write_bt_column(sm.Xt, r, x);
+    part = scan_part(load_g(0), 0);
+    gnext = load_g(1);
+    load_do(0);
   }
-  cp_async_wait<0>();
+  tc::fence_proxy_async();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = sm.tmem;
 
-  if (FOLD) {
-    float* dst = (partA ? a.pairA : a.pairB) + (bh * a.S + seg) * HD * HD + col0;
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = nt * 8 + 2 * t4;
-      *reinterpret_cast<float2*>(dst + r0 * HD + col) = make_float2(x[nt][0], x[nt][1]);
-      *reinterpret_cast<float2*>(dst + r1 * HD + col) = make_float2(x[nt][2], x[nt][3]);
+  if (warp == 4) {
+    // ================================================================= issuer
+    if (lane == 0) {
+      auto issue = [&](int i) {  // TMA request of tile i into slot i % NSLOT
+        if (i >= ntiles) return;
+        const int ci = i / TPC, t = i % TPC;
+        const int c = chunk_of(ci);
+        const int kind = withO ? t : (t == 0 ? 2 : 3);  // 0 P, 1 Q, 2 K, 3 w
+        const long cid = bh * a.NC + c;
+        unsigned char* dst = sm.slot[i % NSLOT];
+        uint64_t* bar = &sm.full[i % NSLOT];
+        tc::arrive_expect_tx(bar, TILE_BYTES);
+        if (kind == 0 || kind == 3) {
+          const CUtensorMap* m = (kind == 0) ? &mp.P : &mp.W;
+          tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
+          tc::tma_load_2d(dst + TILE_BYTES / 2, m, 64, (int)(cid * CH), bar);
+        } else {
+          const CUtensorMap* m = (kind == 1) ? &mp.q : &mp.k;
+          tc::tma_load_4d(dst, m, 0, kh, c * CH, b, bar);
+          tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
+        }
+      };
+      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NSLOT], (i / NSLOT) & 1); };
+      auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NSLOT]); };
+      for (int i = 0; i < NSLOT; ++i) issue(i);
+      for (int ci = 0; ci < n; ++ci) {
+        const uint32_t par = (uint32_t)(ci & 1);
+        const int t0 = ci * TPC;
+        const int iP = t0, iQ = t0 + 1, iK = t0 + (withO ? 2 : 0), iW = t0 + (withO ? 3 : 1);
+        if (withO) {  // the dO products: independent of dh'
+          ok = ok && tc::mbar_wait(&sm.barO, par);
+          wait_tile(iP);
+          tc::fence_after();
+          tc::gemm_amn_k128(tmem + C_P, slot_of(iP), smem_u32(sm.Ot), 32, false);
+          wait_tile(iQ);
+          tc::fence_after();
+          tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iQ), smem_u32(sm.Ogt), 32, false);
+          tc::commit(&sm.barPQ);
+        }
+        ok = ok && tc::mbar_wait(&sm.barXt, par);  // dh' image of this chunk
+        wait_tile(iK);
+        tc::fence_after();
+        tc::gemm_k128(tmem + C_Y, slot_of(iK), smem_u32(sm.Xt), 32, false);
+        tc::commit(&sm.barY);
+        if (withO) {
+          ok = ok && tc::mbar_wait(&sm.barPQ, par);
+          issue(iP + NSLOT);
+          issue(iQ + NSLOT);
+        }
+        ok = ok && tc::mbar_wait(&sm.barY, par);
+        issue(iK + NSLOT);
+        ok = ok && tc::mbar_wait(&sm.barYt, par);  // (-Y)^T written
+        wait_tile(iW);
+        tc::fence_after();
+        tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iW), smem_u32(sm.Yt), 32, withO);
+        tc::commit(&sm.barH);
+        ok = ok && tc::mbar_wait(&sm.barH, par);
+        issue(iW + NSLOT);
+      }
     }
-  } else if (a.dh0 && seg == 0) {
-    float* dst = a.dh0 + bh * HD * HD + col0;
+  } else {
+    // ========================================================== compute threads
+    finish_gates(part, 0);
+    if (withO) {
+      write_do_images();
+      tc::fence_proxy_async();
+      tc::fence_before();
+      arrive(&sm.barO);
+      load_do(1);
+    }
+    arrive(&sm.barXt);  // the first dh' image was written before the block barrier
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+    for (int ci = 0; ci < n; ++ci) {
+      const int c = chunk_of(ci);
+      const uint32_t par = (uint32_t)(ci & 1);
+      if (!FOLD && a.dstates) store_row_bf16(a.dstates + ((bh * a.NC + c) * HD + r) * HD + col0, x);
+      part = scan_part(gnext, ci + 1);  // gates of the next chunk
+      gnext = load_g(ci + 2);
+
+      // ---- Y = diag(ef) K dh' + P^T dO ----------------------------------------------
+      float y[32];
+      ok = ok && tc::mbar_wait(&sm.barY, par);
+      tc::fence_after();
+      tc::ld32(tl + C_Y, y);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = nt * 8 + 2 * t4;
-      *reinterpret_cast<float2*>(dst + r0 * HD + col) = make_float2(x[nt][0], x[nt][1]);
-      *reinterpret_cast<float2*>(dst + r1 * HD + col) = make_float2(x[nt][2], x[nt][3]);
+      for (int q = 0; q < 32; ++q) y[q] *= ef_r;
+      if (withO) {
+        ok = ok && tc::mbar_wait(&sm.barPQ, par);
+        tc::fence_after();
+        float pd[32];
+        tc::ld32(tl + C_P, pd);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) y[q] += pd[q];
+      }
+      if (!FOLD && a.ddelta) store_row_bf16(a.ddelta + ((bh * a.NC + c) * CH + r) * HD + col0, y);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) y[q] = -y[q];
+      write_bt_column(sm.Yt, r, y);
+      tc::fence_proxy_async();
+      tc::fence_before();
+      arrive(&sm.barYt);
+
+      // ---- gates and dO images of the next chunk -------------------------------------
+      const float gC_cur = gC;
+      asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");
+      finish_gates(part, ci + 1);
+      if (withO && ci + 1 < n) {  // the dO products of this chunk have completed
+        write_do_images();
+        tc::fence_proxy_async();
+        tc::fence_before();
+        arrive(&sm.barO);
+        load_do(ci + 2);
+      }
+
+      // ---- dh = gamma_C dh' + Q^T (gamma dO) - w^T Y ---------------------------------
+      ok = ok && tc::mbar_wait(&sm.barH, par);
+      tc::fence_after();
+      float hv[32];
+      tc::ld32(tl + c_q(ci), hv);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) x[q] = gC_cur * x[q] + hv[q];
+      if (ci + 1 < n) {
+        write_bt_column(sm.Xt, r, x);
+        tc::fence_proxy_async();
+        tc::fence_before();
+        arrive(&sm.barXt);
+      }
+    }
+    if (FOLD) {
+      store_row_f32((partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0, x);
+    } else if (a.dh0 && seg == 0) {
+      store_row_f32(a.dh0 + (bh * HD + r) * HD + col0, x);
     }
   }
+  if (!ok && a.status) atomicOr(a.status, 1);
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, 128);
+}
+
+template <bool FOLD>
+cudaError_t launch_one(const WalkBwdArgs& a, const WalkBwdMaps& m, cudaStream_t s) {
+  const size_t smem = sizeof(WalkBwdSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_walk_bwd<FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_walk_bwd<FOLD><<<dim3(FOLD ? 8 : HD / SL, a.S, a.B * a.Hv), NT, smem, s>>>(a, m);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t walk_bwd_smem_bytes(int) { return sizeof(WalkBwdSmem); }
+size_t walk_bwd_smem_bytes(int) { return sizeof(WalkBwdSmem) + 1024; }
 
-cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int fold, cudaStream_t s) {
-  const size_t smem = sizeof(WalkBwdSmem);
-  cudaError_t e;
-  if (fold) {
-    e = cudaFuncSetAttribute(k_walk_bwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_walk_bwd<true><<<dim3(8, a.S, a.B * a.Hv), NTHREADS, smem, s>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(k_walk_bwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_walk_bwd<false><<<dim3(HD / SL, a.S, a.B * a.Hv), NTHREADS, smem, s>>>(a);
-  }
-  return cudaGetLastError();
+cudaError_t launch_walk_bwd(const WalkBwdArgs& a, const WalkBwdMaps& m, int fold, cudaStream_t s) {
+  return fold ? launch_one<true>(a, m, s) : launch_one<false>(a, m, s);
 }
 
 }  // namespace gdn
