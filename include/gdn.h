@@ -42,7 +42,14 @@
  *     leaves the state unchanged), Hv a multiple of Hk.
  *   - Workspace: the caller passes `ws` of at least the size the matching
  *     *_workspace_bytes call returns for the same arguments (256-byte aligned).
- *     Its contents on entry do not matter.
+ *     Its contents on entry do not matter.  Its first 4 bytes are a status
+ *     word: the call clears it, and a kernel sets bit 0 if one of its bounded
+ *     waits gives up (gdn_workspace_status reads it).
+ *   - Bounded waits: the kernels wait only inside one block (for their TMA
+ *     copies, their tensor-core products and hand-offs between their warps);
+ *     every such wait gives up after about one second of wall-clock time, so
+ *     a fault can leave wrong outputs and a set status bit but never a hung
+ *     GPU.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -59,7 +66,7 @@ typedef enum gdn_status {
   GDN_ERR_SHAPE = -2,      /* unsupported d_k, d_v or chunk */
   GDN_ERR_WORKSPACE = -3,  /* workspace missing or smaller than required */
   GDN_ERR_CUDA = -4,       /* a kernel launch failed */
-  GDN_ERR_TIMEOUT = -5,    /* reserved: a bounded in-kernel wait gave up */
+  GDN_ERR_TIMEOUT = -5,    /* a bounded in-kernel wait gave up (see gdn_workspace_status) */
   GDN_ERR_UNSUPPORTED = -6 /* device is not sm_103 / sm_100 class */
 } gdn_status;
 
@@ -192,6 +199,30 @@ int gdn_affine_compose(const float* A, const float* B, float* A_out, float* B_ou
 int gdn_debug_ut(const void* k, const void* v, const float* g,
                  const float* beta, float* S_out, float* T_out, void* w_out, void* u_out,
                  int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk, void* stream);
+
+/*
+ * Status of the bounded in-kernel waits of the last gdn_chunk_fwd,
+ * gdn_chunk_bwd call that used workspace `ws`.
+ * The pages have no counterpart: it reports the failure detection of these
+ * kernels.  Synchronises `stream` (the one exception to "never synchronises")
+ * and reads the workspace's status word.  Returns GDN_OK if no wait gave up,
+ * GDN_ERR_TIMEOUT if one did (the outputs of that call are then not valid),
+ * GDN_ERR_ARG for a null ws, GDN_ERR_CUDA if the stream or the copy failed.
+ */
+int gdn_workspace_status(const void* ws, void* stream);
+
+/*
+ * Self-test of the bounded waits.  The pages have no counterpart.  Enqueues
+ * one block whose wait on a barrier that nothing ever signals has to give up
+ * after limit_ns nanoseconds (1e3 <= limit_ns <= 1e10); the kernel then sets
+ * bit 0 of *status and returns normally (bit 1 would mean the wait completed,
+ * which cannot happen), leaving the context usable.  status: one device int,
+ * cleared by this call.  Synchronises `stream`.  Returns GDN_ERR_TIMEOUT when
+ * the timeout was recorded (the expected outcome), GDN_OK if it was not,
+ * GDN_ERR_ARG for a null status or a limit out of range, GDN_ERR_CUDA on a
+ * CUDA error.
+ */
+int gdn_selftest_wait_timeout(long long limit_ns, int* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -76,6 +76,10 @@ def lib():
         L.gdn_affine_compose.restype = I
         L.gdn_debug_ut.argtypes = [P] * 8 + [I] * 7 + [P]
         L.gdn_debug_ut.restype = I
+        L.gdn_workspace_status.argtypes = [P, P]
+        L.gdn_workspace_status.restype = I
+        L.gdn_selftest_wait_timeout.argtypes = [ctypes.c_longlong, P, P]
+        L.gdn_selftest_wait_timeout.restype = I
         _lib = L
     return _lib
 
@@ -234,6 +238,21 @@ def debug_ut(k, v, g, beta, chunk: int = 128):
     return S, Tm, w, u
 
 
+def workspace_status(ws: torch.Tensor) -> int:
+    """Status code (GDN_OK or GDN_ERR_TIMEOUT) of the bounded in-kernel waits of
+    the last forward/backward call that used workspace `ws`.  Synchronises the
+    current stream."""
+    return lib().gdn_workspace_status(_ptr(ws), _stream(ws.device))
+
+
+def selftest_wait_timeout(limit_ns: int, status: torch.Tensor) -> int:
+    """Runs one block whose bounded wait can never complete and must give up
+    after limit_ns; returns the library's status code (GDN_ERR_TIMEOUT = -5 is
+    the expected outcome).  status: a one-element int32 CUDA tensor."""
+    _check(status, "status", torch.int32, (1,))
+    return lib().gdn_selftest_wait_timeout(int(limit_ns), _ptr(status), _stream(status.device))
+
+
 __all__ = ["build", "lib", "chunk_fwd", "chunk_bwd", "affine_compose", "debug_ut",
            "fwd_workspace_bytes", "bwd_workspace_bytes", "default_segments", "GDNError",
-           "header_functions"]
+           "header_functions", "workspace_status", "selftest_wait_timeout"]

@@ -136,8 +136,7 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
   const uint64_t wrows = (uint64_t)d.BH() * d.NC * CH;
   if (!tmap_heads(&mp.k, k, d.B, d.T, d.Hk, HD) || !tmap_heads(&mp.q, q, d.B, d.T, d.Hk, HD) ||
       !tmap_2d(&mp.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
-      !tmap_2d(&mp.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true) ||
-      !tmap_2d(&mp.U, w.U, HD, wrows, HD * sizeof(bf16), SL, CH, false))
+      !tmap_2d(&mp.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true))
     return GDN_ERR_CUDA;
   if (d.S == 1) {
     w.hstart = h0;
@@ -187,7 +186,7 @@ const char* gdn_strerror(int status) {
     case GDN_ERR_SHAPE: return "unsupported shape (this version needs d_k = d_v = 128 and chunk = 128)";
     case GDN_ERR_WORKSPACE: return "workspace missing or too small";
     case GDN_ERR_CUDA: return "CUDA launch failed";
-    case GDN_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+    case GDN_ERR_TIMEOUT: return "a bounded in-kernel wait gave up";
     case GDN_ERR_UNSUPPORTED: return "unsupported device";
     default: return "unknown status";
   }
@@ -239,6 +238,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   const Layout L = layout(d, false);
   if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
   Marks mk = {events, n_events, 0, s};
+  if ((rc = cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), s)))) return rc;
 
   PrepArgs p;
   memset(&p, 0, sizeof p);
@@ -286,6 +286,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   const Layout L = layout(d, true);
   if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
   Marks mk = {events, n_events, 0, s};
+  if ((rc = cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), s)))) return rc;
 
   // 1. per-chunk UT quantities (w, u, P, T)
   PrepArgs p;
@@ -486,6 +487,25 @@ int gdn_debug_ut(const void* k, const void* v, const float* g, const float* beta
   p.Hv = Hv;
   p.NC = (T + CH - 1) / CH;
   return cuda_status(launch_prep(p, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_workspace_status(const void* ws, void* stream) {
+  if (!ws) return GDN_ERR_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+  int st = 0;  // the status word is the first field of every workspace layout
+  if (cudaMemcpy(&st, ws, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+  return (st & 1) ? GDN_ERR_TIMEOUT : GDN_OK;
+}
+
+int gdn_selftest_wait_timeout(long long limit_ns, int* status, void* stream) {
+  if (!status || limit_ns < 1000LL || limit_ns > 10000000000LL) return GDN_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (launch_selftest_wait((unsigned long long)limit_ns, status, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+  return (st & 1) ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
 }  // extern "C"

@@ -50,9 +50,9 @@ struct WalkFwdArgs {
 
 // TMA tensor maps of the forward walk: K and Q over [B, T, Hk, 128] (boxes of
 // 64 columns x 128 tokens, 128-byte swizzle), w and P over the workspace rows
-// (same boxes), u over the workspace rows (32 columns x 128 rows, no swizzle).
+// (same boxes).
 struct WalkFwdMaps {
-  CUtensorMap k, q, W, P, U;
+  CUtensorMap k, q, W, P;
 };
 
 // Sequential backward walk (state cotangent) over the chunks of one segment.
@@ -127,5 +127,6 @@ cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, const WalkBwdMaps& m, int fold, cudaStream_t s);
 cudaError_t launch_affine_walk(const AffineWalkArgs& a, cudaStream_t s);
 cudaError_t launch_grads(const GradArgs& a, cudaStream_t s);
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, int* status, cudaStream_t s);
 
 }  // namespace gdn

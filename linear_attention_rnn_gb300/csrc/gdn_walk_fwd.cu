@@ -21,8 +21,9 @@
 // operands are signalled ready on mbarriers by the compute threads) and the
 // TMA loads of the chunk tiles into a ring of six 32 KiB slots (w, Q, K, P in
 // the order the MMAs consume them; each slot is refilled as soon as the MMA
-// that read it has completed) and of u.  The compute threads never wait on
-// memory issue, only on MMA completion.  Every wait is bounded; one that
+// that read it has completed).  Each compute thread reads its row of the u
+// slice straight into registers a chunk ahead.  The compute threads never
+// wait on memory issue, only on MMA completion.  Every wait is bounded; one that
 // gives up sets bit 0 of the status word.
 //
 // Modes:
@@ -46,17 +47,15 @@ constexpr int NT = NC_THREADS + 32;            // + the issuer warp
 constexpr int NSLOT = 6;                       // tile ring
 constexpr uint32_t TILE_BYTES = CH * HD * 2;   // 32 KiB
 constexpr uint32_t BT_BYTES = SL * HD * 2;     // 8 KiB: a [32 x 128] B-operand tile
-constexpr uint32_t USL_BYTES = CH * SL * 2;    // 8 KiB: u slice
 
 struct WalkSmem {
   unsigned char slot[NSLOT][TILE_BYTES];
   unsigned char Ht[BT_BYTES];
   unsigned char Dt[BT_BYTES];
   unsigned char Dgt[BT_BYTES];
-  bf16 U[CH * SL];
   float gsum[2][4];
   uint64_t full[NSLOT];
-  uint64_t ufull, barX, barO1, barH, barO2, barDg, barD, barHt;
+  uint64_t barX, barO1, barH, barO2, barDg, barD, barHt;
   uint32_t tmem;
 };
 
@@ -105,7 +104,6 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
 
   if (tid == 0) {
     for (int k = 0; k < NSLOT; ++k) tc::mbar_init(&sm.full[k], 1);
-    tc::mbar_init(&sm.ufull, 1);
     tc::mbar_init(&sm.barX, 1);
     tc::mbar_init(&sm.barO1, 1);
     tc::mbar_init(&sm.barH, 1);
@@ -125,6 +123,14 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
   float gam_r = 0.f, ef_r = 0.f, gC = 0.f;
   auto load_g = [&](int c) {
     return (c < cend && r < rows_of(c)) ? a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j] : 0.f;
+  };
+  // row r of this slice of u for chunk c, loaded a chunk ahead into registers
+  uint4 un[4];
+  auto load_u = [&](int c) {
+    if (partA || c >= cend) return;
+    const bf16* src = a.U + ((bh * a.NC + c) * CH + r) * HD + col0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) un[q] = *reinterpret_cast<const uint4*>(src + 8 * q);
   };
   // gate totals of chunk index i (from the segment start) go to gsum[i & 1]:
   // a warp may post the totals of chunk i + 1 while another still reads those of i
@@ -167,6 +173,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
       }
     }
     write_bt_column(sm.Ht, r, h);
+    load_u(cbeg);
     part = scan_part(load_g(cbeg), 0);
     gnext = load_g(cbeg + 1);
   }
@@ -200,15 +207,9 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
           tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
         }
       };
-      auto issue_u = [&](int c) {
-        if (partA || c >= cend) return;
-        tc::arrive_expect_tx(&sm.ufull, USL_BYTES);
-        tc::tma_load_2d(sm.U, &mp.U, col0, (int)((bh * a.NC + c) * CH), &sm.ufull);
-      };
       auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NSLOT], (i / NSLOT) & 1); };
       auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NSLOT]); };
       for (int i = 0; i < NSLOT; ++i) issue(i);
-      issue_u(cbeg);
       for (int c = cbeg; c < cend; ++c) {
         const int ci = c - cbeg;
         const uint32_t par = (uint32_t)(ci & 1);
@@ -227,8 +228,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
         }
         ok = ok && tc::mbar_wait(&sm.barX, par);
         issue(iW + NSLOT);  // w consumed
-        ok = ok && tc::mbar_wait(&sm.barDg, par);  // (ef Delta)^T written; u read
-        issue_u(c + 1);
+        ok = ok && tc::mbar_wait(&sm.barDg, par);  // (ef Delta)^T written
         wait_tile(iK);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + 32, slot_of(iK), smem_u32(sm.Dgt), 32, false);
@@ -266,11 +266,9 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
       float x[32];
       tc::ld32(tl + 0, x);
       if (!partA) {
-        ok = ok && tc::mbar_wait(&sm.ufull, par);
-        const bf16* ur = sm.U + r * SL;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint4 w4 = *reinterpret_cast<const uint4*>(ur + 8 * q);
+          const uint4 w4 = un[q];
           const float2 f0 = unpack_bf16(w4.x), f1 = unpack_bf16(w4.y), f2 = unpack_bf16(w4.z),
                        f3 = unpack_bf16(w4.w);
           x[8 * q] = f0.x - x[8 * q];
@@ -293,6 +291,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
       tc::fence_proxy_async();
       tc::fence_before();
       arrive(&sm.barDg);
+      load_u(c + 1);
       if (withO) {
         write_bt_column(sm.Dt, r, x);
         tc::fence_proxy_async();
