@@ -47,7 +47,7 @@
  *     waits gives up (gdn_workspace_status reads it).
  *   - Bounded waits: the kernels wait only inside one block (for their TMA
  *     copies, their tensor-core products and hand-offs between their warps);
- *     every such wait gives up after about one second of wall-clock time, so
+ *     every such wait gives up after 2e9 SM cycles (about one second), so
  *     a fault can leave wrong outputs and a set status bit but never a hung
  *     GPU.
  */
@@ -214,7 +214,8 @@ int gdn_workspace_status(const void* ws, void* stream);
 /*
  * Self-test of the bounded waits.  The pages have no counterpart.  Enqueues
  * one block whose wait on a barrier that nothing ever signals has to give up
- * after limit_ns nanoseconds (1e3 <= limit_ns <= 1e10); the kernel then sets
+ * after about limit_ns nanoseconds (1e3 <= limit_ns <= 1e10; counted in SM
+ * cycles at the device's maximum clock, so longer at lower clocks); the kernel then sets
  * bit 0 of *status and returns normally (bit 1 would mean the wait completed,
  * which cannot happen), leaving the context usable.  status: one device int,
  * cleared by this call.  Synchronises `stream`.  Returns GDN_ERR_TIMEOUT when

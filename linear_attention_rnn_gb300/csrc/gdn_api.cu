@@ -501,7 +501,7 @@ int gdn_selftest_wait_timeout(long long limit_ns, int* status, void* stream) {
   if (!status || limit_ns < 1000LL || limit_ns > 10000000000LL) return GDN_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return GDN_ERR_CUDA;
-  if (launch_selftest_wait((unsigned long long)limit_ns, status, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (launch_selftest_wait(limit_ns, status, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
   int st = 0;
   if (cudaMemcpy(&st, status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;

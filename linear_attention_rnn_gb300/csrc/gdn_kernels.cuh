@@ -127,6 +127,6 @@ cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, const WalkBwdMaps& m, int fold, cudaStream_t s);
 cudaError_t launch_affine_walk(const AffineWalkArgs& a, cudaStream_t s);
 cudaError_t launch_grads(const GradArgs& a, cudaStream_t s);
-cudaError_t launch_selftest_wait(unsigned long long limit_ns, int* status, cudaStream_t s);
+cudaError_t launch_selftest_wait(long long limit_ns, int* status, cudaStream_t s);
 
 }  // namespace gdn

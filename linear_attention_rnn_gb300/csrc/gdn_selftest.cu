@@ -12,22 +12,28 @@ namespace gdn {
 
 namespace {
 
-__global__ void k_selftest_wait(unsigned long long limit_ns, int* status) {
+__global__ void k_selftest_wait(long long limit_cycles, int* status) {
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     tc::mbar_init(&bar, 1);
     tc::mbar_fence_init();
   }
   __syncthreads();
-  const bool done = tc::mbar_wait(&bar, 0, limit_ns);  // phase 0 never completes
+  const bool done = tc::mbar_wait(&bar, 0, limit_cycles);  // phase 0 never completes
   __syncthreads();
   if (threadIdx.x == 0) atomicOr(status, done ? 2 : 1);
 }
 
 }  // namespace
 
-cudaError_t launch_selftest_wait(unsigned long long limit_ns, int* status, cudaStream_t s) {
-  k_selftest_wait<<<1, 32, 0, s>>>(limit_ns, status);
+cudaError_t launch_selftest_wait(long long limit_ns, int* status, cudaStream_t s) {
+  // the waits count SM cycles: convert at the device's maximum SM clock
+  int dev = 0, khz = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
+  if (e != cudaSuccess) return e;
+  const long long cycles = limit_ns * (long long)khz / 1000000LL;
+  k_selftest_wait<<<1, 32, 0, s>>>(cycles > 0 ? cycles : 1, status);
   return cudaGetLastError();
 }
 

@@ -128,11 +128,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void mbar_fence_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -143,19 +138,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
-// Every wait of this library's kernels gives up after this long.  A wait is
-// for a TMA copy, an MMA or a handshake inside one CTA, normally microseconds.
-constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
+// Every wait of this library's kernels gives up after this many SM cycles
+// (about one second at the GB300's 2.07 GHz, longer at lower clocks).  A wait
+// is for a TMA copy, an MMA or a handshake inside one CTA, normally
+// microseconds.
+constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;
 // Waits for the phase with the given parity to complete; gives up after
-// limit_ns of wall-clock time and returns false (the caller records an error).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = WAIT_LIMIT_NS) {
+// limit_cycles SM cycles and returns false (the caller records an error).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long limit_cycles = WAIT_LIMIT_CYCLES) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   for (;;) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(a, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (clock64() - t0 > limit_cycles) return false;
   }
 }
 

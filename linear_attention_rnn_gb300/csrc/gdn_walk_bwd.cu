@@ -55,7 +55,7 @@ struct WalkBwdSmem {
   unsigned char Ogt[BT_BYTES];  // (diag(gamma) dO)^T
   float gsum[2][4];
   uint64_t full[NSLOT];
-  uint64_t barO, barXt, barYt, barPQ, barY, barH;
+  uint64_t barO, barXt, barYt, barP, barQ, barY, barH;
   uint32_t tmem;
 };
 
@@ -113,7 +113,8 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
     tc::mbar_init(&sm.barO, NC_THREADS);
     tc::mbar_init(&sm.barXt, NC_THREADS);
     tc::mbar_init(&sm.barYt, NC_THREADS);
-    tc::mbar_init(&sm.barPQ, 1);
+    tc::mbar_init(&sm.barP, 1);
+    tc::mbar_init(&sm.barQ, 1);
     tc::mbar_init(&sm.barY, 1);
     tc::mbar_init(&sm.barH, 1);
     tc::mbar_fence_init();
@@ -234,39 +235,49 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
       auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NSLOT], (i / NSLOT) & 1); };
       auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NSLOT]); };
       for (int i = 0; i < NSLOT; ++i) issue(i);
+      // Order of issue (= order of execution on the tensor core): the chain
+      // K dh' -> (Y formed) -> w^T Y -> (dh formed) runs as soon as its operands
+      // are written; Q^T (gamma dO) fills the gap while Y is formed and the next
+      // chunk's P^T dO the gap while dh is formed.
+      auto issue_p = [&](int ci) {  // P^T dO of chunk ci (its dO images are written)
+        ok = ok && tc::mbar_wait(&sm.barO, (uint32_t)(ci & 1));
+        wait_tile(ci * TPC);
+        tc::fence_after();
+        tc::gemm_amn_k128(tmem + C_P, slot_of(ci * TPC), smem_u32(sm.Ot), 32, false);
+        tc::commit(&sm.barP);
+      };
+      if (withO) issue_p(0);
       for (int ci = 0; ci < n; ++ci) {
         const uint32_t par = (uint32_t)(ci & 1);
         const int t0 = ci * TPC;
         const int iP = t0, iQ = t0 + 1, iK = t0 + (withO ? 2 : 0), iW = t0 + (withO ? 3 : 1);
-        if (withO) {  // the dO products: independent of dh'
-          ok = ok && tc::mbar_wait(&sm.barO, par);
-          wait_tile(iP);
-          tc::fence_after();
-          tc::gemm_amn_k128(tmem + C_P, slot_of(iP), smem_u32(sm.Ot), 32, false);
-          wait_tile(iQ);
-          tc::fence_after();
-          tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iQ), smem_u32(sm.Ogt), 32, false);
-          tc::commit(&sm.barPQ);
-        }
         ok = ok && tc::mbar_wait(&sm.barXt, par);  // dh' image of this chunk
         wait_tile(iK);
         tc::fence_after();
         tc::gemm_k128(tmem + C_Y, slot_of(iK), smem_u32(sm.Xt), 32, false);
         tc::commit(&sm.barY);
         if (withO) {
-          ok = ok && tc::mbar_wait(&sm.barPQ, par);
-          issue(iP + NSLOT);
-          issue(iQ + NSLOT);
+          wait_tile(iQ);
+          tc::fence_after();
+          tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iQ), smem_u32(sm.Ogt), 32, false);
+          tc::commit(&sm.barQ);
+          ok = ok && tc::mbar_wait(&sm.barP, par);
+          issue(iP + NSLOT);  // P consumed
         }
         ok = ok && tc::mbar_wait(&sm.barY, par);
-        issue(iK + NSLOT);
+        issue(iK + NSLOT);  // K consumed
         ok = ok && tc::mbar_wait(&sm.barYt, par);  // (-Y)^T written
         wait_tile(iW);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iW), smem_u32(sm.Yt), 32, withO);
         tc::commit(&sm.barH);
+        if (withO) {
+          ok = ok && tc::mbar_wait(&sm.barQ, par);
+          issue(iQ + NSLOT);  // Q consumed
+          if (ci + 1 < n) issue_p(ci + 1);
+        }
         ok = ok && tc::mbar_wait(&sm.barH, par);
-        issue(iW + NSLOT);
+        issue(iW + NSLOT);  // w consumed
       }
     }
   } else {
@@ -296,7 +307,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
 #pragma unroll
       for (int q = 0; q < 32; ++q) y[q] *= ef_r;
       if (withO) {
-        ok = ok && tc::mbar_wait(&sm.barPQ, par);
+        ok = ok && tc::mbar_wait(&sm.barP, par);
         tc::fence_after();
         float pd[32];
         tc::ld32(tl + C_P, pd);
@@ -315,7 +326,8 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
       const float gC_cur = gC;
       asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");
       finish_gates(part, ci + 1);
-      if (withO && ci + 1 < n) {  // the dO products of this chunk have completed
+      if (withO && ci + 1 < n) {  // both dO products of this chunk have read the images
+        ok = ok && tc::mbar_wait(&sm.barQ, par);
         write_do_images();
         tc::fence_proxy_async();
         tc::fence_before();

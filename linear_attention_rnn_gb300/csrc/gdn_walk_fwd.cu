@@ -50,7 +50,7 @@ constexpr uint32_t BT_BYTES = SL * HD * 2;     // 8 KiB: a [32 x 128] B-operand 
 
 struct WalkSmem {
   unsigned char slot[NSLOT][TILE_BYTES];
-  unsigned char Ht[BT_BYTES];
+  unsigned char Ht[2][BT_BYTES];  // h^T of chunk index i in Ht[i & 1]
   unsigned char Dt[BT_BYTES];
   unsigned char Dgt[BT_BYTES];
   float gsum[2][4];
@@ -143,7 +143,8 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
     if (lane == 31) sm.gsum[i & 1][warp] = gv;
     return gv;
   };
-  auto finish_gates = [&](float p, int i) {  // after a barrier over the compute threads
+  // after a barrier over the compute threads: gamma_r, ef_r and gamma_C of chunk index i
+  auto finish_gates = [&](float p, int i, float& gm, float& ef, float& gc) {
     float off = 0.f, tot = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
@@ -152,9 +153,9 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
       tot += s;
     }
     const float G = p + off;
-    gam_r = expf(G);
-    ef_r = expf(tot - G);
-    gC = expf(tot);
+    gm = expf(G);
+    ef = expf(tot - G);
+    gc = expf(tot);
   };
   if (warp < 4) {
     if (FOLD) {
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
         h[4 * q + 3] = x.w;
       }
     }
-    write_bt_column(sm.Ht, r, h);
+    write_bt_column(sm.Ht[0], r, h);
     load_u(cbeg);
     part = scan_part(load_g(cbeg), 0);
     gnext = load_g(cbeg + 1);
@@ -210,49 +211,55 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
       auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NSLOT], (i / NSLOT) & 1); };
       auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NSLOT]); };
       for (int i = 0; i < NSLOT; ++i) issue(i);
+      // Chain products first: w h(c) as soon as the state image is written, then
+      // K^T (ef Delta) as soon as Delta is; Q h(c) and P Delta fill the gaps.
+      // An MMA issue returns about when the tensor core has taken it, so the
+      // order of issue is the order of execution.  A tile slot is refilled
+      // once a completion that covers its reader has been seen.
       for (int c = cbeg; c < cend; ++c) {
         const int ci = c - cbeg;
         const uint32_t par = (uint32_t)(ci & 1);
         const int t0 = ci * TPC;
         const int iW = t0, iQ = t0 + 1, iK = t0 + tile_of(2), iP = t0 + 3;
+        const uint32_t ht = smem_u32(sm.Ht[ci & 1]);
         if (ci > 0) ok = ok && tc::mbar_wait(&sm.barHt, par ^ 1);  // state image of chunk c
         wait_tile(iW);
         tc::fence_after();
-        tc::gemm_k128(tmem + 0, slot_of(iW), smem_u32(sm.Ht), 32, false);
+        tc::gemm_k128(tmem + 0, slot_of(iW), ht, 32, false);
         tc::commit(&sm.barX);
+        if (ci > 0 && withO) {  // the previous chunk's P (its product has completed)
+          ok = ok && tc::mbar_wait(&sm.barO2, par ^ 1);
+          issue(iP - TPC + NSLOT);
+        }
         if (withO) {
           wait_tile(iQ);
           tc::fence_after();
-          tc::gemm_k128(tmem + o1_col(ci), slot_of(iQ), smem_u32(sm.Ht), 32, false);
+          tc::gemm_k128(tmem + o1_col(ci), slot_of(iQ), ht, 32, false);
           tc::commit(&sm.barO1);
         }
-        ok = ok && tc::mbar_wait(&sm.barX, par);
-        issue(iW + NSLOT);  // w consumed
         ok = ok && tc::mbar_wait(&sm.barDg, par);  // (ef Delta)^T written
         wait_tile(iK);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + 32, slot_of(iK), smem_u32(sm.Dgt), 32, false);
         tc::commit(&sm.barH);
+        ok = ok && tc::mbar_wait(&sm.barX, par);
+        issue(iW + NSLOT);  // w consumed
         if (withO) {
+          ok = ok && tc::mbar_wait(&sm.barO1, par);
+          issue(iQ + NSLOT);  // Q consumed
           ok = ok && tc::mbar_wait(&sm.barD, par);  // Delta^T written
           wait_tile(iP);
           tc::fence_after();
           tc::gemm_k128(tmem + 96, slot_of(iP), smem_u32(sm.Dt), 32, false);
           tc::commit(&sm.barO2);
-          ok = ok && tc::mbar_wait(&sm.barO1, par);
-          issue(iQ + NSLOT);  // Q consumed
         }
         ok = ok && tc::mbar_wait(&sm.barH, par);
         issue(iK + NSLOT);  // K consumed
-        if (withO) {
-          ok = ok && tc::mbar_wait(&sm.barO2, par);
-          issue(iP + NSLOT);  // P consumed
-        }
       }
     }
   } else {
     // ========================================================== compute threads
-    finish_gates(part, 0);
+    finish_gates(part, 0, gam_r, ef_r, gC);
     const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
     for (int c = cbeg; c < cend; ++c) {
       const int ci = c - cbeg;
@@ -299,8 +306,13 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
         arrive(&sm.barD);
       }
       if (!FOLD && a.delta) store_row_bf16(a.delta + ((bh * a.NC + c) * CH + r) * HD + col0, x);
-      part = scan_part(gnext, ci + 1);  // gates of chunk c + 1
+
+      // ---- gates of chunk c + 1, while K^T (ef Delta) runs ----------------------------
+      float gam_n, ef_n, gC_n;
+      part = scan_part(gnext, ci + 1);
       gnext = load_g(c + 2);
+      asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");
+      finish_gates(part, ci + 1, gam_n, ef_n, gC_n);
 
       // ---- h' = gamma_C h + H' ---------------------------------------------------
       ok = ok && tc::mbar_wait(&sm.barH, par);
@@ -309,14 +321,13 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
       tc::ld32(tl + 32, hh);
 #pragma unroll
       for (int n = 0; n < 32; ++n) h[n] = gC * h[n] + hh[n];
-      // Q h has been read by the tensor core before the state image is replaced
-      if (withO) ok = ok && tc::mbar_wait(&sm.barO1, par);
-      write_bt_column(sm.Ht, r, h);
+      // the other image buffer held h of the previous chunk, whose readers have completed
+      write_bt_column(sm.Ht[(ci + 1) & 1], r, h);
       tc::fence_proxy_async();
       tc::fence_before();
       arrive(&sm.barHt);
       if (withO) {  // output epilogue overlaps the next chunk's first product
-        ok = ok && tc::mbar_wait(&sm.barO2, par);
+        ok = ok && tc::mbar_wait(&sm.barO2, par);  // covers Q h as well
         tc::fence_after();
         float o1[32], o2[32];
         tc::ld32(tl + o1_col(ci), o1);
@@ -327,8 +338,9 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
           store_row_bf16(a.o + (((long)b * a.T + (long)c * CH + r) * a.Hv + j) * HD + col0, o1);
         }
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");  // gate totals of chunk c + 1
-      finish_gates(part, ci + 1);
+      gam_r = gam_n;
+      ef_r = ef_n;
+      gC = gC_n;
     }
     if (FOLD) {
       float* dst = (partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0;
