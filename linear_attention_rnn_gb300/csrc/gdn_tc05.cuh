@@ -261,5 +261,19 @@ __device__ __forceinline__ void gemm128(uint32_t tmem_d, uint32_t a_smem, bool a
   }
 }
 
+// ---- TMA tiled stores (shared -> global), tracked by bulk async-groups -----------
+// The shared source must have been written before a fence.proxy.async and a
+// barrier; the issuing thread commits the group and later waits for it.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared sources of every committed store have been read (may be overwritten)
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed store has completed
+__device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 }  // namespace tc
 }  // namespace gdn

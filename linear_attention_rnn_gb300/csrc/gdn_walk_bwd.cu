@@ -21,9 +21,9 @@
 // dO^T, (gamma dO)^T, (-Y)^T, 32 x 128 bf16, 128-byte-swizzled K-major).  The
 // two dO products do not depend on dh', so they run ahead of the chain
 // dh' -> Y -> dh.  A fifth warp issues the MMAs once their operands are
-// signalled ready, and the TMA loads of the chunk tiles (P, Q, K, w in the
-// order consumed) into a ring of six 32 KiB slots, refilling each as soon as
-// the MMA that read it completes.  Every wait is bounded; one that gives up
+// signalled ready; a sixth issues the TMA loads of the chunk tiles (P, Q, K, w
+// in the order consumed) into a ring of six 32 KiB slots, refilling each as
+// soon as the MMA that read it completes.  Every wait is bounded; one that gives up
 // sets bit 0 of the status word.
 //
 // Modes:
@@ -42,7 +42,7 @@ namespace gdn {
 namespace {
 
 constexpr int NC_THREADS = 128;               // compute threads
-constexpr int NT = NC_THREADS + 32;           // + the issuer warp
+constexpr int NT = NC_THREADS + 64;           // + the MMA issuer warp + the TMA producer warp
 constexpr int NSLOT = 6;
 constexpr uint32_t TILE_BYTES = CH * HD * 2;  // 32 KiB
 constexpr uint32_t BT_BYTES = SL * HD * 2;    // 8 KiB: a [32 x 128] B-operand tile
@@ -54,7 +54,7 @@ struct WalkBwdSmem {
   unsigned char Ot[BT_BYTES];   // dO^T (this slice)
   unsigned char Ogt[BT_BYTES];  // (diag(gamma) dO)^T
   float gsum[2][4];
-  uint64_t full[NSLOT];
+  uint64_t full[NSLOT], empty[NSLOT];
   uint64_t barO, barXt, barYt, barP, barQ, barY, barH;
   uint32_t tmem;
 };
@@ -109,7 +109,10 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
   auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
 
   if (tid == 0) {
-    for (int k = 0; k < NSLOT; ++k) tc::mbar_init(&sm.full[k], 1);
+    for (int k = 0; k < NSLOT; ++k) {
+      tc::mbar_init(&sm.full[k], 1);
+      tc::mbar_init(&sm.empty[k], 1);
+    }
     tc::mbar_init(&sm.barO, NC_THREADS);
     tc::mbar_init(&sm.barXt, NC_THREADS);
     tc::mbar_init(&sm.barYt, NC_THREADS);
@@ -210,74 +213,77 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
   tc::fence_after();
   const uint32_t tmem = sm.tmem;
 
-  if (warp == 4) {
-    // ================================================================= issuer
+  auto issue = [&](int i) {  // TMA request of tile i into slot i % NSLOT
+    const int ci = i / TPC, t = i % TPC;
+    const int c = chunk_of(ci);
+    const int kind = withO ? t : (t == 0 ? 2 : 3);  // 0 P, 1 Q, 2 K, 3 w
+    const long cid = bh * a.NC + c;
+    unsigned char* dst = sm.slot[i % NSLOT];
+    uint64_t* bar = &sm.full[i % NSLOT];
+    tc::arrive_expect_tx(bar, TILE_BYTES);
+    if (kind == 0 || kind == 3) {
+      const CUtensorMap* m = (kind == 0) ? &mp.P : &mp.W;
+      tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
+      tc::tma_load_2d(dst + TILE_BYTES / 2, m, 64, (int)(cid * CH), bar);
+    } else {
+      const CUtensorMap* m = (kind == 1) ? &mp.q : &mp.k;
+      tc::tma_load_4d(dst, m, 0, kh, c * CH, b, bar);
+      tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
+    }
+  };
+
+  if (warp == 5) {
+    // ========================================================== TMA producer
     if (lane == 0) {
-      auto issue = [&](int i) {  // TMA request of tile i into slot i % NSLOT
-        if (i >= ntiles) return;
-        const int ci = i / TPC, t = i % TPC;
-        const int c = chunk_of(ci);
-        const int kind = withO ? t : (t == 0 ? 2 : 3);  // 0 P, 1 Q, 2 K, 3 w
-        const long cid = bh * a.NC + c;
-        unsigned char* dst = sm.slot[i % NSLOT];
-        uint64_t* bar = &sm.full[i % NSLOT];
-        tc::arrive_expect_tx(bar, TILE_BYTES);
-        if (kind == 0 || kind == 3) {
-          const CUtensorMap* m = (kind == 0) ? &mp.P : &mp.W;
-          tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
-          tc::tma_load_2d(dst + TILE_BYTES / 2, m, 64, (int)(cid * CH), bar);
-        } else {
-          const CUtensorMap* m = (kind == 1) ? &mp.q : &mp.k;
-          tc::tma_load_4d(dst, m, 0, kh, c * CH, b, bar);
-          tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
-        }
-      };
+      for (int i = 0; i < ntiles; ++i) {
+        if (i >= NSLOT) ok = ok && tc::mbar_wait(&sm.empty[i % NSLOT], (uint32_t)((i / NSLOT - 1) & 1));
+        issue(i);
+      }
+    }
+  } else if (warp == 4) {
+    // ================================================================ MMA issuer
+    // Order of issue (= order of execution on the tensor core): the chain
+    // K dh' -> (Y formed) -> w^T Y -> (dh formed) runs as soon as its operands
+    // are written; Q^T (gamma dO) fills the gap while Y is formed and the next
+    // chunk's P^T dO the gap while dh is formed.  After each product its tile
+    // slot is released to the producer by a commit to the slot's empty barrier.
+    if (lane == 0) {
       auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NSLOT], (i / NSLOT) & 1); };
       auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NSLOT]); };
-      for (int i = 0; i < NSLOT; ++i) issue(i);
-      // Order of issue (= order of execution on the tensor core): the chain
-      // K dh' -> (Y formed) -> w^T Y -> (dh formed) runs as soon as its operands
-      // are written; Q^T (gamma dO) fills the gap while Y is formed and the next
-      // chunk's P^T dO the gap while dh is formed.
+      auto release = [&](int i) { tc::commit(&sm.empty[i % NSLOT]); };
       auto issue_p = [&](int ci) {  // P^T dO of chunk ci (its dO images are written)
         ok = ok && tc::mbar_wait(&sm.barO, (uint32_t)(ci & 1));
         wait_tile(ci * TPC);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + C_P, slot_of(ci * TPC), smem_u32(sm.Ot), 32, false);
         tc::commit(&sm.barP);
+        release(ci * TPC);
       };
       if (withO) issue_p(0);
       for (int ci = 0; ci < n; ++ci) {
         const uint32_t par = (uint32_t)(ci & 1);
         const int t0 = ci * TPC;
-        const int iP = t0, iQ = t0 + 1, iK = t0 + (withO ? 2 : 0), iW = t0 + (withO ? 3 : 1);
+        const int iQ = t0 + 1, iK = t0 + (withO ? 2 : 0), iW = t0 + (withO ? 3 : 1);
         ok = ok && tc::mbar_wait(&sm.barXt, par);  // dh' image of this chunk
         wait_tile(iK);
         tc::fence_after();
         tc::gemm_k128(tmem + C_Y, slot_of(iK), smem_u32(sm.Xt), 32, false);
         tc::commit(&sm.barY);
+        release(iK);
         if (withO) {
           wait_tile(iQ);
           tc::fence_after();
           tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iQ), smem_u32(sm.Ogt), 32, false);
           tc::commit(&sm.barQ);
-          ok = ok && tc::mbar_wait(&sm.barP, par);
-          issue(iP + NSLOT);  // P consumed
+          release(iQ);
         }
-        ok = ok && tc::mbar_wait(&sm.barY, par);
-        issue(iK + NSLOT);  // K consumed
         ok = ok && tc::mbar_wait(&sm.barYt, par);  // (-Y)^T written
         wait_tile(iW);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iW), smem_u32(sm.Yt), 32, withO);
         tc::commit(&sm.barH);
-        if (withO) {
-          ok = ok && tc::mbar_wait(&sm.barQ, par);
-          issue(iQ + NSLOT);  // Q consumed
-          if (ci + 1 < n) issue_p(ci + 1);
-        }
-        ok = ok && tc::mbar_wait(&sm.barH, par);
-        issue(iW + NSLOT);  // w consumed
+        release(iW);
+        if (withO && ci + 1 < n) issue_p(ci + 1);
       }
     }
   } else {

@@ -17,11 +17,12 @@
 // operands (h^T, Delta^T, (ef Delta)^T, 32 x 128 bf16) are written column by
 // column by the compute threads in the 128-byte-swizzled K-major layout.
 //
-// A fifth warp issues everything asynchronous: the MMAs (as soon as their
-// operands are signalled ready on mbarriers by the compute threads) and the
-// TMA loads of the chunk tiles into a ring of six 32 KiB slots (w, Q, K, P in
-// the order the MMAs consume them; each slot is refilled as soon as the MMA
-// that read it has completed).  Each compute thread reads its row of the u
+// A fifth warp issues the MMAs as soon as their operands are signalled ready
+// on mbarriers by the compute threads; a sixth issues the TMA loads of the
+// chunk tiles into a ring of six 32 KiB slots (w, Q, K, P in the order the
+// MMAs consume them), refilling each slot as soon as the MMA that read it has
+// completed.  A TMA request can block its thread while earlier copies stream
+// in, so the loads never share a thread with the MMA chain.  Each compute thread reads its row of the u
 // slice straight into registers a chunk ahead.  The compute threads never
 // wait on memory issue, only on MMA completion.  Every wait is bounded; one that
 // gives up sets bit 0 of the status word.
@@ -43,7 +44,7 @@ namespace gdn {
 namespace {
 
 constexpr int NC_THREADS = 128;                // compute threads: one per chunk row / state row
-constexpr int NT = NC_THREADS + 32;            // + the issuer warp
+constexpr int NT = NC_THREADS + 64;            // + the MMA issuer warp + the TMA producer warp
 constexpr int NSLOT = 6;                       // tile ring
 constexpr uint32_t TILE_BYTES = CH * HD * 2;   // 32 KiB
 constexpr uint32_t BT_BYTES = SL * HD * 2;     // 8 KiB: a [32 x 128] B-operand tile
@@ -54,7 +55,7 @@ struct WalkSmem {
   unsigned char Dt[BT_BYTES];
   unsigned char Dgt[BT_BYTES];
   float gsum[2][4];
-  uint64_t full[NSLOT];
+  uint64_t full[NSLOT], empty[NSLOT];
   uint64_t barX, barO1, barH, barO2, barDg, barD, barHt;
   uint32_t tmem;
 };
@@ -103,7 +104,10 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
   auto tile_of = [&](int kind) { return withO ? kind : (kind == 0 ? 0 : 1); };  // kind: 0 w, 1 Q, 2 K, 3 P
 
   if (tid == 0) {
-    for (int k = 0; k < NSLOT; ++k) tc::mbar_init(&sm.full[k], 1);
+    for (int k = 0; k < NSLOT; ++k) {
+      tc::mbar_init(&sm.full[k], 1);
+      tc::mbar_init(&sm.empty[k], 1);
+    }
     tc::mbar_init(&sm.barX, 1);
     tc::mbar_init(&sm.barO1, 1);
     tc::mbar_init(&sm.barH, 1);
@@ -187,35 +191,45 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
   const uint32_t tmem = sm.tmem;
   auto o1_col = [](int ci) { return (ci & 1) ? 128u : 64u; };
 
-  if (warp == 4) {
-    // ================================================================= issuer
+  auto issue = [&](int i) {  // TMA request of tile i into slot i % NSLOT
+    const int c = cbeg + i / TPC, t = i % TPC;
+    const int kind = withO ? t : (t == 0 ? 0 : 2);
+    const long cid = bh * a.NC + c;
+    unsigned char* dst = sm.slot[i % NSLOT];
+    uint64_t* bar = &sm.full[i % NSLOT];
+    tc::arrive_expect_tx(bar, TILE_BYTES);
+    if (kind == 0 || kind == 3) {
+      const CUtensorMap* m = (kind == 0) ? &mp.W : &mp.P;
+      tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
+      tc::tma_load_2d(dst + TILE_BYTES / 2, m, 64, (int)(cid * CH), bar);
+    } else {
+      const CUtensorMap* m = (kind == 1) ? &mp.q : &mp.k;
+      tc::tma_load_4d(dst, m, 0, kh, c * CH, b, bar);
+      tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
+    }
+  };
+
+  if (warp == 5) {
+    // ========================================================== TMA producer
+    // Tile i goes into slot i % NSLOT once the product that read tile
+    // i - NSLOT has completed (signalled on that slot's empty barrier).
     if (lane == 0) {
-      auto issue = [&](int i) {  // TMA request of tile i into slot i % NSLOT
-        if (i >= ntiles) return;
-        const int c = cbeg + i / TPC, t = i % TPC;
-        const int kind = withO ? t : (t == 0 ? 0 : 2);
-        const long cid = bh * a.NC + c;
-        unsigned char* dst = sm.slot[i % NSLOT];
-        uint64_t* bar = &sm.full[i % NSLOT];
-        tc::arrive_expect_tx(bar, TILE_BYTES);
-        if (kind == 0 || kind == 3) {
-          const CUtensorMap* m = (kind == 0) ? &mp.W : &mp.P;
-          tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
-          tc::tma_load_2d(dst + TILE_BYTES / 2, m, 64, (int)(cid * CH), bar);
-        } else {
-          const CUtensorMap* m = (kind == 1) ? &mp.q : &mp.k;
-          tc::tma_load_4d(dst, m, 0, kh, c * CH, b, bar);
-          tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
-        }
-      };
+      for (int i = 0; i < ntiles; ++i) {
+        if (i >= NSLOT) ok = ok && tc::mbar_wait(&sm.empty[i % NSLOT], (uint32_t)((i / NSLOT - 1) & 1));
+        issue(i);
+      }
+    }
+  } else if (warp == 4) {
+    // ================================================================ MMA issuer
+    // Chain products first: w h(c) as soon as the state image is written, then
+    // K^T (ef Delta) as soon as Delta is; Q h(c) and P Delta fill the gaps.  An
+    // MMA issue returns about when the tensor core has taken it, so the order
+    // of issue is the order of execution.  After each product its tile slot is
+    // released to the producer by a commit to the slot's empty barrier.
+    if (lane == 0) {
       auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NSLOT], (i / NSLOT) & 1); };
       auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NSLOT]); };
-      for (int i = 0; i < NSLOT; ++i) issue(i);
-      // Chain products first: w h(c) as soon as the state image is written, then
-      // K^T (ef Delta) as soon as Delta is; Q h(c) and P Delta fill the gaps.
-      // An MMA issue returns about when the tensor core has taken it, so the
-      // order of issue is the order of execution.  A tile slot is refilled
-      // once a completion that covers its reader has been seen.
+      auto release = [&](int i) { tc::commit(&sm.empty[i % NSLOT]); };
       for (int c = cbeg; c < cend; ++c) {
         const int ci = c - cbeg;
         const uint32_t par = (uint32_t)(ci & 1);
@@ -227,34 +241,28 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
         tc::fence_after();
         tc::gemm_k128(tmem + 0, slot_of(iW), ht, 32, false);
         tc::commit(&sm.barX);
-        if (ci > 0 && withO) {  // the previous chunk's P (its product has completed)
-          ok = ok && tc::mbar_wait(&sm.barO2, par ^ 1);
-          issue(iP - TPC + NSLOT);
-        }
+        release(iW);
         if (withO) {
           wait_tile(iQ);
           tc::fence_after();
           tc::gemm_k128(tmem + o1_col(ci), slot_of(iQ), ht, 32, false);
           tc::commit(&sm.barO1);
+          release(iQ);
         }
         ok = ok && tc::mbar_wait(&sm.barDg, par);  // (ef Delta)^T written
         wait_tile(iK);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + 32, slot_of(iK), smem_u32(sm.Dgt), 32, false);
         tc::commit(&sm.barH);
-        ok = ok && tc::mbar_wait(&sm.barX, par);
-        issue(iW + NSLOT);  // w consumed
+        release(iK);
         if (withO) {
-          ok = ok && tc::mbar_wait(&sm.barO1, par);
-          issue(iQ + NSLOT);  // Q consumed
           ok = ok && tc::mbar_wait(&sm.barD, par);  // Delta^T written
           wait_tile(iP);
           tc::fence_after();
           tc::gemm_k128(tmem + 96, slot_of(iP), smem_u32(sm.Dt), 32, false);
           tc::commit(&sm.barO2);
+          release(iP);
         }
-        ok = ok && tc::mbar_wait(&sm.barH, par);
-        issue(iK + NSLOT);  // K consumed
       }
     }
   } else {
