@@ -45,10 +45,10 @@ BWD_KERNELS = ["prep", "walk_states", "walk_bwd", "grads"]
 FWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk"]
 BWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk_states", "fold_bwd", "prefix_bwd",
                    "walk_bwd", "grads"]
-KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<false>", "walk_states": "k_walk_fwd<false>",
-                 "walk_bwd": "k_walk_bwd<false>", "grads": "k_grads",
-                 "fold": "k_walk_fwd<true>", "prefix": "k_affine_walk",
-                 "fold_bwd": "k_walk_bwd<true>", "prefix_bwd": "k_affine_walk"}
+KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 0>", "walk_states": "k_walk_fwd<0, 1>",
+                 "walk_bwd": "k_walk_bwd<0>", "grads": "k_grads",
+                 "fold": "k_walk_fwd<1, 0>", "prefix": "k_affine_walk",
+                 "fold_bwd": "k_walk_bwd<1>", "prefix_bwd": "k_affine_walk"}
 # DRAM traffic per launch from the committed ncu capture of the same kernels
 # (profiles/*), keyed by kernel; None until captured for the current code.
 NCU_TRAFFIC = {}

@@ -133,10 +133,13 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
   w.delta = delta;
   w.status = at<int>(ws, Lw.status);
   WalkFwdMaps mp;
+  memset(&mp, 0, sizeof mp);
   const uint64_t wrows = (uint64_t)d.BH() * d.NC * CH;
   if (!tmap_heads(&mp.k, k, d.B, d.T, d.Hk, HD) || !tmap_heads(&mp.q, q, d.B, d.T, d.Hk, HD) ||
       !tmap_2d(&mp.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
-      !tmap_2d(&mp.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true))
+      !tmap_2d(&mp.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true) ||
+      (states && !tmap_2d_sw(&mp.St, states, HD, wrows, HD * sizeof(bf16), SL, CH, CU_TENSOR_MAP_SWIZZLE_64B)) ||
+      (delta && !tmap_2d_sw(&mp.De, delta, HD, wrows, HD * sizeof(bf16), SL, CH, CU_TENSOR_MAP_SWIZZLE_64B)))
     return GDN_ERR_CUDA;
   if (d.S == 1) {
     w.hstart = h0;
@@ -332,11 +335,14 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   w.ddelta = at<bf16>(ws, L.ddelta);
   w.status = at<int>(ws, L.status);
   WalkBwdMaps bm;
+  memset(&bm, 0, sizeof bm);
   {
     const uint64_t wrows = (uint64_t)d.BH() * d.NC * CH;
     if (!tmap_heads(&bm.k, k, d.B, d.T, d.Hk, HD) || !tmap_heads(&bm.q, q, d.B, d.T, d.Hk, HD) ||
         !tmap_2d(&bm.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
-        !tmap_2d(&bm.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true))
+        !tmap_2d(&bm.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true) ||
+        !tmap_2d_sw(&bm.Ds, w.dstates, HD, wrows, HD * sizeof(bf16), SL, CH, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !tmap_2d_sw(&bm.Dd, w.ddelta, HD, wrows, HD * sizeof(bf16), SL, CH, CU_TENSOR_MAP_SWIZZLE_64B))
       return GDN_ERR_CUDA;
   }
   if (d.S == 1) {

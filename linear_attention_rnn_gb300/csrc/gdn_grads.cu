@@ -99,20 +99,9 @@ __device__ __forceinline__ void row32_store(unsigned char* tile, int r, int c0, 
     *reinterpret_cast<uint4*>(tile + tc::sw128_chunk(r, (c0 >> 3) + q, CH)) = o;
   }
 }
-__device__ __forceinline__ void global32_store(bf16* dst, const float (&v)[32], float scale) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 o;
-    o.x = pack_bf16(scale * v[8 * q + 0], scale * v[8 * q + 1]);
-    o.y = pack_bf16(scale * v[8 * q + 2], scale * v[8 * q + 3]);
-    o.z = pack_bf16(scale * v[8 * q + 4], scale * v[8 * q + 5]);
-    o.w = pack_bf16(scale * v[8 * q + 6], scale * v[8 * q + 7]);
-    *reinterpret_cast<uint4*>(dst + 8 * q) = o;
-  }
-}
-
 struct GradMaps {
   CUtensorMap k, q, dO, Tb, ddelta, states, delta, dstates;
+  CUtensorMap dq, dk;  // stores over [B, T, Hk, 128] (rows past T are clipped)
 };
 
 __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_constant__ GradMaps mp) {
@@ -126,7 +115,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
   const int L = min(CH, a.T - t0);
   const int quarter = warp & 3, hh = warp >> 2;
   const int row = 32 * quarter + lane;
-  const long tokq = ((long)b * a.T + t0) * a.Hk + kh;  // row 0 of the q/k tile
 
   auto cid_of = [&](int jj) { return ((long)b * a.Hv + kh * group + jj) * a.NC + c; };
   auto load2d = [&](unsigned char* dst, const CUtensorMap* m, long cid, uint64_t* bar) {
@@ -218,26 +206,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
     const float bgr = br * gr;
     float p_db = 0.f, p_dbg = 0.f, p_def = 0.f, p_rowx = 0.f, p_dgam = 0.f;
 
-    // ---- E1: dv = diag(beta) dV';  dbeta += rowsum(dV' V);  dV' -> W1 ----------------
+    // ---- E1: dV' -> W1 (bf16) ------------------------------------------------------------
     wait_mma();
     if (tid == 0) load2d(sm.W2, &mp.dstates, cid, &sm.barDH);  // dDelta has been read
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 64; cb += 32) {
-      const int c0 = 64 * hh + cb;
       float x[32];
       tc::ld32(tl + C_A + cb, x);
-      if (row < L) {
-        const long off = (tokv + (long)row * a.Hv) * HD + c0;
-        global32_store(a.dv + off, x, br);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 u = *reinterpret_cast<const uint4*>(a.v + off + 8 * q);
-          const float2 v0 = unpack_bf16(u.x), v1 = unpack_bf16(u.y), v2 = unpack_bf16(u.z), v3 = unpack_bf16(u.w);
-          p_db += x[8 * q] * v0.x + x[8 * q + 1] * v0.y + x[8 * q + 2] * v1.x + x[8 * q + 3] * v1.y +
-                  x[8 * q + 4] * v2.x + x[8 * q + 5] * v2.y + x[8 * q + 6] * v3.x + x[8 * q + 7] * v3.y;
-        }
-      }
-      row32_store(sm.W1, row, c0, x);
+      row32_store(sm.W1, row, 64 * hh + cb, x);
     }
     sync_operands();
 
@@ -250,6 +226,42 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
       tc::gemm128(tmem + C_A, smem_u32(sm.W1), false, smem_u32(sm.W3), false, false);
       tc::gemm128(tmem + C_B, smem_u32(sm.W4), false, smem_u32(sm.W2), false, false);
       tc::commit(&sm.barM);
+    }
+    // ---- dv = diag(beta) dV' and dbeta += rowsum(dV' V), while S2/S5 run -----------------
+    // Read back from the bf16 dV' tile with 16 threads per row, so that V is
+    // loaded and dv stored in whole 256-byte rows.
+    {
+      constexpr int NI = (CH * 16) / NTHREADS;  // 8 chunks of 16 bytes per thread
+      uint4 v4[NI];
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {  // all loads in flight before any is used
+        const int idx = tid + i * NTHREADS;
+        const int r = idx >> 4, jc = idx & 15;
+        v4[i] = r < L ? *reinterpret_cast<const uint4*>(a.v + (tokv + (long)r * a.Hv) * HD + 8 * jc)
+                      : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int idx = tid + i * NTHREADS;
+        const int r = idx >> 4, jc = idx & 15;
+        const uint4 d4 = *reinterpret_cast<const uint4*>(sm.W1 + tc::sw128_chunk(r, jc, CH));
+        const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w}, vw[4] = {v4[i].x, v4[i].y, v4[i].z, v4[i].w};
+        const float bt = sm.beta[r];
+        float part = 0.f;
+        uint32_t ow[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 dd = unpack_bf16(dw[e]), vv = unpack_bf16(vw[e]);
+          part += dd.x * vv.x + dd.y * vv.y;
+          ow[e] = pack_bf16(bt * dd.x, bt * dd.y);
+        }
+        if (r < L)
+          *reinterpret_cast<uint4*>(a.dv + (tokv + (long)r * a.Hv) * HD + 8 * jc) =
+              make_uint4(ow[0], ow[1], ow[2], ow[3]);
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if ((lane & 15) == 0) atomicAdd(&sm.dbeta[r], part);
+      }
     }
     {  // <dh', h>: elementwise over two tiles of the same layout
       ok = ok && tc::mbar_wait(&sm.barDH, par);
@@ -274,7 +286,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
 
     // ---- E2: dK (+)= -diag(beta gamma) dV' h^T + diag(ef) Delta dh'^T ---------------------
     wait_mma();
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 64; cb += 32) {
       const int c0 = 64 * hh + cb;
       float kv[32], x[32], acc[32];
@@ -314,7 +326,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
     }
     // ---- E3: dKK = -(ds * M) diag-row(beta), strictly lower -> W1; dbeta, rowX, colX -----
     wait_mma();
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 64; cb += 32) {
       const int c0 = 64 * hh + cb;
       float out[32];
@@ -356,7 +368,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
     }
     // ---- E4: dQK = dP * M (diagonal included) -> W4; rowX, colX --------------------------
     wait_mma();
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 64; cb += 32) {
       const int c0 = 64 * hh + cb;
       float out[32];
@@ -397,7 +409,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
       load2d(sm.W2, &mp.ddelta, nc, &sm.barDD);
       load2d(sm.W3, &mp.states, nc, &sm.barH);
     }
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 64; cb += 32) {
       const int c0 = 64 * hh + cb;
       float qv[32], x[32], acc[32];
@@ -479,16 +491,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
     __syncthreads();
   }
 
-  // ---- dq, dk of the key head ----------------------------------------------------------
-#pragma unroll
+  // ---- dq, dk of the key head: bf16 staging tiles (W1, W2 are free) and TMA stores ------
+#pragma unroll 1
   for (int cb = 0; cb < 64; cb += 32) {
     const int c0 = 64 * hh + cb;
-    const long off = (tokq + (long)row * a.Hk) * HD + c0;
     float x[32];
     tc::ld32(tl + C_DQ + cb, x);
-    if (row < L) global32_store(a.dq + off, x, 1.f);
+    row32_store(sm.W1, row, c0, x);
     tc::ld32(tl + C_DK + cb, x);
-    if (row < L) global32_store(a.dk + off, x, 1.f);
+    row32_store(sm.W2, row, c0, x);
+  }
+  tc::fence_proxy_async();
+  __syncthreads();
+  if (tid == 0) {
+    tc::tma_store_4d(&mp.dq, 0, kh, t0, b, sm.W1);
+    tc::tma_store_4d(&mp.dq, 64, kh, t0, b, sm.W1 + TILE / 2);
+    tc::tma_store_4d(&mp.dk, 0, kh, t0, b, sm.W2);
+    tc::tma_store_4d(&mp.dk, 64, kh, t0, b, sm.W2 + TILE / 2);
+    tc::bulk_commit();
+    tc::bulk_wait();
   }
   if (!ok && a.status) atomicOr(a.status, 1);
   tc::fence_before();
@@ -511,6 +532,7 @@ cudaError_t launch_grads(const GradArgs& a, cudaStream_t s) {
   ok = ok && tmap_2d(&mp.states, a.states, HD, rows, HD * 2, 64, CH, true);
   ok = ok && tmap_2d(&mp.delta, a.delta, HD, rows, HD * 2, 64, CH, true);
   ok = ok && tmap_2d(&mp.dstates, a.dstates, HD, rows, HD * 2, 64, CH, true);
+  ok = ok && tmap_heads(&mp.dq, a.dq, a.B, a.T, a.Hk, HD) && tmap_heads(&mp.dk, a.dk, a.B, a.T, a.Hk, HD);
   if (!ok) return cudaErrorInvalidValue;
   const size_t smem = grad_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

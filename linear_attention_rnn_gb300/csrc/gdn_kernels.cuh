@@ -50,9 +50,11 @@ struct WalkFwdArgs {
 
 // TMA tensor maps of the forward walk: K and Q over [B, T, Hk, 128] (boxes of
 // 64 columns x 128 tokens, 128-byte swizzle), w and P over the workspace rows
-// (same boxes).
+// (same boxes); stores of 32-column slices (64-byte swizzle) of the entering
+// states and Delta over the workspace rows.
 struct WalkFwdMaps {
   CUtensorMap k, q, W, P;
+  CUtensorMap St, De;
 };
 
 // Sequential backward walk (state cotangent) over the chunks of one segment.
@@ -79,6 +81,7 @@ struct WalkBwdArgs {
 // w and P over the workspace rows (64 columns x 128 rows, 128-byte swizzle).
 struct WalkBwdMaps {
   CUtensorMap k, q, W, P;
+  CUtensorMap Ds, Dd;  // stores: leaving-state cotangents and dDelta (32-column slices)
 };
 
 // Sequential affine walk X <- A_i X (+ B_i) over i (segment prefix / compose).

@@ -57,7 +57,8 @@ struct PrepSmem {
 constexpr uint32_t Y_HI = 0, Y_LO = 8192, SD = 16384;  // Y: [64][64] bf16 pair; Sd: [8][16][16] fp32
 
 struct PrepMaps {
-  CUtensorMap q, k, v;
+  CUtensorMap q, k, v;  // loads: [B, T, H, 128] activations
+  CUtensorMap W, U, P;  // stores: [BH * NC * 128, 128] workspace rows
 };
 
 // [rows][64] bf16 tile with 128-byte rows, 16-byte chunk j of row r at j ^ (r & 7)
@@ -102,12 +103,14 @@ __device__ __forceinline__ void ldb_kn_64(uint32_t (&b)[4], bf16* base, int k0, 
   ldsm_x4_t(b, swz64(base, k0 + (lane & 15), (n0 >> 3) + (lane >> 4)));
 }
 
-__device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, bf16* dst0, bf16* dst1) {
+// Columns 64 hh .. 64 hh + 63 of this thread's TMEM row, as bf16, into row
+// `row` of a K-major SW128 [128 x 128] staging tile (the layout a tiled TMA
+// store with 64-column boxes reads).
+__device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, unsigned char* tile, int row, int hh) {
 #pragma unroll
   for (int cb = 0; cb < 64; cb += 32) {
     float v[32];
     tc::ld32(taddr + cb, v);
-    bf16* dst = cb ? dst1 : dst0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint4 o;
@@ -115,7 +118,7 @@ __device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, bf16* dst0, bf1
       o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
       o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
       o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-      *reinterpret_cast<uint4*>(dst + 8 * q) = o;
+      *reinterpret_cast<uint4*>(tile + tc::sw128_chunk(row, 8 * hh + (cb >> 3) + q, CH)) = o;
     }
   }
 }
@@ -273,6 +276,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
     const int j = kh * group + jj;
     const long bh = (long)b * a.Hv + j;
     const long chunk_id = bh * a.NC + c;
+    // the previous value head's stores have read their staging tiles before the
+    // barriers below let anyone rewrite them
+    if (tid == 0 && jj > 0) tc::bulk_wait_read();
     // ---- gates of value head j --------------------------------------------------
     if (tid < CH) {
       const long idx = ((long)b * a.T + t0 + tid) * a.Hv + j;
@@ -323,29 +329,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
       *reinterpret_cast<uint4*>(sm.Kg + off) = o;
     }
 
-    // ---- S (hi/lo into F, fp32 diagonal blocks into Sd) and P (to global) ----------
+    // ---- S (hi/lo into F, fp32 diagonal blocks into Sd) -------------------------------
     {
       const float Glr = sm.Gl[row], br = sm.beta[row];
       float* Sd = reinterpret_cast<float*>(sm.Tp + SD);
-      bf16* prow = needP ? a.P + chunk_id * tile + (long)row * CH : nullptr;
-#pragma unroll
+#pragma unroll 1
       for (int cb = 0; cb < 64; cb += 16) {
         const int c0 = 64 * hh + cb;
-        float sv[16], pv[16];
+        float sv[16];
         if (c0 <= 32 * quarter + 31) {  // warp-uniform: the block reaches the diagonal
           float kk[16];
           tc::ld16(tlane + c0, kk);
-          if (needP) tc::ld16(tlane + 128 + c0, pv);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int s = c0 + i;
-            const float m = (s <= row) ? exp2f(Glr - sm.Gl[s]) : 0.f;
-            sv[i] = (s < row) ? br * kk[i] * m : 0.f;
-            pv[i] = needP ? pv[i] * m : 0.f;
+            const float m = (s < row) ? exp2f(Glr - sm.Gl[s]) : 0.f;
+            sv[i] = br * kk[i] * m;
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sv[i] = pv[i] = 0.f;
+          for (int i = 0; i < 16; ++i) sv[i] = 0.f;
         }
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -359,17 +362,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             *reinterpret_cast<float4*>(sd + 4 * q) = make_float4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
-        }
-        if (needP) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint4 o;
-            o.x = pack_bf16(pv[8 * q + 0], pv[8 * q + 1]);
-            o.y = pack_bf16(pv[8 * q + 2], pv[8 * q + 3]);
-            o.z = pack_bf16(pv[8 * q + 4], pv[8 * q + 5]);
-            o.w = pack_bf16(pv[8 * q + 6], pv[8 * q + 7]);
-            *reinterpret_cast<uint4*>(prow + c0 + 8 * q) = o;
-          }
         }
       }
     }
@@ -441,18 +433,62 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
       mphase ^= 1;
       tc::fence_after();
     }
-    if (needW) {
-      bf16* wrow = a.W + chunk_id * tile + (long)row * CH + 64 * hh;
-      tmem_row_to_bf16(tlane + 256 + 64 * hh, wrow, wrow + 32);
+    // ---- w, u and P leave through shared staging tiles and TMA stores ------------
+    // (diag(gamma) K, T' and S/T are dead now; their buffers hold w, u and P)
+    if (needW) tmem_row_to_tile(tlane + 256 + 64 * hh, sm.Kg, row, hh);
+    if (needU) tmem_row_to_tile(tlane + 384 + 64 * hh, sm.Tp, row, hh);
+    if (needP) {  // P = (Q K^T) * M, diagonal included
+      const float Glr = sm.Gl[row];
+      unsigned char* pt = reinterpret_cast<unsigned char*>(sm.Fh);
+#pragma unroll 1
+      for (int cb = 0; cb < 64; cb += 16) {
+        const int c0 = 64 * hh + cb;
+        float pv[16];
+        if (c0 <= 32 * quarter + 31) {  // warp-uniform
+          tc::ld16(tlane + 128 + c0, pv);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int s = c0 + i;
+            pv[i] = (s <= row) ? pv[i] * exp2f(Glr - sm.Gl[s]) : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pv[i] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint4 o;
+          o.x = pack_bf16(pv[8 * q + 0], pv[8 * q + 1]);
+          o.y = pack_bf16(pv[8 * q + 2], pv[8 * q + 3]);
+          o.z = pack_bf16(pv[8 * q + 4], pv[8 * q + 5]);
+          o.w = pack_bf16(pv[8 * q + 6], pv[8 * q + 7]);
+          *reinterpret_cast<uint4*>(pt + tc::sw128_chunk(row, (c0 >> 3) + q, CH)) = o;
+        }
+      }
     }
-    if (needU) {
-      bf16* urow = a.U + chunk_id * tile + (long)row * HD + 64 * hh;
-      tmem_row_to_bf16(tlane + 384 + 64 * hh, urow, urow + 32);
-    }
+    tc::fence_proxy_async();
     tc::fence_before();
-    __syncthreads();  // TMEM w/u, Tp, Kg, F and the gate vectors are free for the next value head
+    __syncthreads();  // staging tiles complete; TMEM w/u and the gate vectors are free
     tc::fence_after();
+    if (tid == 0 && (needW || needU || needP)) {
+      const int y = (int)(chunk_id * CH);
+      if (needW) {
+        tc::tma_store_2d(&mp.W, 0, y, sm.Kg);
+        tc::tma_store_2d(&mp.W, 64, y, sm.Kg + TILE / 2);
+      }
+      if (needU) {
+        tc::tma_store_2d(&mp.U, 0, y, sm.Tp);
+        tc::tma_store_2d(&mp.U, 64, y, sm.Tp + TILE / 2);
+      }
+      if (needP) {
+        const unsigned char* pt = reinterpret_cast<const unsigned char*>(sm.Fh);
+        tc::tma_store_2d(&mp.P, 0, y, pt);
+        tc::tma_store_2d(&mp.P, 64, y, pt + TILE / 2);
+      }
+      tc::bulk_commit();
+    }
   }
+  if (tid == 0) tc::bulk_wait();  // the stores have completed before the block exits
   if (!ok && a.status) atomicOr(a.status, 1);
   tc::fence_before();
   __syncthreads();
@@ -469,6 +505,10 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
   if (!tmap_heads(&mp.k, a.k, a.B, a.T, a.Hk, HD)) return cudaErrorInvalidValue;
   if (a.P && !tmap_heads(&mp.q, a.q, a.B, a.T, a.Hk, HD)) return cudaErrorInvalidValue;
   if (a.U && !tmap_heads(&mp.v, a.v, a.B, a.T, a.Hv, HD)) return cudaErrorInvalidValue;
+  const uint64_t rows = (uint64_t)a.B * a.Hv * a.NC * CH;
+  if (a.W && !tmap_2d(&mp.W, a.W, HD, rows, HD * sizeof(bf16), 64, CH, true)) return cudaErrorInvalidValue;
+  if (a.U && !tmap_2d(&mp.U, a.U, HD, rows, HD * sizeof(bf16), 64, CH, true)) return cudaErrorInvalidValue;
+  if (a.P && !tmap_2d(&mp.P, a.P, CH, rows, CH * sizeof(bf16), 64, CH, true)) return cudaErrorInvalidValue;
   const size_t smem = prep_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -269,11 +269,22 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, con
                "r"(x), "r"(y), "r"(smem_u32(src))
                : "memory");
 }
+__device__ __forceinline__ void tma_store_4d(const void* tmap, int x, int y, int z, int w, const void* src) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(tmap),
+               "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(src))
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the shared sources of every committed store have been read (may be overwritten)
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // every committed store has completed
 __device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// byte offset of the 16-byte chunk j (0..3) of row r in a [rows x 32] bf16 tile
+// with the 64-byte swizzle (chunk j of row r sits at j ^ ((r / 2) % 4))
+__device__ __forceinline__ uint32_t sw64_chunk(int r, int j) {
+  return (uint32_t)(r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+}
 
 }  // namespace tc
 }  // namespace gdn

@@ -40,6 +40,21 @@ inline bool tmap_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ro
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 matrix with an explicit swizzle mode (for 32-column slices: 64-byte
+// swizzle, box of 32 columns x box_rows rows).
+inline bool tmap_2d_sw(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                       uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // bf16 activations [B][T][H][D]; box = 64 columns of one head over 128 tokens
 // (128-byte swizzle), tokens past T read as zero.
 inline bool tmap_heads(CUtensorMap* m, const void* base, int B, int T, int H, int D) {

@@ -43,18 +43,20 @@ namespace {
 
 constexpr int NC_THREADS = 128;               // compute threads
 constexpr int NT = NC_THREADS + 64;           // + the MMA issuer warp + the TMA producer warp
-constexpr int NSLOT = 6;
+constexpr int NRING = 5;                      // tile ring
+constexpr uint32_t STAGE_BYTES = 4 * 8192;    // staging of stored 32-column slices
 constexpr uint32_t TILE_BYTES = CH * HD * 2;  // 32 KiB
 constexpr uint32_t BT_BYTES = SL * HD * 2;    // 8 KiB: a [32 x 128] B-operand tile
 
 struct WalkBwdSmem {
-  unsigned char slot[NSLOT][TILE_BYTES];
+  unsigned char slot[NRING][TILE_BYTES];
+  unsigned char stage[STAGE_BYTES];  // dh' and dDelta slices, double-buffered, 64-byte swizzle
   unsigned char Xt[BT_BYTES];   // dh'^T
   unsigned char Yt[BT_BYTES];   // (-Y)^T
   unsigned char Ot[BT_BYTES];   // dO^T (this slice)
   unsigned char Ogt[BT_BYTES];  // (diag(gamma) dO)^T
   float gsum[2][4];
-  uint64_t full[NSLOT], empty[NSLOT];
+  uint64_t full[NRING], empty[NRING];
   uint64_t barO, barXt, barYt, barP, barQ, barY, barH;
   uint32_t tmem;
 };
@@ -68,7 +70,8 @@ __device__ __forceinline__ void write_bt_column(unsigned char* tile, int k, cons
   for (int n = 0; n < 32; ++n)
     *reinterpret_cast<bf16*>(tile + tc::sw128(n, k, 32)) = __float2bfloat16_rn(v[n]);
 }
-__device__ __forceinline__ void store_row_bf16(bf16* dst, const float (&v)[32]) {
+// row r (32 values) of a [128 x 32] staging slice, 64-byte swizzle
+__device__ __forceinline__ void stage_row(unsigned char* buf, int r, const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint4 o;
@@ -76,7 +79,7 @@ __device__ __forceinline__ void store_row_bf16(bf16* dst, const float (&v)[32]) 
     o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
     o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
     o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-    *reinterpret_cast<uint4*>(dst + 8 * q) = o;
+    *reinterpret_cast<uint4*>(buf + tc::sw64_chunk(r, q)) = o;
   }
 }
 __device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32]) {
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
   auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
 
   if (tid == 0) {
-    for (int k = 0; k < NSLOT; ++k) {
+    for (int k = 0; k < NRING; ++k) {
       tc::mbar_init(&sm.full[k], 1);
       tc::mbar_init(&sm.empty[k], 1);
     }
@@ -213,13 +216,13 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
   tc::fence_after();
   const uint32_t tmem = sm.tmem;
 
-  auto issue = [&](int i) {  // TMA request of tile i into slot i % NSLOT
+  auto issue = [&](int i) {  // TMA request of tile i into slot i % NRING
     const int ci = i / TPC, t = i % TPC;
     const int c = chunk_of(ci);
     const int kind = withO ? t : (t == 0 ? 2 : 3);  // 0 P, 1 Q, 2 K, 3 w
     const long cid = bh * a.NC + c;
-    unsigned char* dst = sm.slot[i % NSLOT];
-    uint64_t* bar = &sm.full[i % NSLOT];
+    unsigned char* dst = sm.slot[i % NRING];
+    uint64_t* bar = &sm.full[i % NRING];
     tc::arrive_expect_tx(bar, TILE_BYTES);
     if (kind == 0 || kind == 3) {
       const CUtensorMap* m = (kind == 0) ? &mp.P : &mp.W;
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
     // ========================================================== TMA producer
     if (lane == 0) {
       for (int i = 0; i < ntiles; ++i) {
-        if (i >= NSLOT) ok = ok && tc::mbar_wait(&sm.empty[i % NSLOT], (uint32_t)((i / NSLOT - 1) & 1));
+        if (i >= NRING) ok = ok && tc::mbar_wait(&sm.empty[i % NRING], (uint32_t)((i / NRING - 1) & 1));
         issue(i);
       }
     }
@@ -248,9 +251,9 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
     // chunk's P^T dO the gap while dh is formed.  After each product its tile
     // slot is released to the producer by a commit to the slot's empty barrier.
     if (lane == 0) {
-      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NSLOT], (i / NSLOT) & 1); };
-      auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NSLOT]); };
-      auto release = [&](int i) { tc::commit(&sm.empty[i % NSLOT]); };
+      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NRING], (i / NRING) & 1); };
+      auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NRING]); };
+      auto release = [&](int i) { tc::commit(&sm.empty[i % NRING]); };
       auto issue_p = [&](int ci) {  // P^T dO of chunk ci (its dO images are written)
         ok = ok && tc::mbar_wait(&sm.barO, (uint32_t)(ci & 1));
         wait_tile(ci * TPC);
@@ -301,7 +304,8 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
     for (int ci = 0; ci < n; ++ci) {
       const int c = chunk_of(ci);
       const uint32_t par = (uint32_t)(ci & 1);
-      if (!FOLD && a.dstates) store_row_bf16(a.dstates + ((bh * a.NC + c) * HD + r) * HD + col0, x);
+      // staging of chunk index i: dh' at stage[(i & 1) * 8192], dDelta at stage[16384 + (i & 1) * 8192]
+      if (!FOLD && a.dstates) stage_row(sm.stage + (ci & 1) * 8192, r, x);
       part = scan_part(gnext, ci + 1);  // gates of the next chunk
       gnext = load_g(ci + 2);
 
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
 #pragma unroll
         for (int q = 0; q < 32; ++q) y[q] += pd[q];
       }
-      if (!FOLD && a.ddelta) store_row_bf16(a.ddelta + ((bh * a.NC + c) * CH + r) * HD + col0, y);
+      if (!FOLD && a.ddelta) stage_row(sm.stage + 16384 + (ci & 1) * 8192, r, y);
 #pragma unroll
       for (int q = 0; q < 32; ++q) y[q] = -y[q];
       write_bt_column(sm.Yt, r, y);
@@ -330,7 +334,17 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
 
       // ---- gates and dO images of the next chunk -------------------------------------
       const float gC_cur = gC;
+      // this chunk's staged slices leave by TMA stores; before the barrier every
+      // earlier store has read its staging buffer
+      tc::fence_proxy_async();
+      if (tid == 0) tc::bulk_wait_read();
       asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");
+      if (tid == 0 && !FOLD && (a.dstates || a.ddelta)) {
+        if (a.dstates) tc::tma_store_2d(&mp.Ds, col0, (int)((bh * a.NC + c) * HD), sm.stage + (ci & 1) * 8192);
+        if (a.ddelta)
+          tc::tma_store_2d(&mp.Dd, col0, (int)((bh * a.NC + c) * CH), sm.stage + 16384 + (ci & 1) * 8192);
+        tc::bulk_commit();
+      }
       finish_gates(part, ci + 1);
       if (withO && ci + 1 < n) {  // both dO products of this chunk have read the images
         ok = ok && tc::mbar_wait(&sm.barQ, par);
@@ -355,6 +369,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
         arrive(&sm.barXt);
       }
     }
+    if (tid == 0) tc::bulk_wait();  // every store has completed before the block exits
     if (FOLD) {
       store_row_f32((partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0, x);
     } else if (a.dh0 && seg == 0) {

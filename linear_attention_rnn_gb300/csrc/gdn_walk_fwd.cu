@@ -45,7 +45,7 @@ namespace {
 
 constexpr int NC_THREADS = 128;                // compute threads: one per chunk row / state row
 constexpr int NT = NC_THREADS + 64;            // + the MMA issuer warp + the TMA producer warp
-constexpr int NSLOT = 6;                       // tile ring
+constexpr int NSLOT = 6;                       // tile ring slots (the last one doubles as staging)
 constexpr uint32_t TILE_BYTES = CH * HD * 2;   // 32 KiB
 constexpr uint32_t BT_BYTES = SL * HD * 2;     // 8 KiB: a [32 x 128] B-operand tile
 
@@ -79,11 +79,25 @@ __device__ __forceinline__ void store_row_bf16(bf16* dst, const float (&v)[32]) 
   }
 }
 
+// row r (32 values) of a [128 x 32] staging slice, 64-byte swizzle
+__device__ __forceinline__ void stage_row(unsigned char* buf, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 o;
+    o.x = pack_bf16(v[8 * q], v[8 * q + 1]);
+    o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(buf + tc::sw64_chunk(r, q)) = o;
+  }
+}
+
 __device__ __forceinline__ void arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-template <bool FOLD>
+// STAGED: the recompute mode (exports h and Delta, no output).
+template <bool FOLD, bool STAGED>
 __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_constant__ WalkFwdMaps mp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -98,6 +112,13 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
   const int TPC = withO ? 4 : 2;  // tiles per chunk: w, (Q,) K (, P)
   const int ntiles = (cend - cbeg) * TPC;
   const int col0 = (slice & 3) * SL;
+  // The recompute mode stages its exported h and Delta slices in the last
+  // slot (four 8 KiB buffers: h and Delta, double-buffered, 64-byte swizzle)
+  // and streams its 2 tiles per chunk through a 5-slot ring; otherwise all 6
+  // slots form the ring (the output's 4 tiles per chunk need the depth).
+  constexpr bool staged = STAGED;
+  constexpr int nring = STAGED ? NSLOT - 1 : NSLOT;  // compile-time: the ring index is on the issue path
+  unsigned char* stage = sm.slot[NSLOT - 1];
   if (cbeg >= cend) return;
   auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
   // tile sequence of a chunk: w, Q, K, P (with output) or w, K
@@ -191,12 +212,12 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
   const uint32_t tmem = sm.tmem;
   auto o1_col = [](int ci) { return (ci & 1) ? 128u : 64u; };
 
-  auto issue = [&](int i) {  // TMA request of tile i into slot i % NSLOT
+  auto issue = [&](int i) {  // TMA request of tile i into slot i % nring
     const int c = cbeg + i / TPC, t = i % TPC;
     const int kind = withO ? t : (t == 0 ? 0 : 2);
     const long cid = bh * a.NC + c;
-    unsigned char* dst = sm.slot[i % NSLOT];
-    uint64_t* bar = &sm.full[i % NSLOT];
+    unsigned char* dst = sm.slot[i % nring];
+    uint64_t* bar = &sm.full[i % nring];
     tc::arrive_expect_tx(bar, TILE_BYTES);
     if (kind == 0 || kind == 3) {
       const CUtensorMap* m = (kind == 0) ? &mp.W : &mp.P;
@@ -211,11 +232,11 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
 
   if (warp == 5) {
     // ========================================================== TMA producer
-    // Tile i goes into slot i % NSLOT once the product that read tile
-    // i - NSLOT has completed (signalled on that slot's empty barrier).
+    // Tile i goes into slot i % nring once the product that read tile
+    // i - nring has completed (signalled on that slot's empty barrier).
     if (lane == 0) {
       for (int i = 0; i < ntiles; ++i) {
-        if (i >= NSLOT) ok = ok && tc::mbar_wait(&sm.empty[i % NSLOT], (uint32_t)((i / NSLOT - 1) & 1));
+        if (i >= nring) ok = ok && tc::mbar_wait(&sm.empty[i % nring], (uint32_t)((i / nring - 1) & 1));
         issue(i);
       }
     }
@@ -227,9 +248,9 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
     // of issue is the order of execution.  After each product its tile slot is
     // released to the producer by a commit to the slot's empty barrier.
     if (lane == 0) {
-      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NSLOT], (i / NSLOT) & 1); };
-      auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NSLOT]); };
-      auto release = [&](int i) { tc::commit(&sm.empty[i % NSLOT]); };
+      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % nring], (i / nring) & 1); };
+      auto slot_of = [&](int i) { return smem_u32(sm.slot[i % nring]); };
+      auto release = [&](int i) { tc::commit(&sm.empty[i % nring]); };
       for (int c = cbeg; c < cend; ++c) {
         const int ci = c - cbeg;
         const uint32_t par = (uint32_t)(ci & 1);
@@ -272,8 +293,8 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
     for (int c = cbeg; c < cend; ++c) {
       const int ci = c - cbeg;
       const uint32_t par = (uint32_t)(ci & 1);
-      const int L = rows_of(c);
-      if (!FOLD && a.states) store_row_bf16(a.states + ((bh * a.NC + c) * HD + r) * HD + col0, h);
+      // staging of chunk index i: h at stage[(i & 1) * 8192], Delta at stage[16384 + (i & 1) * 8192]
+      if (!FOLD && a.states) stage_row(stage + (ci & 1) * 8192, r, h);
 
       // ---- Delta = u - X -------------------------------------------------------
       ok = ok && tc::mbar_wait(&sm.barX, par);
@@ -313,13 +334,24 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
         tc::fence_before();
         arrive(&sm.barD);
       }
-      if (!FOLD && a.delta) store_row_bf16(a.delta + ((bh * a.NC + c) * CH + r) * HD + col0, x);
+      if (!FOLD && a.delta) stage_row(stage + 16384 + (ci & 1) * 8192, r, x);
 
       // ---- gates of chunk c + 1, while K^T (ef Delta) runs ----------------------------
       float gam_n, ef_n, gC_n;
       part = scan_part(gnext, ci + 1);
       gnext = load_g(c + 2);
+      // this chunk's staged h and Delta leave by TMA stores; before the barrier
+      // every earlier store has read its staging buffer
+      if (staged) {
+        tc::fence_proxy_async();
+        if (tid == 0) tc::bulk_wait_read();
+      }
       asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");
+      if (staged && tid == 0) {
+        if (a.states) tc::tma_store_2d(&mp.St, col0, (int)((bh * a.NC + c) * HD), stage + (ci & 1) * 8192);
+        if (a.delta) tc::tma_store_2d(&mp.De, col0, (int)((bh * a.NC + c) * CH), stage + 16384 + (ci & 1) * 8192);
+        tc::bulk_commit();
+      }
       finish_gates(part, ci + 1, gam_n, ef_n, gC_n);
 
       // ---- h' = gamma_C h + H' ---------------------------------------------------
@@ -340,7 +372,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
         float o1[32], o2[32];
         tc::ld32(tl + o1_col(ci), o1);
         tc::ld32(tl + 96, o2);
-        if (r < L) {
+        if (r < rows_of(c)) {
 #pragma unroll
           for (int n = 0; n < 32; ++n) o1[n] = gam_r * o1[n] + o2[n];
           store_row_bf16(a.o + (((long)b * a.T + (long)c * CH + r) * a.Hv + j) * HD + col0, o1);
@@ -350,6 +382,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
       ef_r = ef_n;
       gC = gC_n;
     }
+    if (staged && tid == 0) tc::bulk_wait();  // every store has completed before the block exits
     if (FOLD) {
       float* dst = (partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0;
 #pragma unroll
@@ -368,12 +401,13 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
   if (warp == 0) tc::dealloc(tmem, 256);
 }
 
-template <bool FOLD>
+template <bool FOLD, bool STAGED>
 cudaError_t launch_one(const WalkFwdArgs& a, const WalkFwdMaps& m, cudaStream_t s) {
   const size_t smem = sizeof(WalkSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_walk_fwd<FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_walk_fwd<FOLD, STAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_walk_fwd<FOLD><<<dim3(FOLD ? 8 : HD / SL, a.S, a.B * a.Hv), NT, smem, s>>>(a, m);
+  k_walk_fwd<FOLD, STAGED><<<dim3(FOLD ? 8 : HD / SL, a.S, a.B * a.Hv), NT, smem, s>>>(a, m);
   return cudaGetLastError();
 }
 
@@ -382,7 +416,10 @@ cudaError_t launch_one(const WalkFwdArgs& a, const WalkFwdMaps& m, cudaStream_t 
 size_t walk_fwd_smem_bytes(int) { return sizeof(WalkSmem) + 1024; }
 
 cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold, cudaStream_t s) {
-  return fold ? launch_one<true>(a, m, s) : launch_one<false>(a, m, s);
+  const bool staged = a.states != nullptr || a.delta != nullptr;
+  if (fold) return launch_one<true, false>(a, m, s);
+  if (staged && a.o) return cudaErrorInvalidValue;  // one mode per launch: they share the last slot
+  return staged ? launch_one<false, true>(a, m, s) : launch_one<false, false>(a, m, s);
 }
 
 }  // namespace gdn
