@@ -49,9 +49,10 @@ KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 0>", "walk_states": "k
                  "walk_bwd": "k_walk_bwd<0>", "grads": "k_grads",
                  "fold": "k_walk_fwd<1, 0>", "prefix": "k_affine_walk",
                  "fold_bwd": "k_walk_bwd<1>", "prefix_bwd": "k_affine_walk"}
-# DRAM traffic per launch from the committed ncu capture of the same kernels
-# (profiles/*), keyed by kernel; None until captured for the current code.
-NCU_TRAFFIC = {}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum, bytes)
+# from the committed ncu capture of the same kernel code (profiles/*), keyed by
+# kernel; a kernel changed since its capture has no entry.
+NCU_TRAFFIC = {"grads": 316925440}  # profiles/k_grads_layer_t4096_ncu_full.md: 270.06 MB + 46.86 MB
 
 
 def algorithmic(wl):
