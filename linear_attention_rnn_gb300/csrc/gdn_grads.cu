@@ -167,6 +167,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
   if (tid == 0) ok = tc::mbar_wait(&sm.barKQ, 0);
   ok = ok && tc::mbar_wait(&sm.barKQ, 0);  // K and Q rows are read by the epilogues too
 
+  // g and beta of row tid for value head kh * group + jj (loaded a head ahead)
+  auto load_gates = [&](int jj, float& gv, float& bv) {
+    gv = bv = 0.f;
+    if (tid < L && jj < group) {
+      const long idx = ((long)b * a.T + t0 + tid) * a.Hv + kh * group + jj;
+      gv = a.g[idx];
+      bv = a.beta[idx];
+    }
+  };
+  float g_next = 0.f, b_next = 0.f;
+  if (tid < CH) load_gates(0, g_next, b_next);
+
   for (int jj = 0; jj < group; ++jj) {
     const int j = kh * group + jj;
     const long cid = cid_of(jj);
@@ -174,9 +186,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
     const uint32_t par = (uint32_t)(jj & 1);
     // ---- gates of value head j; per-row sums cleared ----------------------------
     if (tid < CH) {
-      const long idx = tokv + (long)tid * a.Hv;
-      sm.Gl[tid] = tid < L ? a.g[idx] : 0.f;
-      sm.beta[tid] = tid < L ? a.beta[idx] : 0.f;
+      sm.Gl[tid] = g_next;
+      sm.beta[tid] = b_next;
+      load_gates(jj + 1, g_next, b_next);
       sm.colX[tid] = sm.dbeta[tid] = sm.dbg[tid] = sm.d_ef[tid] = sm.rowX[tid] = sm.dgamO[tid] = 0.f;
     }
     if (tid == 0) {  // S1: dV' = T^T dDelta (both tiles read MN-major)

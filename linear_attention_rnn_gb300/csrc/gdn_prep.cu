@@ -272,18 +272,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
   }
   uint32_t mphase = 0;
 
+  // g and beta of row tid for value head kh * group + jj (loaded a head ahead)
+  auto load_gates = [&](int jj, float& gv, float& bv) {
+    gv = bv = 0.f;
+    if (tid < L && jj < group) {
+      const long idx = ((long)b * a.T + t0 + tid) * a.Hv + kh * group + jj;
+      gv = a.g[idx];
+      bv = a.beta[idx];
+    }
+  };
+  float g_next = 0.f, b_next = 0.f;
+  if (tid < CH) load_gates(0, g_next, b_next);
+
   for (int jj = 0; jj < group; ++jj) {
     const int j = kh * group + jj;
     const long bh = (long)b * a.Hv + j;
     const long chunk_id = bh * a.NC + c;
-    // the previous value head's stores have read their staging tiles before the
-    // barriers below let anyone rewrite them
-    if (tid == 0 && jj > 0) tc::bulk_wait_read();
     // ---- gates of value head j --------------------------------------------------
     if (tid < CH) {
-      const long idx = ((long)b * a.T + t0 + tid) * a.Hv + j;
-      sm.Gl[tid] = tid < L ? a.g[idx] : 0.f;
-      sm.beta[tid] = tid < L ? a.beta[idx] : 0.f;
+      sm.Gl[tid] = g_next;
+      sm.beta[tid] = b_next;
+      load_gates(jj + 1, g_next, b_next);
     }
     __syncthreads();
     if (warp == 0) {
@@ -297,6 +306,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
         sm.gamma[lane * 4 + i] = expf(v[i]);
       }
     }
+    // the previous value head's stores have read their staging tiles (Kg and Tp)
+    // before the barrier below lets anyone rewrite them
+    if (tid == 0 && jj > 0) tc::bulk_wait_read();
     if (jj == 0) {  // K K^T, Q K^T complete; K readable
       ok = ok && tc::mbar_wait(&sm.barKQ, 0);
       ok = ok && tc::mbar_wait(&sm.barM, mphase);
@@ -312,43 +324,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
     }
     __syncthreads();
 
-    // ---- diag(gamma) K ----------------------------------------------------------------
-#pragma unroll
-    for (int i = 0; i < (CH * 16) / NTHREADS; ++i) {
-      const int idx = tid + i * NTHREADS;
-      const int r = idx >> 4, jc = idx & 15;
-      const uint32_t off = tc::sw128_chunk(r, jc, CH);
-      const uint4 x = *reinterpret_cast<const uint4*>(sm.K + off);
-      const float gm = sm.gamma[r];
-      const float2 x0 = unpack_bf16(x.x), x1 = unpack_bf16(x.y), x2 = unpack_bf16(x.z), x3 = unpack_bf16(x.w);
-      uint4 o;
-      o.x = pack_bf16(gm * x0.x, gm * x0.y);
-      o.y = pack_bf16(gm * x1.x, gm * x1.y);
-      o.z = pack_bf16(gm * x2.x, gm * x2.y);
-      o.w = pack_bf16(gm * x3.x, gm * x3.y);
-      *reinterpret_cast<uint4*>(sm.Kg + off) = o;
-    }
-
-    // ---- S (hi/lo into F, fp32 diagonal blocks into Sd) -------------------------------
+    // ---- S (hi/lo into F, fp32 diagonal blocks into Sd) and P (bf16 staging in Kg) ----
     {
       const float Glr = sm.Gl[row], br = sm.beta[row];
       float* Sd = reinterpret_cast<float*>(sm.Tp + SD);
 #pragma unroll 1
       for (int cb = 0; cb < 64; cb += 16) {
         const int c0 = 64 * hh + cb;
-        float sv[16];
+        float sv[16], pv[16];
         if (c0 <= 32 * quarter + 31) {  // warp-uniform: the block reaches the diagonal
           float kk[16];
           tc::ld16(tlane + c0, kk);
+          if (needP) tc::ld16(tlane + 128 + c0, pv);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int s = c0 + i;
-            const float m = (s < row) ? exp2f(Glr - sm.Gl[s]) : 0.f;
-            sv[i] = br * kk[i] * m;
+            const float m = (s <= row) ? exp2f(Glr - sm.Gl[s]) : 0.f;  // one exponential for S and P
+            sv[i] = (s < row) ? br * kk[i] * m : 0.f;
+            pv[i] = needP ? pv[i] * m : 0.f;
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sv[i] = 0.f;
+          for (int i = 0; i < 16; ++i) sv[i] = pv[i] = 0.f;
+        }
+        if (needP) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint4 o;
+            o.x = pack_bf16(pv[8 * q + 0], pv[8 * q + 1]);
+            o.y = pack_bf16(pv[8 * q + 2], pv[8 * q + 3]);
+            o.z = pack_bf16(pv[8 * q + 4], pv[8 * q + 5]);
+            o.w = pack_bf16(pv[8 * q + 6], pv[8 * q + 7]);
+            *reinterpret_cast<uint4*>(sm.Kg + tc::sw128_chunk(row, (c0 >> 3) + q, CH)) = o;
+          }
         }
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -365,8 +373,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
         }
       }
     }
-    tc::fence_proxy_async();  // diag(gamma) K is read by the tensor core
+    tc::fence_proxy_async();  // P is read by a TMA store
     __syncthreads();
+    if (tid == 0 && needP) {  // P leaves while the inverse runs
+      const int y = (int)(chunk_id * CH);
+      tc::tma_store_2d(&mp.P, 0, y, sm.Kg);
+      tc::tma_store_2d(&mp.P, 64, y, sm.Kg + TILE / 2);
+      tc::bulk_commit();
+    }
     auto export_f32 = [&](float* dst) {
       for (int i = tid; i < CH * 16; i += NTHREADS) {
         const int r = i >> 4, jc = i & 15;
@@ -398,6 +412,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
         *reinterpret_cast<uint4*>(dst + r * CH + 8 * jc) = o;
       }
     }
+    // P's store has read Kg before diag(gamma) K is written there
+    if (tid == 0) tc::bulk_wait_read();
+    __syncthreads();
+    // ---- diag(gamma) K (B operand of w) ------------------------------------------------
+#pragma unroll
+    for (int i = 0; i < (CH * 16) / NTHREADS; ++i) {
+      const int idx = tid + i * NTHREADS;
+      const int r = idx >> 4, jc = idx & 15;
+      const uint32_t off = tc::sw128_chunk(r, jc, CH);
+      const uint4 x = *reinterpret_cast<const uint4*>(sm.K + off);
+      const float gm = sm.gamma[r];
+      const float2 x0 = unpack_bf16(x.x), x1 = unpack_bf16(x.y), x2 = unpack_bf16(x.z), x3 = unpack_bf16(x.w);
+      uint4 o;
+      o.x = pack_bf16(gm * x0.x, gm * x0.y);
+      o.y = pack_bf16(gm * x1.x, gm * x1.y);
+      o.z = pack_bf16(gm * x2.x, gm * x2.y);
+      o.w = pack_bf16(gm * x3.x, gm * x3.y);
+      *reinterpret_cast<uint4*>(sm.Kg + off) = o;
+    }
+
     // ---- T' = T diag(beta) (bf16, K-major SW128) --------------------------------------
 #pragma unroll
     for (int i = 0; i < (CH * 16) / NTHREADS; ++i) {
@@ -433,44 +467,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
       mphase ^= 1;
       tc::fence_after();
     }
-    // ---- w, u and P leave through shared staging tiles and TMA stores ------------
-    // (diag(gamma) K, T' and S/T are dead now; their buffers hold w, u and P)
+    // ---- w and u leave through shared staging tiles and TMA stores ------------------
+    // (diag(gamma) K and T' are dead now; their buffers hold w and u)
     if (needW) tmem_row_to_tile(tlane + 256 + 64 * hh, sm.Kg, row, hh);
     if (needU) tmem_row_to_tile(tlane + 384 + 64 * hh, sm.Tp, row, hh);
-    if (needP) {  // P = (Q K^T) * M, diagonal included
-      const float Glr = sm.Gl[row];
-      unsigned char* pt = reinterpret_cast<unsigned char*>(sm.Fh);
-#pragma unroll 1
-      for (int cb = 0; cb < 64; cb += 16) {
-        const int c0 = 64 * hh + cb;
-        float pv[16];
-        if (c0 <= 32 * quarter + 31) {  // warp-uniform
-          tc::ld16(tlane + 128 + c0, pv);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int s = c0 + i;
-            pv[i] = (s <= row) ? pv[i] * exp2f(Glr - sm.Gl[s]) : 0.f;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pv[i] = 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint4 o;
-          o.x = pack_bf16(pv[8 * q + 0], pv[8 * q + 1]);
-          o.y = pack_bf16(pv[8 * q + 2], pv[8 * q + 3]);
-          o.z = pack_bf16(pv[8 * q + 4], pv[8 * q + 5]);
-          o.w = pack_bf16(pv[8 * q + 6], pv[8 * q + 7]);
-          *reinterpret_cast<uint4*>(pt + tc::sw128_chunk(row, (c0 >> 3) + q, CH)) = o;
-        }
-      }
-    }
     tc::fence_proxy_async();
     tc::fence_before();
     __syncthreads();  // staging tiles complete; TMEM w/u and the gate vectors are free
     tc::fence_after();
-    if (tid == 0 && (needW || needU || needP)) {
+    if (tid == 0 && (needW || needU)) {
       const int y = (int)(chunk_id * CH);
       if (needW) {
         tc::tma_store_2d(&mp.W, 0, y, sm.Kg);
@@ -479,11 +484,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
       if (needU) {
         tc::tma_store_2d(&mp.U, 0, y, sm.Tp);
         tc::tma_store_2d(&mp.U, 64, y, sm.Tp + TILE / 2);
-      }
-      if (needP) {
-        const unsigned char* pt = reinterpret_cast<const unsigned char*>(sm.Fh);
-        tc::tma_store_2d(&mp.P, 0, y, pt);
-        tc::tma_store_2d(&mp.P, 64, y, pt + TILE / 2);
       }
       tc::bulk_commit();
     }
