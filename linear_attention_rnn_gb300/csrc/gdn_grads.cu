@@ -47,6 +47,7 @@ struct GradSmem {
   unsigned char W3[TILE];          // h
   unsigned char W4[TILE];          // Delta; dQK
   float Gl[CH], gam[CH], ef[CH], beta[CH];
+  float etab[CH];  // exp2(Gl[c0] - Gl[s]) for the 16-column block c0 of column s
   float colX[CH], dbeta[CH], dbg[CH], d_ef[CH], rowX[CH], dgamO[CH];
   float red[8];
   uint64_t barKQ, barT, barDD, barH, barDl, barDH, barDO, barM;
@@ -212,11 +213,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
         sm.gam[r] = expf(v[i]);
         sm.ef[r] = expf(Glast - v[i]);
       }
+      __syncwarp();  // every Gl of the chunk is written (by this warp)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane * 4 + i;
+        sm.etab[r] = exp2f(sm.Gl[r & ~15] - sm.Gl[r]);  // >= 1
+      }
     }
     __syncthreads();
     const float Glr = sm.Gl[row], br = sm.beta[row], gr = sm.gam[row], efr = sm.ef[row];
     const float bgr = br * gr;
     float p_db = 0.f, p_dbg = 0.f, p_def = 0.f, p_rowx = 0.f, p_dgam = 0.f;
+    // Decays exp2(Gl_r - Gl_s) of columns c0..c0+31 of this thread's row, masked to
+    // s < r (or s <= r).  G is non-increasing, so in each 16-column block b0 the decay
+    // is exp2(Gl_r - Gl_b0) (at most 1) times etab[s] (at least 1); a block whose Gl
+    // drops by more than 100 could overflow etab and takes the direct exponentials.
+    auto fill_decay = [&](int c0, float (&m)[32], bool incl) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b0 = c0 + 16 * h;
+        if (sm.Gl[b0] - sm.Gl[b0 + 15] <= 100.f) {  // block-uniform
+          const float fr = exp2f(Glr - sm.Gl[b0]);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) m[16 * h + i] = fr * sm.etab[b0 + i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) m[16 * h + i] = exp2f(Glr - sm.Gl[b0 + i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int s = c0 + i;
+        m[i] = (incl ? s <= row : s < row) ? m[i] : 0.f;
+      }
+    };
 
     // ---- E1: dV' -> W1 (bf16) ------------------------------------------------------------
     wait_mma();
@@ -346,12 +376,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
         float ds[32], kk[32];
         tc::ld32(tl + C_A + cb, ds);
         tc::ld32(tl + C_B + cb, kk);
+        fill_decay(c0, out, false);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int s = c0 + i;
-          const bool lower = s < row;
-          const float M = lower ? exp2f(Glr - sm.Gl[s]) : 0.f;
-          const float dS = lower ? -ds[i] : 0.f;
+          const float M = out[i];  // 0 off the strict lower triangle
+          const float dS = -ds[i];
           p_db += dS * kk[i] * M;
           const float dkk = dS * br * M;
           out[i] = dkk;
@@ -388,10 +417,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
         float dp[32], qk[32];
         tc::ld32(tl + C_A + cb, dp);
         tc::ld32(tl + C_B + cb, qk);
+        fill_decay(c0, out, true);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int s = c0 + i;
-          const float M = (s <= row) ? exp2f(Glr - sm.Gl[s]) : 0.f;
+          const float M = out[i];  // 0 above the diagonal
           const float d = dp[i] * M;
           out[i] = d;
           dp[i] = d * qk[i];

@@ -49,7 +49,8 @@ struct PrepSmem {
   unsigned char Tp[TILE];  // SW128 [r][s]: T diag(beta); during the inverse its scratch
   bf16 Fh[CH * CH];        // S, overwritten in place by T: high parts (XOR-swizzled rows)
   bf16 Fl[CH * CH];        // low parts
-  float Gl[CH], beta[CH], gamma[CH];
+  float Gl[CH], beta[CH];
+  float etab[CH];  // exp2(Gl[c0] - Gl[s]) for the 16-column block c0 of column s
   uint64_t barKQ, barV[2], barM;
   uint32_t tmem;
 };
@@ -173,8 +174,15 @@ __device__ __forceinline__ void ut_inverse(PrepSmem& sm, int warp, int lane) {
   for (int bs = 16; bs < CH; bs *= 2) {
     const int nb = bs >> 4, per = nb * nb;
     const int ntiles = (CH / (2 * bs)) * per;
+    // at b = 64 a warp takes two tiles whose k-step counts (nb - tn, then tm + 1)
+    // add up to 5, so that no warp carries two of the longest
     for (int t = warp; t < ntiles; t += 8) {
-      const int p = t / per, tm = (t % per) / nb, tn = t % nb;
+      int p = t / per, tm = (t % per) / nb, tn = t % nb;
+      if (nb == 4) {
+        p = 0;
+        tm = warp >> 1;
+        tn = (t < 8) ? (warp & 1) : 3 - (warp & 1);
+      }
       const int s0 = 2 * bs * p;
       float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kb = tn; kb < nb; ++kb) {  // X_A is lower triangular
@@ -194,7 +202,12 @@ __device__ __forceinline__ void ut_inverse(PrepSmem& sm, int warp, int lane) {
     }
     __syncthreads();
     for (int t = warp; t < ntiles; t += 8) {
-      const int p = t / per, tm = (t % per) / nb, tn = t % nb;
+      int p = t / per, tm = (t % per) / nb, tn = t % nb;
+      if (nb == 4) {
+        p = 0;
+        tn = warp >> 1;
+        tm = (t < 8) ? (warp & 1) : 3 - (warp & 1);
+      }
       const int s0 = 2 * bs * p;
       float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kb = 0; kb <= tm; ++kb) {  // X_D is lower triangular
@@ -303,7 +316,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         sm.Gl[lane * 4 + i] = v[i] * LOG2E;
-        sm.gamma[lane * 4 + i] = expf(v[i]);
+      }
+      __syncwarp();  // every Gl of the chunk is written (by this warp)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane * 4 + i;
+        sm.etab[r] = exp2f(sm.Gl[r & ~15] - sm.Gl[r]);  // >= 1
       }
     }
     // the previous value head's stores have read their staging tiles (Kg and Tp)
@@ -325,6 +343,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
     __syncthreads();
 
     // ---- S (hi/lo into F, fp32 diagonal blocks into Sd) and P (bf16 staging in Kg) ----
+    // The decay exp2(Gl_r - Gl_s), s <= r, in a 16-column block starting at c0 is
+    // exp2(Gl_r - Gl_c0) * etab[s]: G is non-increasing, so the first factor is
+    // at most 1 and the second at least 1.  A block whose Gl drops by more than
+    // 100 over its columns could overflow etab and takes the direct exponentials;
+    // elsewhere a row whose first factor underflows has true decays below 2^-26.
     {
       const float Glr = sm.Gl[row], br = sm.beta[row];
       float* Sd = reinterpret_cast<float*>(sm.Tp + SD);
@@ -333,13 +356,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
         const int c0 = 64 * hh + cb;
         float sv[16], pv[16];
         if (c0 <= 32 * quarter + 31) {  // warp-uniform: the block reaches the diagonal
-          float kk[16];
+          float kk[16], mv[16];
           tc::ld16(tlane + c0, kk);
           if (needP) tc::ld16(tlane + 128 + c0, pv);
+          if (sm.Gl[c0] - sm.Gl[c0 + 15] <= 100.f) {  // block-uniform
+            const float fr = exp2f(Glr - sm.Gl[c0]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mv[i] = fr * sm.etab[c0 + i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mv[i] = exp2f(Glr - sm.Gl[c0 + i]);
+          }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int s = c0 + i;
-            const float m = (s <= row) ? exp2f(Glr - sm.Gl[s]) : 0.f;  // one exponential for S and P
+            const float m = (s <= row) ? mv[i] : 0.f;  // one decay for S and P
             sv[i] = (s < row) ? br * kk[i] * m : 0.f;
             pv[i] = needP ? pv[i] * m : 0.f;
           }
@@ -422,7 +453,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
       const int r = idx >> 4, jc = idx & 15;
       const uint32_t off = tc::sw128_chunk(r, jc, CH);
       const uint4 x = *reinterpret_cast<const uint4*>(sm.K + off);
-      const float gm = sm.gamma[r];
+      const float gm = exp2f(sm.Gl[r]);  // gamma_r
       const float2 x0 = unpack_bf16(x.x), x1 = unpack_bf16(x.y), x2 = unpack_bf16(x.z), x3 = unpack_bf16(x.w);
       uint4 o;
       o.x = pack_bf16(gm * x0.x, gm * x0.y);
