@@ -42,7 +42,7 @@ namespace gdn {
 namespace {
 
 constexpr int NC_THREADS = 128;               // compute threads
-constexpr int NT = NC_THREADS + 64;           // + the MMA issuer warp + the TMA producer warp
+constexpr int NT = NC_THREADS + 96;           // + MMA issuer, TMA producer and TMA store warps
 constexpr int NRING = 5;                      // tile ring
 constexpr uint32_t STAGE_BYTES = 4 * 8192;    // staging of stored 32-column slices
 constexpr uint32_t TILE_BYTES = CH * HD * 2;  // 32 KiB
@@ -58,6 +58,7 @@ struct WalkBwdSmem {
   float gsum[2][4];
   uint64_t full[NRING], empty[NRING];
   uint64_t barO, barXt, barYt, barP, barQ, barY, barH;
+  uint64_t sfull[2], sempty[2];  // staging buffer set i & 1: written by the compute threads / read by its stores
   uint32_t tmem;
 };
 
@@ -123,6 +124,10 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
     tc::mbar_init(&sm.barQ, 1);
     tc::mbar_init(&sm.barY, 1);
     tc::mbar_init(&sm.barH, 1);
+    for (int k = 0; k < 2; ++k) {
+      tc::mbar_init(&sm.sfull[k], NC_THREADS);
+      tc::mbar_init(&sm.sempty[k], 1);
+    }
     tc::mbar_fence_init();
   }
   if (warp == 0) tc::alloc(&sm.tmem, 128);
@@ -235,7 +240,25 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
     }
   };
 
-  if (warp == 5) {
+  if (warp == 6) {
+    // ============================================================ TMA stores
+    // The staged dh' and dDelta slices of each chunk leave by TMA stores once the
+    // compute threads have signalled them; when the stores have read the buffers
+    // they are handed back.  A store request can block its thread.
+    if (!FOLD && lane == 0 && (a.dstates || a.ddelta)) {
+      for (int ci = 0; ci < n; ++ci) {
+        const int c = chunk_of(ci);
+        ok = ok && tc::mbar_wait(&sm.sfull[ci & 1], (uint32_t)((ci >> 1) & 1));
+        if (a.dstates) tc::tma_store_2d(&mp.Ds, col0, (int)((bh * a.NC + c) * HD), sm.stage + (ci & 1) * 8192);
+        if (a.ddelta)
+          tc::tma_store_2d(&mp.Dd, col0, (int)((bh * a.NC + c) * CH), sm.stage + 16384 + (ci & 1) * 8192);
+        tc::bulk_commit();
+        tc::bulk_wait_read();
+        arrive(&sm.sempty[ci & 1]);
+      }
+      tc::bulk_wait();  // every store has completed before the block exits
+    }
+  } else if (warp == 5) {
     // ========================================================== TMA producer
     if (lane == 0) {
       for (int i = 0; i < ntiles; ++i) {
@@ -305,6 +328,8 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
       const int c = chunk_of(ci);
       const uint32_t par = (uint32_t)(ci & 1);
       // staging of chunk index i: dh' at stage[(i & 1) * 8192], dDelta at stage[16384 + (i & 1) * 8192]
+      // staging buffer set ci & 1 was last read by the stores of chunk ci - 2
+      if (!FOLD && ci >= 2) ok = ok && tc::mbar_wait(&sm.sempty[ci & 1], (uint32_t)(((ci >> 1) + 1) & 1));
       if (!FOLD && a.dstates) stage_row(sm.stage + (ci & 1) * 8192, r, x);
       part = scan_part(gnext, ci + 1);  // gates of the next chunk
       gnext = load_g(ci + 2);
@@ -325,6 +350,10 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
         for (int q = 0; q < 32; ++q) y[q] += pd[q];
       }
       if (!FOLD && a.ddelta) stage_row(sm.stage + 16384 + (ci & 1) * 8192, r, y);
+      if (!FOLD) {  // dh' and dDelta of this chunk are staged
+        tc::fence_proxy_async();
+        arrive(&sm.sfull[ci & 1]);
+      }
 #pragma unroll
       for (int q = 0; q < 32; ++q) y[q] = -y[q];
       write_bt_column(sm.Yt, r, y);
@@ -334,17 +363,7 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
 
       // ---- gates and dO images of the next chunk -------------------------------------
       const float gC_cur = gC;
-      // this chunk's staged slices leave by TMA stores; before the barrier every
-      // earlier store has read its staging buffer
-      tc::fence_proxy_async();
-      if (tid == 0) tc::bulk_wait_read();
       asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");
-      if (tid == 0 && !FOLD && (a.dstates || a.ddelta)) {
-        if (a.dstates) tc::tma_store_2d(&mp.Ds, col0, (int)((bh * a.NC + c) * HD), sm.stage + (ci & 1) * 8192);
-        if (a.ddelta)
-          tc::tma_store_2d(&mp.Dd, col0, (int)((bh * a.NC + c) * CH), sm.stage + 16384 + (ci & 1) * 8192);
-        tc::bulk_commit();
-      }
       finish_gates(part, ci + 1);
       if (withO && ci + 1 < n) {  // both dO products of this chunk have read the images
         ok = ok && tc::mbar_wait(&sm.barQ, par);
@@ -369,7 +388,6 @@ __global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_
         arrive(&sm.barXt);
       }
     }
-    if (tid == 0) tc::bulk_wait();  // every store has completed before the block exits
     if (FOLD) {
       store_row_f32((partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0, x);
     } else if (a.dh0 && seg == 0) {

@@ -44,7 +44,7 @@ namespace gdn {
 namespace {
 
 constexpr int NC_THREADS = 128;                // compute threads: one per chunk row / state row
-constexpr int NT = NC_THREADS + 64;            // + the MMA issuer warp + the TMA producer warp
+constexpr int NT = NC_THREADS + 96;            // + MMA issuer, TMA producer and TMA store warps
 constexpr int NSLOT = 6;                       // tile ring slots (the last one doubles as staging)
 constexpr uint32_t TILE_BYTES = CH * HD * 2;   // 32 KiB
 constexpr uint32_t BT_BYTES = SL * HD * 2;     // 8 KiB: a [32 x 128] B-operand tile
@@ -57,6 +57,7 @@ struct WalkSmem {
   float gsum[2][4];
   uint64_t full[NSLOT], empty[NSLOT];
   uint64_t barX, barO1, barH, barO2, barDg, barD, barHt;
+  uint64_t sfull[2], sempty[2];  // staging buffer set i & 1: written by the compute threads / read by its stores
   uint32_t tmem;
 };
 
@@ -112,10 +113,12 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
   const int TPC = withO ? 4 : 2;  // tiles per chunk: w, (Q,) K (, P)
   const int ntiles = (cend - cbeg) * TPC;
   const int col0 = (slice & 3) * SL;
-  // The recompute mode stages its exported h and Delta slices in the last
-  // slot (four 8 KiB buffers: h and Delta, double-buffered, 64-byte swizzle)
-  // and streams its 2 tiles per chunk through a 5-slot ring; otherwise all 6
-  // slots form the ring (the output's 4 tiles per chunk need the depth).
+  // The recompute mode stages its exported h and Delta slices in the last slot
+  // (8 KiB each, double-buffered, 64-byte swizzle; a store warp writes them
+  // out) and streams its 2 tiles per chunk through a 5-slot ring.  The output
+  // mode needs all 6 slots for its 4 tiles per chunk and stores O rows
+  // directly (measured faster than staging it at 5 slots); the fold pass
+  // stores nothing per chunk.
   constexpr bool staged = STAGED;
   constexpr int nring = STAGED ? NSLOT - 1 : NSLOT;  // compile-time: the ring index is on the issue path
   unsigned char* stage = sm.slot[NSLOT - 1];
@@ -136,6 +139,10 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
     tc::mbar_init(&sm.barDg, NC_THREADS);
     tc::mbar_init(&sm.barD, NC_THREADS);
     tc::mbar_init(&sm.barHt, NC_THREADS);
+    for (int k = 0; k < 2; ++k) {
+      tc::mbar_init(&sm.sfull[k], NC_THREADS);
+      tc::mbar_init(&sm.sempty[k], 1);
+    }
     tc::mbar_fence_init();
   }
   if (warp == 0) tc::alloc(&sm.tmem, 256);
@@ -230,7 +237,26 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
     }
   };
 
-  if (warp == 5) {
+  if (warp == 6) {
+    // ============================================================ TMA stores
+    // The h and Delta slices staged for chunk index i leave by TMA stores once
+    // the compute threads have signalled them; when the stores have read the
+    // buffers they are handed back.  A store request can block its thread, so
+    // it never runs on a compute or issuing thread.
+    if (staged && lane == 0) {
+      for (int c = cbeg; c < cend; ++c) {
+        const int ci = c - cbeg;
+        ok = ok && tc::mbar_wait(&sm.sfull[ci & 1], (uint32_t)((ci >> 1) & 1));
+        if (a.states) tc::tma_store_2d(&mp.St, col0, (int)((bh * a.NC + c) * HD), stage + (ci & 1) * 8192);
+        if (a.delta)
+          tc::tma_store_2d(&mp.De, col0, (int)((bh * a.NC + c) * CH), stage + 16384 + (ci & 1) * 8192);
+        tc::bulk_commit();
+        tc::bulk_wait_read();
+        arrive(&sm.sempty[ci & 1]);
+      }
+      tc::bulk_wait();  // every store has completed before the block exits
+    }
+  } else if (warp == 5) {
     // ========================================================== TMA producer
     // Tile i goes into slot i % nring once the product that read tile
     // i - nring has completed (signalled on that slot's empty barrier).
@@ -294,6 +320,8 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
       const int ci = c - cbeg;
       const uint32_t par = (uint32_t)(ci & 1);
       // staging of chunk index i: h at stage[(i & 1) * 8192], Delta at stage[16384 + (i & 1) * 8192]
+      // staging buffer set ci & 1 was last read by the stores of chunk ci - 2
+      if (staged && ci >= 2) ok = ok && tc::mbar_wait(&sm.sempty[ci & 1], (uint32_t)(((ci >> 1) + 1) & 1));
       if (!FOLD && a.states) stage_row(stage + (ci & 1) * 8192, r, h);
 
       // ---- Delta = u - X -------------------------------------------------------
@@ -335,23 +363,16 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
         arrive(&sm.barD);
       }
       if (!FOLD && a.delta) stage_row(stage + 16384 + (ci & 1) * 8192, r, x);
+      if (staged) {  // h and Delta of this chunk are staged
+        tc::fence_proxy_async();
+        arrive(&sm.sfull[ci & 1]);
+      }
 
       // ---- gates of chunk c + 1, while K^T (ef Delta) runs ----------------------------
       float gam_n, ef_n, gC_n;
       part = scan_part(gnext, ci + 1);
       gnext = load_g(c + 2);
-      // this chunk's staged h and Delta leave by TMA stores; before the barrier
-      // every earlier store has read its staging buffer
-      if (staged) {
-        tc::fence_proxy_async();
-        if (tid == 0) tc::bulk_wait_read();
-      }
       asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");
-      if (staged && tid == 0) {
-        if (a.states) tc::tma_store_2d(&mp.St, col0, (int)((bh * a.NC + c) * HD), stage + (ci & 1) * 8192);
-        if (a.delta) tc::tma_store_2d(&mp.De, col0, (int)((bh * a.NC + c) * CH), stage + 16384 + (ci & 1) * 8192);
-        tc::bulk_commit();
-      }
       finish_gates(part, ci + 1, gam_n, ef_n, gC_n);
 
       // ---- h' = gamma_C h + H' ---------------------------------------------------
@@ -382,7 +403,6 @@ __global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_
       ef_r = ef_n;
       gC = gC_n;
     }
-    if (staged && tid == 0) tc::bulk_wait();  // every store has completed before the block exits
     if (FOLD) {
       float* dst = (partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0;
 #pragma unroll
