@@ -55,6 +55,14 @@ def test_bwd_slow_decay(gdn_lib):
     _check_bwd(gdn_lib, _small(640, shift=-4.0, h0=0.5, seed=2))
 
 
+@pytest.mark.parametrize("shift", [4.0, 8.0])
+def test_bwd_fast_decay(gdn_lib, shift):
+    # g about -4 and -8 per token: G drops by more than 100 (base 2) inside
+    # some (4.0) or all (8.0) 16-token blocks, so the kernels take the direct
+    # exponentials there instead of the factored decays
+    _check_bwd(gdn_lib, _small(300, shift=shift, h0=0.5, seed=int(shift) + 40))
+
+
 @pytest.mark.parametrize("T", [1, 77, 129])
 def test_bwd_ragged_and_tiny(gdn_lib, T):
     _check_bwd(gdn_lib, _small(T, Hk=2, Hv=4, seed=100 + T))

@@ -51,6 +51,16 @@ def test_ragged_lengths(gdn_lib, T):
     _check_fwd(gdn_lib, inp)
 
 
+@pytest.mark.parametrize("shift", [4.0, 8.0])
+def test_fast_decay(gdn_lib, shift):
+    # g about -4 and -8 per token: G drops by more than 100 (base 2) inside
+    # some (4.0) or all (8.0) 16-token blocks, so prep takes the direct
+    # exponentials there instead of the factored decays
+    inp = make_host(WORKLOADS["tiny_t1024"].replace(T=300, Hk=1, Hv=2, gate_shift=shift,
+                                                    h0_std=0.5, seed=int(shift) + 30))
+    _check_fwd(gdn_lib, inp)
+
+
 @pytest.mark.parametrize("Hk,Hv", [(1, 1), (1, 4), (3, 6), (4, 4)])
 def test_head_groupings(gdn_lib, Hk, Hv):
     inp = make_host(WORKLOADS["tiny_t1024"].replace(T=384, B=2, Hk=Hk, Hv=Hv, h0_std=0.1, seed=3))
