@@ -52,7 +52,7 @@ KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 0>", "walk_states": "k
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum, bytes)
 # from the committed ncu capture of the same kernel code (profiles/*), keyed by
 # kernel; a kernel changed since its capture has no entry.
-NCU_TRAFFIC = {"grads": 316925440}  # profiles/k_grads_layer_t4096_ncu_full.md: 270.06 MB + 46.86 MB
+NCU_TRAFFIC = {"grads": 318789120}  # profiles/k_grads_layer_t4096_ncu_full.md: 271.51 MB + 47.27 MB
 
 
 def algorithmic(wl):
@@ -324,49 +324,70 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_e2e(args, gdn, wl, host, dev, nseg):
-    """Same step through the public API with pinned host buffers: H2D of the
-    step's inputs, forward + backward, D2H of every result, all timed."""
+    """Same step through the public API with pinned host buffers: every step
+    copies its inputs host->device, runs forward + backward and copies every
+    result device->host, all inside the timed region.  Steps are pipelined the
+    way a training loop feeds a GPU: uploads, kernels and downloads run on
+    three streams over two buffer sets, so step i+1's upload and step i-1's
+    download overlap step i's kernels (events order each buffer's reuse)."""
     import torch
     names_in = ["q", "k", "v", "g", "beta", "h0", "dO", "dhT"]
     hin = {n: getattr(host, n).pin_memory() for n in names_in}
-    din = {n: torch.empty_like(hin[n], device=dev) for n in names_in}
+    din = [{n: torch.empty_like(hin[n], device=dev) for n in names_in} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in hin.values())
-    outs_h = None
-    ws_f = torch.empty(gdn.fwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
-                       dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
-                       dtype=torch.uint8, device=dev)
+    ws_f = [torch.empty(gdn.fwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
+                        dtype=torch.uint8, device=dev) for _ in range(2)]
+    ws_b = [torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
+                        dtype=torch.uint8, device=dev) for _ in range(2)]
+    s_up, s_run, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    up_done, run_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    outs_h = [None, None]
+    d2h = [0]
 
-    def one():
-        nonlocal outs_h
-        for n in names_in:
-            din[n].copy_(hin[n], non_blocking=True)
-        o, hT = gdn.chunk_fwd(din["q"], din["k"], din["v"], din["g"], din["beta"], din["h0"],
-                              n_segments=nseg, workspace=ws_f)
-        gr = gdn.chunk_bwd(din["q"], din["k"], din["v"], din["g"], din["beta"], din["h0"],
-                           din["dO"], din["dhT"], n_segments=nseg, workspace=ws_b)
-        outs = [o, hT, *gr]
-        if outs_h is None:
-            outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-        for hb, t in zip(outs_h, outs):
-            hb.copy_(t, non_blocking=True)
+    def one(i):
+        k = i & 1
+        with torch.cuda.stream(s_up):
+            if i >= 2:
+                s_up.wait_event(run_done[k])  # step i-2's kernels have read din[k]
+            for n in names_in:
+                din[k][n].copy_(hin[n], non_blocking=True)
+            up_done[k].record(s_up)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(up_done[k])
+            x = din[k]
+            o, hT = gdn.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                                  n_segments=nseg, workspace=ws_f[k])
+            gr = gdn.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                               x["dO"], x["dhT"], n_segments=nseg, workspace=ws_b[k])
+            outs = [o, hT, *gr]
+            run_done[k].record(s_run)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(run_done[k])
+            if outs_h[k] is None:
+                outs_h[k] = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+                d2h[0] = sum(t.numel() * t.element_size() for t in outs)
+            for hb, t in zip(outs_h[k], outs):
+                hb.copy_(t, non_blocking=True)
+                t.record_stream(s_down)  # the allocator keeps t until its download is done
+            down_done[k].record(s_down)
 
-    for _ in range(max(3, args.warmup)):
-        one()
+    for i in range(max(3, args.warmup)):
+        one(i)
     torch.cuda.synchronize()
     K = args.steps
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(K):
-        one()
-    e1.record()
+    e0.record(s_up)
+    for i in range(K):
+        one(i)
+    e1.record(s_down)  # after the last download, which follows every other step's work
     e1.synchronize()
+    torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    d2h = sum(t.numel() * t.element_size() for t in outs_h)
     return {"value": round(wl.tokens * K / (ms * 1e-3), 1), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / K, 5)}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h[0],
+            "ms_per_step": round(ms / K, 5), "pipelined": "3 streams (upload, kernels, download), 2 buffer sets"}
 
 
 # ---------------------------------------------------------------- oracle arm
