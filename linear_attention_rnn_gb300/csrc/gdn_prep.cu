@@ -39,6 +39,7 @@ namespace gdn {
 namespace {
 
 constexpr uint32_t TILE = CH * HD * 2;  // 32 KiB bf16 tile
+constexpr int PT = 512, PW = PT / 32;  // 16 warps: an epilogue thread owns 32 columns of its row
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct PrepSmem {
@@ -104,23 +105,20 @@ __device__ __forceinline__ void ldb_kn_64(uint32_t (&b)[4], bf16* base, int k0, 
   ldsm_x4_t(b, swz64(base, k0 + (lane & 15), (n0 >> 3) + (lane >> 4)));
 }
 
-// Columns 64 hh .. 64 hh + 63 of this thread's TMEM row, as bf16, into row
+// Columns 32 cq .. 32 cq + 31 of this thread's TMEM row, as bf16, into row
 // `row` of a K-major SW128 [128 x 128] staging tile (the layout a tiled TMA
 // store with 64-column boxes reads).
-__device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, unsigned char* tile, int row, int hh) {
+__device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, unsigned char* tile, int row, int cq) {
+  float v[32];
+  tc::ld32(taddr, v);
 #pragma unroll
-  for (int cb = 0; cb < 64; cb += 32) {
-    float v[32];
-    tc::ld32(taddr + cb, v);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 o;
-      o.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
-      o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-      o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-      o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-      *reinterpret_cast<uint4*>(tile + tc::sw128_chunk(row, 8 * hh + (cb >> 3) + q, CH)) = o;
-    }
+  for (int q = 0; q < 4; ++q) {
+    uint4 o;
+    o.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+    o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(tile + tc::sw128_chunk(row, 4 * cq + q, CH)) = o;
   }
 }
 
@@ -147,9 +145,9 @@ __device__ __forceinline__ void ut_inverse(PrepSmem& sm, int warp, int lane) {
   bf16* Yl = reinterpret_cast<bf16*>(sm.Tp + Y_LO);
   const float* Sd = reinterpret_cast<const float*>(sm.Tp + SD);
   const int g4 = lane >> 2, t4 = lane & 3;
-  // (1) exact forward substitution of diagonal block `warp`: lane j (mod 16)
-  //     carries column j; lanes 0-15 store the high parts, 16-31 the low parts
-  {
+  // (1) exact forward substitution of diagonal block `warp` (warps 0-7): lane
+  //     j (mod 16) carries column j; lanes 0-15 store the high parts, 16-31 the low parts
+  if (warp < CH / 16) {
     const float* blk = Sd + warp * 256;
     const int jl = lane & 15;
     float t[16];
@@ -174,15 +172,9 @@ __device__ __forceinline__ void ut_inverse(PrepSmem& sm, int warp, int lane) {
   for (int bs = 16; bs < CH; bs *= 2) {
     const int nb = bs >> 4, per = nb * nb;
     const int ntiles = (CH / (2 * bs)) * per;
-    // at b = 64 a warp takes two tiles whose k-step counts (nb - tn, then tm + 1)
-    // add up to 5, so that no warp carries two of the longest
-    for (int t = warp; t < ntiles; t += 8) {
-      int p = t / per, tm = (t % per) / nb, tn = t % nb;
-      if (nb == 4) {
-        p = 0;
-        tm = warp >> 1;
-        tn = (t < 8) ? (warp & 1) : 3 - (warp & 1);
-      }
+    // (at most 16 tiles per phase: one per warp)
+    for (int t = warp; t < ntiles; t += PW) {
+      const int p = t / per, tm = (t % per) / nb, tn = t % nb;
       const int s0 = 2 * bs * p;
       float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kb = tn; kb < nb; ++kb) {  // X_A is lower triangular
@@ -201,13 +193,8 @@ __device__ __forceinline__ void ut_inverse(PrepSmem& sm, int warp, int lane) {
                   1.f);
     }
     __syncthreads();
-    for (int t = warp; t < ntiles; t += 8) {
-      int p = t / per, tm = (t % per) / nb, tn = t % nb;
-      if (nb == 4) {
-        p = 0;
-        tn = warp >> 1;
-        tm = (t < 8) ? (warp & 1) : 3 - (warp & 1);
-      }
+    for (int t = warp; t < ntiles; t += PW) {
+      const int p = t / per, tm = (t % per) / nb, tn = t % nb;
       const int s0 = 2 * bs * p;
       float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kb = 0; kb <= tm; ++kb) {  // X_D is lower triangular
@@ -228,7 +215,7 @@ __device__ __forceinline__ void ut_inverse(PrepSmem& sm, int warp, int lane) {
   }
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_constant__ PrepMaps mp) {
+__global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constant__ PrepMaps mp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   PrepSmem& sm = *reinterpret_cast<PrepSmem*>(base);
@@ -238,8 +225,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
   const int t0 = c * CH;
   const int L = min(CH, a.T - t0);
   const bool needP = a.P != nullptr, needU = a.U != nullptr, needW = a.W != nullptr;
-  // TMEM row of this thread in the epilogues: lane quarter of the warp, column half
-  const int quarter = warp & 3, hh = warp >> 2;
+  // TMEM row of this thread in the epilogues: lane quarter of the warp, column quarter
+  const int quarter = warp & 3, cq = warp >> 2;
   const int row = 32 * quarter + lane;
   const long tile = (long)CH * CH;  // w, u and P tiles: [128][128] row-major in global memory
 
@@ -352,8 +339,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
       const float Glr = sm.Gl[row], br = sm.beta[row];
       float* Sd = reinterpret_cast<float*>(sm.Tp + SD);
 #pragma unroll 1
-      for (int cb = 0; cb < 64; cb += 16) {
-        const int c0 = 64 * hh + cb;
+      for (int cb = 0; cb < 32; cb += 16) {
+        const int c0 = 32 * cq + cb;
         float sv[16], pv[16];
         if (c0 <= 32 * quarter + 31) {  // warp-uniform: the block reaches the diagonal
           float kk[16], mv[16];
@@ -413,7 +400,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
       tc::bulk_commit();
     }
     auto export_f32 = [&](float* dst) {
-      for (int i = tid; i < CH * 16; i += NTHREADS) {
+      for (int i = tid; i < CH * 16; i += PT) {
         const int r = i >> 4, jc = i & 15;
         float v[8];
         join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
@@ -431,7 +418,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
     if (a.T_dbg) export_f32(a.T_dbg + chunk_id * tile);
     if (a.Tb) {
       bf16* dst = a.Tb + chunk_id * tile;
-      for (int i = tid; i < CH * 16; i += NTHREADS) {
+      for (int i = tid; i < CH * 16; i += PT) {
         const int r = i >> 4, jc = i & 15;
         float v[8];
         join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
@@ -448,8 +435,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
     __syncthreads();
     // ---- diag(gamma) K (B operand of w) ------------------------------------------------
 #pragma unroll
-    for (int i = 0; i < (CH * 16) / NTHREADS; ++i) {
-      const int idx = tid + i * NTHREADS;
+    for (int i = 0; i < (CH * 16) / PT; ++i) {
+      const int idx = tid + i * PT;
       const int r = idx >> 4, jc = idx & 15;
       const uint32_t off = tc::sw128_chunk(r, jc, CH);
       const uint4 x = *reinterpret_cast<const uint4*>(sm.K + off);
@@ -465,8 +452,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
 
     // ---- T' = T diag(beta) (bf16, K-major SW128) --------------------------------------
 #pragma unroll
-    for (int i = 0; i < (CH * 16) / NTHREADS; ++i) {
-      const int idx = tid + i * NTHREADS;
+    for (int i = 0; i < (CH * 16) / PT; ++i) {
+      const int idx = tid + i * PT;
       const int r = idx >> 4, jc = idx & 15;
       float v[8];
       join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
@@ -500,8 +487,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_prep(PrepArgs a, const __grid_c
     }
     // ---- w and u leave through shared staging tiles and TMA stores ------------------
     // (diag(gamma) K and T' are dead now; their buffers hold w and u)
-    if (needW) tmem_row_to_tile(tlane + 256 + 64 * hh, sm.Kg, row, hh);
-    if (needU) tmem_row_to_tile(tlane + 384 + 64 * hh, sm.Tp, row, hh);
+    if (needW) tmem_row_to_tile(tlane + 256 + 32 * cq, sm.Kg, row, cq);
+    if (needU) tmem_row_to_tile(tlane + 384 + 32 * cq, sm.Tp, row, cq);
     tc::fence_proxy_async();
     tc::fence_before();
     __syncthreads();  // staging tiles complete; TMEM w/u and the gate vectors are free
@@ -544,7 +531,7 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.NC, a.Hk, a.B);
-  k_prep<<<grid, NTHREADS, smem, s>>>(a, mp);
+  k_prep<<<grid, PT, smem, s>>>(a, mp);
   return cudaGetLastError();
 }
 
