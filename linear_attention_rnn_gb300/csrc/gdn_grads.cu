@@ -25,7 +25,8 @@
 // dh'^T, diag(gamma) dO h^T) are formed by the epilogue threads from scratch
 // products and written into the accumulators with tcgen05.st; the plain
 // products (dKK K, dKK^T K, dQK^T Q, dQK K) then accumulate onto them.
-// Epilogue thread (row r, half hh) owns TMEM lane r, columns 64 hh .. 64 hh + 63.
+// 16 warps: epilogue thread (row r, quarter cq) owns TMEM lane r, columns
+// 32 cq .. 32 cq + 31.
 // Operands are SW128 tiles: the stored tiles arrive by TMA, dV', dKK and dQK
 // are written by the epilogues, and each product reads its tiles K-major or
 // MN-major as the product needs (no transposes).
@@ -38,6 +39,7 @@ namespace gdn {
 namespace {
 
 constexpr uint32_t TILE = CH * HD * 2;
+constexpr int GT = 512, GW = GT / 32;  // 16 warps
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct GradSmem {
@@ -49,7 +51,7 @@ struct GradSmem {
   float Gl[CH], gam[CH], ef[CH], beta[CH];
   float etab[CH];  // exp2(Gl[c0] - Gl[s]) for the 16-column block c0 of column s
   float colX[CH], dbeta[CH], dbg[CH], d_ef[CH], rowX[CH], dgamO[CH];
-  float red[8];
+  float red[GW];
   uint64_t barKQ, barT, barDD, barH, barDl, barDH, barDO, barM;
   uint32_t tmem;
 };
@@ -105,7 +107,7 @@ struct GradMaps {
   CUtensorMap dq, dk;  // stores over [B, T, Hk, 128] (rows past T are clipped)
 };
 
-__global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_constant__ GradMaps mp) {
+__global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_constant__ GradMaps mp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   GradSmem& sm = *reinterpret_cast<GradSmem*>(base);
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
   const int group = a.Hv / a.Hk;
   const int t0 = c * CH;
   const int L = min(CH, a.T - t0);
-  const int quarter = warp & 3, hh = warp >> 2;
+  const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
   const int row = 32 * quarter + lane;
 
   auto cid_of = [&](int jj) { return ((long)b * a.Hv + kh * group + jj) * a.NC + c; };
@@ -151,7 +153,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = sm.tmem;
-  const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16) + 64u * hh;  // lane row, column half
+  const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16) + 32u * cq;  // lane row, column quarter
+  const int c0 = 32 * cq;
   bool ok = true;
   uint32_t mc = 0;  // completed-commit count of barM seen by this thread
   auto wait_mma = [&]() {
@@ -251,11 +254,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
     // ---- E1: dV' -> W1 (bf16) ------------------------------------------------------------
     wait_mma();
     if (tid == 0) load2d(sm.W2, &mp.dstates, cid, &sm.barDH);  // dDelta has been read
-#pragma unroll 1
-    for (int cb = 0; cb < 64; cb += 32) {
+    {
       float x[32];
-      tc::ld32(tl + C_A + cb, x);
-      row32_store(sm.W1, row, 64 * hh + cb, x);
+      tc::ld32(tl + C_A, x);
+      row32_store(sm.W1, row, c0, x);
     }
     sync_operands();
 
@@ -273,18 +275,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
     // Read back from the bf16 dV' tile with 16 threads per row, so that V is
     // loaded and dv stored in whole 256-byte rows.
     {
-      constexpr int NI = (CH * 16) / NTHREADS;  // 8 chunks of 16 bytes per thread
+      constexpr int NI = (CH * 16) / GT;  // 4 chunks of 16 bytes per thread
       uint4 v4[NI];
 #pragma unroll
       for (int i = 0; i < NI; ++i) {  // all loads in flight before any is used
-        const int idx = tid + i * NTHREADS;
+        const int idx = tid + i * GT;
         const int r = idx >> 4, jc = idx & 15;
         v4[i] = r < L ? *reinterpret_cast<const uint4*>(a.v + (tokv + (long)r * a.Hv) * HD + 8 * jc)
                       : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
-        const int idx = tid + i * NTHREADS;
+        const int idx = tid + i * GT;
         const int r = idx >> 4, jc = idx & 15;
         const uint4 d4 = *reinterpret_cast<const uint4*>(sm.W1 + tc::sw128_chunk(r, jc, CH));
         const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w}, vw[4] = {v4[i].x, v4[i].y, v4[i].z, v4[i].w};
@@ -310,8 +312,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
       ok = ok && tc::mbar_wait(&sm.barH, par);
       float d = 0.f;
 #pragma unroll
-      for (int i = 0; i < (int)(TILE / 16) / NTHREADS; ++i) {
-        const uint32_t off = (uint32_t)(tid + i * NTHREADS) * 16u;
+      for (int i = 0; i < (int)(TILE / 16) / GT; ++i) {
+        const uint32_t off = (uint32_t)(tid + i * GT) * 16u;
         const uint4 x = *reinterpret_cast<const uint4*>(sm.W2 + off);
         const uint4 y = *reinterpret_cast<const uint4*>(sm.W3 + off);
         const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
@@ -328,30 +330,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
 
     // ---- E2: dK (+)= -diag(beta gamma) dV' h^T + diag(ef) Delta dh'^T ---------------------
     wait_mma();
-#pragma unroll 1
-    for (int cb = 0; cb < 64; cb += 32) {
-      const int c0 = 64 * hh + cb;
+    {
       float kv[32], x[32], acc[32];
       row32_load(sm.K, row, c0, kv);
       if (jj > 0) {
-        tc::ld32(tl + C_DK + cb, acc);
+        tc::ld32(tl + C_DK, acc);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[i] = 0.f;
       }
-      tc::ld32(tl + C_A + cb, x);
+      tc::ld32(tl + C_A, x);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         p_dbg -= x[i] * kv[i];
         acc[i] -= bgr * x[i];
       }
-      tc::ld32(tl + C_B + cb, x);
+      tc::ld32(tl + C_B, x);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         p_def += x[i] * kv[i];
         acc[i] += efr * x[i];
       }
-      tc::st32(tl + C_DK + cb, acc);
+      tc::st32(tl + C_DK, acc);
     }
     tc::wait_st();
     tc::fence_before();
@@ -368,14 +368,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
     }
     // ---- E3: dKK = -(ds * M) diag-row(beta), strictly lower -> W1; dbeta, rowX, colX -----
     wait_mma();
-#pragma unroll 1
-    for (int cb = 0; cb < 64; cb += 32) {
-      const int c0 = 64 * hh + cb;
+    {
       float out[32];
-      if (c0 <= 32 * quarter + 31) {  // warp-uniform: the block reaches the diagonal
+      if (cq <= quarter) {  // warp-uniform: the block reaches the diagonal
         float ds[32], kk[32];
-        tc::ld32(tl + C_A + cb, ds);
-        tc::ld32(tl + C_B + cb, kk);
+        tc::ld32(tl + C_A, ds);
+        tc::ld32(tl + C_B, kk);
         fill_decay(c0, out, false);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -409,14 +407,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
     }
     // ---- E4: dQK = dP * M (diagonal included) -> W4; rowX, colX --------------------------
     wait_mma();
-#pragma unroll 1
-    for (int cb = 0; cb < 64; cb += 32) {
-      const int c0 = 64 * hh + cb;
+    {
       float out[32];
-      if (c0 <= 32 * quarter + 31) {
+      if (cq <= quarter) {
         float dp[32], qk[32];
-        tc::ld32(tl + C_A + cb, dp);
-        tc::ld32(tl + C_B + cb, qk);
+        tc::ld32(tl + C_A, dp);
+        tc::ld32(tl + C_B, qk);
         fill_decay(c0, out, true);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -450,14 +446,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
       load2d(sm.W2, &mp.ddelta, nc, &sm.barDD);
       load2d(sm.W3, &mp.states, nc, &sm.barH);
     }
-#pragma unroll 1
-    for (int cb = 0; cb < 64; cb += 32) {
-      const int c0 = 64 * hh + cb;
+    {
       float qv[32], x[32], acc[32];
       row32_load(sm.Q, row, c0, qv);
-      tc::ld32(tl + C_A + cb, x);
+      tc::ld32(tl + C_A, x);
       if (jj > 0) {
-        tc::ld32(tl + C_DQ + cb, acc);
+        tc::ld32(tl + C_DQ, acc);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[i] = 0.f;
@@ -467,7 +461,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
         p_dgam += x[i] * qv[i];
         acc[i] += gr * x[i];
       }
-      tc::st32(tl + C_DQ + cb, acc);
+      tc::st32(tl + C_DQ, acc);
     }
     tc::wait_st();
     tc::fence_before();
@@ -491,7 +485,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
     if (warp == 0) {
       float dgC = 0.f;
 #pragma unroll
-      for (int w = 0; w < 8; ++w) dgC += sm.red[w];
+      for (int w = 0; w < GW; ++w) dgC += sm.red[w];
       float sum_def = 0.f;
       float dG[4];
 #pragma unroll
@@ -533,13 +527,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_grads(GradArgs a, const __grid_
   }
 
   // ---- dq, dk of the key head: bf16 staging tiles (W1, W2 are free) and TMA stores ------
-#pragma unroll 1
-  for (int cb = 0; cb < 64; cb += 32) {
-    const int c0 = 64 * hh + cb;
+  {
     float x[32];
-    tc::ld32(tl + C_DQ + cb, x);
+    tc::ld32(tl + C_DQ, x);
     row32_store(sm.W1, row, c0, x);
-    tc::ld32(tl + C_DK + cb, x);
+    tc::ld32(tl + C_DK, x);
     row32_store(sm.W2, row, c0, x);
   }
   tc::fence_proxy_async();
@@ -578,7 +570,7 @@ cudaError_t launch_grads(const GradArgs& a, cudaStream_t s) {
   const size_t smem = grad_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_grads<<<dim3(a.NC, a.Hk, a.B), NTHREADS, smem, s>>>(a, mp);
+  k_grads<<<dim3(a.NC, a.Hk, a.B), GT, smem, s>>>(a, mp);
   return cudaGetLastError();
 }
 
