@@ -52,7 +52,7 @@ KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 0>", "walk_states": "k
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum, bytes)
 # from the committed ncu capture of the same kernel code (profiles/*), keyed by
 # kernel; a kernel changed since its capture has no entry.
-NCU_TRAFFIC = {}  # per-launch dram bytes from an ncu capture of the current kernels (none yet)
+NCU_TRAFFIC = {"grads": 318751232}  # profiles/k_grads_layer_t4096_ncu_full.md: 271.51 MB + 47.24 MB
 
 
 def algorithmic(wl):
