@@ -40,15 +40,14 @@ FLOPS = {  # per (chunk, value head), per kernel
     "walk_bwd": 3 * FLOP_FULL + FLOP_TRI,  # K dh', Q^T dO, w^T dDelta, P^T dO
     "grads": 3 * FLOP_FULL + 9 * FLOP_TRI,
 }
+FLOPS["walks"] = FLOPS["walk_states"] + FLOPS["walk_bwd"]  # both walks of the backward, one launch
 FWD_KERNELS = ["prep", "walk"]
-BWD_KERNELS = ["prep", "walk_states", "walk_bwd", "grads"]
+BWD_KERNELS = ["prep", "walks", "grads"]
 FWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk"]
-BWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk_states", "fold_bwd", "prefix_bwd",
-                   "walk_bwd", "grads"]
-KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 0>", "walk_states": "k_walk_fwd<0, 1>",
-                 "walk_bwd": "k_walk_bwd<0>", "grads": "k_grads",
-                 "fold": "k_walk_fwd<1, 0>", "prefix": "k_affine_walk",
-                 "fold_bwd": "k_walk_bwd<1>", "prefix_bwd": "k_affine_walk"}
+BWD_KERNELS_SEG = ["prep", "fold", "prefix", "fold_bwd", "prefix_bwd", "walks", "grads"]
+KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 0, 32>", "walks": "k_walk_pair", "grads": "k_grads",
+                 "fold": "k_walk_fwd<1, 0, 32>", "prefix": "k_affine_walk",
+                 "fold_bwd": "k_walk_bwd<1, 32>", "prefix_bwd": "k_affine_walk"}
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum, bytes)
 # from the committed ncu capture of the same kernel code (profiles/*), keyed by
 # kernel; a kernel changed since its capture has no entry.

@@ -154,9 +154,10 @@ int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
  * caller's (cudaEvent_t handles created by the caller).  Launch order:
  *   forward,  n_segments = 1:  prep, walk
  *   forward,  n_segments > 1:  prep, fold, segment prefix, walk
- *   backward, n_segments = 1:  prep, forward walk, reverse walk, gradients, dq/dk sum
- *   backward, n_segments > 1:  prep, fold, prefix, forward walk, reverse fold,
- *                              reverse prefix, reverse walk, gradients, dq/dk sum
+ *   backward, n_segments = 1:  prep, walks (state recompute beside the reverse
+ *                              walk, one launch), gradients
+ *   backward, n_segments > 1:  prep, fold, prefix, reverse fold, reverse prefix,
+ *                              walks (the two replays, one launch), gradients
  * With T == 0 or B == 0 no kernel is launched and no event is recorded.
  * Pages: none (instrumentation of the same operations).
  */

@@ -50,7 +50,7 @@ Dims make_dims(int B, int T, int Hk, int Hv, int n_segments) {
 // bf16 entering states, Delta, the state cotangents, dDelta and the fp32
 // per-value-head dq/dk.
 struct Layout {
-  size_t status, W, U, P, Tb, pairA, pairB, hin, states, delta, dstates, ddelta, total;
+  size_t status, W, U, P, Tb, pairA, pairB, hin, dhin, states, delta, dstates, ddelta, total;
 };
 
 Layout layout(const Dims& d, bool bwd) {
@@ -75,6 +75,7 @@ Layout layout(const Dims& d, bool bwd) {
     L.hin = take(pair);
   }
   if (bwd) {
+    if (d.S > 1) L.dhin = take((size_t)d.BH() * d.S * HD * HD * sizeof(float));  // entering cotangents
     L.Tb = take(chunks * tile);
     L.states = take(chunks * tile);
     L.delta = take(chunks * tile);
@@ -89,6 +90,9 @@ template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
+
+// swizzle of a stored [128 x sw] bf16 walk slice: its rows are 2 sw bytes
+CUtensorMapSwizzle slice_swizzle(int sw) { return sw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
 
@@ -109,11 +113,13 @@ struct Marks {
   }
 };
 
-// Forward states: prep has run; walk (with segments: fold, cross, replay).
-int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, const void* k,
-                      const float* g, const float* h0, void* o, float* hT, bf16* states,
-                      bf16* delta, cudaStream_t s, Marks& mk) {
-  WalkFwdArgs w;
+// Forward walk set-up: prep has run.  Fills the walk's arguments and tensor
+// maps; with segments it also runs the fold and the cross-segment prefix, so
+// that the walk (launched by the caller) replays every segment from its
+// entering state.
+int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const void* q, const void* k,
+                         const float* g, const float* h0, void* o, float* hT, bf16* states,
+                         bf16* delta, cudaStream_t s, Marks& mk, WalkFwdArgs& w, WalkFwdMaps& mp) {
   memset(&w, 0, sizeof w);
   w.W = at<bf16>(ws, Lw.W);
   w.U = at<bf16>(ws, Lw.U);
@@ -132,21 +138,19 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
   w.states = states;
   w.delta = delta;
   w.status = at<int>(ws, Lw.status);
-  WalkFwdMaps mp;
   memset(&mp, 0, sizeof mp);
   const uint64_t wrows = (uint64_t)d.BH() * d.NC * CH;
   if (!tmap_heads(&mp.k, k, d.B, d.T, d.Hk, HD) || !tmap_heads(&mp.q, q, d.B, d.T, d.Hk, HD) ||
       !tmap_2d(&mp.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
       !tmap_2d(&mp.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true) ||
-      (states && !tmap_2d_sw(&mp.St, states, HD, wrows, HD * sizeof(bf16), SL, CH, CU_TENSOR_MAP_SWIZZLE_64B)) ||
-      (delta && !tmap_2d_sw(&mp.De, delta, HD, wrows, HD * sizeof(bf16), SL, CH, CU_TENSOR_MAP_SWIZZLE_64B)))
+      (states && !tmap_2d_sw(&mp.St, states, HD, wrows, HD * sizeof(bf16), WALK_STATES_SW, CH, slice_swizzle(WALK_STATES_SW))) ||
+      (delta && !tmap_2d_sw(&mp.De, delta, HD, wrows, HD * sizeof(bf16), WALK_STATES_SW, CH, slice_swizzle(WALK_STATES_SW))))
     return GDN_ERR_CUDA;
   if (d.S == 1) {
     w.hstart = h0;
     w.hstart_bh_stride = (long)HD * HD;
     w.hstart_seg_stride = 0;
-    int r = cuda_status(launch_walk_fwd(w, mp, 0, s));
-    return r ? r : mk.rec();
+    return GDN_OK;
   }
   WalkFwdArgs f = w;
   f.pairA = at<float>(ws, Lw.pairA);
@@ -174,8 +178,7 @@ int run_forward_walks(const Dims& d, const Layout& Lw, void* ws, const void* q, 
   w.hstart = at<float>(ws, Lw.hin);
   w.hstart_bh_stride = (long)d.S * HD * HD;
   w.hstart_seg_stride = (long)HD * HD;
-  rc = cuda_status(launch_walk_fwd(w, mp, 0, s));
-  return rc ? rc : mk.rec();
+  return GDN_OK;
 }
 
 }  // namespace
@@ -261,7 +264,11 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   p.NC = d.NC;
   rc = cuda_status(launch_prep(p, s));
   if (rc || (rc = mk.rec())) return rc;
-  return run_forward_walks(d, L, ws, q, k, g, h0, o, hT, nullptr, nullptr, s, mk);
+  WalkFwdArgs w;
+  WalkFwdMaps mp;
+  if ((rc = prepare_forward_walk(d, L, ws, q, k, g, h0, o, hT, nullptr, nullptr, s, mk, w, mp))) return rc;
+  if ((rc = cuda_status(launch_walk_fwd(w, mp, 0, s)))) return rc;
+  return mk.rec();
 }
 
 static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
@@ -311,11 +318,16 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   p.NC = d.NC;
   rc = cuda_status(launch_prep(p, s));
   if (rc || (rc = mk.rec())) return rc;
-  // 2. recompute the state entering every chunk, and Delta
-  rc = run_forward_walks(d, L, ws, q, k, g, h0, nullptr, nullptr, at<bf16>(ws, L.states),
-                         at<bf16>(ws, L.delta), s, mk);
+  // 2. recompute of the state entering every chunk, and Delta (with segments:
+  //    its fold and cross-segment prefix now, the replay below)
+  WalkFwdArgs fw;
+  WalkFwdMaps fm;
+  rc = prepare_forward_walk(d, L, ws, q, k, g, h0, nullptr, nullptr, at<bf16>(ws, L.states),
+                            at<bf16>(ws, L.delta), s, mk, fw, fm);
   if (rc) return rc;
-  // 3. reverse walk of the state cotangent
+  // 3. reverse walk of the state cotangent (with segments: its fold and prefix
+  //    now); it needs nothing from the recompute, so the two walks run side by
+  //    side in one launch
   WalkBwdArgs w;
   memset(&w, 0, sizeof w);
   w.W = at<bf16>(ws, L.W);
@@ -341,16 +353,14 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
     if (!tmap_heads(&bm.k, k, d.B, d.T, d.Hk, HD) || !tmap_heads(&bm.q, q, d.B, d.T, d.Hk, HD) ||
         !tmap_2d(&bm.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
         !tmap_2d(&bm.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true) ||
-        !tmap_2d_sw(&bm.Ds, w.dstates, HD, wrows, HD * sizeof(bf16), SL, CH, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !tmap_2d_sw(&bm.Dd, w.ddelta, HD, wrows, HD * sizeof(bf16), SL, CH, CU_TENSOR_MAP_SWIZZLE_64B))
+        !tmap_2d_sw(&bm.Ds, w.dstates, HD, wrows, HD * sizeof(bf16), WALK_BWD_SW, CH, slice_swizzle(WALK_BWD_SW)) ||
+        !tmap_2d_sw(&bm.Dd, w.ddelta, HD, wrows, HD * sizeof(bf16), WALK_BWD_SW, CH, slice_swizzle(WALK_BWD_SW)))
       return GDN_ERR_CUDA;
   }
   if (d.S == 1) {
     w.hstart = dhT;
     w.hstart_bh_stride = (long)HD * HD;
     w.hstart_seg_stride = 0;
-    rc = cuda_status(launch_walk_bwd(w, bm, 0, s));
-    if (!rc) rc = mk.rec();
   } else {
     WalkBwdArgs f = w;
     f.pairA = at<float>(ws, L.pairA);
@@ -363,7 +373,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
     x.A = f.pairA;
     x.Bv = f.pairB;
     x.init = dhT;
-    x.outB = at<float>(ws, L.hin);
+    x.outB = at<float>(ws, L.dhin);
     x.batch = (int)d.BH();
     x.n = d.S;
     x.dv = HD;
@@ -372,13 +382,11 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
     x.reverse = 1;
     rc = cuda_status(launch_affine_walk(x, s));
     if (rc || (rc = mk.rec())) return rc;
-    w.hstart = at<float>(ws, L.hin);
+    w.hstart = at<float>(ws, L.dhin);
     w.hstart_bh_stride = (long)d.S * HD * HD;
     w.hstart_seg_stride = (long)HD * HD;
-    rc = cuda_status(launch_walk_bwd(w, bm, 0, s));
-    if (!rc) rc = mk.rec();
   }
-  if (rc) return rc;
+  if ((rc = cuda_status(launch_walk_pair(fw, fm, w, bm, s))) || (rc = mk.rec())) return rc;
   // 4. chunk-parallel gradients (dq and dk summed over the value heads of each key head)
   GradArgs ga;
   memset(&ga, 0, sizeof ga);

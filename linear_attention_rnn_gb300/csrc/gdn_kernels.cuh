@@ -48,10 +48,15 @@ struct WalkFwdArgs {
   int B, T, Hk, Hv, NC, S;
 };
 
+// State columns per CTA of the forward walk's recompute mode (the output walk
+// and the segment fold keep 32): a 64-column slice halves the CTAs for about
+// 20% more time per chunk.
+constexpr int WALK_STATES_SW = 64;
+
 // TMA tensor maps of the forward walk: K and Q over [B, T, Hk, 128] (boxes of
 // 64 columns x 128 tokens, 128-byte swizzle), w and P over the workspace rows
-// (same boxes); stores of 32-column slices (64-byte swizzle) of the entering
-// states and Delta over the workspace rows.
+// (same boxes); stores of WALK_STATES_SW-column slices of the entering states
+// and Delta over the workspace rows.
 struct WalkFwdMaps {
   CUtensorMap k, q, W, P;
   CUtensorMap St, De;
@@ -77,11 +82,15 @@ struct WalkBwdArgs {
   int B, T, Hk, Hv, NC, S;
 };
 
+// State columns per CTA of the backward walk (the segment fold keeps 32): a
+// 64-column slice halves the CTAs for about 20% more time per chunk.
+constexpr int WALK_BWD_SW = 64;
+
 // Tensor maps of the backward walk's tiles: k and q as for the forward walk,
 // w and P over the workspace rows (64 columns x 128 rows, 128-byte swizzle).
 struct WalkBwdMaps {
   CUtensorMap k, q, W, P;
-  CUtensorMap Ds, Dd;  // stores: leaving-state cotangents and dDelta (32-column slices)
+  CUtensorMap Ds, Dd;  // stores: leaving-state cotangents and dDelta (WALK_BWD_SW-column slices)
 };
 
 // Sequential affine walk X <- A_i X (+ B_i) over i (segment prefix / compose).
@@ -126,8 +135,13 @@ size_t affine_walk_smem_bytes();
 size_t grad_smem_bytes();
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
+// The forward walk: its segment fold (fold = 1) or the walk with output.
 cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold, cudaStream_t s);
+// The backward walk's segment fold (fold = 1 only).
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, const WalkBwdMaps& m, int fold, cudaStream_t s);
+// The forward walk's recompute mode and the backward walk (fold = 0 both) in one launch.
+cudaError_t launch_walk_pair(const WalkFwdArgs& fa, const WalkFwdMaps& fm, const WalkBwdArgs& ba,
+                             const WalkBwdMaps& bm, cudaStream_t s);
 cudaError_t launch_affine_walk(const AffineWalkArgs& a, cudaStream_t s);
 cudaError_t launch_grads(const GradArgs& a, cudaStream_t s);
 cudaError_t launch_selftest_wait(long long limit_ns, int* status, cudaStream_t s);

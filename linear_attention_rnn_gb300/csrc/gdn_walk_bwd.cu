@@ -1,420 +1,39 @@
-// gdn_walk_bwd.cu -- reverse walk of the state cotangent over the chunks of a segment.
-//
-// The backward "walks the chunks in reverse" ("Fuse the Gated Delta Net
-// inter-chunk scan into a Pallas TPU kernel", section "Changes").  With dh' the
-// cotangent of the state leaving chunk c, the chunk forward
-//     Delta = u - w h,  O = diag(gamma) Q h + P Delta,  h' = gamma_C h + k_g^T Delta
-// gives
-//     Y = dDelta = diag(ef) K dh' + P^T dO
-//     dh = gamma_C dh' + Q^T diag(gamma) dO - w^T Y,
-// an affine map of dh' with matrix A_c^T, so it segments exactly like the
-// forward (the transposed maps compose in reverse order).
-//
-// One CTA walks a 32-column slice of dh (columns are independent).  Compute
-// thread r (of 128) owns row r of the slice in fp32 registers and TMEM lane r
-// of every product.  Per chunk the tcgen05 products (M = 128, N = 32, K = 128)
-//     K dh'            (A = K, K-major)
-//     P^T dO           (A = the P tile read MN-major)
-//     Q^T (gamma dO)   (A = the Q tile read MN-major), then += w^T (-Y) on top
-//                      (A = the w tile read MN-major)
-// take B operands written column by column by the compute threads (dh'^T,
-// dO^T, (gamma dO)^T, (-Y)^T, 32 x 128 bf16, 128-byte-swizzled K-major).  The
-// two dO products do not depend on dh', so they run ahead of the chain
-// dh' -> Y -> dh.  A fifth warp issues the MMAs once their operands are
-// signalled ready; a sixth issues the TMA loads of the chunk tiles (P, Q, K, w
-// in the order consumed) into a ring of six 32 KiB slots, refilling each as
-// soon as the MMA that read it completes.  Every wait is bounded; one that gives up
-// sets bit 0 of the status word.
-//
-// Modes:
-//   WALK (fold = 0): from the cotangent leaving the segment, store for every
-//     chunk the bf16 cotangent of the state leaving it and dDelta; segment 0
-//     writes dh0 (the cotangent of the initial state).
-//   FOLD (fold = 1): push [Abar | Bbar] from [I | 0] backwards through the
-//     segment's chunks; the Abar columns take no dO terms.  The result maps
-//     the cotangent leaving the segment to the one entering it:
-//     dh_in = Abar dh_out + Bbar.
-#include "gdn_kernels.cuh"
-#include "gdn_tc05.cuh"
+// gdn_walk_bwd.cu -- the segment fold of the reverse walk of the state
+// cotangent (the body is in gdn_walk_bwd.cuh; gdn_walk_pair.cu runs the walk
+// itself beside the forward state recompute).
+#include "gdn_walk_bwd.cuh"
 
 namespace gdn {
 
 namespace {
 
-constexpr int NC_THREADS = 128;               // compute threads
-constexpr int NT = NC_THREADS + 96;           // + MMA issuer, TMA producer and TMA store warps
-constexpr int NRING = 5;                      // tile ring
-constexpr uint32_t STAGE_BYTES = 4 * 8192;    // staging of stored 32-column slices
-constexpr uint32_t TILE_BYTES = CH * HD * 2;  // 32 KiB
-constexpr uint32_t BT_BYTES = SL * HD * 2;    // 8 KiB: a [32 x 128] B-operand tile
-
-struct WalkBwdSmem {
-  unsigned char slot[NRING][TILE_BYTES];
-  unsigned char stage[STAGE_BYTES];  // dh' and dDelta slices, double-buffered, 64-byte swizzle
-  unsigned char Xt[BT_BYTES];   // dh'^T
-  unsigned char Yt[BT_BYTES];   // (-Y)^T
-  unsigned char Ot[BT_BYTES];   // dO^T (this slice)
-  unsigned char Ogt[BT_BYTES];  // (diag(gamma) dO)^T
-  float gsum[2][4];
-  uint64_t full[NRING], empty[NRING];
-  uint64_t barO, barXt, barYt, barP, barQ, barY, barH;
-  uint64_t sfull[2], sempty[2];  // staging buffer set i & 1: written by the compute threads / read by its stores
-  uint32_t tmem;
-};
-
-// TMEM columns: K dh' at 0, P^T dO at 32; Q^T (gamma dO) - w^T Y alternates 64 / 96
-constexpr uint32_t C_Y = 0, C_P = 32;
-__device__ __forceinline__ uint32_t c_q(int ci) { return (ci & 1) ? 96u : 64u; }
-
-__device__ __forceinline__ void write_bt_column(unsigned char* tile, int k, const float (&v)[32]) {
-#pragma unroll
-  for (int n = 0; n < 32; ++n)
-    *reinterpret_cast<bf16*>(tile + tc::sw128(n, k, 32)) = __float2bfloat16_rn(v[n]);
-}
-// row r (32 values) of a [128 x 32] staging slice, 64-byte swizzle
-__device__ __forceinline__ void stage_row(unsigned char* buf, int r, const float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 o;
-    o.x = pack_bf16(v[8 * q], v[8 * q + 1]);
-    o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-    o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-    o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-    *reinterpret_cast<uint4*>(buf + tc::sw64_chunk(r, q)) = o;
-  }
-}
-__device__ __forceinline__ void store_row_f32(float* dst, const float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-__device__ __forceinline__ void arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-template <bool FOLD>
-__global__ void __launch_bounds__(NT, 1) k_walk_bwd(WalkBwdArgs a, const __grid_constant__ WalkBwdMaps mp) {
+template <bool FOLD, int SW>
+__global__ void __launch_bounds__(walkb::BwdCfg<SW>::NT, 1)
+    k_walk_bwd(WalkBwdArgs a, const __grid_constant__ WalkBwdMaps mp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  WalkBwdSmem& sm = *reinterpret_cast<WalkBwdSmem*>(base);
-  const int slice = blockIdx.x, seg = blockIdx.y, bhi = blockIdx.z;
-  const int b = bhi / a.Hv, j = bhi % a.Hv, kh = j / (a.Hv / a.Hk);
-  const long bh = bhi;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int cbeg = (int)((long)seg * a.NC / a.S), cend = (int)((long)(seg + 1) * a.NC / a.S);
-  const bool partA = FOLD && slice < 4;  // Abar columns: no dO terms
-  const bool withO = !partA;
-  const int TPC = withO ? 4 : 2;  // tiles per chunk: P, Q, K, w (or K, w)
-  const int n = cend - cbeg;
-  const int ntiles = n * TPC;
-  const int col0 = (slice & 3) * SL;
-  if (n <= 0) return;
-  auto chunk_of = [&](int ci) { return cend - 1 - ci; };  // walk order
-  auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
-
-  if (tid == 0) {
-    for (int k = 0; k < NRING; ++k) {
-      tc::mbar_init(&sm.full[k], 1);
-      tc::mbar_init(&sm.empty[k], 1);
-    }
-    tc::mbar_init(&sm.barO, NC_THREADS);
-    tc::mbar_init(&sm.barXt, NC_THREADS);
-    tc::mbar_init(&sm.barYt, NC_THREADS);
-    tc::mbar_init(&sm.barP, 1);
-    tc::mbar_init(&sm.barQ, 1);
-    tc::mbar_init(&sm.barY, 1);
-    tc::mbar_init(&sm.barH, 1);
-    for (int k = 0; k < 2; ++k) {
-      tc::mbar_init(&sm.sfull[k], NC_THREADS);
-      tc::mbar_init(&sm.sempty[k], 1);
-    }
-    tc::mbar_fence_init();
-  }
-  if (warp == 0) tc::alloc(&sm.tmem, 128);
-  bool ok = true;
-
-  const int r = tid;  // compute threads: row r of the slice / of the chunk
-  float x[32];
-  float gnext = 0.f, part = 0.f;
-  float gam_r = 0.f, ef_r = 0.f, gC = 0.f;
-  uint4 don[4];  // dO row r of the next chunk's images (this slice's 32 columns)
-  auto load_g = [&](int ci) {
-    if (ci >= n) return 0.f;
-    const int c = chunk_of(ci);
-    return r < rows_of(c) ? a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j] : 0.f;
-  };
-  auto load_do = [&](int ci) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) don[q] = make_uint4(0u, 0u, 0u, 0u);
-    if (!withO || ci >= n) return;
-    const int c = chunk_of(ci);
-    if (r < rows_of(c)) {
-      const bf16* src = a.dO + (((long)b * a.T + (long)c * CH + r) * a.Hv + j) * HD + col0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) don[q] = *reinterpret_cast<const uint4*>(src + 8 * q);
-    }
-  };
-  // dO^T and (gamma dO)^T images of the chunk whose dO rows are in don
-  auto write_do_images = [&]() {
-    float d[32], dg[32];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t w4[4] = {don[q].x, don[q].y, don[q].z, don[q].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = unpack_bf16(w4[e]);
-        d[8 * q + 2 * e] = f.x;
-        d[8 * q + 2 * e + 1] = f.y;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) dg[i] = gam_r * d[i];
-    write_bt_column(sm.Ot, r, d);
-    write_bt_column(sm.Ogt, r, dg);
-  };
-  auto scan_part = [&](float gv, int i) {  // warp-inclusive scan; warp totals to gsum[i & 1]
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float o = __shfl_up_sync(0xffffffffu, gv, off);
-      if (lane >= off) gv += o;
-    }
-    if (lane == 31) sm.gsum[i & 1][warp] = gv;
-    return gv;
-  };
-  auto finish_gates = [&](float p, int i) {  // after a barrier over the compute threads
-    float off = 0.f, tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float s = sm.gsum[i & 1][w];
-      off += (w < warp) ? s : 0.f;
-      tot += s;
-    }
-    const float G = p + off;
-    gam_r = expf(G);
-    ef_r = expf(tot - G);
-    gC = expf(tot);
-  };
-  if (warp < 4) {
-    if (FOLD) {
-#pragma unroll
-      for (int q = 0; q < 32; ++q) x[q] = (partA && r == col0 + q) ? 1.f : 0.f;
-    } else {
-      const float* hs = a.hstart ? a.hstart + bh * a.hstart_bh_stride + seg * a.hstart_seg_stride : nullptr;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (hs) v = *reinterpret_cast<const float4*>(hs + (long)r * HD + col0 + 4 * q);
-        x[4 * q] = v.x;
-        x[4 * q + 1] = v.y;
-        x[4 * q + 2] = v.z;
-        x[4 * q + 3] = v.w;
-      }
-    }
-    write_bt_column(sm.Xt, r, x);
-    part = scan_part(load_g(0), 0);
-    gnext = load_g(1);
-    load_do(0);
-  }
-  tc::fence_proxy_async();
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  const uint32_t tmem = sm.tmem;
-
-  auto issue = [&](int i) {  // TMA request of tile i into slot i % NRING
-    const int ci = i / TPC, t = i % TPC;
-    const int c = chunk_of(ci);
-    const int kind = withO ? t : (t == 0 ? 2 : 3);  // 0 P, 1 Q, 2 K, 3 w
-    const long cid = bh * a.NC + c;
-    unsigned char* dst = sm.slot[i % NRING];
-    uint64_t* bar = &sm.full[i % NRING];
-    tc::arrive_expect_tx(bar, TILE_BYTES);
-    if (kind == 0 || kind == 3) {
-      const CUtensorMap* m = (kind == 0) ? &mp.P : &mp.W;
-      tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
-      tc::tma_load_2d(dst + TILE_BYTES / 2, m, 64, (int)(cid * CH), bar);
-    } else {
-      const CUtensorMap* m = (kind == 1) ? &mp.q : &mp.k;
-      tc::tma_load_4d(dst, m, 0, kh, c * CH, b, bar);
-      tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
-    }
-  };
-
-  if (warp == 6) {
-    // ============================================================ TMA stores
-    // The staged dh' and dDelta slices of each chunk leave by TMA stores once the
-    // compute threads have signalled them; when the stores have read the buffers
-    // they are handed back.  A store request can block its thread.
-    if (!FOLD && lane == 0 && (a.dstates || a.ddelta)) {
-      for (int ci = 0; ci < n; ++ci) {
-        const int c = chunk_of(ci);
-        ok = ok && tc::mbar_wait(&sm.sfull[ci & 1], (uint32_t)((ci >> 1) & 1));
-        if (a.dstates) tc::tma_store_2d(&mp.Ds, col0, (int)((bh * a.NC + c) * HD), sm.stage + (ci & 1) * 8192);
-        if (a.ddelta)
-          tc::tma_store_2d(&mp.Dd, col0, (int)((bh * a.NC + c) * CH), sm.stage + 16384 + (ci & 1) * 8192);
-        tc::bulk_commit();
-        tc::bulk_wait_read();
-        arrive(&sm.sempty[ci & 1]);
-      }
-      tc::bulk_wait();  // every store has completed before the block exits
-    }
-  } else if (warp == 5) {
-    // ========================================================== TMA producer
-    if (lane == 0) {
-      for (int i = 0; i < ntiles; ++i) {
-        if (i >= NRING) ok = ok && tc::mbar_wait(&sm.empty[i % NRING], (uint32_t)((i / NRING - 1) & 1));
-        issue(i);
-      }
-    }
-  } else if (warp == 4) {
-    // ================================================================ MMA issuer
-    // Order of issue (= order of execution on the tensor core): the chain
-    // K dh' -> (Y formed) -> w^T Y -> (dh formed) runs as soon as its operands
-    // are written; Q^T (gamma dO) fills the gap while Y is formed and the next
-    // chunk's P^T dO the gap while dh is formed.  After each product its tile
-    // slot is released to the producer by a commit to the slot's empty barrier.
-    if (lane == 0) {
-      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NRING], (i / NRING) & 1); };
-      auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NRING]); };
-      auto release = [&](int i) { tc::commit(&sm.empty[i % NRING]); };
-      auto issue_p = [&](int ci) {  // P^T dO of chunk ci (its dO images are written)
-        ok = ok && tc::mbar_wait(&sm.barO, (uint32_t)(ci & 1));
-        wait_tile(ci * TPC);
-        tc::fence_after();
-        tc::gemm_amn_k128(tmem + C_P, slot_of(ci * TPC), smem_u32(sm.Ot), 32, false);
-        tc::commit(&sm.barP);
-        release(ci * TPC);
-      };
-      if (withO) issue_p(0);
-      for (int ci = 0; ci < n; ++ci) {
-        const uint32_t par = (uint32_t)(ci & 1);
-        const int t0 = ci * TPC;
-        const int iQ = t0 + 1, iK = t0 + (withO ? 2 : 0), iW = t0 + (withO ? 3 : 1);
-        ok = ok && tc::mbar_wait(&sm.barXt, par);  // dh' image of this chunk
-        wait_tile(iK);
-        tc::fence_after();
-        tc::gemm_k128(tmem + C_Y, slot_of(iK), smem_u32(sm.Xt), 32, false);
-        tc::commit(&sm.barY);
-        release(iK);
-        if (withO) {
-          wait_tile(iQ);
-          tc::fence_after();
-          tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iQ), smem_u32(sm.Ogt), 32, false);
-          tc::commit(&sm.barQ);
-          release(iQ);
-        }
-        ok = ok && tc::mbar_wait(&sm.barYt, par);  // (-Y)^T written
-        wait_tile(iW);
-        tc::fence_after();
-        tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iW), smem_u32(sm.Yt), 32, withO);
-        tc::commit(&sm.barH);
-        release(iW);
-        if (withO && ci + 1 < n) issue_p(ci + 1);
-      }
-    }
-  } else {
-    // ========================================================== compute threads
-    finish_gates(part, 0);
-    if (withO) {
-      write_do_images();
-      tc::fence_proxy_async();
-      tc::fence_before();
-      arrive(&sm.barO);
-      load_do(1);
-    }
-    arrive(&sm.barXt);  // the first dh' image was written before the block barrier
-    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
-    for (int ci = 0; ci < n; ++ci) {
-      const int c = chunk_of(ci);
-      const uint32_t par = (uint32_t)(ci & 1);
-      // staging of chunk index i: dh' at stage[(i & 1) * 8192], dDelta at stage[16384 + (i & 1) * 8192]
-      // staging buffer set ci & 1 was last read by the stores of chunk ci - 2
-      if (!FOLD && ci >= 2) ok = ok && tc::mbar_wait(&sm.sempty[ci & 1], (uint32_t)(((ci >> 1) + 1) & 1));
-      if (!FOLD && a.dstates) stage_row(sm.stage + (ci & 1) * 8192, r, x);
-      part = scan_part(gnext, ci + 1);  // gates of the next chunk
-      gnext = load_g(ci + 2);
-
-      // ---- Y = diag(ef) K dh' + P^T dO ----------------------------------------------
-      float y[32];
-      ok = ok && tc::mbar_wait(&sm.barY, par);
-      tc::fence_after();
-      tc::ld32(tl + C_Y, y);
-#pragma unroll
-      for (int q = 0; q < 32; ++q) y[q] *= ef_r;
-      if (withO) {
-        ok = ok && tc::mbar_wait(&sm.barP, par);
-        tc::fence_after();
-        float pd[32];
-        tc::ld32(tl + C_P, pd);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) y[q] += pd[q];
-      }
-      if (!FOLD && a.ddelta) stage_row(sm.stage + 16384 + (ci & 1) * 8192, r, y);
-      if (!FOLD) {  // dh' and dDelta of this chunk are staged
-        tc::fence_proxy_async();
-        arrive(&sm.sfull[ci & 1]);
-      }
-#pragma unroll
-      for (int q = 0; q < 32; ++q) y[q] = -y[q];
-      write_bt_column(sm.Yt, r, y);
-      tc::fence_proxy_async();
-      tc::fence_before();
-      arrive(&sm.barYt);
-
-      // ---- gates and dO images of the next chunk -------------------------------------
-      const float gC_cur = gC;
-      asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");
-      finish_gates(part, ci + 1);
-      if (withO && ci + 1 < n) {  // both dO products of this chunk have read the images
-        ok = ok && tc::mbar_wait(&sm.barQ, par);
-        write_do_images();
-        tc::fence_proxy_async();
-        tc::fence_before();
-        arrive(&sm.barO);
-        load_do(ci + 2);
-      }
-
-      // ---- dh = gamma_C dh' + Q^T (gamma dO) - w^T Y ---------------------------------
-      ok = ok && tc::mbar_wait(&sm.barH, par);
-      tc::fence_after();
-      float hv[32];
-      tc::ld32(tl + c_q(ci), hv);
-#pragma unroll
-      for (int q = 0; q < 32; ++q) x[q] = gC_cur * x[q] + hv[q];
-      if (ci + 1 < n) {
-        write_bt_column(sm.Xt, r, x);
-        tc::fence_proxy_async();
-        tc::fence_before();
-        arrive(&sm.barXt);
-      }
-    }
-    if (FOLD) {
-      store_row_f32((partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0, x);
-    } else if (a.dh0 && seg == 0) {
-      store_row_f32(a.dh0 + (bh * HD + r) * HD + col0, x);
-    }
-  }
-  if (!ok && a.status) atomicOr(a.status, 1);
-  tc::fence_before();
-  __syncthreads();
-  if (warp == 0) tc::dealloc(tmem, 128);
+  walkb::walk<FOLD, SW>(a, mp, base, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
-template <bool FOLD>
+template <bool FOLD, int SW>
 cudaError_t launch_one(const WalkBwdArgs& a, const WalkBwdMaps& m, cudaStream_t s) {
-  const size_t smem = sizeof(WalkBwdSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_walk_bwd<FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = sizeof(walkb::WalkBwdSmem<SW>) + 1024;
+  cudaError_t e =
+      cudaFuncSetAttribute(k_walk_bwd<FOLD, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_walk_bwd<FOLD><<<dim3(FOLD ? 8 : HD / SL, a.S, a.B * a.Hv), NT, smem, s>>>(a, m);
+  constexpr int NSL = HD / SW;
+  k_walk_bwd<FOLD, SW><<<dim3(FOLD ? 2 * NSL : NSL, a.S, a.B * a.Hv), walkb::BwdCfg<SW>::NT, smem, s>>>(a, m);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t walk_bwd_smem_bytes(int) { return sizeof(WalkBwdSmem) + 1024; }
+size_t walk_bwd_smem_bytes(int) { return sizeof(walkb::WalkBwdSmem<32>) + 1024; }
 
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, const WalkBwdMaps& m, int fold, cudaStream_t s) {
-  return fold ? launch_one<true>(a, m, s) : launch_one<false>(a, m, s);
+  // the fold, on 32-column slices; the walk runs in the pair launch
+  if (!fold) return cudaErrorInvalidValue;
+  return launch_one<true, 32>(a, m, s);
 }
 
 }  // namespace gdn

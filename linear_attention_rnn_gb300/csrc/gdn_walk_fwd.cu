@@ -1,445 +1,39 @@
-// gdn_walk_fwd.cu -- sequential forward walk over the chunks of a segment.
-//
-// Inter-chunk step ("GatedDeltaNet does not support ici_context_parallelism",
-// section "The recurrence is affine, so it can be parallelized"):
-//     Delta = u - w h,     h' = exp(g_last) h + k_g^T Delta,
-// with k_g = diag(exp(G_last - G)) K, and the masked intra-chunk output
-//     O = diag(gamma) Q h + P Delta,      P = (Q K^T) * decay (diagonal included).
-//
-// One CTA walks a 32-column slice of one head's state (columns of h evolve
-// independently: every matrix of the step acts on h from the left).  Compute
-// thread r (of 128) owns row r: row r of the state slice in fp32 registers for
-// the whole segment, and TMEM lane r of every product.  Per chunk the products
-//     X  = w h            (A = w, K-major)
-//     H' = K^T (ef Delta) (A = the K tile read MN-major: no transpose pass)
-//     O1 = Q h,  O2 = P Delta
-// are tcgen05 MMAs (M = 128, N = 32, K = 128) into tensor memory.  Their B
-// operands (h^T, Delta^T, (ef Delta)^T, 32 x 128 bf16) are written column by
-// column by the compute threads in the 128-byte-swizzled K-major layout.
-//
-// A fifth warp issues the MMAs as soon as their operands are signalled ready
-// on mbarriers by the compute threads; a sixth issues the TMA loads of the
-// chunk tiles into a ring of six 32 KiB slots (w, Q, K, P in the order the
-// MMAs consume them), refilling each slot as soon as the MMA that read it has
-// completed.  A TMA request can block its thread while earlier copies stream
-// in, so the loads never share a thread with the MMA chain.  Each compute thread reads its row of the u
-// slice straight into registers a chunk ahead.  The compute threads never
-// wait on memory issue, only on MMA completion.  Every wait is bounded; one that
-// gives up sets bit 0 of the status word.
-//
-// Modes:
-//   RECUR (fold = 0): walk from the segment's entering state, write O (if o
-//     is given), and optionally the bf16 entering state and Delta of every
-//     chunk (backward recomputation) and the final state (last segment).
-//   FOLD  (fold = 1): pass 1 of the two-pass segment scan ("Shard the
-//     GatedDeltaNet sequence under ici_context_parallelism", description):
-//     push the augmented state [A | B] through the segment's chunks starting
-//     from [I | 0]; the A columns take no u term.  CTAs 0-3 hold A's column
-//     slices, 4-7 hold B's.
-#include "gdn_kernels.cuh"
-#include "gdn_tc05.cuh"
+// gdn_walk_fwd.cu -- kernels of the sequential forward walk (the body is in
+// gdn_walk_fwd.cuh): the segment fold and the walk with output.  The state
+// recompute of the backward runs in gdn_walk_pair.cu, beside the backward walk.
+#include "gdn_walk_fwd.cuh"
 
 namespace gdn {
 
 namespace {
 
-constexpr int NC_THREADS = 128;                // compute threads: one per chunk row / state row
-constexpr int NT = NC_THREADS + 96;            // + MMA issuer, TMA producer and TMA store warps
-constexpr int NSLOT = 6;                       // tile ring slots (the last one doubles as staging)
-constexpr uint32_t TILE_BYTES = CH * HD * 2;   // 32 KiB
-constexpr uint32_t BT_BYTES = SL * HD * 2;     // 8 KiB: a [32 x 128] B-operand tile
-
-struct WalkSmem {
-  unsigned char slot[NSLOT][TILE_BYTES];
-  unsigned char Ht[2][BT_BYTES];  // h^T of chunk index i in Ht[i & 1]
-  unsigned char Dt[BT_BYTES];
-  unsigned char Dgt[BT_BYTES];
-  float gsum[2][4];
-  uint64_t full[NSLOT], empty[NSLOT];
-  uint64_t barX, barO1, barH, barO2, barDg, barD, barHt;
-  uint64_t sfull[2], sempty[2];  // staging buffer set i & 1: written by the compute threads / read by its stores
-  uint32_t tmem;
-};
-
-// Column k of a [32 x 128] K-major SW128 B tile from 32 fp32 values (rows n).
-__device__ __forceinline__ void write_bt_column(unsigned char* tile, int k, const float (&v)[32]) {
-#pragma unroll
-  for (int n = 0; n < 32; ++n)
-    *reinterpret_cast<bf16*>(tile + tc::sw128(n, k, 32)) = __float2bfloat16_rn(v[n]);
-}
-
-__device__ __forceinline__ void store_row_bf16(bf16* dst, const float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 o;
-    o.x = pack_bf16(v[8 * q], v[8 * q + 1]);
-    o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-    o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-    o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-    *reinterpret_cast<uint4*>(dst + 8 * q) = o;
-  }
-}
-
-// row r (32 values) of a [128 x 32] staging slice, 64-byte swizzle
-__device__ __forceinline__ void stage_row(unsigned char* buf, int r, const float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 o;
-    o.x = pack_bf16(v[8 * q], v[8 * q + 1]);
-    o.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-    o.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-    o.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-    *reinterpret_cast<uint4*>(buf + tc::sw64_chunk(r, q)) = o;
-  }
-}
-
-__device__ __forceinline__ void arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// STAGED: the recompute mode (exports h and Delta, no output).
-template <bool FOLD, bool STAGED>
-__global__ void __launch_bounds__(NT, 1) k_walk_fwd(WalkFwdArgs a, const __grid_constant__ WalkFwdMaps mp) {
+template <bool FOLD, bool STAGED, int SW>
+__global__ void __launch_bounds__(walkf::FwdCfg<SW>::NT, 1)
+    k_walk_fwd(WalkFwdArgs a, const __grid_constant__ WalkFwdMaps mp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  WalkSmem& sm = *reinterpret_cast<WalkSmem*>(base);
-  const int slice = blockIdx.x, seg = blockIdx.y, bhi = blockIdx.z;
-  const int b = bhi / a.Hv, j = bhi % a.Hv, kh = j / (a.Hv / a.Hk);
-  const long bh = bhi;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int cbeg = (int)((long)seg * a.NC / a.S), cend = (int)((long)(seg + 1) * a.NC / a.S);
-  const bool partA = FOLD && slice < 4;  // A columns: no u term
-  const bool withO = !FOLD && a.o != nullptr;
-  const int TPC = withO ? 4 : 2;  // tiles per chunk: w, (Q,) K (, P)
-  const int ntiles = (cend - cbeg) * TPC;
-  const int col0 = (slice & 3) * SL;
-  // The recompute mode stages its exported h and Delta slices in the last slot
-  // (8 KiB each, double-buffered, 64-byte swizzle; a store warp writes them
-  // out) and streams its 2 tiles per chunk through a 5-slot ring.  The output
-  // mode needs all 6 slots for its 4 tiles per chunk and stores O rows
-  // directly (measured faster than staging it at 5 slots); the fold pass
-  // stores nothing per chunk.
-  constexpr bool staged = STAGED;
-  constexpr int nring = STAGED ? NSLOT - 1 : NSLOT;  // compile-time: the ring index is on the issue path
-  unsigned char* stage = sm.slot[NSLOT - 1];
-  if (cbeg >= cend) return;
-  auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
-  // tile sequence of a chunk: w, Q, K, P (with output) or w, K
-  auto tile_of = [&](int kind) { return withO ? kind : (kind == 0 ? 0 : 1); };  // kind: 0 w, 1 Q, 2 K, 3 P
-
-  if (tid == 0) {
-    for (int k = 0; k < NSLOT; ++k) {
-      tc::mbar_init(&sm.full[k], 1);
-      tc::mbar_init(&sm.empty[k], 1);
-    }
-    tc::mbar_init(&sm.barX, 1);
-    tc::mbar_init(&sm.barO1, 1);
-    tc::mbar_init(&sm.barH, 1);
-    tc::mbar_init(&sm.barO2, 1);
-    tc::mbar_init(&sm.barDg, NC_THREADS);
-    tc::mbar_init(&sm.barD, NC_THREADS);
-    tc::mbar_init(&sm.barHt, NC_THREADS);
-    for (int k = 0; k < 2; ++k) {
-      tc::mbar_init(&sm.sfull[k], NC_THREADS);
-      tc::mbar_init(&sm.sempty[k], 1);
-    }
-    tc::mbar_fence_init();
-  }
-  if (warp == 0) tc::alloc(&sm.tmem, 256);
-  bool ok = true;
-
-  // state row r = tid (compute threads), columns col0..col0+31
-  const int r = tid;
-  float h[32];
-  float gnext = 0.f, part = 0.f;
-  float gam_r = 0.f, ef_r = 0.f, gC = 0.f;
-  auto load_g = [&](int c) {
-    return (c < cend && r < rows_of(c)) ? a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j] : 0.f;
-  };
-  // row r of this slice of u for chunk c, loaded a chunk ahead into registers
-  uint4 un[4];
-  auto load_u = [&](int c) {
-    if (partA || c >= cend) return;
-    const bf16* src = a.U + ((bh * a.NC + c) * CH + r) * HD + col0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) un[q] = *reinterpret_cast<const uint4*>(src + 8 * q);
-  };
-  // gate totals of chunk index i (from the segment start) go to gsum[i & 1]:
-  // a warp may post the totals of chunk i + 1 while another still reads those of i
-  auto scan_part = [&](float gv, int i) {  // warp-inclusive scan; warp totals to smem
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float o = __shfl_up_sync(0xffffffffu, gv, off);
-      if (lane >= off) gv += o;
-    }
-    if (lane == 31) sm.gsum[i & 1][warp] = gv;
-    return gv;
-  };
-  // after a barrier over the compute threads: gamma_r, ef_r and gamma_C of chunk index i
-  auto finish_gates = [&](float p, int i, float& gm, float& ef, float& gc) {
-    float off = 0.f, tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float s = sm.gsum[i & 1][w];
-      off += (w < warp) ? s : 0.f;
-      tot += s;
-    }
-    const float G = p + off;
-    gm = expf(G);
-    ef = expf(tot - G);
-    gc = expf(tot);
-  };
-  if (warp < 4) {
-    if (FOLD) {
-#pragma unroll
-      for (int n = 0; n < 32; ++n) h[n] = (partA && r == col0 + n) ? 1.f : 0.f;
-    } else {
-      const float* hs = a.hstart ? a.hstart + bh * a.hstart_bh_stride + seg * a.hstart_seg_stride : nullptr;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (hs) x = *reinterpret_cast<const float4*>(hs + (long)r * HD + col0 + 4 * q);
-        h[4 * q] = x.x;
-        h[4 * q + 1] = x.y;
-        h[4 * q + 2] = x.z;
-        h[4 * q + 3] = x.w;
-      }
-    }
-    write_bt_column(sm.Ht[0], r, h);
-    load_u(cbeg);
-    part = scan_part(load_g(cbeg), 0);
-    gnext = load_g(cbeg + 1);
-  }
-  tc::fence_proxy_async();
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  // TMEM columns: X = w h at 0, H' at 32, P Delta at 96; Q h alternates between
-  // 64 and 128 (it is read after the next chunk's Q h may have been issued)
-  const uint32_t tmem = sm.tmem;
-  auto o1_col = [](int ci) { return (ci & 1) ? 128u : 64u; };
-
-  auto issue = [&](int i) {  // TMA request of tile i into slot i % nring
-    const int c = cbeg + i / TPC, t = i % TPC;
-    const int kind = withO ? t : (t == 0 ? 0 : 2);
-    const long cid = bh * a.NC + c;
-    unsigned char* dst = sm.slot[i % nring];
-    uint64_t* bar = &sm.full[i % nring];
-    tc::arrive_expect_tx(bar, TILE_BYTES);
-    if (kind == 0 || kind == 3) {
-      const CUtensorMap* m = (kind == 0) ? &mp.W : &mp.P;
-      tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
-      tc::tma_load_2d(dst + TILE_BYTES / 2, m, 64, (int)(cid * CH), bar);
-    } else {
-      const CUtensorMap* m = (kind == 1) ? &mp.q : &mp.k;
-      tc::tma_load_4d(dst, m, 0, kh, c * CH, b, bar);
-      tc::tma_load_4d(dst + TILE_BYTES / 2, m, 64, kh, c * CH, b, bar);
-    }
-  };
-
-  if (warp == 6) {
-    // ============================================================ TMA stores
-    // The h and Delta slices staged for chunk index i leave by TMA stores once
-    // the compute threads have signalled them; when the stores have read the
-    // buffers they are handed back.  A store request can block its thread, so
-    // it never runs on a compute or issuing thread.
-    if (staged && lane == 0) {
-      for (int c = cbeg; c < cend; ++c) {
-        const int ci = c - cbeg;
-        ok = ok && tc::mbar_wait(&sm.sfull[ci & 1], (uint32_t)((ci >> 1) & 1));
-        if (a.states) tc::tma_store_2d(&mp.St, col0, (int)((bh * a.NC + c) * HD), stage + (ci & 1) * 8192);
-        if (a.delta)
-          tc::tma_store_2d(&mp.De, col0, (int)((bh * a.NC + c) * CH), stage + 16384 + (ci & 1) * 8192);
-        tc::bulk_commit();
-        tc::bulk_wait_read();
-        arrive(&sm.sempty[ci & 1]);
-      }
-      tc::bulk_wait();  // every store has completed before the block exits
-    }
-  } else if (warp == 5) {
-    // ========================================================== TMA producer
-    // Tile i goes into slot i % nring once the product that read tile
-    // i - nring has completed (signalled on that slot's empty barrier).
-    if (lane == 0) {
-      for (int i = 0; i < ntiles; ++i) {
-        if (i >= nring) ok = ok && tc::mbar_wait(&sm.empty[i % nring], (uint32_t)((i / nring - 1) & 1));
-        issue(i);
-      }
-    }
-  } else if (warp == 4) {
-    // ================================================================ MMA issuer
-    // Chain products first: w h(c) as soon as the state image is written, then
-    // K^T (ef Delta) as soon as Delta is; Q h(c) and P Delta fill the gaps.  An
-    // MMA issue returns about when the tensor core has taken it, so the order
-    // of issue is the order of execution.  After each product its tile slot is
-    // released to the producer by a commit to the slot's empty barrier.
-    if (lane == 0) {
-      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % nring], (i / nring) & 1); };
-      auto slot_of = [&](int i) { return smem_u32(sm.slot[i % nring]); };
-      auto release = [&](int i) { tc::commit(&sm.empty[i % nring]); };
-      for (int c = cbeg; c < cend; ++c) {
-        const int ci = c - cbeg;
-        const uint32_t par = (uint32_t)(ci & 1);
-        const int t0 = ci * TPC;
-        const int iW = t0, iQ = t0 + 1, iK = t0 + tile_of(2), iP = t0 + 3;
-        const uint32_t ht = smem_u32(sm.Ht[ci & 1]);
-        if (ci > 0) ok = ok && tc::mbar_wait(&sm.barHt, par ^ 1);  // state image of chunk c
-        wait_tile(iW);
-        tc::fence_after();
-        tc::gemm_k128(tmem + 0, slot_of(iW), ht, 32, false);
-        tc::commit(&sm.barX);
-        release(iW);
-        if (withO) {
-          wait_tile(iQ);
-          tc::fence_after();
-          tc::gemm_k128(tmem + o1_col(ci), slot_of(iQ), ht, 32, false);
-          tc::commit(&sm.barO1);
-          release(iQ);
-        }
-        ok = ok && tc::mbar_wait(&sm.barDg, par);  // (ef Delta)^T written
-        wait_tile(iK);
-        tc::fence_after();
-        tc::gemm_amn_k128(tmem + 32, slot_of(iK), smem_u32(sm.Dgt), 32, false);
-        tc::commit(&sm.barH);
-        release(iK);
-        if (withO) {
-          ok = ok && tc::mbar_wait(&sm.barD, par);  // Delta^T written
-          wait_tile(iP);
-          tc::fence_after();
-          tc::gemm_k128(tmem + 96, slot_of(iP), smem_u32(sm.Dt), 32, false);
-          tc::commit(&sm.barO2);
-          release(iP);
-        }
-      }
-    }
-  } else {
-    // ========================================================== compute threads
-    finish_gates(part, 0, gam_r, ef_r, gC);
-    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
-    for (int c = cbeg; c < cend; ++c) {
-      const int ci = c - cbeg;
-      const uint32_t par = (uint32_t)(ci & 1);
-      // staging of chunk index i: h at stage[(i & 1) * 8192], Delta at stage[16384 + (i & 1) * 8192]
-      // staging buffer set ci & 1 was last read by the stores of chunk ci - 2
-      if (staged && ci >= 2) ok = ok && tc::mbar_wait(&sm.sempty[ci & 1], (uint32_t)(((ci >> 1) + 1) & 1));
-      if (!FOLD && a.states) stage_row(stage + (ci & 1) * 8192, r, h);
-
-      // ---- Delta = u - X -------------------------------------------------------
-      ok = ok && tc::mbar_wait(&sm.barX, par);
-      tc::fence_after();
-      float x[32];
-      tc::ld32(tl + 0, x);
-      if (!partA) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 w4 = un[q];
-          const float2 f0 = unpack_bf16(w4.x), f1 = unpack_bf16(w4.y), f2 = unpack_bf16(w4.z),
-                       f3 = unpack_bf16(w4.w);
-          x[8 * q] = f0.x - x[8 * q];
-          x[8 * q + 1] = f0.y - x[8 * q + 1];
-          x[8 * q + 2] = f1.x - x[8 * q + 2];
-          x[8 * q + 3] = f1.y - x[8 * q + 3];
-          x[8 * q + 4] = f2.x - x[8 * q + 4];
-          x[8 * q + 5] = f2.y - x[8 * q + 5];
-          x[8 * q + 6] = f3.x - x[8 * q + 6];
-          x[8 * q + 7] = f3.y - x[8 * q + 7];
-        }
-      } else {
-#pragma unroll
-        for (int n = 0; n < 32; ++n) x[n] = -x[n];
-      }
-      float xg[32];
-#pragma unroll
-      for (int n = 0; n < 32; ++n) xg[n] = x[n] * ef_r;
-      write_bt_column(sm.Dgt, r, xg);  // operand of the state update: first
-      tc::fence_proxy_async();
-      tc::fence_before();
-      arrive(&sm.barDg);
-      load_u(c + 1);
-      if (withO) {
-        write_bt_column(sm.Dt, r, x);
-        tc::fence_proxy_async();
-        tc::fence_before();
-        arrive(&sm.barD);
-      }
-      if (!FOLD && a.delta) stage_row(stage + 16384 + (ci & 1) * 8192, r, x);
-      if (staged) {  // h and Delta of this chunk are staged
-        tc::fence_proxy_async();
-        arrive(&sm.sfull[ci & 1]);
-      }
-
-      // ---- gates of chunk c + 1, while K^T (ef Delta) runs ----------------------------
-      float gam_n, ef_n, gC_n;
-      part = scan_part(gnext, ci + 1);
-      gnext = load_g(c + 2);
-      asm volatile("bar.sync 1, %0;" ::"r"(NC_THREADS) : "memory");
-      finish_gates(part, ci + 1, gam_n, ef_n, gC_n);
-
-      // ---- h' = gamma_C h + H' ---------------------------------------------------
-      ok = ok && tc::mbar_wait(&sm.barH, par);
-      tc::fence_after();
-      float hh[32];
-      tc::ld32(tl + 32, hh);
-#pragma unroll
-      for (int n = 0; n < 32; ++n) h[n] = gC * h[n] + hh[n];
-      // the other image buffer held h of the previous chunk, whose readers have completed
-      write_bt_column(sm.Ht[(ci + 1) & 1], r, h);
-      tc::fence_proxy_async();
-      tc::fence_before();
-      arrive(&sm.barHt);
-      if (withO) {  // output epilogue overlaps the next chunk's first product
-        ok = ok && tc::mbar_wait(&sm.barO2, par);  // covers Q h as well
-        tc::fence_after();
-        float o1[32], o2[32];
-        tc::ld32(tl + o1_col(ci), o1);
-        tc::ld32(tl + 96, o2);
-        if (r < rows_of(c)) {
-#pragma unroll
-          for (int n = 0; n < 32; ++n) o1[n] = gam_r * o1[n] + o2[n];
-          store_row_bf16(a.o + (((long)b * a.T + (long)c * CH + r) * a.Hv + j) * HD + col0, o1);
-        }
-      }
-      gam_r = gam_n;
-      ef_r = ef_n;
-      gC = gC_n;
-    }
-    if (FOLD) {
-      float* dst = (partA ? a.pairA : a.pairB) + ((bh * a.S + seg) * HD + r) * HD + col0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-    } else if (a.hT && seg == a.S - 1) {
-      float* dst = a.hT + (bh * HD + r) * HD + col0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-    }
-  }
-  if (!ok && a.status) atomicOr(a.status, 1);
-  tc::fence_before();
-  __syncthreads();
-  if (warp == 0) tc::dealloc(tmem, 256);
+  walkf::walk<FOLD, STAGED, SW>(a, mp, base, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
-template <bool FOLD, bool STAGED>
+template <bool FOLD, bool STAGED, int SW>
 cudaError_t launch_one(const WalkFwdArgs& a, const WalkFwdMaps& m, cudaStream_t s) {
-  const size_t smem = sizeof(WalkSmem) + 1024;
+  const size_t smem = sizeof(walkf::WalkSmem<SW>) + 1024;
   cudaError_t e =
-      cudaFuncSetAttribute(k_walk_fwd<FOLD, STAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(k_walk_fwd<FOLD, STAGED, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_walk_fwd<FOLD, STAGED><<<dim3(FOLD ? 8 : HD / SL, a.S, a.B * a.Hv), NT, smem, s>>>(a, m);
+  constexpr int NSL = HD / SW;
+  k_walk_fwd<FOLD, STAGED, SW><<<dim3(FOLD ? 2 * NSL : NSL, a.S, a.B * a.Hv), walkf::FwdCfg<SW>::NT, smem, s>>>(a, m);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t walk_fwd_smem_bytes(int) { return sizeof(WalkSmem) + 1024; }
+size_t walk_fwd_smem_bytes(int) { return sizeof(walkf::WalkSmem<32>) + 1024; }
 
 cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold, cudaStream_t s) {
-  const bool staged = a.states != nullptr || a.delta != nullptr;
-  if (fold) return launch_one<true, false>(a, m, s);
-  if (staged && a.o) return cudaErrorInvalidValue;  // one mode per launch: they share the last slot
-  return staged ? launch_one<false, true>(a, m, s) : launch_one<false, false>(a, m, s);
+  if (fold) return launch_one<true, false, 32>(a, m, s);
+  if (a.states || a.delta || !a.o) return cudaErrorInvalidValue;  // the recompute runs in the pair launch
+  return launch_one<false, false, 32>(a, m, s);
 }
 
 }  // namespace gdn
