@@ -172,21 +172,32 @@ def chunk_fwd(q, k, v, g, beta, h0=None, *, chunk: int = 128, n_segments: int = 
 
 
 def chunk_bwd(q, k, v, g, beta, h0, dO, dhT=None, *, chunk: int = 128, n_segments: int = 0,
-              want_dh0: bool = True, workspace=None, events=None):
+              want_dh0: bool = True, out=None, workspace=None, events=None):
     """Backward of the chunked gated delta rule.
     Returns (dq, dk, dv, dg, dbeta, dh0).
+    out: optional (dq, dk, dv, dg, dbeta, dh0) tensors to write (dh0 may be
+    None), e.g. views of one buffer that leaves the device in one copy.
     events: optional torch.cuda.Event list recorded after each kernel launch."""
     B, T, Hk, Hv, dk, dv = _dims(q, k, v, g, beta)
     dev = q.device
     _check(h0, "h0", torch.float32, (B, Hv, dk, dv))
     _check(dO, "dO", torch.bfloat16, (B, T, Hv, dv))
     _check(dhT, "dhT", torch.float32, (B, Hv, dk, dv))
-    dq = torch.empty_like(q)
-    dk_ = torch.empty_like(k)
-    dv_ = torch.empty_like(v)
-    dg = torch.empty_like(g)
-    db = torch.empty_like(beta)
-    dh0 = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=dev) if want_dh0 else None
+    if out is not None:
+        dq, dk_, dv_, dg, db, dh0 = out
+        _check(dq, "dq", torch.bfloat16, tuple(q.shape))
+        _check(dk_, "dk", torch.bfloat16, tuple(k.shape))
+        _check(dv_, "dv", torch.bfloat16, tuple(v.shape))
+        _check(dg, "dg", torch.float32, tuple(g.shape))
+        _check(db, "dbeta", torch.float32, tuple(beta.shape))
+        _check(dh0, "dh0", torch.float32, (B, Hv, dk, dv))
+    else:
+        dq = torch.empty_like(q)
+        dk_ = torch.empty_like(k)
+        dv_ = torch.empty_like(v)
+        dg = torch.empty_like(g)
+        db = torch.empty_like(beta)
+        dh0 = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=dev) if want_dh0 else None
     nbytes = bwd_workspace_bytes(B, T, Hk, Hv, dk, dv, chunk, n_segments)
     ws = _workspace(nbytes, dev, workspace)
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(dO), _ptr(dhT),
