@@ -260,7 +260,36 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
     }
   };
 
-  if (warp == NCW + 2) {
+  if (warp == NCW + 2 && withO) {
+    // ======================================================= output products
+    // Q h(c) once w h(c) has completed (the chain's product goes first) and
+    // P Delta(c) once Delta^T is written, issued from this warp so that their
+    // issue never holds the chain's issuer.  The compute threads wait for
+    // P Delta(c) (which covers Q h(c), issued before it from this thread)
+    // before they overwrite the images or the output columns these read.
+    if (lane == 0) {
+      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % nring], (i / nring) & 1); };
+      auto slot_of = [&](int i) { return smem_u32(sm.slot[i % nring]); };
+      auto release = [&](int i) { tc::commit(&sm.empty[i % nring]); };
+      for (int c = cbeg; c < cend; ++c) {
+        const int ci = c - cbeg;
+        const uint32_t par = (uint32_t)(ci & 1);
+        const int iQ = ci * TPC + 1, iP = ci * TPC + 3;
+        ok = ok && tc::mbar_wait(&sm.barX, par);  // w h(c) done: h(c) is in Ht[ci & 1]
+        wait_tile(iQ);
+        tc::fence_after();
+        tc::gemm_k128(tmem + o1_col(ci), slot_of(iQ), smem_u32(sm.Ht[ci & 1]), SW, false);
+        tc::commit(&sm.barO1);
+        release(iQ);
+        ok = ok && tc::mbar_wait(&sm.barD, par);  // Delta^T written
+        wait_tile(iP);
+        tc::fence_after();
+        tc::gemm_k128(tmem + C_O2, slot_of(iP), smem_u32(sm.Dt), SW, false);
+        tc::commit(&sm.barO2);
+        release(iP);
+      }
+    }
+  } else if (warp == NCW + 2) {
     // ============================================================ TMA stores
     // The h and Delta slices staged for chunk index i leave by TMA stores once
     // the compute threads have signalled them; when the stores have read the
@@ -312,27 +341,14 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
         tc::gemm_k128(tmem + 0, slot_of(iW), ht, SW, false);
         tc::commit(&sm.barX);
         release(iW);
-        if (withO) {
-          wait_tile(iQ);
-          tc::fence_after();
-          tc::gemm_k128(tmem + o1_col(ci), slot_of(iQ), ht, SW, false);
-          tc::commit(&sm.barO1);
-          release(iQ);
-        }
         ok = ok && tc::mbar_wait(&sm.barDg, par);  // (ef Delta)^T written
         wait_tile(iK);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + C_H, slot_of(iK), smem_u32(sm.Dgt), SW, false);
         tc::commit(&sm.barH);
         release(iK);
-        if (withO) {
-          ok = ok && tc::mbar_wait(&sm.barD, par);  // Delta^T written
-          wait_tile(iP);
-          tc::fence_after();
-          tc::gemm_k128(tmem + C_O2, slot_of(iP), smem_u32(sm.Dt), SW, false);
-          tc::commit(&sm.barO2);
-          release(iP);
-        }
+        (void)iQ;
+        (void)iP;
       }
     }
   } else {
