@@ -9,7 +9,7 @@
 
 namespace gdn {
 
-// Per-chunk UT/WY preparation: one CTA per (chunk, value head, batch row).
+// Per-chunk UT/WY preparation: persistent CTAs over (batch row, chunk, key head, value head) units.
 struct PrepArgs {
   const bf16* q;
   const bf16* k;

@@ -1,8 +1,12 @@
 // gdn_prep.cu -- per-chunk UT/WY preparation of the chunked gated delta rule.
 //
-// One CTA per (chunk c, key head, batch row b) serves every value head j that
-// shares the key head.  For the 128 rows of the chunk (zero-padded past T
-// with g = 0, beta = 0):
+// Persistent CTAs, one per SM, each take a contiguous range of units (batch
+// row b, chunk c, key head, value head j), value heads fastest, so a CTA
+// serves the value heads of one (chunk, key head) in a row: it loads K and Q
+// and forms K K^T and Q K^T once for them.  (The range balances the work to
+// within one unit per SM; a grid of one CTA per (chunk, key head) ran in
+// ceil(units / 2 / SMs) rounds of two heads.)  For the 128 rows of the chunk
+// (zero-padded past T with g = 0, beta = 0):
 //   K K^T and Q K^T              tcgen05 products into tensor memory (once per key head)
 //   gates  G = chunk-local cumsum of g, gamma = exp(G)               (per value head)
 //   S = tril(diag(beta) (K K^T * M), -1),  M_rs = exp(G_r - G_s) for s <= r,
@@ -219,42 +223,35 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   PrepSmem& sm = *reinterpret_cast<PrepSmem*>(base);
-  const int c = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int group = a.Hv / a.Hk;
-  const int t0 = c * CH;
-  const int L = min(CH, a.T - t0);
   const bool needP = a.P != nullptr, needU = a.U != nullptr, needW = a.W != nullptr;
   // TMEM row of this thread in the epilogues: lane quarter of the warp, column quarter
   const int quarter = warp & 3, cq = warp >> 2;
   const int row = 32 * quarter + lane;
   const long tile = (long)CH * CH;  // w, u and P tiles: [128][128] row-major in global memory
-
-  // V of value head kh * group + jj into buffer jj % 2 (thread 0)
-  auto load_v = [&](int jj) {
-    unsigned char* dst = (jj & 1) ? sm.Q : sm.V;
-    uint64_t* bar = &sm.barV[jj & 1];
-    tc::arrive_expect_tx(bar, TILE);
-    tc::tma_load_4d(dst, &mp.v, 0, kh * group + jj, t0, b, bar);
-    tc::tma_load_4d(dst + TILE / 2, &mp.v, 64, kh * group + jj, t0, b, bar);
+  // Persistent CTAs: this CTA's contiguous range of units (b, c, kh, jj), jj fastest
+  const long U = (long)a.B * a.NC * a.Hk * group;
+  const long u_begin = (long)blockIdx.x * U / gridDim.x, u_end = (long)(blockIdx.x + 1) * U / gridDim.x;
+  struct Unit {
+    int b, c, kh, jj;
   };
+  auto decode = [&](long u) {
+    Unit x;
+    x.jj = (int)(u % group);
+    const long gidx = u / group;
+    x.kh = (int)(gidx % a.Hk);
+    x.c = (int)((gidx / a.Hk) % a.NC);
+    x.b = (int)(gidx / ((long)a.Hk * a.NC));
+    return x;
+  };
+
   if (tid == 0) {
     tc::mbar_init(&sm.barKQ, 1);
     tc::mbar_init(&sm.barV[0], 1);
     tc::mbar_init(&sm.barV[1], 1);
     tc::mbar_init(&sm.barM, 1);
     tc::mbar_fence_init();
-    tc::arrive_expect_tx(&sm.barKQ, needP ? 2 * TILE : TILE);
-    tc::tma_load_4d(sm.K, &mp.k, 0, kh, t0, b, &sm.barKQ);
-    tc::tma_load_4d(sm.K + TILE / 2, &mp.k, 64, kh, t0, b, &sm.barKQ);
-    if (needP) {
-      tc::tma_load_4d(sm.Q, &mp.q, 0, kh, t0, b, &sm.barKQ);
-      tc::tma_load_4d(sm.Q + TILE / 2, &mp.q, 64, kh, t0, b, &sm.barKQ);
-    }
-    if (needU) {
-      load_v(0);
-      if (group > 1 && !needP) load_v(1);  // the Q buffer is not needed
-    }
   }
   if (warp == 0) tc::alloc(&sm.tmem, 512);
   tc::fence_before();
@@ -263,248 +260,287 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
   const uint32_t tmem = sm.tmem;  // columns: K K^T 0, Q K^T 128, w 256, u 384
   const uint32_t tlane = tmem + ((uint32_t)(32 * quarter) << 16);
   bool ok = true;
-  if (tid == 0) {
-    ok = tc::mbar_wait(&sm.barKQ, 0);
-    tc::fence_after();
-    tc::gemm_k128(tmem + 0, smem_u32(sm.K), smem_u32(sm.K), 128, false);
-    if (needP) tc::gemm_k128(tmem + 128, smem_u32(sm.Q), smem_u32(sm.K), 128, false);
-    tc::commit(&sm.barM);
-  }
-  uint32_t mphase = 0;
+  uint32_t mphase = 0;        // barM phases seen
+  int kq_uses = 0;            // barKQ phases (one per key-head group)
+  uint32_t v_use0 = 0, v_use1 = 0;  // barV[0], barV[1] phases
 
-  // g and beta of row tid for value head kh * group + jj (loaded a head ahead)
-  auto load_gates = [&](int jj, float& gv, float& bv) {
+  // g and beta of row tid for unit u (loaded a head ahead; zero past the range or T)
+  auto load_gates = [&](long u, float& gv, float& bv) {
     gv = bv = 0.f;
-    if (tid < L && jj < group) {
-      const long idx = ((long)b * a.T + t0 + tid) * a.Hv + kh * group + jj;
-      gv = a.g[idx];
-      bv = a.beta[idx];
+    if (u < u_end && tid < CH) {
+      const Unit x = decode(u);
+      if (tid < min(CH, a.T - x.c * CH)) {
+        const long idx = ((long)x.b * a.T + x.c * CH + tid) * a.Hv + x.kh * group + x.jj;
+        gv = a.g[idx];
+        bv = a.beta[idx];
+      }
     }
   };
   float g_next = 0.f, b_next = 0.f;
-  if (tid < CH) load_gates(0, g_next, b_next);
+  load_gates(u_begin, g_next, b_next);
 
-  for (int jj = 0; jj < group; ++jj) {
-    const int j = kh * group + jj;
-    const long bh = (long)b * a.Hv + j;
-    const long chunk_id = bh * a.NC + c;
-    // ---- gates of value head j --------------------------------------------------
-    if (tid < CH) {
-      sm.Gl[tid] = g_next;
-      sm.beta[tid] = b_next;
-      load_gates(jj + 1, g_next, b_next);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      float v[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = sm.Gl[lane * 4 + i];
-      warp_cumsum128(v, lane);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        sm.Gl[lane * 4 + i] = v[i] * LOG2E;
+  for (long ug = u_begin; ug < u_end;) {
+    // ---- a key-head group: value heads jj0 .. jj1 - 1 of (b, c, kh) -------------------
+    const Unit x0 = decode(ug);
+    const int c = x0.c, kh = x0.kh, b = x0.b, jj0 = x0.jj;
+    const int jj1 = (int)min((long)group, jj0 + (u_end - ug));
+    const int t0 = c * CH;
+    // V of value head kh * group + jj, the k-th head of the group, into buffer k % 2 (thread 0)
+    auto load_v = [&](int jj) {
+      const int k = jj - jj0;
+      unsigned char* dst = (k & 1) ? sm.Q : sm.V;
+      uint64_t* bar = &sm.barV[k & 1];
+      tc::arrive_expect_tx(bar, TILE);
+      tc::tma_load_4d(dst, &mp.v, 0, kh * group + jj, t0, b, bar);
+      tc::tma_load_4d(dst + TILE / 2, &mp.v, 64, kh * group + jj, t0, b, bar);
+    };
+    // K, Q and the first V; the previous group's products have completed and
+    // every thread has passed the barrier after them, so the buffers are free
+    if (tid == 0) {
+      tc::arrive_expect_tx(&sm.barKQ, needP ? 2 * TILE : TILE);
+      tc::tma_load_4d(sm.K, &mp.k, 0, kh, t0, b, &sm.barKQ);
+      tc::tma_load_4d(sm.K + TILE / 2, &mp.k, 64, kh, t0, b, &sm.barKQ);
+      if (needP) {
+        tc::tma_load_4d(sm.Q, &mp.q, 0, kh, t0, b, &sm.barKQ);
+        tc::tma_load_4d(sm.Q + TILE / 2, &mp.q, 64, kh, t0, b, &sm.barKQ);
       }
-      __syncwarp();  // every Gl of the chunk is written (by this warp)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = lane * 4 + i;
-        sm.etab[r] = exp2f(sm.Gl[r & ~15] - sm.Gl[r]);  // >= 1
+      if (needU) {
+        load_v(jj0);
+        if (jj0 + 1 < jj1 && !needP) load_v(jj0 + 1);  // the Q buffer is not needed
       }
-    }
-    // the previous value head's stores have read their staging tiles (Kg and Tp)
-    // before the barrier below lets anyone rewrite them
-    if (tid == 0 && jj > 0) tc::bulk_wait_read();
-    if (jj == 0) {  // K K^T, Q K^T complete; K readable
-      ok = ok && tc::mbar_wait(&sm.barKQ, 0);
-      ok = ok && tc::mbar_wait(&sm.barM, mphase);
-      mphase ^= 1;
+      ok = ok && tc::mbar_wait(&sm.barKQ, (uint32_t)(kq_uses & 1));
       tc::fence_after();
+      tc::gemm_k128(tmem + 0, smem_u32(sm.K), smem_u32(sm.K), 128, false);
+      if (needP) tc::gemm_k128(tmem + 128, smem_u32(sm.Q), smem_u32(sm.K), 128, false);
+      tc::commit(&sm.barM);
     }
-    if (tid == 0 && needU) {  // prefetch V of the next value head into the free buffer
-      if (jj == 0) {
-        if (group > 1 && needP) load_v(1);  // Q K^T has read Q
-      } else if (jj + 1 < group) {
-        load_v(jj + 1);  // its buffer held V of head jj - 1, whose u is complete
-      }
-    }
-    __syncthreads();
 
-    // ---- S (hi/lo into F, fp32 diagonal blocks into Sd) and P (bf16 staging in Kg) ----
-    // The decay exp2(Gl_r - Gl_s), s <= r, in a 16-column block starting at c0 is
-    // exp2(Gl_r - Gl_c0) * etab[s]: G is non-increasing, so the first factor is
-    // at most 1 and the second at least 1.  A block whose Gl drops by more than
-    // 100 over its columns could overflow etab and takes the direct exponentials;
-    // elsewhere a row whose first factor underflows has true decays below 2^-26.
-    {
-      const float Glr = sm.Gl[row], br = sm.beta[row];
-      float* Sd = reinterpret_cast<float*>(sm.Tp + SD);
-#pragma unroll 1
-      for (int cb = 0; cb < 32; cb += 16) {
-        const int c0 = 32 * cq + cb;
-        float sv[16], pv[16];
-        if (c0 <= 32 * quarter + 31) {  // warp-uniform: the block reaches the diagonal
-          float kk[16], mv[16];
-          tc::ld16(tlane + c0, kk);
-          if (needP) tc::ld16(tlane + 128 + c0, pv);
-          if (sm.Gl[c0] - sm.Gl[c0 + 15] <= 100.f) {  // block-uniform
-            const float fr = exp2f(Glr - sm.Gl[c0]);
+    for (int jj = jj0; jj < jj1; ++jj) {
+      const int j = kh * group + jj;
+      const long bh = (long)b * a.Hv + j;
+      const long chunk_id = bh * a.NC + c;
+      const int vb = (jj - jj0) & 1;  // V buffer of this head
+      // ---- gates of value head j --------------------------------------------------
+      if (tid < CH) {
+        sm.Gl[tid] = g_next;
+        sm.beta[tid] = b_next;
+      }
+      load_gates(ug + (jj - jj0) + 1, g_next, b_next);
+      __syncthreads();
+      if (warp == 0) {
+        float v[4];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) mv[i] = fr * sm.etab[c0 + i];
+        for (int i = 0; i < 4; ++i) v[i] = sm.Gl[lane * 4 + i];
+        warp_cumsum128(v, lane);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          sm.Gl[lane * 4 + i] = v[i] * LOG2E;
+        }
+        __syncwarp();  // every Gl of the chunk is written (by this warp)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane * 4 + i;
+          sm.etab[r] = exp2f(sm.Gl[r & ~15] - sm.Gl[r]);  // >= 1
+        }
+      }
+      // the previous head's stores have read their staging tiles (Kg, Tp, F)
+      // before the barrier below lets anyone rewrite them
+      if (tid == 0 && (ug > u_begin || jj > jj0)) tc::bulk_wait_read();
+      if (jj == jj0) {  // K K^T, Q K^T complete; K readable
+        ok = ok && tc::mbar_wait(&sm.barKQ, (uint32_t)(kq_uses & 1));
+        ok = ok && tc::mbar_wait(&sm.barM, mphase);
+        mphase ^= 1;
+        tc::fence_after();
+      }
+      if (tid == 0 && needU) {  // prefetch V of the next value head into the free buffer
+        if (jj == jj0) {
+          if (jj0 + 1 < jj1 && needP) load_v(jj0 + 1);  // Q K^T has read Q
+        } else if (jj + 1 < jj1) {
+          load_v(jj + 1);  // its buffer held V of head jj - 1, whose u is complete
+        }
+      }
+      __syncthreads();
+
+      // ---- S (hi/lo into F, fp32 diagonal blocks into Sd) and P (bf16 staging in Kg) ----
+      // The decay exp2(Gl_r - Gl_s), s <= r, in a 16-column block starting at c0 is
+      // exp2(Gl_r - Gl_c0) * etab[s]: G is non-increasing, so the first factor is
+      // at most 1 and the second at least 1.  A block whose Gl drops by more than
+      // 100 over its columns could overflow etab and takes the direct exponentials;
+      // elsewhere a row whose first factor underflows has true decays below 2^-26.
+      {
+        const float Glr = sm.Gl[row], br = sm.beta[row];
+        float* Sd = reinterpret_cast<float*>(sm.Tp + SD);
+#pragma unroll 1
+        for (int cb = 0; cb < 32; cb += 16) {
+          const int c0 = 32 * cq + cb;
+          float sv[16], pv[16];
+          if (c0 <= 32 * quarter + 31) {  // warp-uniform: the block reaches the diagonal
+            float kk[16], mv[16];
+            tc::ld16(tlane + c0, kk);
+            if (needP) tc::ld16(tlane + 128 + c0, pv);
+            if (sm.Gl[c0] - sm.Gl[c0 + 15] <= 100.f) {  // block-uniform
+              const float fr = exp2f(Glr - sm.Gl[c0]);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) mv[i] = fr * sm.etab[c0 + i];
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) mv[i] = exp2f(Glr - sm.Gl[c0 + i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int s = c0 + i;
+              const float m = (s <= row) ? mv[i] : 0.f;  // one decay for S and P
+              sv[i] = (s < row) ? br * kk[i] * m : 0.f;
+              pv[i] = needP ? pv[i] * m : 0.f;
+            }
           } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) mv[i] = exp2f(Glr - sm.Gl[c0 + i]);
+            for (int i = 0; i < 16; ++i) sv[i] = pv[i] = 0.f;
           }
+          if (needP) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int s = c0 + i;
-            const float m = (s <= row) ? mv[i] : 0.f;  // one decay for S and P
-            sv[i] = (s < row) ? br * kk[i] * m : 0.f;
-            pv[i] = needP ? pv[i] * m : 0.f;
+            for (int q = 0; q < 2; ++q) {
+              uint4 o;
+              o.x = pack_bf16(pv[8 * q + 0], pv[8 * q + 1]);
+              o.y = pack_bf16(pv[8 * q + 2], pv[8 * q + 3]);
+              o.z = pack_bf16(pv[8 * q + 4], pv[8 * q + 5]);
+              o.w = pack_bf16(pv[8 * q + 6], pv[8 * q + 7]);
+              *reinterpret_cast<uint4*>(sm.Kg + tc::sw128_chunk(row, (c0 >> 3) + q, CH)) = o;
+            }
           }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) sv[i] = pv[i] = 0.f;
-        }
-        if (needP) {
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
-            uint4 o;
-            o.x = pack_bf16(pv[8 * q + 0], pv[8 * q + 1]);
-            o.y = pack_bf16(pv[8 * q + 2], pv[8 * q + 3]);
-            o.z = pack_bf16(pv[8 * q + 4], pv[8 * q + 5]);
-            o.w = pack_bf16(pv[8 * q + 6], pv[8 * q + 7]);
-            *reinterpret_cast<uint4*>(sm.Kg + tc::sw128_chunk(row, (c0 >> 3) + q, CH)) = o;
+            uint4 hi, lo;
+            split8(sv + 8 * q, hi, lo);
+            *reinterpret_cast<uint4*>(swz(sm.Fh, row, (c0 >> 3) + q)) = hi;
+            *reinterpret_cast<uint4*>(swz(sm.Fl, row, (c0 >> 3) + q)) = lo;
+          }
+          if (((row >> 4) << 4) == c0) {  // this row's diagonal block, kept in fp32
+            float* sd = Sd + (row >> 4) * 256 + (row & 15) * 16;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<float4*>(sd + 4 * q) = make_float4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
           }
         }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint4 hi, lo;
-          split8(sv + 8 * q, hi, lo);
-          *reinterpret_cast<uint4*>(swz(sm.Fh, row, (c0 >> 3) + q)) = hi;
-          *reinterpret_cast<uint4*>(swz(sm.Fl, row, (c0 >> 3) + q)) = lo;
-        }
-        if (((row >> 4) << 4) == c0) {  // this row's diagonal block, kept in fp32
-          float* sd = Sd + (row >> 4) * 256 + (row & 15) * 16;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<float4*>(sd + 4 * q) = make_float4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
-        }
       }
-    }
-    tc::fence_proxy_async();  // P is read by a TMA store
-    __syncthreads();
-    if (tid == 0 && needP) {  // P leaves while the inverse runs
-      const int y = (int)(chunk_id * CH);
-      tc::tma_store_2d(&mp.P, 0, y, sm.Kg);
-      tc::tma_store_2d(&mp.P, 64, y, sm.Kg + TILE / 2);
-      tc::bulk_commit();
-    }
-    auto export_f32 = [&](float* dst) {
-      for (int i = tid; i < CH * 16; i += PT) {
-        const int r = i >> 4, jc = i & 15;
-        float v[8];
-        join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
-        *reinterpret_cast<float4*>(dst + r * CH + 8 * jc) = make_float4(v[0], v[1], v[2], v[3]);
-        *reinterpret_cast<float4*>(dst + r * CH + 8 * jc + 4) = make_float4(v[4], v[5], v[6], v[7]);
-      }
-    };
-    if (a.S_dbg) {
-      export_f32(a.S_dbg + chunk_id * tile);
+      tc::fence_proxy_async();  // P is read by a TMA store
       __syncthreads();
-    }
+      if (tid == 0 && needP) {  // P leaves while the inverse runs
+        const int y = (int)(chunk_id * CH);
+        tc::tma_store_2d(&mp.P, 0, y, sm.Kg);
+        tc::tma_store_2d(&mp.P, 64, y, sm.Kg + TILE / 2);
+        tc::bulk_commit();
+      }
+      auto export_f32 = [&](float* dst) {
+        for (int i = tid; i < CH * 16; i += PT) {
+          const int r = i >> 4, jc = i & 15;
+          float v[8];
+          join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
+          *reinterpret_cast<float4*>(dst + r * CH + 8 * jc) = make_float4(v[0], v[1], v[2], v[3]);
+          *reinterpret_cast<float4*>(dst + r * CH + 8 * jc + 4) = make_float4(v[4], v[5], v[6], v[7]);
+        }
+      };
+      if (a.S_dbg) {
+        export_f32(a.S_dbg + chunk_id * tile);
+        __syncthreads();
+      }
 
-    // ---- T = (I + S)^-1 -------------------------------------------------------------
-    ut_inverse(sm, warp, lane);
-    if (a.T_dbg) export_f32(a.T_dbg + chunk_id * tile);
-    if (a.Tb) {
-      bf16* dst = a.Tb + chunk_id * tile;
-      for (int i = tid; i < CH * 16; i += PT) {
-        const int r = i >> 4, jc = i & 15;
+      // ---- T = (I + S)^-1 -------------------------------------------------------------
+      ut_inverse(sm, warp, lane);
+      if (a.T_dbg) export_f32(a.T_dbg + chunk_id * tile);
+      if (a.Tb) {
+        bf16* dst = a.Tb + chunk_id * tile;
+        for (int i = tid; i < CH * 16; i += PT) {
+          const int r = i >> 4, jc = i & 15;
+          float v[8];
+          join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
+          uint4 o;
+          o.x = pack_bf16(v[0], v[1]);
+          o.y = pack_bf16(v[2], v[3]);
+          o.z = pack_bf16(v[4], v[5]);
+          o.w = pack_bf16(v[6], v[7]);
+          *reinterpret_cast<uint4*>(dst + r * CH + 8 * jc) = o;
+        }
+      }
+      // P's store has read Kg before diag(gamma) K is written there
+      if (tid == 0) tc::bulk_wait_read();
+      __syncthreads();
+      // ---- diag(gamma) K (B operand of w) ------------------------------------------------
+#pragma unroll
+      for (int i = 0; i < (CH * 16) / PT; ++i) {
+        const int idx = tid + i * PT;
+        const int r = idx >> 4, jc = idx & 15;
+        const uint32_t off = tc::sw128_chunk(r, jc, CH);
+        const uint4 x = *reinterpret_cast<const uint4*>(sm.K + off);
+        const float gm = exp2f(sm.Gl[r]);  // gamma_r
+        const float2 x0 = unpack_bf16(x.x), x1 = unpack_bf16(x.y), x2 = unpack_bf16(x.z), x3 = unpack_bf16(x.w);
+        uint4 o;
+        o.x = pack_bf16(gm * x0.x, gm * x0.y);
+        o.y = pack_bf16(gm * x1.x, gm * x1.y);
+        o.z = pack_bf16(gm * x2.x, gm * x2.y);
+        o.w = pack_bf16(gm * x3.x, gm * x3.y);
+        *reinterpret_cast<uint4*>(sm.Kg + off) = o;
+      }
+
+      // ---- T' = T diag(beta) (bf16, K-major SW128) --------------------------------------
+#pragma unroll
+      for (int i = 0; i < (CH * 16) / PT; ++i) {
+        const int idx = tid + i * PT;
+        const int r = idx >> 4, jc = idx & 15;
         float v[8];
         join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
+        const float4 b0 = *reinterpret_cast<const float4*>(&sm.beta[8 * jc]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&sm.beta[8 * jc + 4]);
         uint4 o;
-        o.x = pack_bf16(v[0], v[1]);
-        o.y = pack_bf16(v[2], v[3]);
-        o.z = pack_bf16(v[4], v[5]);
-        o.w = pack_bf16(v[6], v[7]);
-        *reinterpret_cast<uint4*>(dst + r * CH + 8 * jc) = o;
+        o.x = pack_bf16(v[0] * b0.x, v[1] * b0.y);
+        o.y = pack_bf16(v[2] * b0.z, v[3] * b0.w);
+        o.z = pack_bf16(v[4] * b1.x, v[5] * b1.y);
+        o.w = pack_bf16(v[6] * b1.z, v[7] * b1.w);
+        *reinterpret_cast<uint4*>(sm.Tp + tc::sw128_chunk(r, jc, CH)) = o;
       }
-    }
-    // P's store has read Kg before diag(gamma) K is written there
-    if (tid == 0) tc::bulk_wait_read();
-    __syncthreads();
-    // ---- diag(gamma) K (B operand of w) ------------------------------------------------
-#pragma unroll
-    for (int i = 0; i < (CH * 16) / PT; ++i) {
-      const int idx = tid + i * PT;
-      const int r = idx >> 4, jc = idx & 15;
-      const uint32_t off = tc::sw128_chunk(r, jc, CH);
-      const uint4 x = *reinterpret_cast<const uint4*>(sm.K + off);
-      const float gm = exp2f(sm.Gl[r]);  // gamma_r
-      const float2 x0 = unpack_bf16(x.x), x1 = unpack_bf16(x.y), x2 = unpack_bf16(x.z), x3 = unpack_bf16(x.w);
-      uint4 o;
-      o.x = pack_bf16(gm * x0.x, gm * x0.y);
-      o.y = pack_bf16(gm * x1.x, gm * x1.y);
-      o.z = pack_bf16(gm * x2.x, gm * x2.y);
-      o.w = pack_bf16(gm * x3.x, gm * x3.y);
-      *reinterpret_cast<uint4*>(sm.Kg + off) = o;
-    }
-
-    // ---- T' = T diag(beta) (bf16, K-major SW128) --------------------------------------
-#pragma unroll
-    for (int i = 0; i < (CH * 16) / PT; ++i) {
-      const int idx = tid + i * PT;
-      const int r = idx >> 4, jc = idx & 15;
-      float v[8];
-      join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
-      const float4 b0 = *reinterpret_cast<const float4*>(&sm.beta[8 * jc]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&sm.beta[8 * jc + 4]);
-      uint4 o;
-      o.x = pack_bf16(v[0] * b0.x, v[1] * b0.y);
-      o.y = pack_bf16(v[2] * b0.z, v[3] * b0.w);
-      o.z = pack_bf16(v[4] * b1.x, v[5] * b1.y);
-      o.w = pack_bf16(v[6] * b1.z, v[7] * b1.w);
-      *reinterpret_cast<uint4*>(sm.Tp + tc::sw128_chunk(r, jc, CH)) = o;
-    }
-    tc::fence_proxy_async();
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    // ---- u = T' V,  w = T' diag(gamma) K ------------------------------------------------
-    if (tid == 0) {
-      if (needU) {
-        ok = ok && tc::mbar_wait(&sm.barV[jj & 1], (uint32_t)((jj >> 1) & 1));
-        tc::fence_after();
-        tc::gemm_bmn_k128(tmem + 384, smem_u32(sm.Tp), smem_u32((jj & 1) ? sm.Q : sm.V), false);
-      }
-      if (needW) tc::gemm_bmn_k128(tmem + 256, smem_u32(sm.Tp), smem_u32(sm.Kg), false);
-      if (needU || needW) tc::commit(&sm.barM);
-    }
-    if (needU || needW) {
-      ok = ok && tc::mbar_wait(&sm.barM, mphase);
-      mphase ^= 1;
+      tc::fence_proxy_async();
+      tc::fence_before();
+      __syncthreads();
       tc::fence_after();
-    }
-    // ---- w and u leave through shared staging tiles and TMA stores ------------------
-    // (diag(gamma) K and T' are dead now; their buffers hold w and u)
-    if (needW) tmem_row_to_tile(tlane + 256 + 32 * cq, sm.Kg, row, cq);
-    if (needU) tmem_row_to_tile(tlane + 384 + 32 * cq, sm.Tp, row, cq);
-    tc::fence_proxy_async();
-    tc::fence_before();
-    __syncthreads();  // staging tiles complete; TMEM w/u and the gate vectors are free
-    tc::fence_after();
-    if (tid == 0 && (needW || needU)) {
-      const int y = (int)(chunk_id * CH);
-      if (needW) {
-        tc::tma_store_2d(&mp.W, 0, y, sm.Kg);
-        tc::tma_store_2d(&mp.W, 64, y, sm.Kg + TILE / 2);
+      // ---- u = T' V,  w = T' diag(gamma) K ------------------------------------------------
+      if (tid == 0) {
+        if (needU) {
+          ok = ok && tc::mbar_wait(&sm.barV[vb], (vb ? v_use1 : v_use0) & 1u);
+          tc::fence_after();
+          tc::gemm_bmn_k128(tmem + 384, smem_u32(sm.Tp), smem_u32(vb ? sm.Q : sm.V), false);
+        }
+        if (needW) tc::gemm_bmn_k128(tmem + 256, smem_u32(sm.Tp), smem_u32(sm.Kg), false);
+        if (needU || needW) tc::commit(&sm.barM);
       }
-      if (needU) {
-        tc::tma_store_2d(&mp.U, 0, y, sm.Tp);
-        tc::tma_store_2d(&mp.U, 64, y, sm.Tp + TILE / 2);
+      if (needU) (vb ? v_use1 : v_use0) += 1;
+      if (needU || needW) {
+        ok = ok && tc::mbar_wait(&sm.barM, mphase);
+        mphase ^= 1;
+        tc::fence_after();
       }
-      tc::bulk_commit();
+      // ---- w and u leave through shared staging tiles and TMA stores ------------------
+      // (diag(gamma) K and T' are dead now; their buffers hold w and u)
+      if (needW) tmem_row_to_tile(tlane + 256 + 32 * cq, sm.Kg, row, cq);
+      if (needU) tmem_row_to_tile(tlane + 384 + 32 * cq, sm.Tp, row, cq);
+      tc::fence_proxy_async();
+      tc::fence_before();
+      __syncthreads();  // staging tiles complete; TMEM w/u and the gate vectors are free
+      tc::fence_after();
+      if (tid == 0 && (needW || needU)) {
+        const int y = (int)(chunk_id * CH);
+        if (needW) {
+          tc::tma_store_2d(&mp.W, 0, y, sm.Kg);
+          tc::tma_store_2d(&mp.W, 64, y, sm.Kg + TILE / 2);
+        }
+        if (needU) {
+          tc::tma_store_2d(&mp.U, 0, y, sm.Tp);
+          tc::tma_store_2d(&mp.U, 64, y, sm.Tp + TILE / 2);
+        }
+        tc::bulk_commit();
+      }
     }
+    ++kq_uses;
+    ug += jj1 - jj0;
   }
   if (tid == 0) tc::bulk_wait();  // the stores have completed before the block exits
   if (!ok && a.status) atomicOr(a.status, 1);
@@ -530,8 +566,15 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
   const size_t smem = prep_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.NC, a.Hk, a.B);
-  k_prep<<<grid, PT, smem, s>>>(a, mp);
+  // persistent CTAs, one per SM (the shared memory admits one), each taking a
+  // contiguous range of (chunk, key head, value head) units
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long units = (long)a.B * a.NC * a.Hv;
+  const int ctas = (int)(units < sms ? units : sms);
+  if (ctas <= 0) return cudaSuccess;
+  k_prep<<<ctas, PT, smem, s>>>(a, mp);
   return cudaGetLastError();
 }
 
