@@ -13,7 +13,8 @@
 //       the exponent masked before exp so nothing overflows
 //   P = (Q K^T) * M, diagonal included (same exponentials as S)      (for the output)
 //   T = (I + S)^-1 by the blockwise doubling ladder
-//   u = T' V and w = T' (diag(gamma) K) with T' = T diag(beta)        tcgen05 products
+//   u = T' V and w = T'' K with T' = T diag(beta), T'' = T diag(beta gamma)
+//                                                                    tcgen05 products
 // The ladder ("Fuse the Gated Delta Net inter-chunk scan into a Pallas TPU
 // kernel", section "Changes", triangular inversion kernel): with X the inverse
 // of I + S on its diagonal blocks of size b, the inverse on blocks of size 2b
@@ -26,12 +27,12 @@
 // bf16(x), lo = bf16(x - hi): about 16 significant bits), so every ladder
 // operand is a plain ldmatrix load; a product is hi*hi + hi*lo + lo*hi with
 // fp32 accumulation.  The zero blocks of the triangular factors are skipped.
-// T' and diag(gamma) K are rounded to bf16 as tensor-core operands; w and u
-// are bf16 outputs themselves.
+// T' and T'' are rounded to bf16 as tensor-core operands; w and u are bf16
+// outputs themselves.
 //
 // Operands arrive by TMA in the 128-byte-swizzled layout: K and Q serve
-// K K^T and Q K^T as K-major operands, and K (scaled) and V serve w and u as
-// MN-major B operands, so nothing is transposed in shared memory.  V of the
+// K K^T and Q K^T as K-major operands, and K and V serve w and u as MN-major
+// B operands as loaded, so nothing is transposed or rescaled in shared memory.  V of the
 // next value head is requested while the current one is processed (the Q
 // buffer takes the odd heads once Q K^T has completed).
 #include "gdn_kernels.cuh"
@@ -50,7 +51,7 @@ struct PrepSmem {
   unsigned char Q[TILE];   // SW128 [s][d]: Q; after Q K^T, V of the odd value heads
   unsigned char K[TILE];   // SW128 [s][d]
   unsigned char V[TILE];   // SW128 [s][v]: V of the even value heads
-  unsigned char Kg[TILE];  // SW128 [s][d]: diag(gamma) K of the current value head
+  unsigned char Kg[TILE];  // SW128: P staging; T'' = T diag(beta gamma) [r][s]; w staging
   unsigned char Tp[TILE];  // SW128 [r][s]: T diag(beta); during the inverse its scratch
   bf16 Fh[CH * CH];        // S, overwritten in place by T: high parts (XOR-swizzled rows)
   bf16 Fl[CH * CH];        // low parts
@@ -462,27 +463,14 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
           *reinterpret_cast<uint4*>(dst + r * CH + 8 * jc) = o;
         }
       }
-      // P's store has read Kg before diag(gamma) K is written there
+      // P's store has read Kg before T diag(beta gamma) is written there; the
+      // decay table is dead, so it takes gamma (etab[s] = exp(G_s))
+      if (tid < CH) sm.etab[tid] = exp2f(sm.Gl[tid]);
       if (tid == 0) tc::bulk_wait_read();
       __syncthreads();
-      // ---- diag(gamma) K (B operand of w) ------------------------------------------------
-#pragma unroll
-      for (int i = 0; i < (CH * 16) / PT; ++i) {
-        const int idx = tid + i * PT;
-        const int r = idx >> 4, jc = idx & 15;
-        const uint32_t off = tc::sw128_chunk(r, jc, CH);
-        const uint4 x = *reinterpret_cast<const uint4*>(sm.K + off);
-        const float gm = exp2f(sm.Gl[r]);  // gamma_r
-        const float2 x0 = unpack_bf16(x.x), x1 = unpack_bf16(x.y), x2 = unpack_bf16(x.z), x3 = unpack_bf16(x.w);
-        uint4 o;
-        o.x = pack_bf16(gm * x0.x, gm * x0.y);
-        o.y = pack_bf16(gm * x1.x, gm * x1.y);
-        o.z = pack_bf16(gm * x2.x, gm * x2.y);
-        o.w = pack_bf16(gm * x3.x, gm * x3.y);
-        *reinterpret_cast<uint4*>(sm.Kg + off) = o;
-      }
-
-      // ---- T' = T diag(beta) (bf16, K-major SW128) --------------------------------------
+      // ---- T' = T diag(beta) and T'' = T diag(beta gamma) (bf16, K-major SW128) ----------
+      // u = T' V and w = T'' K: the gate of w folds into its A operand, so K
+      // serves as w's B operand as loaded
 #pragma unroll
       for (int i = 0; i < (CH * 16) / PT; ++i) {
         const int idx = tid + i * PT;
@@ -491,25 +479,35 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
         join8(*reinterpret_cast<const uint4*>(swz(sm.Fh, r, jc)), *reinterpret_cast<const uint4*>(swz(sm.Fl, r, jc)), v);
         const float4 b0 = *reinterpret_cast<const float4*>(&sm.beta[8 * jc]);
         const float4 b1 = *reinterpret_cast<const float4*>(&sm.beta[8 * jc + 4]);
+        const float4 g0 = *reinterpret_cast<const float4*>(&sm.etab[8 * jc]);
+        const float4 g1 = *reinterpret_cast<const float4*>(&sm.etab[8 * jc + 4]);
+        const float tb[8] = {v[0] * b0.x, v[1] * b0.y, v[2] * b0.z, v[3] * b0.w,
+                             v[4] * b1.x, v[5] * b1.y, v[6] * b1.z, v[7] * b1.w};
+        const uint32_t off = tc::sw128_chunk(r, jc, CH);
         uint4 o;
-        o.x = pack_bf16(v[0] * b0.x, v[1] * b0.y);
-        o.y = pack_bf16(v[2] * b0.z, v[3] * b0.w);
-        o.z = pack_bf16(v[4] * b1.x, v[5] * b1.y);
-        o.w = pack_bf16(v[6] * b1.z, v[7] * b1.w);
-        *reinterpret_cast<uint4*>(sm.Tp + tc::sw128_chunk(r, jc, CH)) = o;
+        o.x = pack_bf16(tb[0], tb[1]);
+        o.y = pack_bf16(tb[2], tb[3]);
+        o.z = pack_bf16(tb[4], tb[5]);
+        o.w = pack_bf16(tb[6], tb[7]);
+        *reinterpret_cast<uint4*>(sm.Tp + off) = o;
+        o.x = pack_bf16(tb[0] * g0.x, tb[1] * g0.y);
+        o.y = pack_bf16(tb[2] * g0.z, tb[3] * g0.w);
+        o.z = pack_bf16(tb[4] * g1.x, tb[5] * g1.y);
+        o.w = pack_bf16(tb[6] * g1.z, tb[7] * g1.w);
+        *reinterpret_cast<uint4*>(sm.Kg + off) = o;
       }
       tc::fence_proxy_async();
       tc::fence_before();
       __syncthreads();
       tc::fence_after();
-      // ---- u = T' V,  w = T' diag(gamma) K ------------------------------------------------
+      // ---- u = T' V,  w = T'' K -----------------------------------------------------------
       if (tid == 0) {
         if (needU) {
           ok = ok && tc::mbar_wait(&sm.barV[vb], (vb ? v_use1 : v_use0) & 1u);
           tc::fence_after();
           tc::gemm_bmn_k128(tmem + 384, smem_u32(sm.Tp), smem_u32(vb ? sm.Q : sm.V), false);
         }
-        if (needW) tc::gemm_bmn_k128(tmem + 256, smem_u32(sm.Tp), smem_u32(sm.Kg), false);
+        if (needW) tc::gemm_bmn_k128(tmem + 256, smem_u32(sm.Kg), smem_u32(sm.K), false);
         if (needU || needW) tc::commit(&sm.barM);
       }
       if (needU) (vb ? v_use1 : v_use0) += 1;
@@ -519,7 +517,7 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
         tc::fence_after();
       }
       // ---- w and u leave through shared staging tiles and TMA stores ------------------
-      // (diag(gamma) K and T' are dead now; their buffers hold w and u)
+      // (T'' and T' are dead now; their buffers hold w and u)
       if (needW) tmem_row_to_tile(tlane + 256 + 32 * cq, sm.Kg, row, cq);
       if (needU) tmem_row_to_tile(tlane + 384 + 32 * cq, sm.Tp, row, cq);
       tc::fence_proxy_async();

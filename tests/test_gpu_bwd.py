@@ -68,6 +68,13 @@ def test_bwd_ragged_and_tiny(gdn_lib, T):
     _check_bwd(gdn_lib, _small(T, Hk=2, Hv=4, seed=100 + T))
 
 
+@pytest.mark.parametrize("B,T,Hk,Hv", [(3, 333, 3, 6), (1, 40 * 128, 1, 4)])
+def test_bwd_unit_ranges(gdn_lib, B, T, Hk, Hv):
+    """Preparation ranges that start inside a key head's group or cut it (see
+    the forward test of the same name), through the backward path."""
+    _check_bwd(gdn_lib, _small(T, Hk=Hk, Hv=Hv, seed=T + Hv, B=B))
+
+
 @pytest.mark.parametrize("S", [2, 3, 7])
 def test_bwd_segment_counts(gdn_lib, S):
     _check_bwd(gdn_lib, _small(1024 + 50, shift=-5.0, h0=0.5, seed=5), n_segments=S)

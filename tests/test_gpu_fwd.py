@@ -67,6 +67,16 @@ def test_head_groupings(gdn_lib, Hk, Hv):
     _check_fwd(gdn_lib, inp)
 
 
+@pytest.mark.parametrize("B,T,Hk,Hv", [(3, 333, 3, 6), (1, 40 * 128, 1, 4)])
+def test_unit_ranges(gdn_lib, B, T, Hk, Hv):
+    """The preparation runs one CTA per SM over contiguous ranges of (batch row,
+    chunk, key head, value head) units: fewer units than SMs (every CTA one
+    unit, odd units starting inside a key head's group), and 160 units with
+    four value heads per key head (ranges that cut groups)."""
+    inp = make_host(WORKLOADS["tiny_t1024"].replace(B=B, T=T, Hk=Hk, Hv=Hv, h0_std=0.2, seed=T + Hv))
+    _check_fwd(gdn_lib, inp)
+
+
 @pytest.mark.parametrize("S", [1, 2, 3, 7, 16])
 def test_segment_counts_slow_decay(gdn_lib, S):
     """Slow decay (g ~ -0.05 per token) so the incoming state of every
