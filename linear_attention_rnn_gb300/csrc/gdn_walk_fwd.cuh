@@ -7,26 +7,29 @@
 // with k_g = diag(exp(G_last - G)) K, and the masked intra-chunk output
 //     O = diag(gamma) Q h + P Delta,      P = (Q K^T) * decay (diagonal included).
 //
-// One CTA walks a 32-column slice of one head's state (columns of h evolve
-// independently: every matrix of the step acts on h from the left).  Compute
-// thread r (of 128) owns row r: row r of the state slice in fp32 registers for
-// the whole segment, and TMEM lane r of every product.  Per chunk the products
+// One CTA walks a slice of SW = 32 or 64 columns of one head's state (columns
+// of h evolve independently: every matrix of the step acts on h from the
+// left).  Compute thread (r, g) owns row r, columns 32 g .. 32 g + 31 of the
+// slice in fp32 registers for the whole segment, and those columns of TMEM
+// lane r in every product.  Per chunk the products
 //     X  = w h            (A = w, K-major)
 //     H' = K^T (ef Delta) (A = the K tile read MN-major: no transpose pass)
 //     O1 = Q h,  O2 = P Delta
-// are tcgen05 MMAs (M = 128, N = 32, K = 128) into tensor memory.  Their B
-// operands (h^T, Delta^T, (ef Delta)^T, 32 x 128 bf16) are written column by
+// are tcgen05 MMAs (M = 128, N = SW, K = 128) into tensor memory.  Their B
+// operands (h^T, Delta^T, (ef Delta)^T, SW x 128 bf16) are written column by
 // column by the compute threads in the 128-byte-swizzled K-major layout.
 //
-// A fifth warp issues the MMAs as soon as their operands are signalled ready
-// on mbarriers by the compute threads; a sixth issues the TMA loads of the
-// chunk tiles into a ring of six 32 KiB slots (w, Q, K, P in the order the
-// MMAs consume them), refilling each slot as soon as the MMA that read it has
-// completed.  A TMA request can block its thread while earlier copies stream
-// in, so the loads never share a thread with the MMA chain.  Each compute thread reads its row of the u
-// slice straight into registers a chunk ahead.  The compute threads never
-// wait on memory issue, only on MMA completion.  Every wait is bounded; one that
-// gives up sets bit 0 of the status word.
+// Warp roles after the compute warps: a chain issuer (X, H' as soon as their
+// operands are signalled ready on mbarriers), a TMA producer (the chunk tiles
+// w, Q, K, P in the order consumed, into a ring of 32 KiB slots, each refilled
+// as soon as the MMA that read it has completed), and a third warp that, in
+// the output mode, issues O1 and O2 (so that their issue never holds the
+// chain's issuer) and, in the recompute mode, stores the staged exports.  A
+// TMA request can block its thread while earlier copies stream in, so the
+// loads never share a thread with an MMA issuer.  Each compute thread reads
+// its row of the u slice straight into registers a chunk ahead.  The compute
+// threads never wait on memory issue, only on MMA completion.  Every wait is
+// bounded; one that gives up sets bit 0 of the status word.
 //
 // Modes:
 //   RECUR (fold = 0): walk from the segment's entering state, write O (if o
