@@ -129,9 +129,6 @@ struct GradArgs {
 };
 
 size_t prep_smem_bytes();
-size_t walk_fwd_smem_bytes(int fold);
-size_t walk_bwd_smem_bytes(int fold);
-size_t affine_walk_smem_bytes();
 size_t grad_smem_bytes();
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);

@@ -145,8 +145,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_affine_walk(AffineWalkArgs a) {
 
 }  // namespace
 
-size_t affine_walk_smem_bytes() { return 2 * HD * LDX * sizeof(bf16); }
-
 cudaError_t launch_affine_walk(const AffineWalkArgs& a, cudaStream_t s) {
   const int ncols = (a.with_A ? HD : 0) + a.dv;
   dim3 grid(ncols / XC, a.batch);

@@ -28,8 +28,6 @@ cudaError_t launch_one(const WalkBwdArgs& a, const WalkBwdMaps& m, cudaStream_t 
 
 }  // namespace
 
-size_t walk_bwd_smem_bytes(int) { return sizeof(walkb::WalkBwdSmem<32>) + 1024; }
-
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, const WalkBwdMaps& m, int fold, cudaStream_t s) {
   // the fold, on 32-column slices; the walk runs in the pair launch
   if (!fold) return cudaErrorInvalidValue;

@@ -28,8 +28,6 @@ cudaError_t launch_one(const WalkFwdArgs& a, const WalkFwdMaps& m, cudaStream_t 
 
 }  // namespace
 
-size_t walk_fwd_smem_bytes(int) { return sizeof(walkf::WalkSmem<32>) + 1024; }
-
 cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold, cudaStream_t s) {
   if (fold) return launch_one<true, false, 32>(a, m, s);
   if (a.states || a.delta || !a.o) return cudaErrorInvalidValue;  // the recompute runs in the pair launch
