@@ -158,6 +158,22 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- our arm
+def combine_ranks(total_ms, tokens_per_rank, world, rank, device=None):
+    """Whole-job timing of `world` independent replicas: the slowest rank's
+    timed span (a max over the process group when world > 1) and the tokens all
+    ranks processed in it.  Returns (span_ms, tokens_per_s) on rank 0 and None
+    on the other ranks, which print nothing."""
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if rank != 0:
+        return None
+    return total_ms, world * tokens_per_rank / (total_ms / 1e3)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import linear_attention_rnn_gb300 as gdn
@@ -244,17 +260,13 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         e2e = run_e2e(args, gdn, wl, host, dev, nseg)
 
-    local = dict(total_ms=total_ms, tokens=wl.tokens * K)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    if rank != 0:
+    job = combine_ranks(total_ms, wl.tokens * K, world, rank, device=dev)
+    if job is None:
         return None
+    total_ms, value = job
     alg = algorithmic(wl)
     pk = peaks()
     mean_step = total_ms / K
-    value = world * wl.tokens * K / (total_ms / 1e3)
     fwd_mean = statistics.mean(fwd_ms)
     bwd_mean = statistics.mean(bwd_ms)
 
