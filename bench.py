@@ -158,6 +158,33 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- our arm
+def kernel_table(kern, alg, pk, mean_step):
+    """Per-kernel lines (mean ms per launch from CUDA events, share of the step,
+    algorithmic TFLOP/s) and the roofline of the dominant kernel: its
+    algorithmic FLOPs per launch over its mean launch time, against the
+    measured bf16 peak, with the DRAM traffic of its ncu capture when the
+    kernel is unchanged since.  Backward launches of a kernel carry "_b"."""
+    kernels = {}
+    for name, ms in kern.items():
+        base = name[:-2] if name.endswith("_b") else name
+        fl = kernel_flops(base, alg)
+        kernels[name] = {"symbol": KERNEL_SYMBOL.get(base, base), "ms": round(ms, 5),
+                         "share": round(ms / mean_step, 4)}
+        if fl:
+            kernels[name]["tflops"] = round(fl / (ms * 1e-3) / 1e12, 2)
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    dbase = dom[:-2] if dom.endswith("_b") else dom
+    dfl = kernel_flops(dbase, alg) or 0
+    dms = kernels[dom]["ms"]
+    achieved = dfl / (dms * 1e-3) / 1e12 if dfl else 0.0
+    peak = pk["bf16"]
+    roofline = {"kernel": KERNEL_SYMBOL.get(dbase, dbase), "bound": "tensor",
+                "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": NCU_TRAFFIC.get(dom),
+                "peak_source": f"bf16 burst, {pk['source']}"}
+    return kernels, roofline
+
+
 def combine_ranks(total_ms, tokens_per_rank, world, rank, device=None):
     """Whole-job timing of `world` independent replicas: the slowest rank's
     timed span (a max over the process group when world > 1) and the tokens all
@@ -278,21 +305,7 @@ def run_ours(args, rank, world, local_rank):
                 "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": round(t_roof / ms, 4),
                 "algorithmic_bytes": bytes_, "algorithmic_flops": flops}
 
-    kernels = {}
-    for name, ms in kern.items():
-        base = name[:-2] if name.endswith("_b") else name
-        fl = kernel_flops(base, alg)
-        kernels[name] = {"symbol": KERNEL_SYMBOL.get(base, base), "ms": round(ms, 5),
-                         "share": round(ms / mean_step, 4)}
-        if fl:
-            kernels[name]["tflops"] = round(fl / (ms * 1e-3) / 1e12, 2)
-    dom = max(kernels, key=lambda n: kernels[n]["ms"])
-    dbase = dom[:-2] if dom.endswith("_b") else dom
-    dfl = kernel_flops(dbase, alg) or 0
-    dms = kernels[dom]["ms"]
-    achieved = dfl / (dms * 1e-3) / 1e12 if dfl else 0.0
-    peak = pk["bf16"]
-    traffic = NCU_TRAFFIC.get(dom)
+    kernels, roofline = kernel_table(kern, alg, pk, mean_step)
     clocks = sampler.summary(t0, t1)
     out = {
         "metric": "GDN chunk fwd+bwd tokens/s (T=4096, H_v=32, d=128) and % of roofline",
@@ -311,10 +324,7 @@ def run_ours(args, rank, world, local_rank):
                                f"dk=dv={wl.dk} chunk={wl.chunk} segments={nseg}",
                    "l2": "flushed (512 MiB write) before every timed step",
                    "parallelism": f"replicas x{world} (independent problems)"},
-        "roofline": {"kernel": KERNEL_SYMBOL.get(dbase, dbase), "bound": "tensor",
-                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"bf16 burst, {pk['source']}"},
+        "roofline": roofline,
         "path_roofline": {"fwd": path(alg["fwd_bytes"], alg["fwd_flops"], fwd_mean),
                           "bwd": path(alg["bwd_bytes"], alg["bwd_flops"], bwd_mean),
                           "step": path(alg["fwd_bytes"] + alg["bwd_bytes"],
