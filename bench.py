@@ -525,6 +525,114 @@ def run_reference(args, rank, world):
     }
 
 
+# ---------------------------------------------------------------- all workloads
+def run_sweep(args):
+    """Times every workload (the five configurations plus the slow-decay
+    reading of the million-token one) on one GPU: per workload, the median
+    over timed steps of the forward (and backward where the workload has one),
+    the per-kernel split from CUDA events after each launch (for segmented
+    runs: prep, fold, prefix, replay walk), the whole-path roofline fraction,
+    and the oracle's rate on a bounded sample.  Inputs are generated on the
+    device and resident in HBM; L2 is flushed before every timed step.
+    Prints one JSON line per workload."""
+    import torch
+    import linear_attention_rnn_gb300 as gdn
+    import oracle
+    from linear_attention_rnn_gb300.inputs import WORKLOADS, make_device, make_host
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    gdn.build()
+    pk = peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    names = args.sweep.split(",") if args.sweep != "all" else list(WORKLOADS)
+    for name in names:
+        wl = WORKLOADS[name]
+        bwd = wl.backward
+        nseg = wl.n_segments or gdn.default_segments(wl.B, wl.T, wl.Hv)
+        big = wl.tokens > (1 << 16)
+        steps = 5 if big else 20
+        d = make_device(wl, dev)
+        ws_f = torch.empty(gdn.fwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
+                           dtype=torch.uint8, device=dev)
+        ws_b = (torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
+                            dtype=torch.uint8, device=dev) if bwd else None)
+        fk = FWD_KERNELS if nseg == 1 else FWD_KERNELS_SEG
+        bk = BWD_KERNELS if nseg == 1 else BWD_KERNELS_SEG
+
+        def evs(n):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+            for x in e:
+                x.record()
+            return e
+        start = [evs(1)[0] for _ in range(steps)]
+        fev = [evs(len(fk)) for _ in range(steps)]
+        bev = [evs(len(bk)) for _ in range(steps)] if bwd else None
+
+        def step(i=None):
+            gdn.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=nseg, workspace=ws_f,
+                          events=None if i is None else fev[i])
+            if bwd:
+                gdn.chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.dO, d.dhT, n_segments=nseg,
+                              workspace=ws_b, events=None if i is None else bev[i])
+        for _ in range(2 if big else 5):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        for i in range(steps):
+            flush.zero_()
+            start[i].record()
+            step(i)
+        torch.cuda.synchronize()
+        fwd_ms = statistics.median(start[i].elapsed_time(fev[i][-1]) for i in range(steps))
+        split = {}
+        for kidx, kname in enumerate(fk):
+            split[kname] = round(statistics.median(
+                (start[i] if kidx == 0 else fev[i][kidx - 1]).elapsed_time(fev[i][kidx])
+                for i in range(steps)), 5)
+        alg = algorithmic(wl)
+
+        def path(bytes_, flops, ms):
+            t_hbm = bytes_ / (pk["hbm"] * 1e9) * 1e3
+            t_tc = flops / (pk["bf16"] * 1e12) * 1e3
+            t_roof = max(t_hbm, t_tc)
+            return {"ms": round(ms, 5), "roof_ms": round(t_roof, 5),
+                    "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": round(t_roof / ms, 4)}
+        line = {"workload": name, "B": wl.B, "T": wl.T, "Hk": wl.Hk, "Hv": wl.Hv,
+                "segments": nseg, "timed_steps": steps, "reported": "median",
+                "fwd": path(alg["fwd_bytes"], alg["fwd_flops"], fwd_ms),
+                "fwd_tokens_per_s": round(wl.tokens / (fwd_ms * 1e-3), 1),
+                "fwd_kernels_ms": split}
+        if bwd:
+            bwd_ms = statistics.median(fev[i][-1].elapsed_time(bev[i][-1]) for i in range(steps))
+            bsplit = {}
+            for kidx, kname in enumerate(bk):
+                bsplit[kname] = round(statistics.median(
+                    (fev[i][-1] if kidx == 0 else bev[i][kidx - 1]).elapsed_time(bev[i][kidx])
+                    for i in range(steps)), 5)
+            line["bwd"] = path(alg["bwd_bytes"], alg["bwd_flops"], bwd_ms)
+            line["bwd_kernels_ms"] = bsplit
+            line["step_tokens_per_s"] = round(wl.tokens / ((fwd_ms + bwd_ms) * 1e-3), 1)
+        # the oracle on a bounded sample: key head 0 (its value heads), at most
+        # 65,536 tokens of batch row 0, forward (+ backward), scaled to tokens/s
+        # of the whole workload
+        ts = min(wl.T, 1 << 16)
+        sub = make_host(wl.replace(B=1, T=ts, Hk=1, Hv=wl.Hv // wl.Hk, backward=bwd))
+        oracle.lib()
+        t = time.time()
+        oracle.fwd(sub)
+        if bwd:
+            oracle.bwd(sub)
+        dt = time.time() - t
+        line["oracle"] = {"tokens_per_s": round(ts / dt / wl.Hk, 2), "cores": oracle.num_threads(),
+                          "sample": f"key head 0 of {wl.Hk} ({wl.Hv // wl.Hk} value heads), "
+                                    f"{ts} tokens, {'fwd+bwd' if bwd else 'fwd'}, {dt:.1f} s; "
+                                    f"rate scaled by 1/{wl.Hk}"}
+        print(json.dumps(line), flush=True)
+        del d, ws_f, ws_b
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -537,6 +645,9 @@ def main():
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep warming up until this much wall time has passed")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default=None,
+                    help="time these workloads (comma-separated names, or 'all') instead of "
+                         "the headline step; one JSON line per workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -544,6 +655,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores only; other ranks exit at once
         out = run_reference(args, rank, world)

@@ -28,7 +28,10 @@
  *     address), contiguous, 16-byte aligned.  bf16 tensors are passed as
  *     void* to raw IEEE bfloat16 data.  The caller owns all memory; the
  *     library allocates nothing, keeps no state between calls and never
- *     synchronises the stream.
+ *     synchronises the stream -- except gdn_chunk_fwd_noalloc, whose fixed
+ *     scratch array (in the library's device image) and per-device address
+ *     cache persist between calls (see its declaration), and the status
+ *     readers, which synchronise.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work
  *     is enqueued on it asynchronously; outputs are valid once it has run.
  *   - Layouts: q, k [B, T, Hk, d_k]; v, o, dO, dv [B, T, Hv, d_v];
@@ -117,6 +120,42 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   size_t ws_bytes, void* stream);
 
 /*
+ * One GatedDeltaNet layer's use of the rule, with the element-wise operations
+ * around it (PR "Shard the GatedDeltaNet sequence under
+ * ici_context_parallelism", description: the layer's "qkvz" activations
+ * [B, T, H, D], of which q and k enter the rule normalised and z gates its
+ * output; the pages do not define these operations further, so the plain
+ * forms below are this library's reading):
+ *   q_n = q / sqrt(sum q^2 + 1e-6), k_n likewise, per token and key head;
+ *   beta = sigmoid(b), g = -softplus(a), per token and value head -- applied
+ *     by the rule's kernels where they load the gates (the logits a and b
+ *     are what the caller passes);
+ *   o = the rule on (q_n, k_n, v, g, beta, h0)            (as gdn_chunk_fwd);
+ *   y = o * silu(z), silu(z) = z sigmoid(z)                 (z NULL: y = o).
+ * Forward: q, k, v, z bf16 (layouts of gdn_chunk_fwd; z as v); a, b fp32
+ * [B, T, Hv]; writes y (bf16), o (bf16, the ungated output the backward needs
+ * when z is given; NULL = not kept) and hT (NULL = not written).
+ * Backward: the forward's inputs, o (required when z is given), the output
+ * cotangent dy and dhT (NULL = 0); writes dq, dk (bf16, raw q and k, summed over
+ * the value heads of each key head), dv (bf16), da, db (fp32, the logits), dz
+ * (bf16, required when z is given) and dh0 (NULL = not written).
+ * ws: at least gdn_layer_workspace_bytes(backward, ...) bytes; its first word
+ * is the rule's status word (gdn_workspace_status).  Other conventions as for
+ * gdn_chunk_fwd / gdn_chunk_bwd.
+ */
+size_t gdn_layer_workspace_bytes(int backward, int B, int T, int Hk, int Hv, int d_k, int d_v,
+                                 int chunk, int n_segments);
+int gdn_layer_fwd(const void* q, const void* k, const void* v, const float* a, const float* b,
+                  const void* z, const float* h0, void* y, void* o, float* hT, int B, int T, int Hk,
+                  int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws, size_t ws_bytes,
+                  void* stream);
+int gdn_layer_bwd(const void* q, const void* k, const void* v, const float* a, const float* b,
+                  const void* z, const float* h0, const void* o, const void* dy, const float* dhT,
+                  void* dq, void* dk, void* dv, float* da, float* db, void* dz, float* dh0, int B,
+                  int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
+                  size_t ws_bytes, void* stream);
+
+/*
  * Forward that allocates nothing and takes no workspace.  The pages have no
  * counterpart of this entry point; it exists for callers that may not
  * allocate device memory at call time and cannot lend a scratch buffer:
@@ -132,20 +171,35 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
  * larger problems are refused with GDN_ERR_WORKSPACE before anything is
  * enqueued.  Every GPU that loads the library keeps that array until the
  * process exits.
- * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.
+ * Set-up: a call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress) whenever `stream` is not capturing, and caches it per
+ * device; a call made while `stream` is being captured uses that cache, so
+ * make the first call on each device before any stream capture, and make one
+ * again after a device reset (which reloads the library's device image at a
+ * new address).
  * Sharing: all calls on a device use the same array, and its contents persist
  * from call to call.  Nothing in it needs to start at zero (each call writes
  * every scratch byte it reads before reading it), but calls whose executions
  * overlap on the GPU (different streams, or several host threads without
  * ordering) race on the array and may return wrong results: order them.
  * Never calls cudaMalloc, cudaFree or any allocating routine.
+ * Failure detection: the call's kernels report a bounded wait that gave up in
+ * the array's status word, which gdn_noalloc_status reads.
  */
 #define GDN_NOALLOC_MAX_UNITS 256
 int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
                           const float* beta, const float* h0, void* o, float* hT, int B, int T,
                           int Hk, int Hv, int d_k, int d_v, int chunk, void* stream);
+
+/*
+ * Status of the bounded in-kernel waits of the last gdn_chunk_fwd_noalloc
+ * call on the current device: synchronises `stream` (pass the stream that
+ * call used) and reads the status word of the fixed scratch array.  Returns
+ * GDN_OK if no wait gave up, GDN_ERR_TIMEOUT if one did (that call's outputs
+ * are then not valid), GDN_ERR_CUDA if the stream or the read failed.  The
+ * pages have no counterpart.
+ */
+int gdn_noalloc_status(void* stream);
 
 /*
  * Timing variants of gdn_chunk_fwd / gdn_chunk_bwd: identical results, plus
@@ -186,6 +240,33 @@ int gdn_chunk_bwd_timed(const void* q, const void* k, const void* v, const float
  */
 int gdn_affine_compose(const float* A, const float* B, float* A_out, float* B_out, int batch,
                        int n, int d_k, int d_v, void* stream);
+
+/*
+ * Per-segment affine maps of the inter-chunk recurrence (pass 1 of the
+ * two-pass scan, returned to the caller).  The N = ceil(T/chunk) chunks of
+ * each (b, value head) are split into n_segments segments of whole chunks
+ * (segment s holds chunks [floor(sN/S), floor((s+1)N/S))), and each segment's
+ * chunk maps h' = A_c h + B_c, A_c = exp(g_last) I - k_g^T w, B_c = k_g^T u, are
+ * composed in order: for every segment
+ *     A_s = A_{last} ... A_{first},   B_s = the state the segment leaves from h = 0,
+ * so the state leaving segment s is A_s h_in + B_s.  A caller that holds a
+ * sequence split across devices folds each device's chunks (n_segments = 1),
+ * gathers the pairs, takes the exclusive prefix (gdn_affine_compose and one
+ * application to h0) and replays with gdn_chunk_fwd from its incoming state.
+ * Sources: PR "Shard the GatedDeltaNet sequence under ici_context_parallelism",
+ * description (each device folds its chunks into one (A, B), the pairs are
+ * gathered and prefix-composed), and the A-output design question in the
+ * review thread of PR "Fuse the Gated Delta Net inter-chunk scan into a
+ * Pallas TPU kernel" (A as an optional output beside B).
+ * A_out: fp32 [B, Hv, n_segments, d_k, d_k] (NULL = not written);
+ * B_out: fp32 [B, Hv, n_segments, d_k, d_v] (required).  Row-major.
+ * 1 <= n_segments <= max(1, N), else GDN_ERR_ARG.  T = 0 gives (I, 0).
+ * ws: at least gdn_fwd_workspace_bytes(B, T, Hk, Hv, d_k, d_v, chunk, 1)
+ * bytes, with the status word as for the forward (gdn_workspace_status).
+ */
+int gdn_segment_fold(const void* k, const void* v, const float* g, const float* beta,
+                     float* A_out, float* B_out, int B, int T, int Hk, int Hv, int d_k, int d_v,
+                     int chunk, int n_segments, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Debug export of the per-chunk UT quantities, for tests.  For every

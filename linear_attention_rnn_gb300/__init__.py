@@ -78,6 +78,18 @@ def lib():
         L.gdn_debug_ut.restype = I
         L.gdn_workspace_status.argtypes = [P, P]
         L.gdn_workspace_status.restype = I
+        L.gdn_layer_workspace_bytes.argtypes = [I] * 9
+        L.gdn_layer_workspace_bytes.restype = Z
+        L.gdn_layer_fwd.argtypes = [P] * 10 + [I] * 8 + [P, Z, P]
+        L.gdn_layer_fwd.restype = I
+        L.gdn_layer_bwd.argtypes = [P] * 17 + [I] * 8 + [P, Z, P]
+        L.gdn_layer_bwd.restype = I
+        L.gdn_segment_fold.argtypes = [P] * 6 + [I] * 8 + [P, Z, P]
+        L.gdn_segment_fold.restype = I
+        L.gdn_chunk_fwd_noalloc.argtypes = [P] * 8 + [I] * 7 + [P]
+        L.gdn_chunk_fwd_noalloc.restype = I
+        L.gdn_noalloc_status.argtypes = [P]
+        L.gdn_noalloc_status.restype = I
         L.gdn_selftest_wait_timeout.argtypes = [ctypes.c_longlong, P, P]
         L.gdn_selftest_wait_timeout.restype = I
         _lib = L
@@ -212,6 +224,59 @@ def chunk_bwd(q, k, v, g, beta, h0, dO, dhT=None, *, chunk: int = 128, n_segment
     return dq, dk_, dv_, dg, db, dh0
 
 
+def layer_workspace_bytes(backward, B, T, Hk, Hv, dk=128, dv=128, chunk=128, n_segments=0) -> int:
+    return int(lib().gdn_layer_workspace_bytes(int(backward), B, T, Hk, Hv, dk, dv, chunk,
+                                               n_segments))
+
+
+def layer_fwd(q, k, v, a, b, z=None, h0=None, *, chunk: int = 128, n_segments: int = 0,
+              keep_o: bool = True, want_hT: bool = True, workspace=None):
+    """Layer forward: q, k raw (normalised inside), a, b gate logits
+    (g = -softplus(a), beta = sigmoid(b)), optional output gate z.
+    Returns (y, o, hT): o is the ungated output (None unless keep_o and z)."""
+    B, T, Hk, Hv, dk, dv = _dims(q, k, v, a, b)
+    dev = q.device
+    _check(z, "z", torch.bfloat16, (B, T, Hv, dv))
+    _check(h0, "h0", torch.float32, (B, Hv, dk, dv))
+    y = torch.empty((B, T, Hv, dv), dtype=torch.bfloat16, device=dev)
+    o = torch.empty_like(y) if (keep_o and z is not None) else None
+    hT = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=dev) if want_hT else None
+    ws = _workspace(layer_workspace_bytes(0, B, T, Hk, Hv, dk, dv, chunk, n_segments), dev,
+                    workspace)
+    rc = lib().gdn_layer_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(h0),
+                             _ptr(y), _ptr(o), _ptr(hT), B, T, Hk, Hv, dk, dv, chunk, n_segments,
+                             _ptr(ws), ws.numel(), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_layer_fwd")
+    return y, o, hT
+
+
+def layer_bwd(q, k, v, a, b, z, h0, o, dy, dhT=None, *, chunk: int = 128, n_segments: int = 0,
+              want_dh0: bool = True, workspace=None):
+    """Layer backward.  Returns (dq, dk, dv, da, db, dz, dh0) for the raw q, k
+    and the gate logits; dz is None without a gate."""
+    B, T, Hk, Hv, dk, dv = _dims(q, k, v, a, b)
+    dev = q.device
+    _check(z, "z", torch.bfloat16, (B, T, Hv, dv))
+    _check(o, "o", torch.bfloat16, (B, T, Hv, dv))
+    _check(dy, "dy", torch.bfloat16, (B, T, Hv, dv))
+    _check(h0, "h0", torch.float32, (B, Hv, dk, dv))
+    _check(dhT, "dhT", torch.float32, (B, Hv, dk, dv))
+    dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    da, db = torch.empty_like(a), torch.empty_like(b)
+    dz = torch.empty_like(z) if z is not None else None
+    dh0 = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=dev) if want_dh0 else None
+    ws = _workspace(layer_workspace_bytes(1, B, T, Hk, Hv, dk, dv, chunk, n_segments), dev,
+                    workspace)
+    rc = lib().gdn_layer_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(z), _ptr(h0),
+                             _ptr(o), _ptr(dy), _ptr(dhT), _ptr(dq), _ptr(dk_), _ptr(dv_),
+                             _ptr(da), _ptr(db), _ptr(dz), _ptr(dh0), B, T, Hk, Hv, dk, dv, chunk,
+                             n_segments, _ptr(ws), ws.numel(), _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_layer_bwd")
+    return dq, dk_, dv_, da, db, dz, dh0
+
+
 def affine_compose(A: torch.Tensor, Bm: torch.Tensor):
     """Inclusive prefix of affine maps along dim 1: A [batch, n, dk, dk],
     B [batch, n, dk, dv] (fp32)."""
@@ -226,6 +291,31 @@ def affine_compose(A: torch.Tensor, Bm: torch.Tensor):
     if rc != GDN_OK:
         raise GDNError(rc, "gdn_affine_compose")
     return Ao, Bo
+
+
+def segment_fold(k, v, g, beta, n_segments: int = 1, *, chunk: int = 128, want_A: bool = True,
+                 workspace=None):
+    """Per-segment affine maps (A_s, B_s) of the inter-chunk recurrence:
+    A [B, Hv, S, dk, dk] (None if want_A is False) and B [B, Hv, S, dk, dv],
+    fp32, with the state leaving segment s equal to A_s h_in + B_s."""
+    B, T, Hk, dk = k.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    _check(k, "k", torch.bfloat16)
+    _check(v, "v", torch.bfloat16, (B, T, Hv, dv))
+    _check(g, "g", torch.float32, (B, T, Hv))
+    _check(beta, "beta", torch.float32, (B, T, Hv))
+    dev = k.device
+    A = (torch.empty((B, Hv, n_segments, dk, dk), dtype=torch.float32, device=dev)
+         if want_A else None)
+    Bm = torch.empty((B, Hv, n_segments, dk, dv), dtype=torch.float32, device=dev)
+    nbytes = fwd_workspace_bytes(B, T, Hk, Hv, dk, dv, chunk, 1)
+    ws = _workspace(nbytes, dev, workspace)
+    rc = lib().gdn_segment_fold(_ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A), _ptr(Bm), B, T,
+                                Hk, Hv, dk, dv, chunk, n_segments, _ptr(ws), ws.numel(),
+                                _stream(dev))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_segment_fold")
+    return A, Bm
 
 
 def debug_ut(k, v, g, beta, chunk: int = 128):
@@ -264,6 +354,7 @@ def selftest_wait_timeout(limit_ns: int, status: torch.Tensor) -> int:
     return lib().gdn_selftest_wait_timeout(int(limit_ns), _ptr(status), _stream(status.device))
 
 
-__all__ = ["build", "lib", "chunk_fwd", "chunk_bwd", "affine_compose", "debug_ut",
+__all__ = ["build", "lib", "chunk_fwd", "chunk_bwd", "layer_fwd", "layer_bwd",
+           "layer_workspace_bytes", "affine_compose", "segment_fold", "debug_ut",
            "fwd_workspace_bytes", "bwd_workspace_bytes", "default_segments", "GDNError",
            "header_functions", "workspace_status", "selftest_wait_timeout"]

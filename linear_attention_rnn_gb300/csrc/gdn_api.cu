@@ -119,8 +119,10 @@ struct Marks {
 // entering state.
 int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const void* q, const void* k,
                          const float* g, const float* h0, void* o, float* hT, bf16* states,
-                         bf16* delta, cudaStream_t s, Marks& mk, WalkFwdArgs& w, WalkFwdMaps& mp) {
+                         bf16* delta, int gate_logits, cudaStream_t s, Marks& mk, WalkFwdArgs& w,
+                         WalkFwdMaps& mp) {
   memset(&w, 0, sizeof w);
+  w.gate_logits = gate_logits;
   w.W = at<bf16>(ws, Lw.W);
   w.U = at<bf16>(ws, Lw.U);
   w.P = at<bf16>(ws, Lw.P);
@@ -224,7 +226,8 @@ size_t gdn_bwd_workspace_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, i
 static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
                     const float* beta, const float* h0, void* o, float* hT, int B, int T, int Hk,
                     int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
-                    size_t ws_bytes, void* stream, void* const* events, int n_events) {
+                    size_t ws_bytes, void* stream, void* const* events, int n_events,
+                    int gate_logits = 0) {
   int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
   if (rc) return rc;
   const long tokens = (long)B * T;
@@ -257,6 +260,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   p.U = at<bf16>(ws, L.U);
   p.P = at<bf16>(ws, L.P);
   p.status = at<int>(ws, L.status);
+  p.gate_logits = gate_logits;
   p.B = B;
   p.T = T;
   p.Hk = Hk;
@@ -266,7 +270,9 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   if (rc || (rc = mk.rec())) return rc;
   WalkFwdArgs w;
   WalkFwdMaps mp;
-  if ((rc = prepare_forward_walk(d, L, ws, q, k, g, h0, o, hT, nullptr, nullptr, s, mk, w, mp))) return rc;
+  if ((rc = prepare_forward_walk(d, L, ws, q, k, g, h0, o, hT, nullptr, nullptr, gate_logits, s, mk, w,
+                                 mp)))
+    return rc;
   if ((rc = cuda_status(launch_walk_fwd(w, mp, 0, s)))) return rc;
   return mk.rec();
 }
@@ -275,7 +281,8 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
                     const float* beta, const float* h0, const void* dO, const float* dhT,
                     void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0, int B,
                     int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
-                    size_t ws_bytes, void* stream, void* const* events, int n_events) {
+                    size_t ws_bytes, void* stream, void* const* events, int n_events,
+                    int gate_logits = 0) {
   int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
   if (rc) return rc;
   const long tokens = (long)B * T;
@@ -311,6 +318,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   p.P = at<bf16>(ws, L.P);
   p.Tb = at<bf16>(ws, L.Tb);
   p.status = at<int>(ws, L.status);
+  p.gate_logits = gate_logits;
   p.B = B;
   p.T = T;
   p.Hk = Hk;
@@ -323,7 +331,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   WalkFwdArgs fw;
   WalkFwdMaps fm;
   rc = prepare_forward_walk(d, L, ws, q, k, g, h0, nullptr, nullptr, at<bf16>(ws, L.states),
-                            at<bf16>(ws, L.delta), s, mk, fw, fm);
+                            at<bf16>(ws, L.delta), gate_logits, s, mk, fw, fm);
   if (rc) return rc;
   // 3. reverse walk of the state cotangent (with segments: its fold and prefix
   //    now); it needs nothing from the recompute, so the two walks run side by
@@ -346,6 +354,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   w.dstates = at<bf16>(ws, L.dstates);
   w.ddelta = at<bf16>(ws, L.ddelta);
   w.status = at<int>(ws, L.status);
+  w.gate_logits = gate_logits;
   WalkBwdMaps bm;
   memset(&bm, 0, sizeof bm);
   {
@@ -404,6 +413,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   ga.dq = static_cast<bf16*>(dq);
   ga.dk = static_cast<bf16*>(dk);
   ga.status = at<int>(ws, L.status);
+  ga.gate_logits = gate_logits;
   ga.dv = static_cast<bf16*>(dv);
   ga.dg = dg;
   ga.dbeta = dbeta;
@@ -449,6 +459,134 @@ int gdn_chunk_bwd_timed(const void* q, const void* k, const void* v, const float
                   d_v, chunk, n_segments, ws, ws_bytes, stream, events, n_events);
 }
 
+// ---- layer entry points: normalised q/k, gate logits, output gate -------------------
+// Workspace of a layer call: the rule's own workspace first (so that its
+// status word is the first word, as gdn_workspace_status reads it), then the
+// normalised q and k (bf16, [B, T, Hk, 128] each), a [B, T, Hv, 128] bf16
+// buffer (forward: the rule's output when the caller keeps none; backward:
+// the rule's output cotangent), and for the backward the cotangents of the
+// normalised q and k.
+struct LayerLayout {
+  size_t core, qn, kn, obuf, dO, dqn, dkn, total;
+};
+
+static LayerLayout layer_layout(int backward, int B, int T, int Hk, int Hv, int n_segments) {
+  LayerLayout L;
+  memset(&L, 0, sizeof L);
+  const size_t qk = (size_t)B * T * Hk * HD * sizeof(bf16);
+  const size_t vv = (size_t)B * T * Hv * HD * sizeof(bf16);
+  const Dims d = make_dims(B, T, Hk, Hv, n_segments);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += up(bytes);
+    return o;
+  };
+  L.core = take(layout(d, backward != 0).total);
+  L.qn = take(qk);
+  L.kn = take(qk);
+  L.obuf = take(vv);
+  L.dO = L.obuf;
+  if (backward) {
+    L.dqn = take(qk);
+    L.dkn = take(qk);
+  }
+  L.total = off;
+  return L;
+}
+
+constexpr float kL2Eps = 1e-6f;
+
+size_t gdn_layer_workspace_bytes(int backward, int B, int T, int Hk, int Hv, int d_k, int d_v,
+                                 int chunk, int n_segments) {
+  if (check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments) != GDN_OK) return 0;
+  return layer_layout(backward, B, T, Hk, Hv, n_segments).total;
+}
+
+int gdn_layer_fwd(const void* q, const void* k, const void* v, const float* a, const float* b,
+                  const void* z, const float* h0, void* y, void* o, float* hT, int B, int T, int Hk,
+                  int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws, size_t ws_bytes,
+                  void* stream) {
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
+  if (rc) return rc;
+  const long tokens = (long)B * T;
+  if (tokens > 0 && (!q || !k || !v || !a || !b || !y)) return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, a, b, z, h0, y, o, hT, ws};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_ARG;
+  if (B == 0) return GDN_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0)  // no tokens: the final state is the initial state
+    return fwd_impl(q, k, v, a, b, h0, y, hT, B, T, Hk, Hv, d_k, d_v, chunk, n_segments, nullptr, 0,
+                    stream, nullptr, 0, 1);
+  const LayerLayout L = layer_layout(0, B, T, Hk, Hv, n_segments);
+  if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  bf16* qn = at<bf16>(ws, L.qn);
+  bf16* kn = at<bf16>(ws, L.kn);
+  if ((rc = cuda_status(launch_l2norm(static_cast<const bf16*>(q), qn, tokens * Hk, kL2Eps, s)))) return rc;
+  if ((rc = cuda_status(launch_l2norm(static_cast<const bf16*>(k), kn, tokens * Hk, kL2Eps, s)))) return rc;
+  // the rule's output: straight into y without a gate, else into o (or the workspace)
+  void* core_o = !z ? y : (o ? o : at<void>(ws, L.obuf));
+  rc = fwd_impl(qn, kn, v, a, b, h0, core_o, hT, B, T, Hk, Hv, d_k, d_v, chunk, n_segments,
+                at<void>(ws, L.core), L.qn - L.core, stream, nullptr, 0, 1);
+  if (rc) return rc;
+  if (z) {
+    rc = cuda_status(launch_out_gate(static_cast<const bf16*>(core_o), static_cast<const bf16*>(z),
+                                     static_cast<bf16*>(y), tokens * Hv, s));
+    if (rc) return rc;
+  } else if (o) {
+    rc = cuda_status(cudaMemcpyAsync(o, y, (size_t)tokens * Hv * HD * sizeof(bf16),
+                                     cudaMemcpyDeviceToDevice, s));
+  }
+  return rc;
+}
+
+int gdn_layer_bwd(const void* q, const void* k, const void* v, const float* a, const float* b,
+                  const void* z, const float* h0, const void* o, const void* dy, const float* dhT,
+                  void* dq, void* dk, void* dv, float* da, float* db, void* dz, float* dh0, int B,
+                  int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
+                  size_t ws_bytes, void* stream) {
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
+  if (rc) return rc;
+  const long tokens = (long)B * T;
+  if (tokens > 0 && (!q || !k || !v || !a || !b || !dy || !dq || !dk || !dv || !da || !db))
+    return GDN_ERR_ARG;
+  if (tokens > 0 && z && (!o || !dz)) return GDN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, a, b, z, h0, o, dy, dhT, dq, dk, dv, da, db, dz, dh0, ws};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_ARG;
+  if (B == 0) return GDN_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0)
+    return bwd_impl(q, k, v, a, b, h0, dy, dhT, dq, dk, dv, da, db, dh0, B, T, Hk, Hv, d_k, d_v, chunk,
+                    n_segments, nullptr, 0, stream, nullptr, 0, 1);
+  const LayerLayout L = layer_layout(1, B, T, Hk, Hv, n_segments);
+  if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  bf16* qn = at<bf16>(ws, L.qn);
+  bf16* kn = at<bf16>(ws, L.kn);
+  bf16* dqn = at<bf16>(ws, L.dqn);
+  bf16* dkn = at<bf16>(ws, L.dkn);
+  if ((rc = cuda_status(launch_l2norm(static_cast<const bf16*>(q), qn, tokens * Hk, kL2Eps, s)))) return rc;
+  if ((rc = cuda_status(launch_l2norm(static_cast<const bf16*>(k), kn, tokens * Hk, kL2Eps, s)))) return rc;
+  const void* dO = dy;
+  if (z) {  // the gate's backward gives the rule's output cotangent and dz
+    bf16* dOb = at<bf16>(ws, L.dO);
+    rc = cuda_status(launch_out_gate_bwd(static_cast<const bf16*>(o), static_cast<const bf16*>(z),
+                                         static_cast<const bf16*>(dy), dOb, static_cast<bf16*>(dz),
+                                         tokens * Hv, s));
+    if (rc) return rc;
+    dO = dOb;
+  }
+  rc = bwd_impl(qn, kn, v, a, b, h0, dO, dhT, dqn, dkn, dv, da, db, dh0, B, T, Hk, Hv, d_k, d_v, chunk,
+                n_segments, at<void>(ws, L.core), L.qn - L.core, stream, nullptr, 0, 1);
+  if (rc) return rc;
+  if ((rc = cuda_status(launch_l2norm_bwd(static_cast<const bf16*>(q), dqn, static_cast<bf16*>(dq),
+                                          tokens * Hk, kL2Eps, s))))
+    return rc;
+  return cuda_status(launch_l2norm_bwd(static_cast<const bf16*>(k), dkn, static_cast<bf16*>(dk), tokens * Hk,
+                                       kL2Eps, s));
+}
+
 int gdn_affine_compose(const float* A, const float* B, float* A_out, float* B_out, int batch,
                        int n, int d_k, int d_v, void* stream) {
   if (batch < 0 || n < 0) return GDN_ERR_ARG;
@@ -472,6 +610,70 @@ int gdn_affine_compose(const float* A, const float* B, float* A_out, float* B_ou
   x.exclusive = 0;
   x.reverse = 0;
   return cuda_status(launch_affine_walk(x, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_segment_fold(const void* k, const void* v, const float* g, const float* beta,
+                     float* A_out, float* B_out, int B, int T, int Hk, int Hv, int d_k, int d_v,
+                     int chunk, int n_segments, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
+  if (rc) return rc;
+  const int NC = (T + CH - 1) / CH;
+  if (n_segments < 1 || n_segments > (NC > 1 ? NC : 1)) return GDN_ERR_ARG;
+  if (B == 0) return GDN_OK;
+  if (!B_out) return GDN_ERR_ARG;
+  if (T > 0 && (!k || !v || !g || !beta)) return GDN_ERR_ARG;
+  const void* ptrs[] = {k, v, g, beta, A_out, B_out, ws};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) return cuda_status(launch_identity_pairs(A_out, B_out, (long)B * Hv, s));
+  const Dims d = make_dims(B, T, Hk, Hv, 1);
+  const Layout L = layout(d, false);
+  if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  if ((rc = cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), s)))) return rc;
+  // w and u of every chunk (no output, so no P)
+  PrepArgs p;
+  memset(&p, 0, sizeof p);
+  p.q = static_cast<const bf16*>(k);  // unused: P is not requested
+  p.k = static_cast<const bf16*>(k);
+  p.v = static_cast<const bf16*>(v);
+  p.g = g;
+  p.beta = beta;
+  p.W = at<bf16>(ws, L.W);
+  p.U = at<bf16>(ws, L.U);
+  p.status = at<int>(ws, L.status);
+  p.B = B;
+  p.T = T;
+  p.Hk = Hk;
+  p.Hv = Hv;
+  p.NC = NC;
+  if ((rc = cuda_status(launch_prep(p, s)))) return rc;
+  // pass 1 of the segment scan: each segment's chunks pushed through [A | B] from [I | 0]
+  WalkFwdArgs f;
+  memset(&f, 0, sizeof f);
+  f.W = p.W;
+  f.U = p.U;
+  f.P = at<bf16>(ws, L.P);
+  f.q = static_cast<const bf16*>(k);
+  f.k = static_cast<const bf16*>(k);
+  f.g = g;
+  f.B = B;
+  f.T = T;
+  f.Hk = Hk;
+  f.Hv = Hv;
+  f.NC = NC;
+  f.S = n_segments;
+  f.pairA = A_out;
+  f.pairB = B_out;
+  f.status = p.status;
+  WalkFwdMaps mp;
+  memset(&mp, 0, sizeof mp);
+  const uint64_t wrows = (uint64_t)d.BH() * NC * CH;
+  if (!tmap_heads(&mp.k, k, B, T, Hk, HD) || !tmap_heads(&mp.q, k, B, T, Hk, HD) ||
+      !tmap_2d(&mp.W, f.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
+      !tmap_2d(&mp.P, f.P, CH, wrows, CH * sizeof(bf16), 64, CH, true))
+    return GDN_ERR_CUDA;
+  return cuda_status(launch_walk_fwd(f, mp, 1, s));
 }
 
 int gdn_debug_ut(const void* k, const void* v, const float* g, const float* beta, float* S_out,
@@ -551,16 +753,23 @@ void* g_noalloc_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  The name of a
 // __device__ array in host code is only a host-side stand-in, so the address
-// is looked up once per device, with that device current, and cached.
-int noalloc_scratch(void** out) {
+// is looked up with the device current.  Outside stream capture it is looked
+// up on every call (cheap once the module is loaded, and correct after the
+// device's context was reset and the module reloaded at a new address);
+// during a capture the address cached by the last call outside capture is used.
+int noalloc_scratch(cudaStream_t s, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return GDN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_addr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
     g_noalloc_addr[dev] = p;
+  } else if (!g_noalloc_addr[dev]) {
+    return GDN_ERR_CUDA;  // no call outside capture has looked the address up yet
   }
   *out = g_noalloc_addr[dev];
   return GDN_OK;
@@ -577,7 +786,18 @@ extern "C" int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v
   const long units = (long)B * Hv * ((T + CH - 1) / CH);
   if (units > GDN_NOALLOC_MAX_UNITS) return GDN_ERR_WORKSPACE;
   void* scratch = nullptr;
-  if (units > 0 && (rc = noalloc_scratch(&scratch))) return rc;
+  if (units > 0 && (rc = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch))) return rc;
   return fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, Hk, Hv, d_k, d_v, chunk, 1, scratch,
                   kNoAllocScratchBytes, stream, nullptr, 0);
+}
+
+// The status word of the fixed scratch array (its first 4 bytes, as in every
+// workspace layout) after the last gdn_chunk_fwd_noalloc on the current device.
+extern "C" int gdn_noalloc_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpyFromSymbol(&st, g_noalloc_scratch, sizeof st, 0, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return (st & 1) ? GDN_ERR_TIMEOUT : GDN_OK;
 }

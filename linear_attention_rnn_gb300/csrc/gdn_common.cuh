@@ -112,4 +112,15 @@ __device__ __forceinline__ void warp_cumsum128(float (&v)[4], int lane) {
   v[3] += excl;
 }
 
+// Gate activations, applied where the kernels load the gates when the caller
+// passes logits (logits != 0): beta = sigmoid(b) and g = -softplus(a), the
+// decay exp(g) = 1 / (1 + exp(a)).  softplus(a) = max(a, 0) + log1p(exp(-|a|)).
+__device__ __forceinline__ float act_g(float a, int logits) {
+  return logits ? -(fmaxf(a, 0.f) + log1pf(expf(-fabsf(a)))) : a;
+}
+__device__ __forceinline__ float act_beta(float b, int logits) {
+  return logits ? 1.f / (1.f + expf(-b)) : b;
+}
+
 }  // namespace gdn
+

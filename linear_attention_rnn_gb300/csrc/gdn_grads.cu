@@ -176,8 +176,8 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     gv = bv = 0.f;
     if (tid < L && jj < group) {
       const long idx = ((long)b * a.T + t0 + tid) * a.Hv + kh * group + jj;
-      gv = a.g[idx];
-      bv = a.beta[idx];
+      gv = act_g(a.g[idx], a.gate_logits);
+      bv = act_beta(a.beta[idx], a.gate_logits);
     }
   };
   float g_next = 0.f, b_next = 0.f;
@@ -518,8 +518,15 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       for (int i = 0; i < 4; ++i) {
         const int r = lane * 4 + i;
         if (r < L) {
-          a.dg[tokv + (long)r * a.Hv] = dg[i];
-          a.dbeta[tokv + (long)r * a.Hv] = sm.dbeta[r] + sm.gam[r] * sm.dbg[r];
+          const long t = tokv + (long)r * a.Hv;
+          float dgv = dg[i], dbv = sm.dbeta[r] + sm.gam[r] * sm.dbg[r];
+          if (a.gate_logits) {  // chain rule through g = -softplus(a) and beta = sigmoid(b)
+            const float sa = act_beta(a.g[t], 1), sb = act_beta(a.beta[t], 1);
+            dgv *= -sa;
+            dbv *= sb * (1.f - sb);
+          }
+          a.dg[t] = dgv;
+          a.dbeta[t] = dbv;
         }
       }
     }

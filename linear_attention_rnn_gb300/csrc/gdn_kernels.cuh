@@ -23,6 +23,7 @@ struct PrepArgs {
   float* S_dbg;  // [BH][NC][CH][CH]  fp32 S  (debug export)        (nullable)
   float* T_dbg;  // [BH][NC][CH][CH]  fp32 T  (debug export)        (nullable)
   int* status;   // bit 0 set if a bounded wait gave up (nullable)
+  int gate_logits;         // 1: g and beta hold logits a, b (g = -softplus(a), beta = sigmoid(b))
   int B, T, Hk, Hv, NC;
 };
 
@@ -45,6 +46,7 @@ struct WalkFwdArgs {
   float* pairA;            // fold output [BH][S][HD][HD]
   float* pairB;            // fold output [BH][S][HD][HD]
   int* status;             // bit 0 set if a bounded wait gave up (nullable)
+  int gate_logits;         // 1: g and beta hold logits a, b (g = -softplus(a), beta = sigmoid(b))
   int B, T, Hk, Hv, NC, S;
 };
 
@@ -79,6 +81,7 @@ struct WalkBwdArgs {
   float* pairA;            // fold output
   float* pairB;
   int* status;             // bit 0 set if a bounded wait gave up (nullable)
+  int gate_logits;         // 1: g and beta hold logits a, b (g = -softplus(a), beta = sigmoid(b))
   int B, T, Hk, Hv, NC, S;
 };
 
@@ -125,6 +128,7 @@ struct GradArgs {
   float* dg;            // [B,T,Hv]
   float* dbeta;         // [B,T,Hv]
   int* status;          // bit 0 set if a bounded wait gave up (nullable)
+  int gate_logits;         // 1: g and beta hold logits a, b (g = -softplus(a), beta = sigmoid(b))
   int B, T, Hk, Hv, NC;
 };
 
@@ -140,6 +144,14 @@ cudaError_t launch_walk_bwd(const WalkBwdArgs& a, const WalkBwdMaps& m, int fold
 cudaError_t launch_walk_pair(const WalkFwdArgs& fa, const WalkFwdMaps& fm, const WalkBwdArgs& ba,
                              const WalkBwdMaps& bm, cudaStream_t s);
 cudaError_t launch_affine_walk(const AffineWalkArgs& a, cudaStream_t s);
+// Element-wise layer operations on rows of HD bf16 values (gdn_layer.cu).
+cudaError_t launch_l2norm(const bf16* x, bf16* y, long rows, float eps, cudaStream_t s);
+cudaError_t launch_l2norm_bwd(const bf16* x, const bf16* dy, bf16* dx, long rows, float eps, cudaStream_t s);
+cudaError_t launch_out_gate(const bf16* o, const bf16* z, bf16* y, long rows, cudaStream_t s);
+cudaError_t launch_out_gate_bwd(const bf16* o, const bf16* z, const bf16* dy, bf16* dO, bf16* dz, long rows,
+                                cudaStream_t s);
+// (A, B) = (I, 0) for n [HD x HD] fp32 pairs (A nullable).
+cudaError_t launch_identity_pairs(float* A, float* Bv, long n, cudaStream_t s);
 cudaError_t launch_grads(const GradArgs& a, cudaStream_t s);
 cudaError_t launch_selftest_wait(long long limit_ns, int* status, cudaStream_t s);
 

@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       const Unit x = decode(u);
       if (tid < min(CH, a.T - x.c * CH)) {
         const long idx = ((long)x.b * a.T + x.c * CH + tid) * a.Hv + x.kh * group + x.jj;
-        gv = a.g[idx];
-        bv = a.beta[idx];
+        gv = act_g(a.g[idx], a.gate_logits);
+        bv = act_beta(a.beta[idx], a.gate_logits);
       }
     }
   };

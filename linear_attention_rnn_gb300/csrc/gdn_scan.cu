@@ -152,4 +152,22 @@ cudaError_t launch_affine_walk(const AffineWalkArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// (A, B) = (I, 0) for n pairs: the fold of an empty stretch of chunks.
+__global__ void k_identity_pairs(float* A, float* Bv, long n) {
+  const long per = (long)HD * HD;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n * per; i += (long)gridDim.x * blockDim.x) {
+    const long e = i % per;
+    if (A) A[i] = (e / HD == e % HD) ? 1.f : 0.f;
+    Bv[i] = 0.f;
+  }
+}
+
+cudaError_t launch_identity_pairs(float* A, float* Bv, long n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const long total = n * HD * HD;
+  const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+  k_identity_pairs<<<blocks, 256, 0, s>>>(A, Bv, n);
+  return cudaGetLastError();
+}
+
 }  // namespace gdn

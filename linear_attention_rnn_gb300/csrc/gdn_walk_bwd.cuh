@@ -164,7 +164,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
   auto load_g = [&](int ci) {
     if (ci >= n) return 0.f;
     const int c = chunk_of(ci);
-    return r < rows_of(c) ? a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j] : 0.f;
+    return r < rows_of(c) ? act_g(a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j], a.gate_logits) : 0.f;
   };
   auto load_do = [&](int ci) {
 #pragma unroll

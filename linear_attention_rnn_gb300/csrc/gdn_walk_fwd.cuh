@@ -148,6 +148,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
   constexpr int nring = STAGED ? NSLOT - 1 : NSLOT;  // compile-time: the ring index is on the issue path
   unsigned char* stage = sm.slot[NSLOT - 1];
   if (cbeg >= cend) return;
+  if (partA && a.pairA == nullptr) return;  // fold without the A output: B columns only
   auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
   // tile sequence of a chunk: w, Q, K, P (with output) or w, K
   auto tile_of = [&](int kind) { return withO ? kind : (kind == 0 ? 0 : 1); };  // kind: 0 w, 1 Q, 2 K, 3 P
@@ -179,7 +180,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
   float gnext = 0.f, part = 0.f;
   float gam_r = 0.f, ef_r = 0.f, gC = 0.f;
   auto load_g = [&](int c) {
-    return (c < cend && r < rows_of(c)) ? a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j] : 0.f;
+    return (c < cend && r < rows_of(c)) ? act_g(a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j], a.gate_logits) : 0.f;
   };
   // row r of this slice of u for chunk c, loaded a chunk ahead into registers
   uint4 un[4];

@@ -186,4 +186,48 @@ def make_device(wl: Workload, device, backward: Optional[bool] = None) -> Inputs
     return Inputs(wl, q, k, v, g, beta, h0, dO, dhT)
 
 
-__all__ = ["Workload", "WORKLOADS", "Inputs", "make_host", "make_device"]
+@dataclasses.dataclass
+class LayerInputs:
+    """Raw inputs of one GatedDeltaNet layer's use of the rule: q, k
+    unnormalised, a and b the gate logits (g = -softplus(a), beta =
+    sigmoid(b)), z the output gate, and the backward's cotangents."""
+    wl: Workload
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    a: torch.Tensor
+    b: torch.Tensor
+    z: torch.Tensor
+    h0: Optional[torch.Tensor]
+    dy: torch.Tensor
+    dhT: torch.Tensor
+
+    def to(self, device) -> "LayerInputs":
+        f = lambda x: None if x is None else x.to(device)
+        return LayerInputs(self.wl, f(self.q), f(self.k), f(self.v), f(self.a), f(self.b),
+                           f(self.z), f(self.h0), f(self.dy), f(self.dhT))
+
+
+def make_layer_host(wl: Workload, qk_scale: float = 3.0) -> LayerInputs:
+    """Raw layer inputs on the host: q, k ~ N(0, qk_scale^2) (not normalised),
+    v, z, dy ~ N(0, 1) (bf16), a ~ N(gate_shift, 1) and b ~ N(0, 1) (fp32
+    logits), h0 ~ N(0, h0_std^2), dhT ~ N(0, 0.1^2); one default_rng([seed, 7])
+    stream in that order."""
+    B, T, Hk, Hv, dk, dv = wl.B, wl.T, wl.Hk, wl.Hv, wl.dk, wl.dv
+    rng = np.random.default_rng([wl.seed, 7])
+    q = rng.standard_normal((B, T, Hk, dk)) * qk_scale
+    k = rng.standard_normal((B, T, Hk, dk)) * qk_scale
+    v = rng.standard_normal((B, T, Hv, dv))
+    a = rng.standard_normal((B, T, Hv)) + wl.gate_shift
+    b = rng.standard_normal((B, T, Hv))
+    z = rng.standard_normal((B, T, Hv, dv))
+    h0 = rng.standard_normal((B, Hv, dk, dv)) * wl.h0_std
+    dy = rng.standard_normal((B, T, Hv, dv))
+    dhT = rng.standard_normal((B, Hv, dk, dv)) * 0.1
+    f32 = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32))
+    return LayerInputs(wl, _to_bf16(q), _to_bf16(k), _to_bf16(v), f32(a), f32(b), _to_bf16(z),
+                       f32(h0) if wl.h0_std > 0 else None, _to_bf16(dy), f32(dhT))
+
+
+__all__ = ["Workload", "WORKLOADS", "Inputs", "make_host", "make_device", "LayerInputs",
+           "make_layer_host"]

@@ -79,6 +79,19 @@ def test_compose_argument_errors(L):
     assert L.gdn_affine_compose(None, None, None, None, 0, 4, 128, 128, None) == 0
 
 
+def test_segment_fold_argument_errors(L):
+    def call(S=1, T=256, A=FAKE, Bo=FAKE, dk=128, ws=FAKE, ws_bytes=0):
+        return L.gdn_segment_fold(FAKE, FAKE, FAKE, FAKE, A, Bo, 1, T, 2, 4, dk, 128, 128, S, ws,
+                                  ws_bytes, None)
+    assert call(dk=64) == -2
+    assert call(S=0) == -1
+    assert call(S=3) == -1          # 2 chunks
+    assert call(Bo=None) == -1
+    assert call(A=MISAL) == -1
+    assert call() == -3             # workspace of 0 bytes
+    assert call(S=2, A=None, ws=None) == -3
+
+
 def test_workspace_sizes(L):
     f = gdn.fwd_workspace_bytes
     b = gdn.bwd_workspace_bytes

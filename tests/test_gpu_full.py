@@ -44,15 +44,15 @@ def _fwd_check(gdn, wl, key_heads, check_o=True):
     sub, vh = heads_slice(inp, 0, key_heads)
     ro, rh = oracle.fwd(sub, want_o=check_o)
     for i, j in enumerate(vh):
-        assert_rel(hT[0, j].cpu().numpy(), rh[i], H_TOL, f"hT[{j}]")
+        assert_rel(hT[0, j].cpu().numpy(), rh[i], H_TOL, f"hT[{j}]", (wl.name, "hT"))
         if check_o:
-            assert_rel(o[0, :, j].float().cpu().numpy(), ro[i], O_TOL, f"o[{j}]")
+            assert_rel(o[0, :, j].float().cpu().numpy(), ro[i], O_TOL, f"o[{j}]", (wl.name, "o"))
     return inp, o, hT
 
 
 def test_long_sequence_forward_148_segments(gdn_lib):
     wl = WORKLOADS["long_t262144"]
-    inp, o, hT = _fwd_check(gdn_lib, wl, [0, 15])
+    inp, o, hT = _fwd_check(gdn_lib, wl, list(range(wl.Hk)))  # every head
     # the same result from a single sequential walk (every head)
     o1, h1 = gdn_lib.chunk_fwd(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.h0, n_segments=1)
     assert_rel(o.float().cpu().numpy(), o1.float().cpu().numpy(), O_TOL, "o: 148 vs 1 segments")
@@ -65,16 +65,19 @@ def test_long_sequence_backward_148_segments(gdn_lib):
     dq, dk, dv, dg, db, dh0 = gdn_lib.chunk_bwd(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.h0,
                                                 inp.dO, inp.dhT, n_segments=wl.n_segments)
     torch.cuda.synchronize()
-    sub, vh = heads_slice(inp, 0, [7])
+    key_heads = [0, 7, 12, 15]
+    sub, vh = heads_slice(inp, 0, key_heads)
     res = oracle.bwd(sub, ckpt=256)
-    kq = oracle.key_head_grads(sub.wl, res)[(0, 0)]
-    assert_rel(dq[0, :, 7].float().cpu().numpy(), kq[0], G_TOL, "dq")
-    assert_rel(dk[0, :, 7].float().cpu().numpy(), kq[1], G_TOL, "dk")
+    kq = oracle.key_head_grads(sub.wl, res)
+    m = lambda t: (wl.name, t)
+    for i, kh in enumerate(key_heads):
+        assert_rel(dq[0, :, kh].float().cpu().numpy(), kq[(0, i)][0], G_TOL, f"dq[{kh}]", m("dq"))
+        assert_rel(dk[0, :, kh].float().cpu().numpy(), kq[(0, i)][1], G_TOL, f"dk[{kh}]", m("dk"))
     for i, j in enumerate(vh):
-        assert_rel(dv[0, :, j].float().cpu().numpy(), res["dv"][i], G_TOL, f"dv[{j}]")
-        assert_rel(dg[0, :, j].cpu().numpy(), res["dg"][i], G_TOL, f"dg[{j}]")
-        assert_rel(db[0, :, j].cpu().numpy(), res["dbeta"][i], G_TOL, f"dbeta[{j}]")
-        assert_rel(dh0[0, j].cpu().numpy(), res["dh0"][i], G_TOL, f"dh0[{j}]")
+        assert_rel(dv[0, :, j].float().cpu().numpy(), res["dv"][i], G_TOL, f"dv[{j}]", m("dv"))
+        assert_rel(dg[0, :, j].cpu().numpy(), res["dg"][i], G_TOL, f"dg[{j}]", m("dg"))
+        assert_rel(db[0, :, j].cpu().numpy(), res["dbeta"][i], G_TOL, f"dbeta[{j}]", m("dbeta"))
+        assert_rel(dh0[0, j].cpu().numpy(), res["dh0"][i], G_TOL, f"dh0[{j}]", m("dh0"))
     # segment-count invariance of the backward on every head
     g1 = gdn_lib.chunk_bwd(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.h0, inp.dO, inp.dhT,
                            n_segments=1)
@@ -86,4 +89,4 @@ def test_long_sequence_backward_148_segments(gdn_lib):
 @pytest.mark.parametrize("name", ["million_t1048576", "million_t1048576_slow"])
 def test_million_token_forward_148_segments(gdn_lib, name):
     wl = WORKLOADS[name]
-    _fwd_check(gdn_lib, wl, [0, 15])
+    _fwd_check(gdn_lib, wl, [0, 5, 10, 15])

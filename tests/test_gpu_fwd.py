@@ -11,7 +11,7 @@ import torch
 import oracle
 from oracle import chunked
 from linear_attention_rnn_gb300.inputs import WORKLOADS, make_host
-from conftest import as64, assert_rel, from_arrays, head, key_head_slice, random_small
+from conftest import as64, assert_rel, from_arrays, head, key_head_slice, random_small, record_margin
 
 pytestmark = pytest.mark.gpu
 
@@ -22,7 +22,10 @@ def _cuda(inp):
     return inp.to("cuda")
 
 
-def _check_fwd(gdn, inp, n_segments=0, heads=None):
+def _check_fwd(gdn, inp, n_segments=0, heads=None, record=False):
+    """Device forward against the oracle on the given (b, j) heads (default:
+    all); record=True enters the errors in the margin table under the
+    workload's name."""
     d = _cuda(inp)
     o, hT = gdn.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=n_segments)
     torch.cuda.synchronize()
@@ -30,19 +33,28 @@ def _check_fwd(gdn, inp, n_segments=0, heads=None):
     hT = hT.cpu().numpy()
     heads = heads or [(b, j) for b in range(inp.wl.B) for j in range(inp.wl.Hv)]
     ro, rh = oracle.fwd(inp, heads=heads)
-    eo = max(assert_rel(o[b, :, j], ro[i], O_TOL, f"o[{b},{j}]") for i, (b, j) in enumerate(heads))
-    eh = max(assert_rel(hT[b, j], rh[i], H_TOL, f"hT[{b},{j}]") for i, (b, j) in enumerate(heads))
+    mo = (inp.wl.name, "o") if record else None
+    mh = (inp.wl.name, "hT") if record else None
+    eo = max(assert_rel(o[b, :, j], ro[i], O_TOL, f"o[{b},{j}]", mo) for i, (b, j) in enumerate(heads))
+    eh = max(assert_rel(hT[b, j], rh[i], H_TOL, f"hT[{b},{j}]", mh) for i, (b, j) in enumerate(heads))
     return eo, eh
 
 
 def test_tiny_workload(gdn_lib):
     inp = make_host(WORKLOADS["tiny_t1024"])
-    _check_fwd(gdn_lib, inp)
+    _check_fwd(gdn_lib, inp, record=True)
 
 
 def test_layer_workload_all_heads(gdn_lib):
     inp = make_host(WORKLOADS["layer_t4096"], backward=False)
-    _check_fwd(gdn_lib, inp)
+    _check_fwd(gdn_lib, inp, record=True)
+
+
+def test_batched_workload_fwd(gdn_lib):
+    """B=2, T=8192, 16 key heads shared by 32 value heads: o and hT of every
+    value head of both batch rows against the oracle."""
+    inp = make_host(WORKLOADS["batched_b2_t8192"], backward=False)
+    _check_fwd(gdn_lib, inp, record=True)
 
 
 @pytest.mark.parametrize("T", [1, 5, 127, 128, 129, 300, 1000])
@@ -136,7 +148,7 @@ def test_ut_intermediates_and_ladder_residual(gdn_lib, name):
     S, T, w, u = gdn_lib.debug_ut(d.k, d.v, d.g, d.beta)
     torch.cuda.synchronize()
     S, T, w, u = (x.float().cpu().numpy() for x in (S, T, w, u))
-    heads = [(0, 0), (0, wl.Hv - 1)] if wl.Hv > 2 else [(0, j) for j in range(wl.Hv)]
+    heads = [(b, j) for b in range(wl.B) for j in range(wl.Hv)]  # every chunk of every head
     I = np.eye(128)
     worst = 0.0
     for b, j in heads:
@@ -146,12 +158,13 @@ def test_ut_intermediates_and_ladder_residual(gdn_lib, name):
             it = chunked.chunk_intermediates(q[sl], k[sl], v[sl], g[sl], beta[sl])
             # fp32 gates: G reaches ~ -170 over a chunk here, so G_r - G_s keeps
             # ~1e-5 relative accuracy after cancellation (fp32 cumsum)
-            assert_rel(S[b, j, c], it["S"], 1e-4, f"S[{b},{j},{c}]")
+            assert_rel(S[b, j, c], it["S"], 1e-4, f"S[{b},{j},{c}]", (name, "S (per chunk)"))
             res = np.max(np.abs((I + it["S"]) @ T[b, j, c].astype(np.float64) - I))
             worst = max(worst, res)
             assert res <= RES_TOL, f"ladder residual {res:.2e} at {(b, j, c)}"
-            assert_rel(w[b, j, c], it["w"], 1e-2, "w")
-            assert_rel(u[b, j, c], it["u"], 1e-2, "u")
+            assert_rel(w[b, j, c], it["w"], 1e-2, "w", (name, "w (per chunk)"))
+            assert_rel(u[b, j, c], it["u"], 1e-2, "u", (name, "u (per chunk)"))
+    record_margin(name, "ladder residual max|(I+S)T - I|", worst, RES_TOL)
     assert worst <= RES_TOL
 
 
@@ -225,3 +238,46 @@ def test_segment_negative_control_on_device_states(gdn_lib):
     dev = o[0, :, 0].float().cpu().numpy()
     assert_rel(dev, ro[0], O_TOL, "segmented o")
     assert np.max(np.abs(bad - ro[0])) > O_TOL * np.max(np.abs(ro[0]))
+
+
+# ------------------------------------------------------------ segment fold
+@pytest.mark.parametrize("S", [1, 2, 5])
+def test_segment_fold_matches_oracle(gdn_lib, S):
+    """gdn_segment_fold returns each segment's composed chunk maps (A_s, B_s):
+    against the oracle's pass-1 fold, and, for one segment, against the
+    per-token rule (A h0 + B is the final state from h0)."""
+    wl = WORKLOADS["tiny_t1024"].replace(T=5 * 128 + 37, Hk=1, Hv=2, gate_shift=-4.0,
+                                         h0_std=0.5, seed=15)
+    inp = make_host(wl)
+    d = _cuda(inp)
+    A, Bm = gdn_lib.segment_fold(d.k, d.v, d.g, d.beta, S)
+    torch.cuda.synchronize()
+    A, Bm = A.cpu().numpy(), Bm.cpu().numpy()
+    for j in range(wl.Hv):
+        pairs = chunked.head_fwd_segmented(*head(inp, 0, j), 128, S)[2]
+        for s, (rA, rB) in enumerate(pairs):
+            assert_rel(A[0, j, s], rA, H_TOL, f"A[{j},{s}]", ("segment fold", "A_s"))
+            assert_rel(Bm[0, j, s], rB, H_TOL, f"B[{j},{s}]", ("segment fold", "B_s"))
+    if S == 1:
+        _, rh = oracle.fwd(inp)
+        h0 = as64(inp, "h0")[0]
+        for j in range(wl.Hv):
+            assert_rel(A[0, j, 0].astype(np.float64) @ h0[j] + Bm[0, j, 0], rh[j], H_TOL,
+                       f"A h0 + B vs per-token hT[{j}]")
+
+
+def test_segment_fold_without_A_and_empty(gdn_lib):
+    wl = WORKLOADS["tiny_t1024"].replace(T=300, Hk=1, Hv=2, gate_shift=-4.0, seed=16)
+    inp = make_host(wl)
+    d = _cuda(inp)
+    A1, B1 = gdn_lib.segment_fold(d.k, d.v, d.g, d.beta, 2)
+    A0, B0 = gdn_lib.segment_fold(d.k, d.v, d.g, d.beta, 2, want_A=False)
+    assert A0 is None
+    assert torch.equal(B0, B1)
+    e = make_host(wl.replace(T=0))
+    de = _cuda(e)
+    Ae, Be = gdn_lib.segment_fold(de.k, de.v, de.g, de.beta, 1)
+    assert torch.equal(Ae[0, 0, 0].cpu(), torch.eye(128))
+    assert torch.count_nonzero(Be) == 0
+    with pytest.raises(gdn_lib.GDNError):
+        gdn_lib.segment_fold(d.k, d.v, d.g, d.beta, 4)  # more segments than the 3 chunks

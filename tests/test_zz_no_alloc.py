@@ -6,7 +6,9 @@ locked its device memory at start-up, or a plug-in whose host framework owns
 all device memory.  Its scratch is a fixed array inside the library, shared by
 every call and never cleared, so these tests call it twice in a row with
 different inputs and sizes and compare each result with the ordinary
-gdn_chunk_fwd (which uses a caller workspace), through the C ABI.
+gdn_chunk_fwd (which uses a caller workspace), through the C ABI: the two run
+the same deterministic kernels, so their outputs must be equal bit for bit;
+each result is also checked against the fp64 oracle.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
@@ -16,6 +18,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from linear_attention_rnn_gb300.inputs import WORKLOADS, make_host
 from conftest import assert_rel
 
@@ -51,12 +54,22 @@ def test_noalloc_forward_matches_workspace_forward_twice(gdn_lib):
                                         seed=42),
     ]
     for wl in cases:  # two calls in a row; the second finds the first one's scratch
-        d = make_host(wl).to("cuda")
+        host = make_host(wl)
+        d = host.to("cuda")
         o1, h1 = _call(gdn_lib, f, d)
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        assert gdn_lib.lib().gdn_noalloc_status(stream) == 0  # no bounded wait gave up
         o2, h2 = gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=1)
         torch.cuda.synchronize()
-        assert_rel(o1.float().cpu().numpy(), o2.float().cpu().numpy(), O_TOL, "o (no-alloc)")
-        assert_rel(h1.cpu().numpy(), h2.cpu().numpy(), H_TOL, "hT (no-alloc)")
+        assert torch.equal(o1, o2), "o (no-alloc) differs from the workspace forward"
+        assert torch.equal(h1, h2), "hT (no-alloc) differs from the workspace forward"
+        ro, rh = oracle.fwd(host)
+        o1, h1 = o1.float().cpu().numpy(), h1.cpu().numpy()
+        for b in range(wl.B):
+            for j in range(wl.Hv):
+                i = b * wl.Hv + j
+                assert_rel(o1[b, :, j], ro[i], O_TOL, f"o[{b},{j}] (no-alloc)")
+                assert_rel(h1[b, j], rh[i], H_TOL, f"hT[{b},{j}] (no-alloc)")
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(gdn_lib):
