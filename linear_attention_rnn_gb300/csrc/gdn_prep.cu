@@ -48,12 +48,12 @@ constexpr int PT = 512, PW = PT / 32;  // 16 warps: an epilogue thread owns 32 c
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct PrepSmem {
-  unsigned char Q[TILE];   // SW128 [s][d]: Q; after Q K^T, V of the odd value heads
-  unsigned char K[TILE];   // SW128 [s][d]
-  unsigned char V[TILE];   // SW128 [s][v]: V of the even value heads
+  unsigned char A[3][TILE];  // SW128 [s][d] tiles: K of the key head and V of two value heads,
+                             // the roles rotating from one key-head group to the next
   unsigned char Kg[TILE];  // SW128: P staging; T'' = T diag(beta gamma) [r][s]; w staging
   unsigned char Tp[TILE];  // SW128 [r][s]: T diag(beta); during the inverse its scratch
-  bf16 Fh[CH * CH];        // S, overwritten in place by T: high parts (XOR-swizzled rows)
+  bf16 Fh[CH * CH];        // S, overwritten in place by T: high parts (XOR-swizzled rows);
+                           // at a group's start, its Q (SW128) until Q K^T has read it
   bf16 Fl[CH * CH];        // low parts
   float Gl[CH], beta[CH];
   float etab[CH];  // exp2(Gl[c0] - Gl[s]) for the 16-column block c0 of column s
@@ -237,13 +237,15 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
   struct Unit {
     int b, c, kh, jj;
   };
-  auto decode = [&](long u) {
+  auto decode = [&](long u) {  // 32-bit arithmetic: the unit count is below 2^31
     Unit x;
-    x.jj = (int)(u % group);
-    const long gidx = u / group;
-    x.kh = (int)(gidx % a.Hk);
-    x.c = (int)((gidx / a.Hk) % a.NC);
-    x.b = (int)(gidx / ((long)a.Hk * a.NC));
+    const int uu = (int)u;
+    x.jj = uu % group;
+    const int gidx = uu / group;
+    x.kh = gidx % a.Hk;
+    const int ci = gidx / a.Hk;
+    x.c = ci % a.NC;
+    x.b = ci / a.NC;
     return x;
   };
 
@@ -279,42 +281,62 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
   };
   float g_next = 0.f, b_next = 0.f;
   load_gates(u_begin, g_next, b_next);
+  unsigned char* const qbuf = reinterpret_cast<unsigned char*>(sm.Fh);
+  // K and Q of the key-head group (b, c, kh): K into tile kbuf, Q into the Fh region
+  auto load_kq = [&](int bb, int cc, int kk, unsigned char* kdst) {
+    tc::arrive_expect_tx(&sm.barKQ, needP ? 2 * TILE : TILE);
+    tc::tma_load_4d(kdst, &mp.k, 0, kk, cc * CH, bb, &sm.barKQ);
+    tc::tma_load_4d(kdst + TILE / 2, &mp.k, 64, kk, cc * CH, bb, &sm.barKQ);
+    if (needP) {
+      tc::tma_load_4d(qbuf, &mp.q, 0, kk, cc * CH, bb, &sm.barKQ);
+      tc::tma_load_4d(qbuf + TILE / 2, &mp.q, 64, kk, cc * CH, bb, &sm.barKQ);
+    }
+  };
+  // V of value head j of (b, c) into tile dst, on barV[parity]
+  auto load_v_to = [&](int bb, int cc, int j, unsigned char* dst, int parity) {
+    uint64_t* bar = &sm.barV[parity];
+    tc::arrive_expect_tx(bar, TILE);
+    tc::tma_load_4d(dst, &mp.v, 0, j, cc * CH, bb, bar);
+    tc::tma_load_4d(dst + TILE / 2, &mp.v, 64, j, cc * CH, bb, bar);
+  };
+  // Roles of the three tiles: K of the group in A[kb], V of the group's value
+  // heads of even / odd position in A[vbi[0]] / A[vbi[1]].  During the last
+  // value head of a group, the tile its predecessor's V used is free: the next
+  // group's K goes there (and its Q into the Fh region once the inverse has
+  // released it), so the next group starts with its K and Q already loaded;
+  // its first two V go into the tiles the current group's K and last V held.
+  int kb = 1, vbi[2] = {2, 0};
+  bool next_loaded = false;     // K, Q (and the first V) of the next group already requested
+  const int loader = 32;        // warp 1, lane 0: requests loads while thread 0 issues products
 
   for (long ug = u_begin; ug < u_end;) {
     // ---- a key-head group: value heads jj0 .. jj1 - 1 of (b, c, kh) -------------------
     const Unit x0 = decode(ug);
     const int c = x0.c, kh = x0.kh, b = x0.b, jj0 = x0.jj;
     const int jj1 = (int)min((long)group, jj0 + (u_end - ug));
-    const int t0 = c * CH;
-    // V of value head kh * group + jj, the k-th head of the group, into buffer k % 2 (thread 0)
+    // V of value head kh * group + jj, the k-th head of the group, into its buffer
     auto load_v = [&](int jj) {
       const int k = jj - jj0;
-      unsigned char* dst = (k & 1) ? sm.Q : sm.V;
-      uint64_t* bar = &sm.barV[k & 1];
-      tc::arrive_expect_tx(bar, TILE);
-      tc::tma_load_4d(dst, &mp.v, 0, kh * group + jj, t0, b, bar);
-      tc::tma_load_4d(dst + TILE / 2, &mp.v, 64, kh * group + jj, t0, b, bar);
+      load_v_to(b, c, kh * group + jj, sm.A[vbi[k & 1]], k & 1);
     };
-    // K, Q and the first V; the previous group's products have completed and
-    // every thread has passed the barrier after them, so the buffers are free
+    // the next group of this CTA's range (valid if ug + jj1 - jj0 < u_end)
+    const long ug_next = ug + (jj1 - jj0);
+    const Unit xn = decode(ug_next < u_end ? ug_next : ug);
     if (tid == 0) {
-      tc::arrive_expect_tx(&sm.barKQ, needP ? 2 * TILE : TILE);
-      tc::tma_load_4d(sm.K, &mp.k, 0, kh, t0, b, &sm.barKQ);
-      tc::tma_load_4d(sm.K + TILE / 2, &mp.k, 64, kh, t0, b, &sm.barKQ);
-      if (needP) {
-        tc::tma_load_4d(sm.Q, &mp.q, 0, kh, t0, b, &sm.barKQ);
-        tc::tma_load_4d(sm.Q + TILE / 2, &mp.q, 64, kh, t0, b, &sm.barKQ);
-      }
-      if (needU) {
-        load_v(jj0);
-        if (jj0 + 1 < jj1 && !needP) load_v(jj0 + 1);  // the Q buffer is not needed
+      if (!next_loaded) {  // the first group of the range
+        load_kq(b, c, kh, sm.A[kb]);
+        if (needU) {
+          load_v(jj0);
+          if (jj0 + 1 < jj1) load_v(jj0 + 1);
+        }
       }
       ok = ok && tc::mbar_wait(&sm.barKQ, (uint32_t)(kq_uses & 1));
       tc::fence_after();
-      tc::gemm_k128(tmem + 0, smem_u32(sm.K), smem_u32(sm.K), 128, false);
-      if (needP) tc::gemm_k128(tmem + 128, smem_u32(sm.Q), smem_u32(sm.K), 128, false);
+      tc::gemm_k128(tmem + 0, smem_u32(sm.A[kb]), smem_u32(sm.A[kb]), 128, false);
+      if (needP) tc::gemm_k128(tmem + 128, smem_u32(qbuf), smem_u32(sm.A[kb]), 128, false);
       tc::commit(&sm.barM);
     }
+    next_loaded = false;
 
     for (int jj = jj0; jj < jj1; ++jj) {
       const int j = kh * group + jj;
@@ -353,13 +375,8 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
         mphase ^= 1;
         tc::fence_after();
       }
-      if (tid == 0 && needU) {  // prefetch V of the next value head into the free buffer
-        if (jj == jj0) {
-          if (jj0 + 1 < jj1 && needP) load_v(jj0 + 1);  // Q K^T has read Q
-        } else if (jj + 1 < jj1) {
-          load_v(jj + 1);  // its buffer held V of head jj - 1, whose u is complete
-        }
-      }
+      if (tid == 0 && needU && jj > jj0 && jj + 1 < jj1)
+        load_v(jj + 1);  // its buffer held V of head jj - 1, whose u is complete
       __syncthreads();
 
       // ---- S (hi/lo into F, fp32 diagonal blocks into Sd) and P (bf16 staging in Kg) ----
@@ -501,20 +518,37 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       __syncthreads();
       tc::fence_after();
       // ---- u = T' V,  w = T'' K -----------------------------------------------------------
+      // the last value head of a group that has a successor in this CTA's range
+      const bool last = (jj + 1 == jj1) && ug_next < u_end;
       if (tid == 0) {
         if (needU) {
           ok = ok && tc::mbar_wait(&sm.barV[vb], (vb ? v_use1 : v_use0) & 1u);
           tc::fence_after();
-          tc::gemm_bmn_k128(tmem + 384, smem_u32(sm.Tp), smem_u32(vb ? sm.Q : sm.V), false);
+          tc::gemm_bmn_k128(tmem + 384, smem_u32(sm.Tp), smem_u32(sm.A[vbi[vb]]), false);
         }
-        if (needW) tc::gemm_bmn_k128(tmem + 256, smem_u32(sm.Kg), smem_u32(sm.K), false);
+        if (needW) tc::gemm_bmn_k128(tmem + 256, smem_u32(sm.Kg), smem_u32(sm.A[kb]), false);
         if (needU || needW) tc::commit(&sm.barM);
       }
+      // the next group's K into the tile no V of this group needs any more, its Q
+      // into the Fh region (the T' / T'' build has read it), while the products run
+      if (tid == loader && last) load_kq(xn.b, xn.c, xn.kh, sm.A[vbi[(jj1 - jj0) & 1]]);
       if (needU) (vb ? v_use1 : v_use0) += 1;
       if (needU || needW) {
         ok = ok && tc::mbar_wait(&sm.barM, mphase);
         mphase ^= 1;
         tc::fence_after();
+      }
+      if (last) {  // the products have read this group's K and last V: the next group's V go there
+        if (tid == loader && needU) {
+          const int jj1n = (int)min((long)group, xn.jj + (u_end - ug_next));
+          load_v_to(xn.b, xn.c, xn.kh * group + xn.jj, sm.A[kb], 0);
+          if (xn.jj + 1 < jj1n) load_v_to(xn.b, xn.c, xn.kh * group + xn.jj + 1, sm.A[vbi[vb]], 1);
+        }
+        const int kb_next = vbi[(jj1 - jj0) & 1];
+        vbi[1] = vbi[vb];
+        vbi[0] = kb;
+        kb = kb_next;
+        next_loaded = true;
       }
       // ---- w and u leave through shared staging tiles and TMA stores ------------------
       // (T'' and T' are dead now; their buffers hold w and u)
