@@ -7,7 +7,9 @@ h0 ~ N(0, 0.1^2), g = -softplus(N(0,1) + 1), cotangents dO ~ N(0,1),
 dhT ~ N(0, 0.1^2)), and the fraction of the binding roofline.
 
 A step is one forward (o, hT) plus one backward (dq, dk, dv, dg, dbeta,
-dh0) over one batch.  Inputs are resident in HBM; L2 is flushed (a 512 MiB
+dh0) over one batch; the forward keeps its per-chunk w, u, P and T for the
+backward (as a training step's autograd would), so the backward runs no
+preparation of its own.  Inputs are resident in HBM; L2 is flushed (a 512 MiB
 write) before every timed step, outside the step's events.  Each rank runs
 the same per-GPU workload (weak scaling, no collective on the data path).
 
@@ -42,9 +44,10 @@ FLOPS = {  # per (chunk, value head), per kernel
 }
 FLOPS["walks"] = FLOPS["walk_states"] + FLOPS["walk_bwd"]  # both walks of the backward, one launch
 FWD_KERNELS = ["prep", "walk"]
-BWD_KERNELS = ["prep", "walks", "grads"]
 FWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk"]
-BWD_KERNELS_SEG = ["prep", "fold", "prefix", "fold_bwd", "prefix_bwd", "walks", "grads"]
+# the backward of a step reads the w, u, P and T the forward kept (no preparation)
+BWD_KERNELS = ["walks", "grads"]
+BWD_KERNELS_SEG = ["fold", "prefix", "fold_bwd", "prefix_bwd", "walks", "grads"]
 KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 0, 32>", "walks": "k_walk_pair", "grads": "k_grads",
                  "fold": "k_walk_fwd<1, 0, 32>", "prefix": "k_affine_walk",
                  "fold_bwd": "k_walk_bwd<1, 32>", "prefix_bwd": "k_affine_walk"}
@@ -66,8 +69,9 @@ def algorithmic(wl):
     bwd_bytes = qk + vv + gb + st + vv + st + qk + vv + gb + st  # + dO dhT; dq dk dv dg dbeta dh0
     units, kunits = B * Hv * NC, B * Hk * NC
     fwd_flops = kunits * FLOP_PER_CHUNK_KHEAD + units * (FLOPS["prep"] + FLOPS["walk"])
-    bwd_flops = (kunits * FLOP_PER_CHUNK_KHEAD + units * (FLOPS["prep"] + FLOPS["walk_states"]
-                 + FLOPS["walk_bwd"] + FLOPS["grads"]))
+    # the backward takes w, u, P and T from the forward: the states' recompute,
+    # the reverse walk and the chunk gradients
+    bwd_flops = units * (FLOPS["walk_states"] + FLOPS["walk_bwd"] + FLOPS["grads"])
     return dict(fwd_bytes=fwd_bytes, bwd_bytes=bwd_bytes, fwd_flops=fwd_flops,
                 bwd_flops=bwd_flops, units=units, kunits=kunits)
 
@@ -157,6 +161,73 @@ class ClockSampler:
                 "samples": len(win), "window": note}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (ctypes, read-only
+    queries) every millisecond, so that a timed region of a few milliseconds is
+    still sampled many times.  Falls back silently when NVML is unavailable."""
+    # clock-event reason bits (nvml.h): SW power cap, HW slowdown, SW thermal, HW thermal
+    BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, gpu_index, period_s=0.001):
+        self.samples = []
+        self.gpu = gpu_index
+        self.period = period_s
+        self.thread = None
+        self.stop_flag = threading.Event()
+        self.lib = None
+        self.handle = None
+        self.max_mhz = None
+
+    def start(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        except (OSError, AttributeError):
+            return
+        self.lib, self.handle = lib, h
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _run(self):
+        import ctypes
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            t = time.time()
+            if self.lib.nvmlDeviceGetClockInfo(self.handle, ctypes.c_int(1), ctypes.byref(clk)) == 0:
+                r = None
+                if self.reasons_fn is not None and self.reasons_fn(self.handle, ctypes.byref(rs)) == 0:
+                    r = int(rs.value)
+                self.samples.append((t, float(clk.value), r))
+            time.sleep(self.period)
+
+    def stop(self):
+        self.stop_flag.set()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        win = [x for x in self.samples if t0 <= x[0] <= t1]
+        if not win:
+            return None
+        reasons = sorted({name for (_, _, r) in win if r is not None
+                          for bit, name in self.BITS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for (_, m, _) in win), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(win),
+                "window": "timed window, NVML every 1 ms"}
+
+
 # ---------------------------------------------------------------- our arm
 def kernel_table(kern, alg, pk, mean_step):
     """Per-kernel lines (mean ms per launch from CUDA events, share of the step,
@@ -217,6 +288,7 @@ def run_ours(args, rank, world, local_rank):
                        dtype=torch.uint8, device=dev)
     ws_b = torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
                        dtype=torch.uint8, device=dev)
+    sv = torch.empty(gdn.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     fk = FWD_KERNELS if nseg == 1 else FWD_KERNELS_SEG
     bk = BWD_KERNELS if nseg == 1 else BWD_KERNELS_SEG
@@ -235,13 +307,15 @@ def run_ours(args, rank, world, local_rank):
 
     def step(i=None):
         o, hT = gdn.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=nseg, workspace=ws_f,
-                              events=None if i is None else fev[i])
+                              events=None if i is None else fev[i], saved=sv)
         gr = gdn.chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.dO, d.dhT, n_segments=nseg,
-                           workspace=ws_b, events=None if i is None else bev[i])
+                           workspace=ws_b, events=None if i is None else bev[i], saved=sv)
         return o, hT, gr
 
     sampler = ClockSampler(local_rank)
     sampler.start()
+    fast = NvmlSampler(local_rank)
+    fast.start()
     # warm-up: at least W steps and at least ~1 s of device work
     t_w = time.time()
     n_w = 0
@@ -267,6 +341,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.stop()
+    fast.stop()
 
     step_ms = [starts[i].elapsed_time(bev[i][-1]) for i in range(K)]
     fwd_ms = [starts[i].elapsed_time(fev[i][-1]) for i in range(K)]
@@ -306,7 +381,8 @@ def run_ours(args, rank, world, local_rank):
                 "algorithmic_bytes": bytes_, "algorithmic_flops": flops}
 
     kernels, roofline = kernel_table(kern, alg, pk, mean_step)
-    clocks = sampler.summary(t0, t1)
+    clocks = fast.summary(t0, t1) or sampler.summary(t0, t1)
+    clocks["nvidia_smi"] = {k: v for k, v in sampler.summary(t0, t1).items() if k != "window"}
     out = {
         "metric": "GDN chunk fwd+bwd tokens/s (T=4096, H_v=32, d=128) and % of roofline",
         "value": round(value, 1),
@@ -394,6 +470,8 @@ def run_e2e(args, gdn, wl, host, dev, nseg):
                         dtype=torch.uint8, device=dev) for _ in range(2)]
     ws_b = [torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
                         dtype=torch.uint8, device=dev) for _ in range(2)]
+    svs = [torch.empty(gdn.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv), dtype=torch.uint8, device=dev)
+           for _ in range(2)]
     s_up, s_run, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
     ev = lambda: torch.cuda.Event()  # noqa: E731
     up_done, run_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
@@ -411,9 +489,9 @@ def run_e2e(args, gdn, wl, host, dev, nseg):
                 s_run.wait_event(down_done[k])  # step i-2's results have left dout[k]
             x, y = din[k].views, dout[k].views
             gdn.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], n_segments=nseg,
-                          o=y["o"], hT=y["hT"], workspace=ws_f[k])
+                          o=y["o"], hT=y["hT"], workspace=ws_f[k], saved=svs[k])
             gdn.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], x["dO"], x["dhT"],
-                          n_segments=nseg, workspace=ws_b[k],
+                          n_segments=nseg, workspace=ws_b[k], saved=svs[k],
                           out=(y["dq"], y["dk"], y["dv"], y["dg"], y["dbeta"], y["dh0"]))
             run_done[k].record(s_run)
         with torch.cuda.stream(s_down):
@@ -557,6 +635,8 @@ def run_sweep(args):
                            dtype=torch.uint8, device=dev)
         ws_b = (torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
                             dtype=torch.uint8, device=dev) if bwd else None)
+        sv = (torch.empty(gdn.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv), dtype=torch.uint8, device=dev)
+              if bwd else None)
         fk = FWD_KERNELS if nseg == 1 else FWD_KERNELS_SEG
         bk = BWD_KERNELS if nseg == 1 else BWD_KERNELS_SEG
 
@@ -571,10 +651,10 @@ def run_sweep(args):
 
         def step(i=None):
             gdn.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=nseg, workspace=ws_f,
-                          events=None if i is None else fev[i])
+                          events=None if i is None else fev[i], saved=sv)
             if bwd:
                 gdn.chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.dO, d.dhT, n_segments=nseg,
-                              workspace=ws_b, events=None if i is None else bev[i])
+                              workspace=ws_b, events=None if i is None else bev[i], saved=sv)
         for _ in range(2 if big else 5):
             flush.zero_()
             step()
@@ -629,7 +709,7 @@ def run_sweep(args):
                                     f"{ts} tokens, {'fwd+bwd' if bwd else 'fwd'}, {dt:.1f} s; "
                                     f"rate scaled by 1/{wl.Hk}"}
         print(json.dumps(line), flush=True)
-        del d, ws_f, ws_b
+        del d, ws_f, ws_b, sv
         torch.cuda.empty_cache()
 
 

@@ -120,6 +120,41 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   size_t ws_bytes, void* stream);
 
 /*
+ * Keeping the forward's per-chunk quantities for the backward.  The backward
+ * needs, per chunk, the forward's w, u, P and the UT inverse T; gdn_chunk_bwd
+ * recomputes them (one launch of the preparation).  A training step that runs
+ * the backward of the same inputs right after the forward can instead let the
+ * forward keep them in a caller buffer `saved` of gdn_saved_bytes bytes (w, u,
+ * P and T, bf16, [B, Hv, ceil(T/chunk), 128, 128] each) and pass it to the
+ * backward, which then skips the preparation.  The pages' own fused kernel
+ * keeps the inverse for its backward in the same way (PR "Fuse the Gated
+ * Delta Net inter-chunk scan into a Pallas TPU kernel", section "Changes":
+ * the backward's analytic inverse gradient takes T from the forward).
+ *
+ * gdn_chunk_fwd_ex / gdn_chunk_bwd_ex are gdn_chunk_fwd / gdn_chunk_bwd (and,
+ * with events, their timing variants) with that buffer: saved = NULL gives
+ * exactly the plain calls; otherwise the forward writes w, u, P, T into it and
+ * the backward reads them there, and must be given the forward's inputs
+ * unchanged (q, k, v, g, beta, B, T, Hk, Hv).  Results are identical to the
+ * plain calls'.  saved is 16-byte aligned; a smaller saved_bytes than
+ * gdn_saved_bytes gives GDN_ERR_WORKSPACE.  Launch order of the backward with
+ * a saved buffer: walks (or fold, prefix, reverse fold, reverse prefix, walks
+ * with segments), gradients -- no preparation.
+ */
+size_t gdn_saved_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk);
+int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                     const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                     int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* saved,
+                     size_t saved_bytes, void* ws, size_t ws_bytes, void* stream,
+                     void* const* events, int n_events);
+int gdn_chunk_bwd_ex(const void* q, const void* k, const void* v, const float* g,
+                     const float* beta, const float* h0, const void* dO, const float* dhT,
+                     void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0, int B,
+                     int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments,
+                     const void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                     void* stream, void* const* events, int n_events);
+
+/*
  * One GatedDeltaNet layer's use of the rule, with the element-wise operations
  * around it (PR "Shard the GatedDeltaNet sequence under
  * ici_context_parallelism", description: the layer's "qkvz" activations

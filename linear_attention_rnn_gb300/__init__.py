@@ -72,6 +72,12 @@ def lib():
         L.gdn_chunk_fwd_timed.restype = I
         L.gdn_chunk_bwd_timed.argtypes = [P] * 14 + [I] * 8 + [P, Z, P, P, I]
         L.gdn_chunk_bwd_timed.restype = I
+        L.gdn_saved_bytes.argtypes = [I] * 7
+        L.gdn_saved_bytes.restype = Z
+        L.gdn_chunk_fwd_ex.argtypes = [P] * 8 + [I] * 8 + [P, Z, P, Z, P, P, I]
+        L.gdn_chunk_fwd_ex.restype = I
+        L.gdn_chunk_bwd_ex.argtypes = [P] * 14 + [I] * 8 + [P, Z, P, Z, P, P, I]
+        L.gdn_chunk_bwd_ex.restype = I
         L.gdn_affine_compose.argtypes = [P] * 4 + [I] * 4 + [P]
         L.gdn_affine_compose.restype = I
         L.gdn_debug_ut.argtypes = [P] * 8 + [I] * 7 + [P]
@@ -142,6 +148,11 @@ def bwd_workspace_bytes(B, T, Hk, Hv, dk=128, dv=128, chunk=128, n_segments=0) -
     return int(lib().gdn_bwd_workspace_bytes(B, T, Hk, Hv, dk, dv, chunk, n_segments))
 
 
+def saved_bytes(B, T, Hk, Hv, dk=128, dv=128, chunk=128) -> int:
+    """Bytes of the buffer in which a forward keeps w, u, P and T for its backward."""
+    return int(lib().gdn_saved_bytes(B, T, Hk, Hv, dk, dv, chunk))
+
+
 def _events(events):
     """ctypes array of raw cudaEvent_t handles of torch.cuda.Event objects
     (each must have been recorded once, so that it exists)."""
@@ -158,10 +169,12 @@ def _workspace(nbytes, device, ws):
 
 
 def chunk_fwd(q, k, v, g, beta, h0=None, *, chunk: int = 128, n_segments: int = 0,
-              want_hT: bool = True, o=None, hT=None, workspace=None, events=None
+              want_hT: bool = True, o=None, hT=None, workspace=None, events=None, saved=None
               ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Forward of the chunked gated delta rule.  Returns (o, hT).
-    events: optional torch.cuda.Event list recorded after each kernel launch."""
+    events: optional torch.cuda.Event list recorded after each kernel launch.
+    saved: optional uint8 CUDA buffer of saved_bytes(...) bytes in which the
+    forward keeps w, u, P and T for chunk_bwd(..., saved=the same buffer)."""
     B, T, Hk, Hv, dk, dv = _dims(q, k, v, g, beta)
     dev = q.device
     _check(h0, "h0", torch.float32, (B, Hv, dk, dv))
@@ -172,6 +185,15 @@ def chunk_fwd(q, k, v, g, beta, h0=None, *, chunk: int = 128, n_segments: int = 
         hT = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=dev)
     nbytes = fwd_workspace_bytes(B, T, Hk, Hv, dk, dv, chunk, n_segments)
     ws = _workspace(nbytes, dev, workspace)
+    if saved is not None:
+        ev = _events(events) if events else (None, 0)
+        rc = lib().gdn_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                    _ptr(o), _ptr(hT), B, T, Hk, Hv, dk, dv, chunk, n_segments,
+                                    _ptr(saved), saved.numel() * saved.element_size(), _ptr(ws),
+                                    ws.numel(), _stream(dev), *ev)
+        if rc != GDN_OK:
+            raise GDNError(rc, "gdn_chunk_fwd_ex")
+        return o, hT
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(hT), B, T,
             Hk, Hv, dk, dv, chunk, n_segments, _ptr(ws), ws.numel(), _stream(dev)]
     if events:
@@ -184,7 +206,7 @@ def chunk_fwd(q, k, v, g, beta, h0=None, *, chunk: int = 128, n_segments: int = 
 
 
 def chunk_bwd(q, k, v, g, beta, h0, dO, dhT=None, *, chunk: int = 128, n_segments: int = 0,
-              want_dh0: bool = True, out=None, workspace=None, events=None):
+              want_dh0: bool = True, out=None, workspace=None, events=None, saved=None):
     """Backward of the chunked gated delta rule.
     Returns (dq, dk, dv, dg, dbeta, dh0).
     out: optional (dq, dk, dv, dg, dbeta, dh0) tensors to write (dh0 may be
@@ -212,6 +234,16 @@ def chunk_bwd(q, k, v, g, beta, h0, dO, dhT=None, *, chunk: int = 128, n_segment
         dh0 = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=dev) if want_dh0 else None
     nbytes = bwd_workspace_bytes(B, T, Hk, Hv, dk, dv, chunk, n_segments)
     ws = _workspace(nbytes, dev, workspace)
+    if saved is not None:  # w, u, P, T kept by chunk_fwd(..., saved=saved) on these inputs
+        ev = _events(events) if events else (None, 0)
+        rc = lib().gdn_chunk_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                    _ptr(dO), _ptr(dhT), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg),
+                                    _ptr(db), _ptr(dh0), B, T, Hk, Hv, dk, dv, chunk, n_segments,
+                                    _ptr(saved), saved.numel() * saved.element_size(), _ptr(ws),
+                                    ws.numel(), _stream(dev), *ev)
+        if rc != GDN_OK:
+            raise GDNError(rc, "gdn_chunk_bwd_ex")
+        return dq, dk_, dv_, dg, db, dh0
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(dO), _ptr(dhT),
             _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(db), _ptr(dh0), B, T, Hk, Hv, dk, dv,
             chunk, n_segments, _ptr(ws), ws.numel(), _stream(dev)]
@@ -355,6 +387,6 @@ def selftest_wait_timeout(limit_ns: int, status: torch.Tensor) -> int:
 
 
 __all__ = ["build", "lib", "chunk_fwd", "chunk_bwd", "layer_fwd", "layer_bwd",
-           "layer_workspace_bytes", "affine_compose", "segment_fold", "debug_ut",
+           "layer_workspace_bytes", "saved_bytes", "affine_compose", "segment_fold", "debug_ut",
            "fwd_workspace_bytes", "bwd_workspace_bytes", "default_segments", "GDNError",
            "header_functions", "workspace_status", "selftest_wait_timeout"]

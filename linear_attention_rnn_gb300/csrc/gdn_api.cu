@@ -91,6 +91,35 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
+// The per-chunk quantities of the UT/WY preparation (w, u, P and, for the
+// backward, T): in the workspace, or in a caller's buffer that a forward fills
+// and the backward of the same inputs reads instead of recomputing them.
+struct Tiles {
+  bf16 *W, *U, *P, *Tb;
+};
+
+Tiles ws_tiles(void* ws, const Layout& L) {
+  Tiles t;
+  t.W = at<bf16>(ws, L.W);
+  t.U = at<bf16>(ws, L.U);
+  t.P = at<bf16>(ws, L.P);
+  t.Tb = L.Tb ? at<bf16>(ws, L.Tb) : nullptr;
+  return t;
+}
+
+// saved buffer: w, u, P, T, each [B Hv][NC][128][128] bf16
+size_t saved_total(const Dims& d) { return 4 * up((size_t)d.BH() * d.NC * CH * HD * sizeof(bf16)); }
+
+Tiles saved_tiles(void* saved, const Dims& d) {
+  const size_t part = up((size_t)d.BH() * d.NC * CH * HD * sizeof(bf16));
+  Tiles t;
+  t.W = at<bf16>(saved, 0);
+  t.U = at<bf16>(saved, part);
+  t.P = at<bf16>(saved, 2 * part);
+  t.Tb = at<bf16>(saved, 3 * part);
+  return t;
+}
+
 // swizzle of a stored [128 x sw] bf16 walk slice: its rows are 2 sw bytes
 CUtensorMapSwizzle slice_swizzle(int sw) { return sw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B; }
 
@@ -117,15 +146,15 @@ struct Marks {
 // maps; with segments it also runs the fold and the cross-segment prefix, so
 // that the walk (launched by the caller) replays every segment from its
 // entering state.
-int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const void* q, const void* k,
-                         const float* g, const float* h0, void* o, float* hT, bf16* states,
-                         bf16* delta, int gate_logits, cudaStream_t s, Marks& mk, WalkFwdArgs& w,
-                         WalkFwdMaps& mp) {
+int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const Tiles& tl, const void* q,
+                         const void* k, const float* g, const float* h0, void* o, float* hT,
+                         bf16* states, bf16* delta, int gate_logits, cudaStream_t s, Marks& mk,
+                         WalkFwdArgs& w, WalkFwdMaps& mp) {
   memset(&w, 0, sizeof w);
   w.gate_logits = gate_logits;
-  w.W = at<bf16>(ws, Lw.W);
-  w.U = at<bf16>(ws, Lw.U);
-  w.P = at<bf16>(ws, Lw.P);
+  w.W = tl.W;
+  w.U = tl.U;
+  w.P = tl.P;
   w.q = static_cast<const bf16*>(q);
   w.k = static_cast<const bf16*>(k);
   w.g = g;
@@ -227,12 +256,12 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
                     const float* beta, const float* h0, void* o, float* hT, int B, int T, int Hk,
                     int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
                     size_t ws_bytes, void* stream, void* const* events, int n_events,
-                    int gate_logits = 0) {
+                    int gate_logits = 0, void* saved = nullptr, size_t saved_bytes = 0) {
   int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
   if (rc) return rc;
   const long tokens = (long)B * T;
   if (tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_ARG;
-  const void* ptrs[] = {q, k, v, g, beta, h0, o, hT, ws};
+  const void* ptrs[] = {q, k, v, g, beta, h0, o, hT, ws, saved};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return GDN_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -246,8 +275,11 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   }
   const Layout L = layout(d, false);
   if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  if (saved && saved_bytes < saved_total(d)) return GDN_ERR_WORKSPACE;
   Marks mk = {events, n_events, 0, s};
   if ((rc = cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), s)))) return rc;
+  // with a saved buffer, prep's w, u and P go there, and T beside them, for the backward
+  const Tiles tl = saved ? saved_tiles(saved, d) : ws_tiles(ws, L);
 
   PrepArgs p;
   memset(&p, 0, sizeof p);
@@ -256,9 +288,10 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   p.v = static_cast<const bf16*>(v);
   p.g = g;
   p.beta = beta;
-  p.W = at<bf16>(ws, L.W);
-  p.U = at<bf16>(ws, L.U);
-  p.P = at<bf16>(ws, L.P);
+  p.W = tl.W;
+  p.U = tl.U;
+  p.P = tl.P;
+  p.Tb = saved ? tl.Tb : nullptr;
   p.status = at<int>(ws, L.status);
   p.gate_logits = gate_logits;
   p.B = B;
@@ -270,8 +303,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   if (rc || (rc = mk.rec())) return rc;
   WalkFwdArgs w;
   WalkFwdMaps mp;
-  if ((rc = prepare_forward_walk(d, L, ws, q, k, g, h0, o, hT, nullptr, nullptr, gate_logits, s, mk, w,
-                                 mp)))
+  if ((rc = prepare_forward_walk(d, L, ws, tl, q, k, g, h0, o, hT, nullptr, nullptr, gate_logits, s, mk,
+                                 w, mp)))
     return rc;
   if ((rc = cuda_status(launch_walk_fwd(w, mp, 0, s)))) return rc;
   return mk.rec();
@@ -282,13 +315,13 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
                     void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0, int B,
                     int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
                     size_t ws_bytes, void* stream, void* const* events, int n_events,
-                    int gate_logits = 0) {
+                    int gate_logits = 0, const void* saved = nullptr, size_t saved_bytes = 0) {
   int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
   if (rc) return rc;
   const long tokens = (long)B * T;
   if (tokens > 0 && (!q || !k || !v || !g || !beta || !dO || !dq || !dk || !dv || !dg || !dbeta))
     return GDN_ERR_ARG;
-  const void* ptrs[] = {q, k, v, g, beta, h0, dO, dhT, dq, dk, dv, dg, dbeta, dh0, ws};
+  const void* ptrs[] = {q, k, v, g, beta, h0, dO, dhT, dq, dk, dv, dg, dbeta, dh0, ws, saved};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return GDN_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -302,35 +335,39 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   }
   const Layout L = layout(d, true);
   if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  if (saved && saved_bytes < saved_total(d)) return GDN_ERR_WORKSPACE;
   Marks mk = {events, n_events, 0, s};
   if ((rc = cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), s)))) return rc;
+  const Tiles tl = saved ? saved_tiles(const_cast<void*>(saved), d) : ws_tiles(ws, L);
 
-  // 1. per-chunk UT quantities (w, u, P, T)
-  PrepArgs p;
-  memset(&p, 0, sizeof p);
-  p.q = static_cast<const bf16*>(q);
-  p.k = static_cast<const bf16*>(k);
-  p.v = static_cast<const bf16*>(v);
-  p.g = g;
-  p.beta = beta;
-  p.W = at<bf16>(ws, L.W);
-  p.U = at<bf16>(ws, L.U);
-  p.P = at<bf16>(ws, L.P);
-  p.Tb = at<bf16>(ws, L.Tb);
-  p.status = at<int>(ws, L.status);
-  p.gate_logits = gate_logits;
-  p.B = B;
-  p.T = T;
-  p.Hk = Hk;
-  p.Hv = Hv;
-  p.NC = d.NC;
-  rc = cuda_status(launch_prep(p, s));
-  if (rc || (rc = mk.rec())) return rc;
+  // 1. per-chunk UT quantities (w, u, P, T), unless the forward kept them
+  if (!saved) {
+    PrepArgs p;
+    memset(&p, 0, sizeof p);
+    p.q = static_cast<const bf16*>(q);
+    p.k = static_cast<const bf16*>(k);
+    p.v = static_cast<const bf16*>(v);
+    p.g = g;
+    p.beta = beta;
+    p.W = tl.W;
+    p.U = tl.U;
+    p.P = tl.P;
+    p.Tb = tl.Tb;
+    p.status = at<int>(ws, L.status);
+    p.gate_logits = gate_logits;
+    p.B = B;
+    p.T = T;
+    p.Hk = Hk;
+    p.Hv = Hv;
+    p.NC = d.NC;
+    rc = cuda_status(launch_prep(p, s));
+    if (rc || (rc = mk.rec())) return rc;
+  }
   // 2. recompute of the state entering every chunk, and Delta (with segments:
   //    its fold and cross-segment prefix now, the replay below)
   WalkFwdArgs fw;
   WalkFwdMaps fm;
-  rc = prepare_forward_walk(d, L, ws, q, k, g, h0, nullptr, nullptr, at<bf16>(ws, L.states),
+  rc = prepare_forward_walk(d, L, ws, tl, q, k, g, h0, nullptr, nullptr, at<bf16>(ws, L.states),
                             at<bf16>(ws, L.delta), gate_logits, s, mk, fw, fm);
   if (rc) return rc;
   // 3. reverse walk of the state cotangent (with segments: its fold and prefix
@@ -338,8 +375,8 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   //    side in one launch
   WalkBwdArgs w;
   memset(&w, 0, sizeof w);
-  w.W = at<bf16>(ws, L.W);
-  w.P = at<bf16>(ws, L.P);
+  w.W = tl.W;
+  w.P = tl.P;
   w.q = static_cast<const bf16*>(q);
   w.k = static_cast<const bf16*>(k);
   w.dO = static_cast<const bf16*>(dO);
@@ -405,7 +442,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   ga.g = g;
   ga.beta = beta;
   ga.dO = static_cast<const bf16*>(dO);
-  ga.Tb = at<bf16>(ws, L.Tb);
+  ga.Tb = tl.Tb;
   ga.states = at<bf16>(ws, L.states);
   ga.dstates = at<bf16>(ws, L.dstates);
   ga.delta = at<bf16>(ws, L.delta);
@@ -424,6 +461,29 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   ga.NC = d.NC;
   rc = cuda_status(launch_grads(ga, s));
   return rc ? rc : mk.rec();
+}
+
+size_t gdn_saved_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk) {
+  if (check_dims(B, T, Hk, Hv, d_k, d_v, chunk, 1) != GDN_OK) return 0;
+  return saved_total(make_dims(B, T, Hk, Hv, 1));
+}
+
+int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                     const float* h0, void* o, float* hT, int B, int T, int Hk, int Hv, int d_k,
+                     int d_v, int chunk, int n_segments, void* saved, size_t saved_bytes, void* ws,
+                     size_t ws_bytes, void* stream, void* const* events, int n_events) {
+  return fwd_impl(q, k, v, g, beta, h0, o, hT, B, T, Hk, Hv, d_k, d_v, chunk, n_segments, ws,
+                  ws_bytes, stream, events, n_events, 0, saved, saved_bytes);
+}
+
+int gdn_chunk_bwd_ex(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                     const float* h0, const void* dO, const float* dhT, void* dq, void* dk, void* dv,
+                     float* dg, float* dbeta, float* dh0, int B, int T, int Hk, int Hv, int d_k,
+                     int d_v, int chunk, int n_segments, const void* saved, size_t saved_bytes,
+                     void* ws, size_t ws_bytes, void* stream, void* const* events, int n_events) {
+  return bwd_impl(q, k, v, g, beta, h0, dO, dhT, dq, dk, dv, dg, dbeta, dh0, B, T, Hk, Hv, d_k,
+                  d_v, chunk, n_segments, ws, ws_bytes, stream, events, n_events, 0, saved,
+                  saved_bytes);
 }
 
 int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,

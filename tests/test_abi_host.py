@@ -92,6 +92,22 @@ def test_segment_fold_argument_errors(L):
     assert call(S=2, A=None, ws=None) == -3
 
 
+def test_saved_buffer_argument_errors(L):
+    import linear_attention_rnn_gb300 as g
+    need = g.saved_bytes(1, 256, 2, 4)
+    assert need == 4 * 4 * 2 * 128 * 128 * 2  # w, u, P, T: bf16 tiles per (chunk, value head)
+    assert g.saved_bytes(1, 256, 2, 4, chunk=64) == 0
+    fwd = lambda saved, nbytes: L.gdn_chunk_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None,
+                                                   1, 256, 2, 4, 128, 128, 128, 1, saved, nbytes,
+                                                   FAKE, 1 << 30, None, None, 0)
+    assert fwd(FAKE, need - 1) == -3
+    assert fwd(MISAL, need) == -1
+    args = [FAKE] * 5 + [None, FAKE, None] + [FAKE] * 5 + [None]
+    bwd = lambda saved, nbytes: L.gdn_chunk_bwd_ex(*args, 1, 256, 2, 4, 128, 128, 128, 1, saved,
+                                                   nbytes, FAKE, 1 << 30, None, None, 0)
+    assert bwd(FAKE, 16) == -3
+
+
 def test_workspace_sizes(L):
     f = gdn.fwd_workspace_bytes
     b = gdn.bwd_workspace_bytes

@@ -116,3 +116,48 @@ def test_batched_workload_bwd(gdn_lib):
     every head of both batch rows against the per-token adjoint."""
     inp = make_host(WORKLOADS["batched_b2_t8192"])
     _check_bwd(gdn_lib, inp, record=True)
+
+
+# ------------------------------------------- forward keeps w, u, P, T for the backward
+@pytest.mark.parametrize("name,T,S", [("layer_t4096", 4096, 1), ("tiny_t1024", 300, 1),
+                                      ("tiny_t1024", 1024 + 50, 3)])
+def test_saved_chunk_quantities_give_identical_results(gdn_lib, name, T, S):
+    """The forward that keeps w, u, P and T (gdn_chunk_fwd_ex with a saved
+    buffer) and the backward that reads them (gdn_chunk_bwd_ex) run the same
+    kernels on the same data as the plain calls minus the backward's
+    preparation: the outputs equal the plain calls' bit for bit (dg and dbeta
+    up to the order of their atomic partial sums); the gradients also match
+    the per-token adjoint."""
+    wl = WORKLOADS[name].replace(T=T, backward=True, h0_std=0.2, gate_shift=-2.0 if S > 1 else 0.0,
+                                 seed=70 + S)
+    inp = make_host(wl)
+    d = inp.to("cuda")
+    sv = torch.empty(gdn_lib.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv), dtype=torch.uint8, device="cuda")
+    o1, h1 = gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=S, saved=sv)
+    g1 = gdn_lib.chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.dO, d.dhT, n_segments=S, saved=sv)
+    o2, h2 = gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=S)
+    g2 = gdn_lib.chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.dO, d.dhT, n_segments=S)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    for name_, a, b in zip(("dq", "dk", "dv", "dh0"), (g1[0], g1[1], g1[2], g1[5]),
+                           (g2[0], g2[1], g2[2], g2[5])):
+        assert torch.equal(a, b), f"{name_} differs between the saved and the recomputing backward"
+    # dg and dbeta sum per-row partials with shared-memory atomics, whose order
+    # varies from run to run: equal up to fp32 rounding of the sums
+    for name_, a, b in (("dg", g1[3], g2[3]), ("dbeta", g1[4], g2[4])):
+        assert_rel(a.cpu().numpy(), b.cpu().numpy(), 1e-5, f"{name_}: saved vs recomputing")
+    if name == "tiny_t1024":
+        res = oracle.bwd(inp)
+        for j in range(wl.Hv):
+            assert_rel(g1[2][0, :, j].float().cpu().numpy(), res["dv"][j], G_TOL, f"dv[{j}]")
+            assert_rel(g1[5][0, j].cpu().numpy(), res["dh0"][j], G_TOL, f"dh0[{j}]")
+
+
+def test_saved_buffer_too_small_is_refused(gdn_lib):
+    wl = WORKLOADS["tiny_t1024"].replace(T=256, backward=True)
+    d = make_host(wl).to("cuda")
+    sv = torch.empty(gdn_lib.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv) - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gdn_lib.GDNError):
+        gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, saved=sv)
+    with pytest.raises(gdn_lib.GDNError):
+        gdn_lib.chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.dO, d.dhT, saved=sv)
