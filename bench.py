@@ -47,7 +47,7 @@ FWD_KERNELS = ["prep", "walk"]
 FWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk"]
 # the backward of a step reads the w, u, P and T the forward kept (no preparation)
 BWD_KERNELS = ["walks", "grads"]
-BWD_KERNELS_SEG = ["fold", "prefix", "fold_bwd", "prefix_bwd", "walks", "grads"]
+BWD_KERNELS_SEG = ["fold_bwd", "prefix_bwd", "walks", "grads"]
 KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 0, 32>", "walks": "k_walk_pair", "grads": "k_grads",
                  "fold": "k_walk_fwd<1, 0, 32>", "prefix": "k_affine_walk",
                  "fold_bwd": "k_walk_bwd<1, 32>", "prefix_bwd": "k_affine_walk"}
@@ -288,7 +288,8 @@ def run_ours(args, rank, world, local_rank):
                        dtype=torch.uint8, device=dev)
     ws_b = torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
                        dtype=torch.uint8, device=dev)
-    sv = torch.empty(gdn.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv), dtype=torch.uint8, device=dev)
+    sv = torch.empty(gdn.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg), dtype=torch.uint8,
+                     device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     fk = FWD_KERNELS if nseg == 1 else FWD_KERNELS_SEG
     bk = BWD_KERNELS if nseg == 1 else BWD_KERNELS_SEG
@@ -470,8 +471,8 @@ def run_e2e(args, gdn, wl, host, dev, nseg):
                         dtype=torch.uint8, device=dev) for _ in range(2)]
     ws_b = [torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
                         dtype=torch.uint8, device=dev) for _ in range(2)]
-    svs = [torch.empty(gdn.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv), dtype=torch.uint8, device=dev)
-           for _ in range(2)]
+    svs = [torch.empty(gdn.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg), dtype=torch.uint8,
+                       device=dev) for _ in range(2)]
     s_up, s_run, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
     ev = lambda: torch.cuda.Event()  # noqa: E731
     up_done, run_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
@@ -635,8 +636,8 @@ def run_sweep(args):
                            dtype=torch.uint8, device=dev)
         ws_b = (torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
                             dtype=torch.uint8, device=dev) if bwd else None)
-        sv = (torch.empty(gdn.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv), dtype=torch.uint8, device=dev)
-              if bwd else None)
+        sv = (torch.empty(gdn.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg), dtype=torch.uint8,
+                          device=dev) if bwd else None)
         fk = FWD_KERNELS if nseg == 1 else FWD_KERNELS_SEG
         bk = BWD_KERNELS if nseg == 1 else BWD_KERNELS_SEG
 

@@ -125,8 +125,10 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
  * recomputes them (one launch of the preparation).  A training step that runs
  * the backward of the same inputs right after the forward can instead let the
  * forward keep them in a caller buffer `saved` of gdn_saved_bytes bytes (w, u,
- * P and T, bf16, [B, Hv, ceil(T/chunk), 128, 128] each) and pass it to the
- * backward, which then skips the preparation.  The pages' own fused kernel
+ * P and T, bf16, [B, Hv, ceil(T/chunk), 128, 128] each, and with segments the
+ * state entering every segment, fp32 [B, Hv, S, 128, 128]) and pass it to the
+ * backward, which then skips the preparation (and, with segments, the fold
+ * and prefix that recompute the segments' entering states).  The pages' own fused kernel
  * keeps the inverse for its backward in the same way (PR "Fuse the Gated
  * Delta Net inter-chunk scan into a Pallas TPU kernel", section "Changes":
  * the backward's analytic inverse gradient takes T from the forward).
@@ -135,13 +137,13 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
  * with events, their timing variants) with that buffer: saved = NULL gives
  * exactly the plain calls; otherwise the forward writes w, u, P, T into it and
  * the backward reads them there, and must be given the forward's inputs
- * unchanged (q, k, v, g, beta, B, T, Hk, Hv).  Results are identical to the
- * plain calls'.  saved is 16-byte aligned; a smaller saved_bytes than
- * gdn_saved_bytes gives GDN_ERR_WORKSPACE.  Launch order of the backward with
- * a saved buffer: walks (or fold, prefix, reverse fold, reverse prefix, walks
- * with segments), gradients -- no preparation.
+ * unchanged (q, k, v, g, beta, h0, B, T, Hk, Hv, n_segments).  Results are
+ * those of the plain calls.  saved is 16-byte aligned; a smaller saved_bytes
+ * than gdn_saved_bytes (for the same n_segments) gives GDN_ERR_WORKSPACE.
+ * Launch order of the backward with a saved buffer: walks (with segments:
+ * reverse fold, reverse prefix, walks), gradients.
  */
-size_t gdn_saved_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk);
+size_t gdn_saved_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments);
 int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
                      const float* beta, const float* h0, void* o, float* hT, int B, int T,
                      int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments, void* saved,

@@ -72,7 +72,7 @@ def lib():
         L.gdn_chunk_fwd_timed.restype = I
         L.gdn_chunk_bwd_timed.argtypes = [P] * 14 + [I] * 8 + [P, Z, P, P, I]
         L.gdn_chunk_bwd_timed.restype = I
-        L.gdn_saved_bytes.argtypes = [I] * 7
+        L.gdn_saved_bytes.argtypes = [I] * 8
         L.gdn_saved_bytes.restype = Z
         L.gdn_chunk_fwd_ex.argtypes = [P] * 8 + [I] * 8 + [P, Z, P, Z, P, P, I]
         L.gdn_chunk_fwd_ex.restype = I
@@ -148,9 +148,10 @@ def bwd_workspace_bytes(B, T, Hk, Hv, dk=128, dv=128, chunk=128, n_segments=0) -
     return int(lib().gdn_bwd_workspace_bytes(B, T, Hk, Hv, dk, dv, chunk, n_segments))
 
 
-def saved_bytes(B, T, Hk, Hv, dk=128, dv=128, chunk=128) -> int:
-    """Bytes of the buffer in which a forward keeps w, u, P and T for its backward."""
-    return int(lib().gdn_saved_bytes(B, T, Hk, Hv, dk, dv, chunk))
+def saved_bytes(B, T, Hk, Hv, dk=128, dv=128, chunk=128, n_segments=0) -> int:
+    """Bytes of the buffer in which a forward keeps w, u, P and T (and, with
+    segments, the segments' entering states) for its backward."""
+    return int(lib().gdn_saved_bytes(B, T, Hk, Hv, dk, dv, chunk, n_segments))
 
 
 def _events(events):

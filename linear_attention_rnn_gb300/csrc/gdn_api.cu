@@ -96,6 +96,7 @@ T* at(void* ws, size_t off) {
 // and the backward of the same inputs reads instead of recomputing them.
 struct Tiles {
   bf16 *W, *U, *P, *Tb;
+  float* hin;  // with segments: the state entering every segment, [B Hv][S][128][128] fp32
 };
 
 Tiles ws_tiles(void* ws, const Layout& L) {
@@ -104,11 +105,16 @@ Tiles ws_tiles(void* ws, const Layout& L) {
   t.U = at<bf16>(ws, L.U);
   t.P = at<bf16>(ws, L.P);
   t.Tb = L.Tb ? at<bf16>(ws, L.Tb) : nullptr;
+  t.hin = L.hin ? at<float>(ws, L.hin) : nullptr;
   return t;
 }
 
-// saved buffer: w, u, P, T, each [B Hv][NC][128][128] bf16
-size_t saved_total(const Dims& d) { return 4 * up((size_t)d.BH() * d.NC * CH * HD * sizeof(bf16)); }
+// saved buffer: w, u, P, T, each [B Hv][NC][128][128] bf16, and with segments
+// the entering state of every segment, [B Hv][S][128][128] fp32
+size_t saved_total(const Dims& d) {
+  const size_t part = up((size_t)d.BH() * d.NC * CH * HD * sizeof(bf16));
+  return 4 * part + (d.S > 1 ? up((size_t)d.BH() * d.S * HD * HD * sizeof(float)) : 0);
+}
 
 Tiles saved_tiles(void* saved, const Dims& d) {
   const size_t part = up((size_t)d.BH() * d.NC * CH * HD * sizeof(bf16));
@@ -117,6 +123,7 @@ Tiles saved_tiles(void* saved, const Dims& d) {
   t.U = at<bf16>(saved, part);
   t.P = at<bf16>(saved, 2 * part);
   t.Tb = at<bf16>(saved, 3 * part);
+  t.hin = d.S > 1 ? at<float>(saved, 4 * part) : nullptr;
   return t;
 }
 
@@ -146,10 +153,12 @@ struct Marks {
 // maps; with segments it also runs the fold and the cross-segment prefix, so
 // that the walk (launched by the caller) replays every segment from its
 // entering state.
+// hin_ready: the segments' entering states are already in tl.hin (a forward
+// kept them), so the fold and the prefix are not run again.
 int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const Tiles& tl, const void* q,
                          const void* k, const float* g, const float* h0, void* o, float* hT,
-                         bf16* states, bf16* delta, int gate_logits, cudaStream_t s, Marks& mk,
-                         WalkFwdArgs& w, WalkFwdMaps& mp) {
+                         bf16* states, bf16* delta, int gate_logits, bool hin_ready, cudaStream_t s,
+                         Marks& mk, WalkFwdArgs& w, WalkFwdMaps& mp) {
   memset(&w, 0, sizeof w);
   w.gate_logits = gate_logits;
   w.W = tl.W;
@@ -183,6 +192,12 @@ int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const Tiles&
     w.hstart_seg_stride = 0;
     return GDN_OK;
   }
+  if (hin_ready) {
+    w.hstart = tl.hin;
+    w.hstart_bh_stride = (long)d.S * HD * HD;
+    w.hstart_seg_stride = (long)HD * HD;
+    return GDN_OK;
+  }
   WalkFwdArgs f = w;
   f.pairA = at<float>(ws, Lw.pairA);
   f.pairB = at<float>(ws, Lw.pairB);
@@ -197,7 +212,7 @@ int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const Tiles&
   x.A = f.pairA;
   x.Bv = f.pairB;
   x.init = h0;
-  x.outB = at<float>(ws, Lw.hin);
+  x.outB = tl.hin;
   x.batch = (int)d.BH();
   x.n = d.S;
   x.dv = HD;
@@ -206,7 +221,7 @@ int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const Tiles&
   x.reverse = 0;
   rc = cuda_status(launch_affine_walk(x, s));
   if (rc || (rc = mk.rec())) return rc;
-  w.hstart = at<float>(ws, Lw.hin);
+  w.hstart = tl.hin;
   w.hstart_bh_stride = (long)d.S * HD * HD;
   w.hstart_seg_stride = (long)HD * HD;
   return GDN_OK;
@@ -303,8 +318,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   if (rc || (rc = mk.rec())) return rc;
   WalkFwdArgs w;
   WalkFwdMaps mp;
-  if ((rc = prepare_forward_walk(d, L, ws, tl, q, k, g, h0, o, hT, nullptr, nullptr, gate_logits, s, mk,
-                                 w, mp)))
+  if ((rc = prepare_forward_walk(d, L, ws, tl, q, k, g, h0, o, hT, nullptr, nullptr, gate_logits, false,
+                                 s, mk, w, mp)))
     return rc;
   if ((rc = cuda_status(launch_walk_fwd(w, mp, 0, s)))) return rc;
   return mk.rec();
@@ -368,7 +383,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   WalkFwdArgs fw;
   WalkFwdMaps fm;
   rc = prepare_forward_walk(d, L, ws, tl, q, k, g, h0, nullptr, nullptr, at<bf16>(ws, L.states),
-                            at<bf16>(ws, L.delta), gate_logits, s, mk, fw, fm);
+                            at<bf16>(ws, L.delta), gate_logits, saved != nullptr, s, mk, fw, fm);
   if (rc) return rc;
   // 3. reverse walk of the state cotangent (with segments: its fold and prefix
   //    now); it needs nothing from the recompute, so the two walks run side by
@@ -463,9 +478,9 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   return rc ? rc : mk.rec();
 }
 
-size_t gdn_saved_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk) {
-  if (check_dims(B, T, Hk, Hv, d_k, d_v, chunk, 1) != GDN_OK) return 0;
-  return saved_total(make_dims(B, T, Hk, Hv, 1));
+size_t gdn_saved_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments) {
+  if (check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments) != GDN_OK) return 0;
+  return saved_total(make_dims(B, T, Hk, Hv, n_segments));
 }
 
 int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g, const float* beta,

@@ -132,7 +132,8 @@ def test_saved_chunk_quantities_give_identical_results(gdn_lib, name, T, S):
                                  seed=70 + S)
     inp = make_host(wl)
     d = inp.to("cuda")
-    sv = torch.empty(gdn_lib.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv), dtype=torch.uint8, device="cuda")
+    sv = torch.empty(gdn_lib.saved_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=S), dtype=torch.uint8,
+                     device="cuda")
     o1, h1 = gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=S, saved=sv)
     g1 = gdn_lib.chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.dO, d.dhT, n_segments=S, saved=sv)
     o2, h2 = gdn_lib.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=S)
