@@ -625,8 +625,12 @@ def run_sweep(args):
     pk = peaks()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     names = args.sweep.split(",") if args.sweep != "all" else list(WORKLOADS)
-    for name in names:
+    for spec in names:
+        # "name" runs the workload as configured, "name@S" with S segments (0: the library's choice)
+        name, _, segs = spec.partition("@")
         wl = WORKLOADS[name]
+        if segs:
+            wl = wl.replace(n_segments=int(segs))
         bwd = wl.backward
         nseg = wl.n_segments or gdn.default_segments(wl.B, wl.T, wl.Hv)
         big = wl.tokens > (1 << 16)
@@ -679,7 +683,7 @@ def run_sweep(args):
             t_roof = max(t_hbm, t_tc)
             return {"ms": round(ms, 5), "roof_ms": round(t_roof, 5),
                     "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": round(t_roof / ms, 4)}
-        line = {"workload": name, "B": wl.B, "T": wl.T, "Hk": wl.Hk, "Hv": wl.Hv,
+        line = {"workload": spec, "B": wl.B, "T": wl.T, "Hk": wl.Hk, "Hv": wl.Hv,
                 "segments": nseg, "timed_steps": steps, "reported": "median",
                 "fwd": path(alg["fwd_bytes"], alg["fwd_flops"], fwd_ms),
                 "fwd_tokens_per_s": round(wl.tokens / (fwd_ms * 1e-3), 1),

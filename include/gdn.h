@@ -76,7 +76,11 @@ typedef enum gdn_status {
 /* Human-readable text of a status code (static storage, never NULL). */
 const char* gdn_strerror(int status);
 
-/* Number of chunk segments the forward/backward use when n_segments == 0. */
+/* Number of chunk segments the forward/backward use when n_segments == 0: one
+ * when the chunks are few or the batch rows and value heads already keep a
+ * quarter of the SMs busy with the one-segment walk (4 CTAs each), else enough
+ * segments to fill the SMs about twice with the segment fold (8 CTAs per
+ * segment and head), at least 8 chunks each. */
 int gdn_default_segments(int B, int T, int Hv, int chunk);
 
 /*

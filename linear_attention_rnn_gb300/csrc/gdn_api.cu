@@ -245,14 +245,25 @@ const char* gdn_strerror(int status) {
 }
 
 int gdn_default_segments(int B, int T, int Hv, int chunk) {
-  if (chunk <= 0 || T <= 0) return 1;
-  const int NC = (T + chunk - 1) / chunk;
-  (void)B;
-  (void)Hv;
+  if (chunk <= 0 || T <= 0 || B <= 0 || Hv <= 0) return 1;
+  const long NC = (T + chunk - 1) / chunk;
   if (NC <= 64) return 1;
-  int S = NC / 32;
-  if (S > 64) S = 64;
-  return S < 2 ? 2 : S;
+  // The one-segment walk runs 4 CTAs per (batch row, value head).  When those
+  // keep a quarter of the SMs or more busy, segments only add work: the fold
+  // pushes every chunk through the 256 columns of [A | B], and the prefix is
+  // sequential over the segments.  Otherwise take enough segments for the fold
+  // (8 CTAs per segment and head) to fill the SMs about twice, with at least
+  // 8 chunks per segment.
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 152;
+  const long heads = (long)B * Hv;
+  if (4 * heads * 4 >= sms) return 1;
+  long S = (2L * sms + 8 * heads - 1) / (8 * heads);
+  if (S > NC / 8) S = NC / 8;
+  if (S > 256) S = 256;
+  return S < 2 ? 2 : (int)S;
 }
 
 size_t gdn_fwd_workspace_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk,

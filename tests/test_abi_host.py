@@ -125,9 +125,14 @@ def test_workspace_sizes(L):
 def test_default_segments(L):
     assert gdn.default_segments(1, 4096, 32) == 1
     assert gdn.default_segments(1, 0, 32) == 1
-    s = gdn.default_segments(1, 262144, 32)
-    assert 2 <= s <= 64
-    assert gdn.default_segments(1, 1 << 20, 32) == 64
+    # 32 value heads: the one-segment walk keeps 128 CTAs busy, so no segments
+    assert gdn.default_segments(1, 262144, 32) == 1
+    assert gdn.default_segments(1, 1 << 20, 32) == 1
+    # one or two heads: enough segments to fill the SMs, at least 8 chunks each
+    s1 = gdn.default_segments(1, 262144, 1)
+    assert 2 <= s1 <= 2048 // 8
+    assert s1 >= gdn.default_segments(1, 262144, 2) >= 2
+    assert gdn.default_segments(1, 64 * 128 + 1, 1) == 8  # 65 chunks, 8 per segment
 
 
 def test_binding_validates_before_calling():
