@@ -111,23 +111,42 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   GradSmem& sm = *reinterpret_cast<GradSmem*>(base);
-  const int c = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int group = a.Hv / a.Hk;
-  const int t0 = c * CH;
-  const int L = min(CH, a.T - t0);
   const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
   const int row = 32 * quarter + lane;
-
-  auto cid_of = [&](int jj) { return ((long)b * a.Hv + kh * group + jj) * a.NC + c; };
+  // Persistent CTAs, one per SM, over contiguous ranges of (batch row, key head,
+  // chunk) units, chunk fastest: a CTA pays its start-up once, and the tiles of
+  // the next unit's first value head are requested while the current unit ends.
+  const int U = a.B * a.Hk * a.NC;
+  const int u_begin = (int)((long)blockIdx.x * U / gridDim.x);
+  const int u_end = (int)((long)(blockIdx.x + 1) * U / gridDim.x);
+  if (u_begin >= u_end) return;
+  struct GUnit {
+    int b, kh, c;
+  };
+  auto decode = [&](int u) {
+    GUnit x;
+    x.c = u % a.NC;
+    const int r = u / a.NC;
+    x.kh = r % a.Hk;
+    x.b = r / a.Hk;
+    return x;
+  };
+  auto cid_of = [&](const GUnit& x, int jj) { return ((long)x.b * a.Hv + x.kh * group + jj) * a.NC + x.c; };
   auto load2d = [&](unsigned char* dst, const CUtensorMap* m, long cid, uint64_t* bar) {
     tc::arrive_expect_tx(bar, TILE);
     tc::tma_load_2d(dst, m, 0, (int)(cid * CH), bar);
     tc::tma_load_2d(dst + TILE / 2, m, 64, (int)(cid * CH), bar);
   };
-  auto load4d = [&](unsigned char* dst, const CUtensorMap* m, int head, uint64_t* bar) {
-    tc::tma_load_4d(dst, m, 0, head, t0, b, bar);
-    tc::tma_load_4d(dst + TILE / 2, m, 64, head, t0, b, bar);
+  auto load4d = [&](unsigned char* dst, const CUtensorMap* m, const GUnit& x, int head, uint64_t* bar) {
+    tc::tma_load_4d(dst, m, 0, head, x.c * CH, x.b, bar);
+    tc::tma_load_4d(dst + TILE / 2, m, 64, head, x.c * CH, x.b, bar);
+  };
+  auto load_kq = [&](const GUnit& x) {
+    tc::arrive_expect_tx(&sm.barKQ, 2 * TILE);
+    load4d(sm.K, &mp.k, x, x.kh, &sm.barKQ);
+    load4d(sm.Q, &mp.q, x, x.kh, &sm.barKQ);
   };
   if (tid == 0) {
     tc::mbar_init(&sm.barKQ, 1);
@@ -139,10 +158,9 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     tc::mbar_init(&sm.barDO, 1);
     tc::mbar_init(&sm.barM, 1);
     tc::mbar_fence_init();
-    tc::arrive_expect_tx(&sm.barKQ, 2 * TILE);
-    load4d(sm.K, &mp.k, kh, &sm.barKQ);
-    load4d(sm.Q, &mp.q, kh, &sm.barKQ);
-    const long cid0 = cid_of(0);
+    const GUnit x0 = decode(u_begin);
+    load_kq(x0);
+    const long cid0 = cid_of(x0, 0);
     load2d(sm.W1, &mp.Tb, cid0, &sm.barT);
     load2d(sm.W2, &mp.ddelta, cid0, &sm.barDD);
     load2d(sm.W3, &mp.states, cid0, &sm.barH);
@@ -168,31 +186,44 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     __syncthreads();
     tc::fence_after();
   };
-  if (tid == 0) ok = tc::mbar_wait(&sm.barKQ, 0);
-  ok = ok && tc::mbar_wait(&sm.barKQ, 0);  // K and Q rows are read by the epilogues too
-
-  // g and beta of row tid for value head kh * group + jj (loaded a head ahead)
-  auto load_gates = [&](int jj, float& gv, float& bv) {
+  // g and beta of row tid for value head jj of unit x (loaded a head ahead)
+  auto load_gates = [&](const GUnit& x, int jj, float& gv, float& bv) {
     gv = bv = 0.f;
-    if (tid < L && jj < group) {
-      const long idx = ((long)b * a.T + t0 + tid) * a.Hv + kh * group + jj;
+    if (tid < min(CH, a.T - x.c * CH)) {
+      const long idx = ((long)x.b * a.T + x.c * CH + tid) * a.Hv + x.kh * group + jj;
       gv = act_g(a.g[idx], a.gate_logits);
       bv = act_beta(a.beta[idx], a.gate_logits);
     }
   };
   float g_next = 0.f, b_next = 0.f;
-  if (tid < CH) load_gates(0, g_next, b_next);
+  if (tid < CH) load_gates(decode(u_begin), 0, g_next, b_next);
+  int hc = 0;  // value heads processed by this CTA: the parity of the tile barriers
 
+  for (int u = u_begin; u < u_end; ++u) {
+  const GUnit xu = decode(u);
+  const int c = xu.c, kh = xu.kh, b = xu.b;
+  const int t0 = c * CH;
+  const int L = min(CH, a.T - t0);
+  const bool has_next = u + 1 < u_end;
+  const GUnit xn = decode(has_next ? u + 1 : u);
+  const uint32_t kq_par = (uint32_t)((u - u_begin) & 1);
   for (int jj = 0; jj < group; ++jj) {
     const int j = kh * group + jj;
-    const long cid = cid_of(jj);
+    const long cid = cid_of(xu, jj);
     const long tokv = ((long)b * a.T + t0) * a.Hv + j;  // row 0 of the v/dO tile
-    const uint32_t par = (uint32_t)(jj & 1);
+    const uint32_t par = (uint32_t)(hc & 1);
+    // the value head after this one: the next of this unit, or the next unit's first
+    const bool next_here = jj + 1 < group;
+    const bool has_after = next_here || has_next;
+    const long cid_after = next_here ? cid_of(xu, jj + 1) : cid_of(xn, 0);
     // ---- gates of value head j; per-row sums cleared ----------------------------
     if (tid < CH) {
       sm.Gl[tid] = g_next;
       sm.beta[tid] = b_next;
-      load_gates(jj + 1, g_next, b_next);
+      if (next_here)
+        load_gates(xu, jj + 1, g_next, b_next);
+      else if (has_next)
+        load_gates(xn, 0, g_next, b_next);
       sm.colX[tid] = sm.dbeta[tid] = sm.dbg[tid] = sm.d_ef[tid] = sm.rowX[tid] = sm.dgamO[tid] = 0.f;
     }
     if (tid == 0) {  // S1: dV' = T^T dDelta (both tiles read MN-major)
@@ -329,6 +360,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     }
 
     // ---- E2: dK (+)= -diag(beta gamma) dV' h^T + diag(ef) Delta dh'^T ---------------------
+    if (jj == 0) ok = ok && tc::mbar_wait(&sm.barKQ, kq_par);  // the unit's K and Q (read from here on)
     wait_mma();
     {
       float kv[32], x[32], acc[32];
@@ -361,7 +393,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     // ---- S3: ds = dV' Delta^T -> A;  K K^T -> B ----------------------------------------
     if (tid == 0) {
       tc::arrive_expect_tx(&sm.barDO, TILE);
-      load4d(sm.W2, &mp.dO, j, &sm.barDO);
+      load4d(sm.W2, &mp.dO, xu, j, &sm.barDO);
       tc::gemm128(tmem + C_A, smem_u32(sm.W1), false, smem_u32(sm.W4), false, false);
       tc::gemm128(tmem + C_B, smem_u32(sm.K), false, smem_u32(sm.K), false, false);
       tc::commit(&sm.barM);
@@ -440,11 +472,10 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     }
     // ---- E5: dgamma_O = rowsum(Q * (dO h^T));  dQ (+)= diag(gamma) dO h^T ------------------
     wait_mma();
-    if (tid == 0 && jj + 1 < group) {  // next value head: its T, dDelta, h (tiles consumed)
-      const long nc = cid_of(jj + 1);
-      load2d(sm.W1, &mp.Tb, nc, &sm.barT);
-      load2d(sm.W2, &mp.ddelta, nc, &sm.barDD);
-      load2d(sm.W3, &mp.states, nc, &sm.barH);
+    if (tid == 0 && has_after) {  // next value head: its T, dDelta, h (tiles consumed)
+      load2d(sm.W1, &mp.Tb, cid_after, &sm.barT);
+      load2d(sm.W2, &mp.ddelta, cid_after, &sm.barDD);
+      load2d(sm.W3, &mp.states, cid_after, &sm.barH);
     }
     {
       float qv[32], x[32], acc[32];
@@ -478,7 +509,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     atomicAdd(&sm.rowX[row], p_rowx);
     atomicAdd(&sm.dgamO[row], p_dgam);
     wait_mma();
-    if (tid == 0 && jj + 1 < group) load2d(sm.W4, &mp.delta, cid_of(jj + 1), &sm.barDl);
+    if (tid == 0 && has_after) load2d(sm.W4, &mp.delta, cid_after, &sm.barDl);
     __syncthreads();
 
     // ---- gate cotangents of value head j ----------------------------------------------
@@ -531,26 +562,33 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       }
     }
     __syncthreads();
+    ++hc;
   }
 
-  // ---- dq, dk of the key head: bf16 staging tiles (W1, W2 are free) and TMA stores ------
+  // ---- dq, dk of the key head: bf16 staging tiles in the Q and K buffers (the unit's
+  //      last products have read them; W1-W4 already hold the next unit's tiles) -------
   {
     float x[32];
     tc::ld32(tl + C_DQ, x);
-    row32_store(sm.W1, row, c0, x);
+    row32_store(sm.Q, row, c0, x);
     tc::ld32(tl + C_DK, x);
-    row32_store(sm.W2, row, c0, x);
+    row32_store(sm.K, row, c0, x);
   }
   tc::fence_proxy_async();
   __syncthreads();
   if (tid == 0) {
-    tc::tma_store_4d(&mp.dq, 0, kh, t0, b, sm.W1);
-    tc::tma_store_4d(&mp.dq, 64, kh, t0, b, sm.W1 + TILE / 2);
-    tc::tma_store_4d(&mp.dk, 0, kh, t0, b, sm.W2);
-    tc::tma_store_4d(&mp.dk, 64, kh, t0, b, sm.W2 + TILE / 2);
+    tc::tma_store_4d(&mp.dq, 0, kh, t0, b, sm.Q);
+    tc::tma_store_4d(&mp.dq, 64, kh, t0, b, sm.Q + TILE / 2);
+    tc::tma_store_4d(&mp.dk, 0, kh, t0, b, sm.K);
+    tc::tma_store_4d(&mp.dk, 64, kh, t0, b, sm.K + TILE / 2);
     tc::bulk_commit();
-    tc::bulk_wait();
+    if (has_next) {  // the stores have read the staging tiles: the next unit's K and Q
+      tc::bulk_wait_read();
+      load_kq(xn);
+    }
   }
+  }  // units
+  if (tid == 0) tc::bulk_wait();  // every store has completed before the block exits
   if (!ok && a.status) atomicOr(a.status, 1);
   tc::fence_before();
   __syncthreads();
@@ -577,7 +615,15 @@ cudaError_t launch_grads(const GradArgs& a, cudaStream_t s) {
   const size_t smem = grad_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_grads<<<dim3(a.NC, a.Hk, a.B), GT, smem, s>>>(a, mp);
+  // persistent CTAs, one per SM (the shared memory admits one), each over a
+  // contiguous range of (batch row, key head, chunk) units
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long units = (long)a.B * a.Hk * a.NC;
+  const int ctas = (int)(units < sms ? units : sms);
+  if (ctas <= 0) return cudaSuccess;
+  k_grads<<<ctas, GT, smem, s>>>(a, mp);
   return cudaGetLastError();
 }
 
