@@ -7,9 +7,9 @@ h0 ~ N(0, 0.1^2), g = -softplus(N(0,1) + 1), cotangents dO ~ N(0,1),
 dhT ~ N(0, 0.1^2)), and the fraction of the binding roofline.
 
 A step is one forward (o, hT) plus one backward (dq, dk, dv, dg, dbeta,
-dh0) over one batch; the forward keeps its per-chunk w, u, P and T for the
-backward (as a training step's autograd would), so the backward runs no
-preparation of its own.  Inputs are resident in HBM; L2 is flushed (a 512 MiB
+dh0) over one batch; the forward keeps its per-chunk w, u, P, T, states and
+Delta for the backward (as a training step's autograd would), so the backward
+runs only the reverse walk and the gradients.  Inputs are resident in HBM; L2 is flushed (a 512 MiB
 write) before every timed step, outside the step's events.  Each rank runs
 the same per-GPU workload (weak scaling, no collective on the data path).
 
@@ -46,9 +46,10 @@ FLOPS["walks"] = FLOPS["walk_states"] + FLOPS["walk_bwd"]  # both walks of the b
 FWD_KERNELS = ["prep", "walk"]
 FWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk"]
 # the backward of a step reads the w, u, P and T the forward kept (no preparation)
-BWD_KERNELS = ["walks", "grads"]
-BWD_KERNELS_SEG = ["fold_bwd", "prefix_bwd", "walks", "grads"]
-KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 0, 32>", "walks": "k_walk_pair", "grads": "k_grads",
+BWD_KERNELS = ["walk_bwd", "grads"]
+BWD_KERNELS_SEG = ["fold_bwd", "prefix_bwd", "walk_bwd", "grads"]
+KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 1, 32>", "walks": "k_walk_pair", "grads": "k_grads",
+                 "walk_bwd": "k_walk_bwd<0, 32>",
                  "fold": "k_walk_fwd<1, 0, 32>", "prefix": "k_affine_walk",
                  "fold_bwd": "k_walk_bwd<1, 32>", "prefix_bwd": "k_affine_walk"}
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum, bytes)
@@ -69,9 +70,9 @@ def algorithmic(wl):
     bwd_bytes = qk + vv + gb + st + vv + st + qk + vv + gb + st  # + dO dhT; dq dk dv dg dbeta dh0
     units, kunits = B * Hv * NC, B * Hk * NC
     fwd_flops = kunits * FLOP_PER_CHUNK_KHEAD + units * (FLOPS["prep"] + FLOPS["walk"])
-    # the backward takes w, u, P and T from the forward: the states' recompute,
-    # the reverse walk and the chunk gradients
-    bwd_flops = units * (FLOPS["walk_states"] + FLOPS["walk_bwd"] + FLOPS["grads"])
+    # the backward takes w, u, P, T, the states and Delta from the forward: the
+    # reverse walk and the chunk gradients
+    bwd_flops = units * (FLOPS["walk_bwd"] + FLOPS["grads"])
     return dict(fwd_bytes=fwd_bytes, bwd_bytes=bwd_bytes, fwd_flops=fwd_flops,
                 bwd_flops=bwd_flops, units=units, kunits=kunits)
 
@@ -344,6 +345,19 @@ def run_ours(args, rank, world, local_rank):
     sampler.stop()
     fast.stop()
 
+    # the plain forward (gdn_chunk_fwd: o and hT only, nothing kept for a
+    # backward), timed alone after the step's timed region
+    plain = []
+    for i in range(max(K, 10)):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        gdn.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=nseg, workspace=ws_f)
+        e1.record()
+        plain.append((e0, e1))
+    torch.cuda.synchronize()
+    fwd_plain_ms = statistics.median(a.elapsed_time(b) for a, b in plain)
     step_ms = [starts[i].elapsed_time(bev[i][-1]) for i in range(K)]
     fwd_ms = [starts[i].elapsed_time(fev[i][-1]) for i in range(K)]
     bwd_ms = [fev[i][-1].elapsed_time(bev[i][-1]) for i in range(K)]
@@ -403,6 +417,7 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world} (independent problems)"},
         "roofline": roofline,
         "path_roofline": {"fwd": path(alg["fwd_bytes"], alg["fwd_flops"], fwd_mean),
+                          "fwd_plain": path(alg["fwd_bytes"], alg["fwd_flops"], fwd_plain_ms),
                           "bwd": path(alg["bwd_bytes"], alg["bwd_flops"], bwd_mean),
                           "step": path(alg["fwd_bytes"] + alg["bwd_bytes"],
                                        alg["fwd_flops"] + alg["bwd_flops"], mean_step),

@@ -129,10 +129,12 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
  * recomputes them (one launch of the preparation).  A training step that runs
  * the backward of the same inputs right after the forward can instead let the
  * forward keep them in a caller buffer `saved` of gdn_saved_bytes bytes (w, u,
- * P and T, bf16, [B, Hv, ceil(T/chunk), 128, 128] each, and with segments the
- * state entering every segment, fp32 [B, Hv, S, 128, 128]) and pass it to the
- * backward, which then skips the preparation (and, with segments, the fold
- * and prefix that recompute the segments' entering states).  The pages' own fused kernel
+ * P, T, the state entering every chunk and Delta = u - w h, bf16,
+ * [B, Hv, ceil(T/chunk), 128, 128] each, and with segments the state entering
+ * every segment, fp32 [B, Hv, S, 128, 128]) and pass it to the backward, which
+ * then skips the preparation and the recompute of the states (and, with
+ * segments, the fold and prefix that recompute the segments' entering states):
+ * it runs the reverse walk of the state cotangent and the gradients only.  The pages' own fused kernel
  * keeps the inverse for its backward in the same way (PR "Fuse the Gated
  * Delta Net inter-chunk scan into a Pallas TPU kernel", section "Changes":
  * the backward's analytic inverse gradient takes T from the forward).
@@ -144,8 +146,8 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
  * unchanged (q, k, v, g, beta, h0, B, T, Hk, Hv, n_segments).  Results are
  * those of the plain calls.  saved is 16-byte aligned; a smaller saved_bytes
  * than gdn_saved_bytes (for the same n_segments) gives GDN_ERR_WORKSPACE.
- * Launch order of the backward with a saved buffer: walks (with segments:
- * reverse fold, reverse prefix, walks), gradients.
+ * Launch order of the backward with a saved buffer: reverse walk (with
+ * segments: reverse fold, reverse prefix, reverse walk), gradients.
  */
 size_t gdn_saved_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk, int n_segments);
 int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,

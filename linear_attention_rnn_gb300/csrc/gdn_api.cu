@@ -96,7 +96,8 @@ T* at(void* ws, size_t off) {
 // and the backward of the same inputs reads instead of recomputing them.
 struct Tiles {
   bf16 *W, *U, *P, *Tb;
-  float* hin;  // with segments: the state entering every segment, [B Hv][S][128][128] fp32
+  bf16 *states, *delta;  // the state entering every chunk and Delta (backward)
+  float* hin;            // with segments: the state entering every segment, [B Hv][S][128][128] fp32
 };
 
 Tiles ws_tiles(void* ws, const Layout& L) {
@@ -105,15 +106,18 @@ Tiles ws_tiles(void* ws, const Layout& L) {
   t.U = at<bf16>(ws, L.U);
   t.P = at<bf16>(ws, L.P);
   t.Tb = L.Tb ? at<bf16>(ws, L.Tb) : nullptr;
+  t.states = L.states ? at<bf16>(ws, L.states) : nullptr;
+  t.delta = L.delta ? at<bf16>(ws, L.delta) : nullptr;
   t.hin = L.hin ? at<float>(ws, L.hin) : nullptr;
   return t;
 }
 
-// saved buffer: w, u, P, T, each [B Hv][NC][128][128] bf16, and with segments
-// the entering state of every segment, [B Hv][S][128][128] fp32
+// saved buffer: w, u, P, T, the entering state of every chunk and Delta, each
+// [B Hv][NC][128][128] bf16, and with segments the entering state of every
+// segment, [B Hv][S][128][128] fp32
 size_t saved_total(const Dims& d) {
   const size_t part = up((size_t)d.BH() * d.NC * CH * HD * sizeof(bf16));
-  return 4 * part + (d.S > 1 ? up((size_t)d.BH() * d.S * HD * HD * sizeof(float)) : 0);
+  return 6 * part + (d.S > 1 ? up((size_t)d.BH() * d.S * HD * HD * sizeof(float)) : 0);
 }
 
 Tiles saved_tiles(void* saved, const Dims& d) {
@@ -123,7 +127,9 @@ Tiles saved_tiles(void* saved, const Dims& d) {
   t.U = at<bf16>(saved, part);
   t.P = at<bf16>(saved, 2 * part);
   t.Tb = at<bf16>(saved, 3 * part);
-  t.hin = d.S > 1 ? at<float>(saved, 4 * part) : nullptr;
+  t.states = at<bf16>(saved, 4 * part);
+  t.delta = at<bf16>(saved, 5 * part);
+  t.hin = d.S > 1 ? at<float>(saved, 6 * part) : nullptr;
   return t;
 }
 
@@ -155,10 +161,13 @@ struct Marks {
 // entering state.
 // hin_ready: the segments' entering states are already in tl.hin (a forward
 // kept them), so the fold and the prefix are not run again.
+// The exports (states, delta) are stored in slices of 32 columns by the walk
+// with output, of WALK_STATES_SW columns by the recompute beside the reverse walk.
 int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const Tiles& tl, const void* q,
                          const void* k, const float* g, const float* h0, void* o, float* hT,
                          bf16* states, bf16* delta, int gate_logits, bool hin_ready, cudaStream_t s,
                          Marks& mk, WalkFwdArgs& w, WalkFwdMaps& mp) {
+  const int esw = o ? 32 : WALK_STATES_SW;
   memset(&w, 0, sizeof w);
   w.gate_logits = gate_logits;
   w.W = tl.W;
@@ -183,8 +192,8 @@ int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const Tiles&
   if (!tmap_heads(&mp.k, k, d.B, d.T, d.Hk, HD) || !tmap_heads(&mp.q, q, d.B, d.T, d.Hk, HD) ||
       !tmap_2d(&mp.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
       !tmap_2d(&mp.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true) ||
-      (states && !tmap_2d_sw(&mp.St, states, HD, wrows, HD * sizeof(bf16), WALK_STATES_SW, CH, slice_swizzle(WALK_STATES_SW))) ||
-      (delta && !tmap_2d_sw(&mp.De, delta, HD, wrows, HD * sizeof(bf16), WALK_STATES_SW, CH, slice_swizzle(WALK_STATES_SW))))
+      (states && !tmap_2d_sw(&mp.St, states, HD, wrows, HD * sizeof(bf16), esw, CH, slice_swizzle(esw))) ||
+      (delta && !tmap_2d_sw(&mp.De, delta, HD, wrows, HD * sizeof(bf16), esw, CH, slice_swizzle(esw))))
     return GDN_ERR_CUDA;
   if (d.S == 1) {
     w.hstart = h0;
@@ -329,8 +338,9 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   if (rc || (rc = mk.rec())) return rc;
   WalkFwdArgs w;
   WalkFwdMaps mp;
-  if ((rc = prepare_forward_walk(d, L, ws, tl, q, k, g, h0, o, hT, nullptr, nullptr, gate_logits, false,
-                                 s, mk, w, mp)))
+  // with a saved buffer the walk also keeps the entering state of every chunk and Delta
+  if ((rc = prepare_forward_walk(d, L, ws, tl, q, k, g, h0, o, hT, saved ? tl.states : nullptr,
+                                 saved ? tl.delta : nullptr, gate_logits, false, s, mk, w, mp)))
     return rc;
   if ((rc = cuda_status(launch_walk_fwd(w, mp, 0, s)))) return rc;
   return mk.rec();
@@ -390,12 +400,18 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
     if (rc || (rc = mk.rec())) return rc;
   }
   // 2. recompute of the state entering every chunk, and Delta (with segments:
-  //    its fold and cross-segment prefix now, the replay below)
+  //    its fold and cross-segment prefix now, the replay below), unless the
+  //    forward kept them
   WalkFwdArgs fw;
   WalkFwdMaps fm;
-  rc = prepare_forward_walk(d, L, ws, tl, q, k, g, h0, nullptr, nullptr, at<bf16>(ws, L.states),
-                            at<bf16>(ws, L.delta), gate_logits, saved != nullptr, s, mk, fw, fm);
-  if (rc) return rc;
+  if (!saved) {
+    rc = prepare_forward_walk(d, L, ws, tl, q, k, g, h0, nullptr, nullptr, tl.states, tl.delta,
+                              gate_logits, false, s, mk, fw, fm);
+    if (rc) return rc;
+  }
+  // the reverse walk runs alone on 32-column slices when the forward kept the
+  // states, else beside the recompute on WALK_BWD_SW-column slices
+  const int bsw = saved ? 32 : WALK_BWD_SW;
   // 3. reverse walk of the state cotangent (with segments: its fold and prefix
   //    now); it needs nothing from the recompute, so the two walks run side by
   //    side in one launch
@@ -425,8 +441,8 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
     if (!tmap_heads(&bm.k, k, d.B, d.T, d.Hk, HD) || !tmap_heads(&bm.q, q, d.B, d.T, d.Hk, HD) ||
         !tmap_2d(&bm.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
         !tmap_2d(&bm.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true) ||
-        !tmap_2d_sw(&bm.Ds, w.dstates, HD, wrows, HD * sizeof(bf16), WALK_BWD_SW, CH, slice_swizzle(WALK_BWD_SW)) ||
-        !tmap_2d_sw(&bm.Dd, w.ddelta, HD, wrows, HD * sizeof(bf16), WALK_BWD_SW, CH, slice_swizzle(WALK_BWD_SW)))
+        !tmap_2d_sw(&bm.Ds, w.dstates, HD, wrows, HD * sizeof(bf16), bsw, CH, slice_swizzle(bsw)) ||
+        !tmap_2d_sw(&bm.Dd, w.ddelta, HD, wrows, HD * sizeof(bf16), bsw, CH, slice_swizzle(bsw)))
       return GDN_ERR_CUDA;
   }
   if (d.S == 1) {
@@ -458,7 +474,11 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
     w.hstart_bh_stride = (long)d.S * HD * HD;
     w.hstart_seg_stride = (long)HD * HD;
   }
-  if ((rc = cuda_status(launch_walk_pair(fw, fm, w, bm, s))) || (rc = mk.rec())) return rc;
+  if (saved)
+    rc = cuda_status(launch_walk_bwd(w, bm, 0, s));
+  else
+    rc = cuda_status(launch_walk_pair(fw, fm, w, bm, s));
+  if (rc || (rc = mk.rec())) return rc;
   // 4. chunk-parallel gradients (dq and dk summed over the value heads of each key head)
   GradArgs ga;
   memset(&ga, 0, sizeof ga);
@@ -469,9 +489,9 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
   ga.beta = beta;
   ga.dO = static_cast<const bf16*>(dO);
   ga.Tb = tl.Tb;
-  ga.states = at<bf16>(ws, L.states);
+  ga.states = tl.states;
   ga.dstates = at<bf16>(ws, L.dstates);
-  ga.delta = at<bf16>(ws, L.delta);
+  ga.delta = tl.delta;
   ga.ddelta = at<bf16>(ws, L.ddelta);
   ga.dq = static_cast<bf16*>(dq);
   ga.dk = static_cast<bf16*>(dk);

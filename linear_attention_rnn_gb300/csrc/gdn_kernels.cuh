@@ -138,7 +138,8 @@ size_t grad_smem_bytes();
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 // The forward walk: its segment fold (fold = 1) or the walk with output.
 cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold, cudaStream_t s);
-// The backward walk's segment fold (fold = 1 only).
+// The backward walk on 32-column slices: its segment fold (fold = 1), or the
+// walk alone (fold = 0; the maps' dh' and dDelta stores have 32-column boxes).
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, const WalkBwdMaps& m, int fold, cudaStream_t s);
 // The forward walk's recompute mode and the backward walk (fold = 0 both) in one launch.
 cudaError_t launch_walk_pair(const WalkFwdArgs& fa, const WalkFwdMaps& fm, const WalkBwdArgs& ba,

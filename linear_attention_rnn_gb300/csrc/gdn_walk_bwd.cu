@@ -29,9 +29,10 @@ cudaError_t launch_one(const WalkBwdArgs& a, const WalkBwdMaps& m, cudaStream_t 
 }  // namespace
 
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, const WalkBwdMaps& m, int fold, cudaStream_t s) {
-  // the fold, on 32-column slices; the walk runs in the pair launch
-  if (!fold) return cudaErrorInvalidValue;
-  return launch_one<true, 32>(a, m, s);
+  // both on 32-column slices: the fold, or the walk alone (when the states it
+  // needs beside it were kept by the forward; otherwise it runs in the pair launch)
+  if (fold) return launch_one<true, 32>(a, m, s);
+  return launch_one<false, 32>(a, m, s);
 }
 
 }  // namespace gdn

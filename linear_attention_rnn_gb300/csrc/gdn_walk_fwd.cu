@@ -7,8 +7,9 @@ namespace gdn {
 
 namespace {
 
+// (the walk with output and staged exports runs one more warp, the stores')
 template <bool FOLD, bool STAGED, int SW>
-__global__ void __launch_bounds__(walkf::FwdCfg<SW>::NT, 1)
+__global__ void __launch_bounds__(walkf::FwdCfg<SW>::NT + 32, 1)
     k_walk_fwd(WalkFwdArgs a, const __grid_constant__ WalkFwdMaps mp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -22,7 +23,8 @@ cudaError_t launch_one(const WalkFwdArgs& a, const WalkFwdMaps& m, cudaStream_t 
       cudaFuncSetAttribute(k_walk_fwd<FOLD, STAGED, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   constexpr int NSL = HD / SW;
-  k_walk_fwd<FOLD, STAGED, SW><<<dim3(FOLD ? 2 * NSL : NSL, a.S, a.B * a.Hv), walkf::FwdCfg<SW>::NT, smem, s>>>(a, m);
+  const int nt = walkf::FwdCfg<SW>::NT + ((STAGED && a.o) ? 32 : 0);
+  k_walk_fwd<FOLD, STAGED, SW><<<dim3(FOLD ? 2 * NSL : NSL, a.S, a.B * a.Hv), nt, smem, s>>>(a, m);
   return cudaGetLastError();
 }
 
@@ -30,7 +32,11 @@ cudaError_t launch_one(const WalkFwdArgs& a, const WalkFwdMaps& m, cudaStream_t 
 
 cudaError_t launch_walk_fwd(const WalkFwdArgs& a, const WalkFwdMaps& m, int fold, cudaStream_t s) {
   if (fold) return launch_one<true, false, 32>(a, m, s);
-  if (a.states || a.delta || !a.o) return cudaErrorInvalidValue;  // the recompute runs in the pair launch
+  // with output; with the entering states and Delta also (for a backward that
+  // reads them), staged and stored by TMA as the recompute mode does (which
+  // runs in the pair launch)
+  if (!a.o) return cudaErrorInvalidValue;
+  if (a.states || a.delta) return launch_one<false, true, 32>(a, m, s);
   return launch_one<false, false, 32>(a, m, s);
 }
 

@@ -33,8 +33,10 @@
 //
 // Modes:
 //   RECUR (fold = 0): walk from the segment's entering state, write O (if o
-//     is given), and optionally the bf16 entering state and Delta of every
-//     chunk (backward recomputation) and the final state (last segment).
+//     is given), and optionally (STAGED) the bf16 entering state and Delta of
+//     every chunk, for the backward, and the final state (last segment).  With
+//     both output and exports the tile ring has one slot fewer (the last one
+//     stages the exports) and a fourth extra warp stores them.
 //   FOLD  (fold = 1): pass 1 of the two-pass segment scan ("Shard the
 //     GatedDeltaNet sequence under ici_context_parallelism", description):
 //     push the augmented state [A | B] through the segment's chunks starting
@@ -293,8 +295,9 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
         release(iP);
       }
     }
-  } else if (warp == NCW + 2) {
+  } else if (warp == (withO ? NCW + 3 : NCW + 2)) {
     // ============================================================ TMA stores
+    // (with output, the block has a fourth extra warp for them)
     // The h and Delta slices staged for chunk index i leave by TMA stores once
     // the compute threads have signalled them; when the stores have read the
     // buffers they are handed back.  A store request can block its thread, so
@@ -355,7 +358,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
         (void)iP;
       }
     }
-  } else {
+  } else if (warp < NCW) {
     // ========================================================== compute threads
     finish_gates(part, 0, gam_r, ef_r, gC);
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32u * g32;  // lanes of this warp, its columns

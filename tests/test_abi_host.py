@@ -95,7 +95,7 @@ def test_segment_fold_argument_errors(L):
 def test_saved_buffer_argument_errors(L):
     import linear_attention_rnn_gb300 as g
     need = g.saved_bytes(1, 256, 2, 4, n_segments=1)
-    assert need == 4 * 4 * 2 * 128 * 128 * 2  # w, u, P, T: bf16 tiles per (chunk, value head)
+    assert need == 6 * 4 * 2 * 128 * 128 * 2  # w, u, P, T, h, Delta: bf16 tiles per (chunk, value head)
     assert g.saved_bytes(1, 256, 2, 4, chunk=64) == 0
     # with 2 segments also the fp32 state entering each segment of each value head
     assert g.saved_bytes(1, 256, 2, 4, n_segments=2) == need + 4 * 2 * 128 * 128 * 4
