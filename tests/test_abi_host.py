@@ -110,6 +110,37 @@ def test_saved_buffer_argument_errors(L):
     assert bwd(FAKE, 16) == -3
 
 
+def test_layer_argument_errors(L):
+    import linear_attention_rnn_gb300 as g
+    need_f = g.layer_workspace_bytes(0, 1, 256, 2, 4)
+    need_b = g.layer_workspace_bytes(1, 1, 256, 2, 4)
+    # the rule's workspace plus normalised q, k (bf16 [T, Hk, 128]) and a v-shaped bf16 buffer,
+    # and for the backward also the normalised q and k cotangents
+    qk, vv = 256 * 2 * 128 * 2, 256 * 4 * 128 * 2
+    assert need_f == g.fwd_workspace_bytes(1, 256, 2, 4) + 2 * qk + vv
+    assert need_b == g.bwd_workspace_bytes(1, 256, 2, 4) + 4 * qk + vv
+    assert g.layer_workspace_bytes(0, 1, 256, 2, 4, dk=64) == 0
+
+    def fwd(z=FAKE, y=FAKE, a=FAKE, ws=FAKE, nbytes=1 << 30, T=256, dk=128):
+        return L.gdn_layer_fwd(FAKE, FAKE, FAKE, a, FAKE, z, None, y, None, None, 1, T, 2, 4, dk, 128,
+                               128, 1, ws, nbytes, None)
+    assert fwd(dk=64) == -2
+    assert fwd(a=None) == -1
+    assert fwd(y=None) == -1
+    assert fwd(z=MISAL) == -1
+    assert fwd(nbytes=need_f - 1) == -3
+    assert fwd(T=0, ws=None, nbytes=0) == 0  # no tokens, no h0, no hT: nothing to do
+
+    def bwd(z=FAKE, o=FAKE, dz=FAKE, nbytes=1 << 30):
+        return L.gdn_layer_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, z, None, o, FAKE, None, FAKE, FAKE,
+                               FAKE, FAKE, FAKE, dz, None, 1, 256, 2, 4, 128, 128, 128, 1, FAKE,
+                               nbytes, None)
+    assert bwd(o=None) == -1          # the gate's backward needs the ungated output
+    assert bwd(dz=None) == -1
+    assert bwd(nbytes=need_b - 1) == -3
+    assert bwd(z=None, o=None, dz=None, nbytes=16) == -3  # without a gate o and dz are not needed
+
+
 def test_workspace_sizes(L):
     f = gdn.fwd_workspace_bytes
     b = gdn.bwd_workspace_bytes
