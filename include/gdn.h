@@ -175,6 +175,12 @@ int gdn_chunk_bwd_ex(const void* q, const void* k, const void* v, const float* g
  *     are what the caller passes);
  *   o = the rule on (q_n, k_n, v, g, beta, h0)            (as gdn_chunk_fwd);
  *   y = o * silu(z), silu(z) = z sigmoid(z)                 (z NULL: y = o).
+ * The forward never forms q_n, k_n: the preparation kernel takes 1/||q|| and
+ * 1/||k|| of each raw row (fp32) and applies them to its products, and the
+ * walk scales its rows by them, so the unit rows are exact to fp32 rather
+ * than rounded to bf16.  The backward forms bf16 copies of q_n, k_n in its
+ * workspace, runs the rule's backward on them and maps dq_n, dk_n back to
+ * the raw rows.
  * Forward: q, k, v, z bf16 (layouts of gdn_chunk_fwd; z as v); a, b fp32
  * [B, T, Hv]; writes y (bf16), o (bf16, the ungated output the backward needs
  * when z is given; NULL = not kept) and hT (NULL = not written).

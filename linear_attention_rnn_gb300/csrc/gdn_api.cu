@@ -166,10 +166,11 @@ struct Marks {
 int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const Tiles& tl, const void* q,
                          const void* k, const float* g, const float* h0, void* o, float* hT,
                          bf16* states, bf16* delta, int gate_logits, bool hin_ready, cudaStream_t s,
-                         Marks& mk, WalkFwdArgs& w, WalkFwdMaps& mp) {
+                         Marks& mk, WalkFwdArgs& w, WalkFwdMaps& mp, const float* nrm = nullptr) {
   const int esw = o ? 32 : WALK_STATES_SW;
   memset(&w, 0, sizeof w);
   w.gate_logits = gate_logits;
+  w.nrm = nrm;
   w.W = tl.W;
   w.U = tl.U;
   w.P = tl.P;
@@ -291,7 +292,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
                     const float* beta, const float* h0, void* o, float* hT, int B, int T, int Hk,
                     int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws,
                     size_t ws_bytes, void* stream, void* const* events, int n_events,
-                    int gate_logits = 0, void* saved = nullptr, size_t saved_bytes = 0) {
+                    int gate_logits = 0, void* saved = nullptr, size_t saved_bytes = 0,
+                    float* nrm = nullptr) {
   int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
   if (rc) return rc;
   const long tokens = (long)B * T;
@@ -327,6 +329,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   p.U = tl.U;
   p.P = tl.P;
   p.Tb = saved ? tl.Tb : nullptr;
+  p.nrm = nrm;  // raw q and k: prep scales its tiles' rows to unit length
   p.status = at<int>(ws, L.status);
   p.gate_logits = gate_logits;
   p.B = B;
@@ -340,7 +343,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   WalkFwdMaps mp;
   // with a saved buffer the walk also keeps the entering state of every chunk and Delta
   if ((rc = prepare_forward_walk(d, L, ws, tl, q, k, g, h0, o, hT, saved ? tl.states : nullptr,
-                                 saved ? tl.delta : nullptr, gate_logits, false, s, mk, w, mp)))
+                                 saved ? tl.delta : nullptr, gate_logits, false, s, mk, w, mp, nrm)))
     return rc;
   if ((rc = cuda_status(launch_walk_fwd(w, mp, 0, s)))) return rc;
   return mk.rec();
@@ -573,7 +576,7 @@ int gdn_chunk_bwd_timed(const void* q, const void* k, const void* v, const float
 // the rule's output cotangent), and for the backward the cotangents of the
 // normalised q and k.
 struct LayerLayout {
-  size_t core, qn, kn, obuf, dO, dqn, dkn, total;
+  size_t core, nrm, qn, kn, obuf, dO, dqn, dkn, total;
 };
 
 static LayerLayout layer_layout(int backward, int B, int T, int Hk, int Hv, int n_segments) {
@@ -589,13 +592,16 @@ static LayerLayout layer_layout(int backward, int B, int T, int Hk, int Hv, int 
     return o;
   };
   L.core = take(layout(d, backward != 0).total);
-  L.qn = take(qk);
-  L.kn = take(qk);
-  L.obuf = take(vv);
-  L.dO = L.obuf;
-  if (backward) {
+  if (backward) {  // normalised copies of q and k, and their cotangents
+    L.qn = take(qk);
+    L.kn = take(qk);
+    L.obuf = take(vv);
+    L.dO = L.obuf;
     L.dqn = take(qk);
     L.dkn = take(qk);
+  } else {  // the rows' 1/||k||, 1/||q|| (the forward normalises inside its kernels)
+    L.nrm = take((size_t)B * Hk * d.NC * 2 * CH * sizeof(float));
+    L.obuf = take(vv);
   }
   L.total = off;
   return L;
@@ -627,14 +633,13 @@ int gdn_layer_fwd(const void* q, const void* k, const void* v, const float* a, c
                     stream, nullptr, 0, 1);
   const LayerLayout L = layer_layout(0, B, T, Hk, Hv, n_segments);
   if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
-  bf16* qn = at<bf16>(ws, L.qn);
-  bf16* kn = at<bf16>(ws, L.kn);
-  if ((rc = cuda_status(launch_l2norm(static_cast<const bf16*>(q), qn, tokens * Hk, kL2Eps, s)))) return rc;
-  if ((rc = cuda_status(launch_l2norm(static_cast<const bf16*>(k), kn, tokens * Hk, kL2Eps, s)))) return rc;
-  // the rule's output: straight into y without a gate, else into o (or the workspace)
+  // the rule's output: straight into y without a gate, else into o (or the workspace);
+  // q and k go in raw: the preparation normalises the rows of its K and Q tiles and
+  // the walk scales by the same 1/||k||, 1/||q|| where it reads them
   void* core_o = !z ? y : (o ? o : at<void>(ws, L.obuf));
-  rc = fwd_impl(qn, kn, v, a, b, h0, core_o, hT, B, T, Hk, Hv, d_k, d_v, chunk, n_segments,
-                at<void>(ws, L.core), L.qn - L.core, stream, nullptr, 0, 1);
+  rc = fwd_impl(q, k, v, a, b, h0, core_o, hT, B, T, Hk, Hv, d_k, d_v, chunk, n_segments,
+                at<void>(ws, L.core), L.nrm - L.core, stream, nullptr, 0, 1, nullptr, 0,
+                at<float>(ws, L.nrm));
   if (rc) return rc;
   if (z) {
     rc = cuda_status(launch_out_gate(static_cast<const bf16*>(core_o), static_cast<const bf16*>(z),

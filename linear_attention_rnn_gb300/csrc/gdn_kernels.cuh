@@ -23,6 +23,8 @@ struct PrepArgs {
   float* S_dbg;  // [BH][NC][CH][CH]  fp32 S  (debug export)        (nullable)
   float* T_dbg;  // [BH][NC][CH][CH]  fp32 T  (debug export)        (nullable)
   int* status;   // bit 0 set if a bounded wait gave up (nullable)
+  float* nrm;    // non-null: q, k are raw rows; prep normalises its K and Q tiles in shared
+                 // memory and writes 1/||k||, 1/||q|| per row here, [B][Hk][NC][2][CH]
   int gate_logits;         // 1: g and beta hold logits a, b (g = -softplus(a), beta = sigmoid(b))
   int B, T, Hk, Hv, NC;
 };
@@ -46,6 +48,7 @@ struct WalkFwdArgs {
   float* pairA;            // fold output [BH][S][HD][HD]
   float* pairB;            // fold output [BH][S][HD][HD]
   int* status;             // bit 0 set if a bounded wait gave up (nullable)
+  const float* nrm;        // non-null: K and Q tiles are raw rows, these their 1/||.|| (as PrepArgs)
   int gate_logits;         // 1: g and beta hold logits a, b (g = -softplus(a), beta = sigmoid(b))
   int B, T, Hk, Hv, NC, S;
 };

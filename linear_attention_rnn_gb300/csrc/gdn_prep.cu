@@ -322,21 +322,49 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
     // the next group of this CTA's range (valid if ug + jj1 - jj0 < u_end)
     const long ug_next = ug + (jj1 - jj0);
     const Unit xn = decode(ug_next < u_end ? ug_next : ug);
-    if (tid == 0) {
-      if (!next_loaded) {  // the first group of the range
-        load_kq(b, c, kh, sm.A[kb]);
-        if (needU) {
-          load_v(jj0);
-          if (jj0 + 1 < jj1) load_v(jj0 + 1);
-        }
+    if (tid == 0 && !next_loaded) {  // the first group of the range
+      load_kq(b, c, kh, sm.A[kb]);
+      if (needU) {
+        load_v(jj0);
+        if (jj0 + 1 < jj1) load_v(jj0 + 1);
       }
+    }
+    next_loaded = false;
+    if (a.nrm) {
+      // raw q and k: the rows' 1/||k|| and 1/||q||, 1 / sqrt(sum x^2 + 1e-6), go to
+      // nrm (thread t: row t / 4, 32 columns).  The tiles stay raw, as the walk
+      // reads them: K K^T, Q K^T and w = T'' K take the scales in their epilogues.
+      ok = ok && tc::mbar_wait(&sm.barKQ, (uint32_t)(kq_uses & 1));
+      float* nb = a.nrm + ((((long)b * a.Hk + kh) * a.NC + c) << 8);
+      auto row_scale = [&](const unsigned char* tile, float* dst) {
+        const int rr = tid >> 2, q4 = tid & 3;
+        const unsigned char* rowp = tile + (q4 >> 1) * (TILE / 2) + rr * 128;
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 x = *reinterpret_cast<const uint4*>(rowp + (((4 * (q4 & 1) + i) ^ (rr & 7)) << 4));
+          const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16(w4[e]);
+            ss += f.x * f.x + f.y * f.y;
+          }
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        if (q4 == 0) dst[rr] = rsqrtf(ss + 1e-6f);
+      };
+      row_scale(sm.A[kb], nb);
+      if (needP) row_scale(qbuf, nb + CH);
+      __syncthreads();  // the scales are read by every epilogue thread below
+    }
+    if (tid == 0) {
       ok = ok && tc::mbar_wait(&sm.barKQ, (uint32_t)(kq_uses & 1));
       tc::fence_after();
       tc::gemm_k128(tmem + 0, smem_u32(sm.A[kb]), smem_u32(sm.A[kb]), 128, false);
       if (needP) tc::gemm_k128(tmem + 128, smem_u32(qbuf), smem_u32(sm.A[kb]), 128, false);
       tc::commit(&sm.barM);
     }
-    next_loaded = false;
 
     for (int jj = jj0; jj < jj1; ++jj) {
       const int j = kh * group + jj;
@@ -386,7 +414,11 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       // 100 over its columns could overflow etab and takes the direct exponentials;
       // elsewhere a row whose first factor underflows has true decays below 2^-26.
       {
-        const float Glr = sm.Gl[row], br = sm.beta[row];
+        const float Glr = sm.Gl[row];
+        // raw K and Q rows: S takes 1/||k_r|| 1/||k_s||, P 1/||q_r|| 1/||k_s||
+        const float* nb = a.nrm ? a.nrm + ((((long)b * a.Hk + kh) * a.NC + c) << 8) : nullptr;
+        const float br = sm.beta[row] * (nb ? nb[row] : 1.f);
+        const float pr = nb ? nb[CH + row] : 1.f;
         float* Sd = reinterpret_cast<float*>(sm.Tp + SD);
 #pragma unroll 1
         for (int cb = 0; cb < 32; cb += 16) {
@@ -404,12 +436,16 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
 #pragma unroll
               for (int i = 0; i < 16; ++i) mv[i] = exp2f(Glr - sm.Gl[c0 + i]);
             }
+            if (nb) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) mv[i] *= nb[c0 + i];  // 1/||k_s|| of column s
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int s = c0 + i;
               const float m = (s <= row) ? mv[i] : 0.f;  // one decay for S and P
               sv[i] = (s < row) ? br * kk[i] * m : 0.f;
-              pv[i] = needP ? pv[i] * m : 0.f;
+              pv[i] = needP ? pr * pv[i] * m : 0.f;
             }
           } else {
 #pragma unroll
@@ -482,7 +518,9 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       }
       // P's store has read Kg before T diag(beta gamma) is written there; the
       // decay table is dead, so it takes gamma (etab[s] = exp(G_s))
-      if (tid < CH) sm.etab[tid] = exp2f(sm.Gl[tid]);
+      // (with raw K rows also 1/||k_s||: T'' = T diag(beta gamma / ||k||), w = T'' K)
+      if (tid < CH)
+        sm.etab[tid] = exp2f(sm.Gl[tid]) * (a.nrm ? a.nrm[((((long)b * a.Hk + kh) * a.NC + c) << 8) + tid] : 1.f);
       if (tid == 0) tc::bulk_wait_read();
       __syncthreads();
       // ---- T' = T diag(beta) and T'' = T diag(beta gamma) (bf16, K-major SW128) ----------

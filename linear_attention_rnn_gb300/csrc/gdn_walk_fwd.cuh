@@ -203,6 +203,17 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
     if (lane == 31) sm.gsum[i & 1][warp & 3] = gv;  // both column groups post the same totals
     return gv;
   };
+  // raw K and Q rows (a.nrm): this row's 1/||k|| and 1/||q|| in chunk c, which
+  // scale ef (the state update reads K) and gamma (the output reads Q)
+  float nk_next = 1.f, nq_next = 1.f;
+  auto load_n = [&](int c, float& nk, float& nq) {
+    nk = nq = 1.f;
+    if (a.nrm && c < cend) {
+      const float* nb = a.nrm + ((((long)b * a.Hk + kh) * a.NC + c) << 8);
+      nk = nb[r];
+      nq = nb[CH + r];
+    }
+  };
   // after a barrier over the compute threads: gamma_r, ef_r and gamma_C of chunk index i
   auto finish_gates = [&](float p, int i, float& gm, float& ef, float& gc) {
     float off = 0.f, tot = 0.f;
@@ -213,8 +224,8 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
       tot += s;
     }
     const float G = p + off;
-    gm = expf(G);
-    ef = expf(tot - G);
+    gm = expf(G) * nq_next;  // the norms of chunk index i were loaded a chunk ahead
+    ef = expf(tot - G) * nk_next;
     gc = expf(tot);
   };
   if (warp < NCW) {
@@ -237,6 +248,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
     load_u(cbeg);
     part = scan_part(load_g(cbeg), 0);
     gnext = load_g(cbeg + 1);
+    load_n(cbeg, nk_next, nq_next);
   }
   tc::fence_proxy_async();
   tc::fence_before();
@@ -361,6 +373,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
   } else if (warp < NCW) {
     // ========================================================== compute threads
     finish_gates(part, 0, gam_r, ef_r, gC);
+    load_n(cbeg + 1, nk_next, nq_next);
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32u * g32;  // lanes of this warp, its columns
     for (int c = cbeg; c < cend; ++c) {
       const int ci = c - cbeg;
@@ -420,6 +433,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
       gnext = load_g(c + 2);
       asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");
       finish_gates(part, ci + 1, gam_n, ef_n, gC_n);
+      load_n(c + 2, nk_next, nq_next);
 
       // ---- h' = gamma_C h + H' ---------------------------------------------------
       ok = ok && tc::mbar_wait(&sm.barH, par);

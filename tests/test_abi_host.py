@@ -114,10 +114,11 @@ def test_layer_argument_errors(L):
     import linear_attention_rnn_gb300 as g
     need_f = g.layer_workspace_bytes(0, 1, 256, 2, 4)
     need_b = g.layer_workspace_bytes(1, 1, 256, 2, 4)
-    # the rule's workspace plus normalised q, k (bf16 [T, Hk, 128]) and a v-shaped bf16 buffer,
-    # and for the backward also the normalised q and k cotangents
+    # forward: the rule's workspace, the rows' 1/||k|| and 1/||q|| (fp32 [Hk, chunks, 2, 128]) and a
+    # v-shaped bf16 buffer; backward: normalised q, k (bf16 [T, Hk, 128]), their cotangents and
+    # the v-shaped buffer
     qk, vv = 256 * 2 * 128 * 2, 256 * 4 * 128 * 2
-    assert need_f == g.fwd_workspace_bytes(1, 256, 2, 4) + 2 * qk + vv
+    assert need_f == g.fwd_workspace_bytes(1, 256, 2, 4) + 2 * 2 * 2 * 128 * 4 + vv
     assert need_b == g.bwd_workspace_bytes(1, 256, 2, 4) + 4 * qk + vv
     assert g.layer_workspace_bytes(0, 1, 256, 2, 4, dk=64) == 0
 

@@ -1,16 +1,19 @@
 """GPU parity of the layer entry points (gdn_layer_fwd / gdn_layer_bwd)
 against the fp64 oracle: q and k normalised per token, gate logits
 (g = -softplus(a), beta = sigmoid(b)) applied where the rule's kernels load
-the gates, and the output gate y = o * silu(z).  The oracle forms the rule's
-inputs in fp64 (q_n, k_n rounded to bf16, g and beta to fp32), runs the
-per-token rule and its adjoint, and applies the written-out backwards of the
-element-wise operations (oracle/layer.py).  Tolerances as for the rule:
+the gates, and the output gate y = o * silu(z).  The forward normalises q and
+k inside its kernels (the rows stay raw, their 1/||.|| scale the products), so
+its reference runs the chunked route on fp64 unit rows; the backward takes
+bf16 normalised copies, so its reference forms them the same way (rounded to
+bf16), runs the per-token adjoint, and applies the written-out backwards of
+the element-wise operations (oracle/layer.py).  Tolerances as for the rule:
 2e-2 on y and o, 1e-2 on hT, 3e-2 on every gradient."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
+from oracle import chunked
 from oracle import layer as ol
 from linear_attention_rnn_gb300.inputs import WORKLOADS, make_layer_host
 from conftest import assert_rel
@@ -43,12 +46,22 @@ def _check_layer(gdn, raw, gate=True, record=None):
             out[b_, j] = per_head[i]
         return out
 
-    # oracle forward on the rule's inputs formed from the raw ones
+    # oracle forward: the forward normalises q and k inside its kernels without
+    # rounding the unit rows, so the reference takes them in fp64 (the chunked
+    # route, pinned to the per-token rule) on fp64 gates from the fp32 logits
     from linear_attention_rnn_gb300.inputs import Inputs
+    qn, kn = ol.l2norm(_f64(raw.q)), ol.l2norm(_f64(raw.k))
+    g64, b64 = ol.gates(_f64(raw.a), _f64(raw.b))
+    grp = wl.Hv // wl.Hk
+    h0 = None if raw.h0 is None else _f64(raw.h0)
+    o_ref = np.zeros((wl.B, wl.T, wl.Hv, wl.dv))
+    h_ref = np.zeros((wl.B, wl.Hv, wl.dk, wl.dv))
+    for b_, j in heads:
+        o_ref[b_, :, j], h_ref[b_, j] = chunked.head_fwd(
+            qn[b_, :, j // grp], kn[b_, :, j // grp], _f64(raw.v)[b_, :, j], g64[b_, :, j], b64[b_, :, j],
+            None if h0 is None else h0[b_, j], 128)
+    # the backward takes bf16 normalised copies of q and k: its reference rounds them too
     ri = ol.rule_inputs(Inputs(wl, raw.q, raw.k, raw.v, raw.a, raw.b, raw.h0))
-    ro, rh = oracle.fwd(ri)
-    o_ref = np.moveaxis(full(ro, (wl.T, wl.dv)), 1, 2)  # [B, T, Hv, dv]
-    h_ref = full(rh, (wl.dk, wl.dv))
     zz = _f64(raw.z)
     y_ref = ol.out_gate(o_ref, zz) if gate else o_ref
     assert_rel(_f64(y), y_ref, O_TOL, "y", m("y"))
