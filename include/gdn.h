@@ -42,7 +42,16 @@
  *     no effect.  GDN_ERR_CUDA reports a launch failure (cudaGetLastError).
  *   - Supported sizes in this version: d_k = d_v = 128, chunk = 128, any
  *     T >= 0 (a ragged last chunk is zero-padded with g = 0, beta = 0, which
- *     leaves the state unchanged), Hv a multiple of Hk.
+ *     leaves the state unchanged), Hv a multiple of Hk.  The forward entry
+ *     points (gdn_chunk_fwd, its _timed and _ex variants without a saved
+ *     buffer, gdn_chunk_fwd_noalloc, gdn_segment_fold, gdn_layer_fwd,
+ *     gdn_debug_ut and their workspace sizes) also take chunk = 64 (PR "Shard
+ *     the GatedDeltaNet sequence under ici_context_parallelism", review
+ *     thread: forming each device's A_loc with 64-token chunks): the state
+ *     then steps every 64 tokens.  The backward entry points, and a forward
+ *     that keeps tiles for them, take chunk = 128 only (GDN_ERR_SHAPE
+ *     otherwise); their results do not depend on the chunk size beyond
+ *     rounding, so a backward with chunk = 128 serves a forward run with 64.
  *   - Workspace: the caller passes `ws` of at least the size the matching
  *     *_workspace_bytes call returns for the same arguments (256-byte aligned).
  *     Its contents on entry do not matter.  Its first 4 bytes are a status
@@ -325,7 +334,11 @@ int gdn_segment_fold(const void* k, const void* v, const float* g, const float* 
  *   w_out [.., chunk, d_k]   bf16  w = T diag(beta exp(G)) K
  *   u_out [.., chunk, d_v]   bf16  u = T diag(beta) V
  * Any output may be NULL.  Rows of a ragged last chunk beyond T are the
- * zero-padding rows.  Uses no workspace.
+ * zero-padding rows.  Uses no workspace.  With chunk = 64 the outputs are
+ * the device's 128-row tiles, N = ceil(T/128) per (b, j), each holding two
+ * chunks: S_out, T_out [.., 128, 128] block diagonal (chunk 2t in rows and
+ * columns 0-63 of tile t, chunk 2t + 1 in 64-127, zeros elsewhere), w_out and
+ * u_out [.., 128, d] (chunk 2t in rows 0-63, chunk 2t + 1 in rows 64-127).
  */
 int gdn_debug_ut(const void* k, const void* v, const float* g,
                  const float* beta, float* S_out, float* T_out, void* w_out, void* u_out,

@@ -351,25 +351,41 @@ def segment_fold(k, v, g, beta, n_segments: int = 1, *, chunk: int = 128, want_A
     return A, Bm
 
 
-def debug_ut(k, v, g, beta, chunk: int = 128):
-    """Per-chunk S, T (fp32) and w, u (bf16), each [B, Hv, N, chunk, .]."""
+def debug_ut(k, v, g, beta, chunk: int = 128, tiles: bool = False):
+    """Per-chunk S, T (fp32) and w, u (bf16), each [B, Hv, N, chunk, .].
+
+    The library exports 128-row tiles; with chunk = 64 each holds two chunks
+    (S and T block diagonal).  tiles=True returns those tiles as exported,
+    [B, Hv, ceil(T / 128), 128, .]."""
     B, T, Hk, dk = k.shape
     Hv, dv = v.shape[2], v.shape[3]
     _check(k, "k", torch.bfloat16)
     _check(v, "v", torch.bfloat16, (B, T, Hv, dv))
     _check(g, "g", torch.float32, (B, T, Hv))
     _check(beta, "beta", torch.float32, (B, T, Hv))
-    N = (T + chunk - 1) // chunk
+    NT = (T + 127) // 128
     dev = k.device
-    S = torch.empty((B, Hv, N, chunk, chunk), dtype=torch.float32, device=dev)
+    S = torch.empty((B, Hv, NT, 128, 128), dtype=torch.float32, device=dev)
     Tm = torch.empty_like(S)
-    w = torch.empty((B, Hv, N, chunk, dk), dtype=torch.bfloat16, device=dev)
-    u = torch.empty((B, Hv, N, chunk, dv), dtype=torch.bfloat16, device=dev)
+    w = torch.empty((B, Hv, NT, 128, dk), dtype=torch.bfloat16, device=dev)
+    u = torch.empty((B, Hv, NT, 128, dv), dtype=torch.bfloat16, device=dev)
     rc = lib().gdn_debug_ut(_ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S), _ptr(Tm), _ptr(w),
                             _ptr(u), B, T, Hk, Hv, dk, dv, chunk, _stream(dev))
     if rc != GDN_OK:
         raise GDNError(rc, "gdn_debug_ut")
-    return S, Tm, w, u
+    if tiles or chunk == 128:
+        return S, Tm, w, u
+    N = (T + chunk - 1) // chunk  # chunk 64: the diagonal blocks and row halves of the tiles
+
+    def diag(x):
+        x6 = x.view(B, Hv, NT, 2, 64, 2, 64)
+        return torch.stack([x6[:, :, :, 0, :, 0, :], x6[:, :, :, 1, :, 1, :]], 3).reshape(
+            B, Hv, 2 * NT, 64, 64)[:, :, :N]
+
+    def rows(x):
+        return x.reshape(B, Hv, 2 * NT, 64, x.shape[-1])[:, :, :N]
+
+    return diag(S), diag(Tm), rows(w), rows(u)
 
 
 def workspace_status(ws: torch.Tensor) -> int:

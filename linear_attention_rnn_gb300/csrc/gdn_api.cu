@@ -19,26 +19,32 @@ inline size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// C: tokens per chunk (128, or 64 in the forward); NC chunks per sequence; the
+// per-chunk tiles (w, u, P, ...) are stored in NT 128-row tiles per sequence,
+// two 64-token chunks to a tile.
 struct Dims {
-  int B, T, Hk, Hv, NC, S;
+  int B, T, Hk, Hv, NC, S, C, NT;
   long BH() const { return (long)B * Hv; }
 };
 
-int check_dims(int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int n_segments) {
+// chunk = 64 only where the caller allows it (the forward entry points)
+int check_dims(int B, int T, int Hk, int Hv, int dk, int dv, int chunk, int n_segments, bool allow64 = false) {
   if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || n_segments < 0) return GDN_ERR_ARG;
   if (Hv % Hk != 0) return GDN_ERR_ARG;
-  if (dk != HD || dv != HD || chunk != CH) return GDN_ERR_SHAPE;
+  if (dk != HD || dv != HD || !(chunk == CH || (allow64 && chunk == 64))) return GDN_ERR_SHAPE;
   return GDN_OK;
 }
 
-Dims make_dims(int B, int T, int Hk, int Hv, int n_segments) {
+Dims make_dims(int B, int T, int Hk, int Hv, int n_segments, int chunk = CH) {
   Dims d;
   d.B = B;
   d.T = T;
   d.Hk = Hk;
   d.Hv = Hv;
-  d.NC = (T + CH - 1) / CH;
-  int S = n_segments == 0 ? gdn_default_segments(B, T, Hv, CH) : n_segments;
+  d.C = chunk;
+  d.NC = (T + chunk - 1) / chunk;
+  d.NT = (T + CH - 1) / CH;
+  int S = n_segments == 0 ? gdn_default_segments(B, T, Hv, chunk) : n_segments;
   if (S > d.NC) S = d.NC;
   if (S < 1) S = 1;
   d.S = S;
@@ -56,7 +62,7 @@ struct Layout {
 Layout layout(const Dims& d, bool bwd) {
   Layout L;
   memset(&L, 0, sizeof L);
-  const size_t chunks = (size_t)d.BH() * d.NC;
+  const size_t chunks = (size_t)d.BH() * d.NT;  // 128-row tiles
   const size_t tile = (size_t)CH * HD * sizeof(bf16);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -182,6 +188,8 @@ int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const Tiles&
   w.Hk = d.Hk;
   w.Hv = d.Hv;
   w.NC = d.NC;
+  w.NT = d.NT;
+  w.c64 = d.C == 64;
   w.S = d.S;
   w.o = static_cast<bf16*>(o);
   w.hT = hT;
@@ -189,10 +197,11 @@ int prepare_forward_walk(const Dims& d, const Layout& Lw, void* ws, const Tiles&
   w.delta = delta;
   w.status = at<int>(ws, Lw.status);
   memset(&mp, 0, sizeof mp);
-  const uint64_t wrows = (uint64_t)d.BH() * d.NC * CH;
-  if (!tmap_heads(&mp.k, k, d.B, d.T, d.Hk, HD) || !tmap_heads(&mp.q, q, d.B, d.T, d.Hk, HD) ||
-      !tmap_2d(&mp.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
-      !tmap_2d(&mp.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true) ||
+  const uint64_t wrows = (uint64_t)d.BH() * d.NT * CH;
+  const uint32_t box = (uint32_t)d.C;  // tokens (rows) per TMA box: one chunk
+  if (!tmap_heads(&mp.k, k, d.B, d.T, d.Hk, HD, box) || !tmap_heads(&mp.q, q, d.B, d.T, d.Hk, HD, box) ||
+      !tmap_2d(&mp.W, w.W, HD, wrows, HD * sizeof(bf16), 64, box, true) ||
+      !tmap_2d(&mp.P, w.P, CH, wrows, CH * sizeof(bf16), 64, box, true) ||
       (states && !tmap_2d_sw(&mp.St, states, HD, wrows, HD * sizeof(bf16), esw, CH, slice_swizzle(esw))) ||
       (delta && !tmap_2d_sw(&mp.De, delta, HD, wrows, HD * sizeof(bf16), esw, CH, slice_swizzle(esw))))
     return GDN_ERR_CUDA;
@@ -245,7 +254,8 @@ const char* gdn_strerror(int status) {
   switch (status) {
     case GDN_OK: return "ok";
     case GDN_ERR_ARG: return "invalid argument (null pointer, misalignment, negative size or Hv % Hk != 0)";
-    case GDN_ERR_SHAPE: return "unsupported shape (this version needs d_k = d_v = 128 and chunk = 128)";
+    case GDN_ERR_SHAPE:
+      return "unsupported shape (d_k = d_v = 128; chunk = 128, or 64 in the forward entry points)";
     case GDN_ERR_WORKSPACE: return "workspace missing or too small";
     case GDN_ERR_CUDA: return "CUDA launch failed";
     case GDN_ERR_TIMEOUT: return "a bounded in-kernel wait gave up";
@@ -278,8 +288,8 @@ int gdn_default_segments(int B, int T, int Hv, int chunk) {
 
 size_t gdn_fwd_workspace_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk,
                                int n_segments) {
-  if (check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments) != GDN_OK) return 0;
-  return layout(make_dims(B, T, Hk, Hv, n_segments), false).total;
+  if (check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments, true) != GDN_OK) return 0;
+  return layout(make_dims(B, T, Hk, Hv, n_segments, chunk), false).total;
 }
 
 size_t gdn_bwd_workspace_bytes(int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk,
@@ -294,15 +304,16 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
                     size_t ws_bytes, void* stream, void* const* events, int n_events,
                     int gate_logits = 0, void* saved = nullptr, size_t saved_bytes = 0,
                     float* nrm = nullptr) {
-  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments, true);
   if (rc) return rc;
+  if (saved && chunk != CH) return GDN_ERR_SHAPE;  // the backward takes 128-token chunks
   const long tokens = (long)B * T;
   if (tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_ARG;
   const void* ptrs[] = {q, k, v, g, beta, h0, o, hT, ws, saved};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return GDN_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const Dims d = make_dims(B, T, Hk, Hv, n_segments);
+  const Dims d = make_dims(B, T, Hk, Hv, n_segments, chunk);
   if (B == 0) return GDN_OK;
   if (T == 0) {  // no tokens: the final state is the initial state
     if (!hT) return GDN_OK;
@@ -332,11 +343,12 @@ static int fwd_impl(const void* q, const void* k, const void* v, const float* g,
   p.nrm = nrm;  // raw q and k: prep scales its tiles' rows to unit length
   p.status = at<int>(ws, L.status);
   p.gate_logits = gate_logits;
+  p.c64 = d.C == 64;
   p.B = B;
   p.T = T;
   p.Hk = Hk;
   p.Hv = Hv;
-  p.NC = d.NC;
+  p.NC = d.NT;
   rc = cuda_status(launch_prep(p, s));
   if (rc || (rc = mk.rec())) return rc;
   WalkFwdArgs w;
@@ -579,12 +591,12 @@ struct LayerLayout {
   size_t core, nrm, qn, kn, obuf, dO, dqn, dkn, total;
 };
 
-static LayerLayout layer_layout(int backward, int B, int T, int Hk, int Hv, int n_segments) {
+static LayerLayout layer_layout(int backward, int B, int T, int Hk, int Hv, int n_segments, int chunk) {
   LayerLayout L;
   memset(&L, 0, sizeof L);
   const size_t qk = (size_t)B * T * Hk * HD * sizeof(bf16);
   const size_t vv = (size_t)B * T * Hv * HD * sizeof(bf16);
-  const Dims d = make_dims(B, T, Hk, Hv, n_segments);
+  const Dims d = make_dims(B, T, Hk, Hv, n_segments, chunk);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -600,7 +612,7 @@ static LayerLayout layer_layout(int backward, int B, int T, int Hk, int Hv, int 
     L.dqn = take(qk);
     L.dkn = take(qk);
   } else {  // the rows' 1/||k||, 1/||q|| (the forward normalises inside its kernels)
-    L.nrm = take((size_t)B * Hk * d.NC * 2 * CH * sizeof(float));
+    L.nrm = take((size_t)B * Hk * d.NT * 2 * CH * sizeof(float));
     L.obuf = take(vv);
   }
   L.total = off;
@@ -611,15 +623,15 @@ constexpr float kL2Eps = 1e-6f;
 
 size_t gdn_layer_workspace_bytes(int backward, int B, int T, int Hk, int Hv, int d_k, int d_v,
                                  int chunk, int n_segments) {
-  if (check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments) != GDN_OK) return 0;
-  return layer_layout(backward, B, T, Hk, Hv, n_segments).total;
+  if (check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments, !backward) != GDN_OK) return 0;
+  return layer_layout(backward, B, T, Hk, Hv, n_segments, chunk).total;
 }
 
 int gdn_layer_fwd(const void* q, const void* k, const void* v, const float* a, const float* b,
                   const void* z, const float* h0, void* y, void* o, float* hT, int B, int T, int Hk,
                   int Hv, int d_k, int d_v, int chunk, int n_segments, void* ws, size_t ws_bytes,
                   void* stream) {
-  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments, true);
   if (rc) return rc;
   const long tokens = (long)B * T;
   if (tokens > 0 && (!q || !k || !v || !a || !b || !y)) return GDN_ERR_ARG;
@@ -631,7 +643,7 @@ int gdn_layer_fwd(const void* q, const void* k, const void* v, const float* a, c
   if (T == 0)  // no tokens: the final state is the initial state
     return fwd_impl(q, k, v, a, b, h0, y, hT, B, T, Hk, Hv, d_k, d_v, chunk, n_segments, nullptr, 0,
                     stream, nullptr, 0, 1);
-  const LayerLayout L = layer_layout(0, B, T, Hk, Hv, n_segments);
+  const LayerLayout L = layer_layout(0, B, T, Hk, Hv, n_segments, chunk);
   if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
   // the rule's output: straight into y without a gate, else into o (or the workspace);
   // q and k go in raw: the preparation normalises the rows of its K and Q tiles and
@@ -671,7 +683,7 @@ int gdn_layer_bwd(const void* q, const void* k, const void* v, const float* a, c
   if (T == 0)
     return bwd_impl(q, k, v, a, b, h0, dy, dhT, dq, dk, dv, da, db, dh0, B, T, Hk, Hv, d_k, d_v, chunk,
                     n_segments, nullptr, 0, stream, nullptr, 0, 1);
-  const LayerLayout L = layer_layout(1, B, T, Hk, Hv, n_segments);
+  const LayerLayout L = layer_layout(1, B, T, Hk, Hv, n_segments, CH);
   if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
   bf16* qn = at<bf16>(ws, L.qn);
   bf16* kn = at<bf16>(ws, L.kn);
@@ -726,9 +738,9 @@ int gdn_affine_compose(const float* A, const float* B, float* A_out, float* B_ou
 int gdn_segment_fold(const void* k, const void* v, const float* g, const float* beta,
                      float* A_out, float* B_out, int B, int T, int Hk, int Hv, int d_k, int d_v,
                      int chunk, int n_segments, void* ws, size_t ws_bytes, void* stream) {
-  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments);
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, n_segments, true);
   if (rc) return rc;
-  const int NC = (T + CH - 1) / CH;
+  const int NC = (T + chunk - 1) / chunk;
   if (n_segments < 1 || n_segments > (NC > 1 ? NC : 1)) return GDN_ERR_ARG;
   if (B == 0) return GDN_OK;
   if (!B_out) return GDN_ERR_ARG;
@@ -738,7 +750,7 @@ int gdn_segment_fold(const void* k, const void* v, const float* g, const float* 
     if (p && !aligned16(p)) return GDN_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (T == 0) return cuda_status(launch_identity_pairs(A_out, B_out, (long)B * Hv, s));
-  const Dims d = make_dims(B, T, Hk, Hv, 1);
+  const Dims d = make_dims(B, T, Hk, Hv, 1, chunk);
   const Layout L = layout(d, false);
   if (!ws || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
   if ((rc = cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), s)))) return rc;
@@ -753,11 +765,12 @@ int gdn_segment_fold(const void* k, const void* v, const float* g, const float* 
   p.W = at<bf16>(ws, L.W);
   p.U = at<bf16>(ws, L.U);
   p.status = at<int>(ws, L.status);
+  p.c64 = chunk == 64;
   p.B = B;
   p.T = T;
   p.Hk = Hk;
   p.Hv = Hv;
-  p.NC = NC;
+  p.NC = d.NT;
   if ((rc = cuda_status(launch_prep(p, s)))) return rc;
   // pass 1 of the segment scan: each segment's chunks pushed through [A | B] from [I | 0]
   WalkFwdArgs f;
@@ -773,16 +786,19 @@ int gdn_segment_fold(const void* k, const void* v, const float* g, const float* 
   f.Hk = Hk;
   f.Hv = Hv;
   f.NC = NC;
+  f.NT = d.NT;
+  f.c64 = chunk == 64;
   f.S = n_segments;
   f.pairA = A_out;
   f.pairB = B_out;
   f.status = p.status;
   WalkFwdMaps mp;
   memset(&mp, 0, sizeof mp);
-  const uint64_t wrows = (uint64_t)d.BH() * NC * CH;
-  if (!tmap_heads(&mp.k, k, B, T, Hk, HD) || !tmap_heads(&mp.q, k, B, T, Hk, HD) ||
-      !tmap_2d(&mp.W, f.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
-      !tmap_2d(&mp.P, f.P, CH, wrows, CH * sizeof(bf16), 64, CH, true))
+  const uint64_t wrows = (uint64_t)d.BH() * d.NT * CH;
+  const uint32_t box = (uint32_t)chunk;
+  if (!tmap_heads(&mp.k, k, B, T, Hk, HD, box) || !tmap_heads(&mp.q, k, B, T, Hk, HD, box) ||
+      !tmap_2d(&mp.W, f.W, HD, wrows, HD * sizeof(bf16), 64, box, true) ||
+      !tmap_2d(&mp.P, f.P, CH, wrows, CH * sizeof(bf16), 64, box, true))
     return GDN_ERR_CUDA;
   return cuda_status(launch_walk_fwd(f, mp, 1, s));
 }
@@ -790,7 +806,7 @@ int gdn_segment_fold(const void* k, const void* v, const float* g, const float* 
 int gdn_debug_ut(const void* k, const void* v, const float* g, const float* beta, float* S_out,
                  float* T_out, void* w_out, void* u_out, int B, int T, int Hk, int Hv, int d_k,
                  int d_v, int chunk, void* stream) {
-  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, 1);
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, 1, true);
   if (rc) return rc;
   if ((long)B * T == 0) return GDN_OK;
   if (!k || !v || !g || !beta) return GDN_ERR_ARG;
@@ -808,11 +824,12 @@ int gdn_debug_ut(const void* k, const void* v, const float* g, const float* beta
   p.U = static_cast<bf16*>(u_out);
   p.S_dbg = S_out;
   p.T_dbg = T_out;
+  p.c64 = chunk == 64;
   p.B = B;
   p.T = T;
   p.Hk = Hk;
   p.Hv = Hv;
-  p.NC = (T + CH - 1) / CH;
+  p.NC = (T + CH - 1) / CH;  // 128-row tiles
   return cuda_status(launch_prep(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -892,9 +909,9 @@ extern "C" int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v
                                      const float* beta, const float* h0, void* o, float* hT,
                                      int B, int T, int Hk, int Hv, int d_k, int d_v, int chunk,
                                      void* stream) {
-  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, 1);
+  int rc = check_dims(B, T, Hk, Hv, d_k, d_v, chunk, 1, true);
   if (rc) return rc;
-  const long units = (long)B * Hv * ((T + CH - 1) / CH);
+  const long units = (long)B * Hv * ((T + CH - 1) / CH);  // 128-row tiles of w, u and P
   if (units > GDN_NOALLOC_MAX_UNITS) return GDN_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (units > 0 && (rc = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch))) return rc;

@@ -95,7 +95,8 @@ __device__ __forceinline__ void ldb_kn_s(uint32_t (&b)[4], const bf16* base, int
 
 // Inclusive prefix sum over the 128 values held 4-per-lane by one warp
 // (lane l holds rows 4l..4l+3 in v[0..3]).
-__device__ __forceinline__ void warp_cumsum128(float (&v)[4], int lane) {
+// (split64: two independent scans, rows 0..63 and 64..127, i.e. lanes 0-15 and 16-31)
+__device__ __forceinline__ void warp_cumsum128(float (&v)[4], int lane, bool split64 = false) {
   v[1] += v[0];
   v[2] += v[1];
   v[3] += v[2];
@@ -103,7 +104,7 @@ __device__ __forceinline__ void warp_cumsum128(float (&v)[4], int lane) {
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     float o = __shfl_up_sync(0xffffffffu, run, off);
-    if (lane >= off) run += o;
+    if (lane >= off && (!split64 || ((lane ^ (lane - off)) & 16) == 0)) run += o;
   }
   const float excl = run - v[3];
   v[0] += excl;

@@ -26,7 +26,9 @@ struct PrepArgs {
   float* nrm;    // non-null: q, k are raw rows; prep normalises its K and Q tiles in shared
                  // memory and writes 1/||k||, 1/||q|| per row here, [B][Hk][NC][2][CH]
   int gate_logits;         // 1: g and beta hold logits a, b (g = -softplus(a), beta = sigmoid(b))
-  int B, T, Hk, Hv, NC;
+  int c64;                 // 1: 64-token chunks, two to a 128-row tile (block-diagonal S, T and P;
+                           //    the gates restart at row 64)
+  int B, T, Hk, Hv, NC;    // NC: 128-row tiles per sequence
 };
 
 // Sequential forward walk over the chunks of one segment for one
@@ -50,7 +52,9 @@ struct WalkFwdArgs {
   int* status;             // bit 0 set if a bounded wait gave up (nullable)
   const float* nrm;        // non-null: K and Q tiles are raw rows, these their 1/||.|| (as PrepArgs)
   int gate_logits;         // 1: g and beta hold logits a, b (g = -softplus(a), beta = sigmoid(b))
-  int B, T, Hk, Hv, NC, S;
+  int c64;                 // 1: 64-token chunks (w, u, P, nrm in the preparation's 128-row tiles)
+  int B, T, Hk, Hv, NC, S;  // NC: chunks per sequence (of 128 or 64 tokens)
+  int NT;                  // 128-row tiles per sequence in w, u, P and nrm
 };
 
 // State columns per CTA of the forward walk's recompute mode (the output walk
@@ -59,9 +63,9 @@ struct WalkFwdArgs {
 constexpr int WALK_STATES_SW = 64;
 
 // TMA tensor maps of the forward walk: K and Q over [B, T, Hk, 128] (boxes of
-// 64 columns x 128 tokens, 128-byte swizzle), w and P over the workspace rows
-// (same boxes); stores of WALK_STATES_SW-column slices of the entering states
-// and Delta over the workspace rows.
+// 64 columns x 128 tokens, 128-byte swizzle; 64 tokens with 64-token chunks),
+// w and P over the workspace rows (same boxes); stores of WALK_STATES_SW-column
+// slices of the entering states and Delta over the workspace rows.
 struct WalkFwdMaps {
   CUtensorMap k, q, W, P;
   CUtensorMap St, De;

@@ -30,6 +30,11 @@
 // T' and T'' are rounded to bf16 as tensor-core operands; w and u are bf16
 // outputs themselves.
 //
+// 64-token chunks (c64): a 128-row tile holds two chunks.  G restarts at row
+// 64, S and P keep only their two 64 x 64 diagonal blocks, and the ladder stops
+// after level 32, so T, T', T'' are block diagonal and w, u, P of each chunk
+// are its own; everything else runs as for 128-token chunks.
+//
 // Operands arrive by TMA in the 128-byte-swizzled layout: K and Q serve
 // K K^T and Q K^T as K-major operands, and K and V serve w and u as MN-major
 // B operands as loaded, so nothing is transposed or rescaled in shared memory.  V of the
@@ -144,7 +149,10 @@ __device__ __forceinline__ void store_split(bf16* hi0, bf16* lo0, bf16* hi1, bf1
 }
 
 // T = (I + S)^-1 in place in (Fh, Fl); the fp32 diagonal 16 x 16 blocks of S
-// are in the Sd scratch.  All threads of the CTA.
+// are in the Sd scratch.  All threads of the CTA.  The ladder's levels stop
+// below `lim` (64: the inverse of each 64 x 64 diagonal block, for S with no
+// entries outside them).
+template <int LIM>
 __device__ __forceinline__ void ut_inverse(PrepSmem& sm, int warp, int lane) {
   bf16* Yh = reinterpret_cast<bf16*>(sm.Tp + Y_HI);
   bf16* Yl = reinterpret_cast<bf16*>(sm.Tp + Y_LO);
@@ -174,7 +182,7 @@ __device__ __forceinline__ void ut_inverse(PrepSmem& sm, int warp, int lane) {
   __syncthreads();
   // (2) levels b = 16, 32, 64: for every 2b block pair p (rows s0 = 2bp..),
   //     Y = S_C X_A, then T_C = -X_D Y, in 16 x 16 output tiles
-  for (int bs = 16; bs < CH; bs *= 2) {
+  for (int bs = 16; bs < LIM; bs *= 2) {
     const int nb = bs >> 4, per = nb * nb;
     const int ntiles = (CH / (2 * bs)) * per;
     // (at most 16 tiles per phase: one per warp)
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
         float v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] = sm.Gl[lane * 4 + i];
-        warp_cumsum128(v, lane);
+        warp_cumsum128(v, lane, a.c64 != 0);  // 64-token chunks: G restarts at row 64
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           sm.Gl[lane * 4 + i] = v[i] * LOG2E;
@@ -424,7 +432,9 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
         for (int cb = 0; cb < 32; cb += 16) {
           const int c0 = 32 * cq + cb;
           float sv[16], pv[16];
-          if (c0 <= 32 * quarter + 31) {  // warp-uniform: the block reaches the diagonal
+          // warp-uniform: the block reaches the diagonal (and, with 64-token chunks,
+          // lies in the rows' own chunk)
+          if (c0 <= 32 * quarter + 31 && (!a.c64 || (c0 >> 6) == (quarter >> 1))) {
             float kk[16], mv[16];
             tc::ld16(tlane + c0, kk);
             if (needP) tc::ld16(tlane + 128 + c0, pv);
@@ -500,7 +510,10 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       }
 
       // ---- T = (I + S)^-1 -------------------------------------------------------------
-      ut_inverse(sm, warp, lane);
+      if (a.c64)
+        ut_inverse<64>(sm, warp, lane);
+      else
+        ut_inverse<CH>(sm, warp, lane);
       if (a.T_dbg) export_f32(a.T_dbg + chunk_id * tile);
       if (a.Tb) {
         bf16* dst = a.Tb + chunk_id * tile;

@@ -50,13 +50,15 @@ __device__ __forceinline__ void mma(uint32_t tmem_d, uint64_t da, uint64_t db, u
       "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
 }
 
-// D[128 x N] (+)= A[128 x 128] * B[N x 128]^T, both K-major SW128 tiles
-// (A with 128 rows, B with N rows); issued by one thread.
+// D[128 x N] (+)= A[128 x 16 NK] * B[N x 16 NK]^T, both K-major SW128 tiles
+// (A with 128 rows, B with N rows; NK = 8: K = 128 over both 64-column halves,
+// NK = 4: K = 64, the first half only); issued by one thread.
+template <int NK = 8>
 __device__ __forceinline__ void gemm_k128(uint32_t tmem_d, uint32_t a_smem, uint32_t b_smem,
                                           int N, bool accumulate_first) {
   const uint32_t idesc = (N == 128) ? idesc_bf16(128, 128) : idesc_bf16(128, N);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < NK; ++k) {
     const uint32_t koff = (uint32_t)(k & 3) * 32u;
     const uint64_t da = desc_sw128(a_smem + (uint32_t)(k >> 2) * 128u * 128u + koff);
     const uint64_t db = desc_sw128(b_smem + (uint32_t)(k >> 2) * (uint32_t)N * 128u + koff);
@@ -195,13 +197,15 @@ __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t mn_at
   d |= (uint64_t)2 << 61;
   return d;
 }
-// D[128 x N] (+)= A * B^T where A (M = 128, K = 128) is stored MN-major as a
-// [128 (K) rows x 128 (M)] SW128 tile and B is a K-major [N x 128] SW128 tile
+// D[128 x N] (+)= A * B^T where A (M = 128, K = 16 NK) is stored MN-major as a
+// [128 (K) rows x 128 (M)] SW128 tile (NK = 4: its first 64 rows) and B is a
+// K-major [N x 16 NK] SW128 tile
+template <int NK = 8>
 __device__ __forceinline__ void gemm_amn_k128(uint32_t tmem_d, uint32_t a_smem, uint32_t b_smem,
                                               int N, bool accumulate_first) {
   const uint32_t idesc = idesc_bf16(128, N) | (1u << 15);  // A is MN-major
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < NK; ++k) {
     const uint64_t da = desc_sw128_mn(a_smem + (uint32_t)k * 2048u, 128u * 128u);
     const uint32_t koff = (uint32_t)(k & 3) * 32u;
     const uint64_t db = desc_sw128(b_smem + (uint32_t)(k >> 2) * (uint32_t)N * 128u + koff);

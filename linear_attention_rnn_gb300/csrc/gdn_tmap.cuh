@@ -55,14 +55,14 @@ inline bool tmap_2d_sw(CUtensorMap* m, const void* base, uint64_t cols, uint64_t
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// bf16 activations [B][T][H][D]; box = 64 columns of one head over 128 tokens
-// (128-byte swizzle), tokens past T read as zero.
-inline bool tmap_heads(CUtensorMap* m, const void* base, int B, int T, int H, int D) {
+// bf16 activations [B][T][H][D]; box = 64 columns of one head over box_tokens
+// tokens (128 or 64; 128-byte swizzle), tokens past T read as zero.
+inline bool tmap_heads(CUtensorMap* m, const void* base, int B, int T, int H, int D, uint32_t box_tokens = 128) {
   auto enc = tmap_encoder();
   if (!enc) return false;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)T * H * D * 2};
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t box[4] = {64, 1, box_tokens, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -42,6 +42,15 @@
 //     push the augmented state [A | B] through the segment's chunks starting
 //     from [I | 0]; the A columns take no u term.  CTAs 0-3 hold A's column
 //     slices, 4-7 hold B's.
+//
+// 64-token chunks (C64; RECUR without exports, and FOLD): the state steps every
+// 64 tokens and each step keeps 128-row products.  The first product's A
+// operand stacks the chunk's w (rows 0-63) over its Q (rows 64-127), so one
+// product gives both w h (TMEM lanes 0-63) and Q h (lanes 64-127).  Compute
+// threads of rows 0-63 form Delta, whose images hold 64 K-columns; the state
+// update K^T (ef Delta) and P Delta take K = 64, and P Delta's A operand holds
+// the chunk's 64 x 64 P in rows 64-127, so that the output rows meet Q h in
+// lanes 64-127, where the threads of rows 64-127 write them.
 #pragma once
 #include "gdn_kernels.cuh"
 #include "gdn_tc05.cuh"
@@ -121,9 +130,11 @@ __device__ __forceinline__ void arrive(uint64_t* bar) {
 // The walk of CTA (slice, seg, bhi) with FwdCfg<SW>::NT threads; `base` is the
 // 1024-byte-aligned dynamic shared memory (sizeof(WalkSmem<SW>) bytes).
 // STAGED: the recompute mode (exports h and Delta, no output).
-template <bool FOLD, bool STAGED, int SW>
+template <bool FOLD, bool STAGED, int SW, bool C64 = false>
 __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp, unsigned char* base, int slice,
                                      int seg, int bhi) {
+  static_assert(!(C64 && STAGED), "64-token chunks export nothing");
+  constexpr int CC = C64 ? 64 : CH;  // tokens per chunk
   using Cfg = FwdCfg<SW>;
   constexpr int NCT = Cfg::NCT, NCW = Cfg::NCW, NSLOT = Cfg::NSLOT, NSTAGE = Cfg::NSTAGE;
   constexpr uint32_t SLICE = Cfg::SLICE;
@@ -135,7 +146,8 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
   const int cbeg = (int)((long)seg * a.NC / a.S), cend = (int)((long)(seg + 1) * a.NC / a.S);
   const bool partA = FOLD && slice < NSL;  // A columns: no u term
   const bool withO = !FOLD && a.o != nullptr;
-  const int TPC = withO ? 4 : 2;  // tiles per chunk: w, (Q,) K (, P)
+  // tiles per chunk: w, (Q,) K (, P); with 64-token chunks [w; Q] (or w), K (, P)
+  const int TPC = withO ? (C64 ? 3 : 4) : 2;
   const int ntiles = (cend - cbeg) * TPC;
   const int sbase = (slice % NSL) * SW;           // first state column of the slice
   const int g32 = warp < NCW ? (warp >> 2) : 0;   // compute threads: 32-column group in the slice
@@ -151,9 +163,11 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
   unsigned char* stage = sm.slot[NSLOT - 1];
   if (cbeg >= cend) return;
   if (partA && a.pairA == nullptr) return;  // fold without the A output: B columns only
-  auto rows_of = [&](int c) { return min(CH, a.T - c * CH); };
+  auto rows_of = [&](int c) { return min(CC, a.T - c * CC); };
   // tile sequence of a chunk: w, Q, K, P (with output) or w, K
   auto tile_of = [&](int kind) { return withO ? kind : (kind == 0 ? 0 : 1); };  // kind: 0 w, 1 Q, 2 K, 3 P
+  // first workspace row (w, u, P) of chunk c: 128-row tiles, two 64-token chunks to a tile
+  auto ws_row = [&](int c) { return bh * a.NT * CH + (long)c * CC; };
 
   if (tid == 0) {
     for (int k = 0; k < NSLOT; ++k) {
@@ -178,17 +192,22 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
 
   // state row r = tid (compute threads), columns col0..col0+31
   const int r = 32 * (warp & 3) + lane;
+  // with 64-token chunks rows 0-63 form Delta and rows 64-127 the output, both
+  // of token r & 63 (warp-uniform); every thread keeps state row r
+  const bool dRow = !C64 || r < 64;
+  const int tr = C64 ? (r & 63) : r;
   float h[32];
   float gnext = 0.f, part = 0.f;
   float gam_r = 0.f, ef_r = 0.f, gC = 0.f;
   auto load_g = [&](int c) {
-    return (c < cend && r < rows_of(c)) ? act_g(a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j], a.gate_logits) : 0.f;
+    return (c < cend && tr < rows_of(c)) ? act_g(a.g[((long)b * a.T + (long)c * CC + tr) * a.Hv + j], a.gate_logits)
+                                         : 0.f;
   };
   // row r of this slice of u for chunk c, loaded a chunk ahead into registers
   uint4 un[4];
   auto load_u = [&](int c) {
-    if (partA || c >= cend) return;
-    const bf16* src = a.U + ((bh * a.NC + c) * CH + r) * HD + col0;
+    if (partA || c >= cend || !dRow) return;
+    const bf16* src = a.U + (ws_row(c) + r) * HD + col0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) un[q] = *reinterpret_cast<const uint4*>(src + 8 * q);
   };
@@ -209,19 +228,27 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
   auto load_n = [&](int c, float& nk, float& nq) {
     nk = nq = 1.f;
     if (a.nrm && c < cend) {
-      const float* nb = a.nrm + ((((long)b * a.Hk + kh) * a.NC + c) << 8);
-      nk = nb[r];
-      nq = nb[CH + r];
+      const int t = C64 ? (c >> 1) : c, o = C64 ? 64 * (c & 1) + tr : r;  // tile, row in it
+      const float* nb = a.nrm + ((((long)b * a.Hk + kh) * a.NT + t) << 8);
+      nk = nb[o];
+      nq = nb[CH + o];
     }
   };
   // after a barrier over the compute threads: gamma_r, ef_r and gamma_C of chunk index i
+  // (64-token chunks: lane quarters 0-1 and 2-3 each scan the chunk's 64 gates)
   auto finish_gates = [&](float p, int i, float& gm, float& ef, float& gc) {
     float off = 0.f, tot = 0.f;
+    if (C64) {
+      const int q0 = warp & 2;
+      off = (warp & 1) ? sm.gsum[i & 1][q0] : 0.f;
+      tot = sm.gsum[i & 1][q0] + sm.gsum[i & 1][q0 + 1];
+    } else {
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float s = sm.gsum[i & 1][w];
-      off += (w < (warp & 3)) ? s : 0.f;
-      tot += s;
+      for (int w = 0; w < 4; ++w) {
+        const float s = sm.gsum[i & 1][w];
+        off += (w < (warp & 3)) ? s : 0.f;
+        tot += s;
+      }
     }
     const float G = p + off;
     gm = expf(G) * nq_next;  // the norms of chunk index i were loaded a chunk ahead
@@ -262,6 +289,28 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
 
   auto issue = [&](int i) {  // TMA request of tile i into slot i % nring
     const int c = cbeg + i / TPC, t = i % TPC;
+    if (C64) {  // 64-row boxes: [w; Q] (or w), K, P into rows 64-127 of the first half
+      const int row0 = (int)ws_row(c);
+      unsigned char* dst = sm.slot[i % nring];
+      uint64_t* bar = &sm.full[i % nring];
+      if (t == 0) {
+        tc::arrive_expect_tx(bar, withO ? TILE_BYTES : TILE_BYTES / 2);
+        tc::tma_load_2d(dst, &mp.W, 0, row0, bar);
+        tc::tma_load_2d(dst + TILE_BYTES / 2, &mp.W, 64, row0, bar);
+        if (withO) {
+          tc::tma_load_4d(dst + TILE_BYTES / 4, &mp.q, 0, kh, c * CC, b, bar);
+          tc::tma_load_4d(dst + TILE_BYTES / 2 + TILE_BYTES / 4, &mp.q, 64, kh, c * CC, b, bar);
+        }
+      } else if (t == 1) {
+        tc::arrive_expect_tx(bar, TILE_BYTES / 2);
+        tc::tma_load_4d(dst, &mp.k, 0, kh, c * CC, b, bar);
+        tc::tma_load_4d(dst + TILE_BYTES / 2, &mp.k, 64, kh, c * CC, b, bar);
+      } else {
+        tc::arrive_expect_tx(bar, TILE_BYTES / 4);
+        tc::tma_load_2d(dst + TILE_BYTES / 4, &mp.P, 64 * (c & 1), row0, bar);
+      }
+      return;
+    }
     const int kind = withO ? t : (t == 0 ? 0 : 2);
     const long cid = bh * a.NC + c;
     unsigned char* dst = sm.slot[i % nring];
@@ -292,6 +341,16 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
       for (int c = cbeg; c < cend; ++c) {
         const int ci = c - cbeg;
         const uint32_t par = (uint32_t)(ci & 1);
+        if (C64) {  // Q h came with w h; P Delta alone, K = 64
+          const int iP = ci * TPC + 2;
+          ok = ok && tc::mbar_wait(&sm.barD, par);  // Delta^T written
+          wait_tile(iP);
+          tc::fence_after();
+          tc::gemm_k128<4>(tmem + C_O2, slot_of(iP), smem_u32(sm.Dt), SW, false);
+          tc::commit(&sm.barO2);
+          release(iP);
+          continue;
+        }
         const int iQ = ci * TPC + 1, iP = ci * TPC + 3;
         ok = ok && tc::mbar_wait(&sm.barX, par);  // w h(c) done: h(c) is in Ht[ci & 1]
         wait_tile(iQ);
@@ -352,7 +411,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
         const int ci = c - cbeg;
         const uint32_t par = (uint32_t)(ci & 1);
         const int t0 = ci * TPC;
-        const int iW = t0, iQ = t0 + 1, iK = t0 + tile_of(2), iP = t0 + 3;
+        const int iW = t0, iQ = t0 + 1, iK = t0 + (C64 ? 1 : tile_of(2)), iP = t0 + 3;
         const uint32_t ht = smem_u32(sm.Ht[ci & 1]);
         if (ci > 0) ok = ok && tc::mbar_wait(&sm.barHt, par ^ 1);  // state image of chunk c
         wait_tile(iW);
@@ -363,7 +422,10 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
         ok = ok && tc::mbar_wait(&sm.barDg, par);  // (ef Delta)^T written
         wait_tile(iK);
         tc::fence_after();
-        tc::gemm_amn_k128(tmem + C_H, slot_of(iK), smem_u32(sm.Dgt), SW, false);
+        if (C64)
+          tc::gemm_amn_k128<4>(tmem + C_H, slot_of(iK), smem_u32(sm.Dgt), SW, false);
+        else
+          tc::gemm_amn_k128(tmem + C_H, slot_of(iK), smem_u32(sm.Dgt), SW, false);
         tc::commit(&sm.barH);
         release(iK);
         (void)iQ;
@@ -386,9 +448,10 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
       // ---- Delta = u - X -------------------------------------------------------
       ok = ok && tc::mbar_wait(&sm.barX, par);
       tc::fence_after();
-      float x[32];
+      float x[32];  // (64-token chunks, rows 64-127: Q h, kept for the output)
       tc::ld32(tl + 0, x);
-      if (!partA) {
+      if (!dRow) {
+      } else if (!partA) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint4 w4 = un[q];
@@ -407,16 +470,20 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
 #pragma unroll
         for (int n = 0; n < 32; ++n) x[n] = -x[n];
       }
-      float xg[32];
+      if (dRow) {
+        float xg[32];
 #pragma unroll
-      for (int n = 0; n < 32; ++n) xg[n] = x[n] * ef_r;
-      write_bt_column<SW>(sm.Dgt, r, 32 * g32, xg);  // operand of the state update: first
+        for (int n = 0; n < 32; ++n) xg[n] = x[n] * ef_r;
+        write_bt_column<SW>(sm.Dgt, r, 32 * g32, xg);  // operand of the state update: first
+      }
       tc::fence_proxy_async();
       tc::fence_before();
       arrive(&sm.barDg);
       load_u(c + 1);
       if (withO) {
-        write_bt_column<SW>(sm.Dt, r, 32 * g32, x);
+        // (every compute thread arrives: P Delta(c) then also waits for the
+        // output rows' reads of P Delta(c - 1))
+        if (dRow) write_bt_column<SW>(sm.Dt, r, 32 * g32, x);
         tc::fence_proxy_async();
         tc::fence_before();
         arrive(&sm.barD);
@@ -447,7 +514,19 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
       tc::fence_proxy_async();
       tc::fence_before();
       arrive(&sm.barHt);
-      if (withO) {  // output epilogue overlaps the next chunk's first product
+      if (withO && C64) {  // rows 64-127: O = gamma (Q h) + P Delta
+        ok = ok && tc::mbar_wait(&sm.barO2, par);
+        tc::fence_after();
+        if (!dRow) {
+          float o2[32];
+          tc::ld32(tl + C_O2, o2);
+          if (tr < rows_of(c)) {
+#pragma unroll
+            for (int n = 0; n < 32; ++n) o2[n] = gam_r * x[n] + o2[n];
+            store_row_bf16(a.o + (((long)b * a.T + (long)c * CC + tr) * a.Hv + j) * HD + col0, o2);
+          }
+        }
+      } else if (withO) {  // output epilogue overlaps the next chunk's first product
         ok = ok && tc::mbar_wait(&sm.barO2, par);  // covers Q h as well
         tc::fence_after();
         float o1[32], o2[32];

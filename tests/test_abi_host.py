@@ -42,7 +42,8 @@ def _fwd(L, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, o=FAKE, hT=None,
 def test_fwd_argument_errors(L):
     assert _fwd(L, dk=64) == -2
     assert _fwd(L, dv=96) == -2
-    assert _fwd(L, chunk=64) == -2
+    assert _fwd(L, chunk=32) == -2
+    assert _fwd(L, chunk=64) == -3             # 64-token chunks accepted; workspace of 0 bytes
     assert _fwd(L, Hk=3, Hv=4) == -1
     assert _fwd(L, T=-1) == -1
     assert _fwd(L, S=-2) == -1
@@ -64,6 +65,7 @@ def test_bwd_argument_errors(L):
         return L.gdn_chunk_bwd(*a, d["B"], d["T"], d["Hk"], d["Hv"], d["dk"], d["dv"],
                                d["chunk"], d["S"], FAKE, 16, None)
     assert call(args, dk=256) == -2
+    assert call(args, chunk=64) == -2  # the backward takes 128-token chunks
     assert call(args, Hv=5) == -1
     bad = list(args)
     bad[6] = None  # dO
@@ -80,12 +82,15 @@ def test_compose_argument_errors(L):
 
 
 def test_segment_fold_argument_errors(L):
-    def call(S=1, T=256, A=FAKE, Bo=FAKE, dk=128, ws=FAKE, ws_bytes=0):
-        return L.gdn_segment_fold(FAKE, FAKE, FAKE, FAKE, A, Bo, 1, T, 2, 4, dk, 128, 128, S, ws,
+    def call(S=1, T=256, A=FAKE, Bo=FAKE, dk=128, ws=FAKE, ws_bytes=0, chunk=128):
+        return L.gdn_segment_fold(FAKE, FAKE, FAKE, FAKE, A, Bo, 1, T, 2, 4, dk, 128, chunk, S, ws,
                                   ws_bytes, None)
     assert call(dk=64) == -2
+    assert call(chunk=32) == -2
     assert call(S=0) == -1
     assert call(S=3) == -1          # 2 chunks
+    assert call(S=3, chunk=64) == -3  # 4 chunks of 64 tokens; workspace of 0 bytes
+    assert call(S=5, chunk=64) == -1
     assert call(Bo=None) == -1
     assert call(A=MISAL) == -1
     assert call() == -3             # workspace of 0 bytes
@@ -104,6 +109,9 @@ def test_saved_buffer_argument_errors(L):
                                                    FAKE, 1 << 30, None, None, 0)
     assert fwd(FAKE, need - 1) == -3
     assert fwd(MISAL, need) == -1
+    fwd64 = L.gdn_chunk_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 1, 256, 2, 4, 128, 128,
+                               64, 1, FAKE, need, FAKE, 1 << 30, None, None, 0)
+    assert fwd64 == -2  # tiles for the backward: 128-token chunks only
     args = [FAKE] * 5 + [None, FAKE, None] + [FAKE] * 5 + [None]
     bwd = lambda saved, nbytes: L.gdn_chunk_bwd_ex(*args, 1, 256, 2, 4, 128, 128, 128, 1, saved,
                                                    nbytes, FAKE, 1 << 30, None, None, 0)
@@ -121,6 +129,10 @@ def test_layer_argument_errors(L):
     assert need_f == g.fwd_workspace_bytes(1, 256, 2, 4) + 2 * 2 * 2 * 128 * 4 + vv
     assert need_b == g.bwd_workspace_bytes(1, 256, 2, 4) + 4 * qk + vv
     assert g.layer_workspace_bytes(0, 1, 256, 2, 4, dk=64) == 0
+    # 64-token chunks: the forward only; the same tiles (two chunks to a 128-row tile)
+    assert g.layer_workspace_bytes(0, 1, 256, 2, 4, chunk=64) == (
+        g.fwd_workspace_bytes(1, 256, 2, 4, chunk=64) + 2 * 2 * 2 * 128 * 4 + vv)
+    assert g.layer_workspace_bytes(1, 1, 256, 2, 4, chunk=64) == 0
 
     def fwd(z=FAKE, y=FAKE, a=FAKE, ws=FAKE, nbytes=1 << 30, T=256, dk=128):
         return L.gdn_layer_fwd(FAKE, FAKE, FAKE, a, FAKE, z, None, y, None, None, 1, T, 2, 4, dk, 128,
@@ -152,6 +164,11 @@ def test_workspace_sizes(L):
     assert f(1, 4096, 16, 32, n_segments=4) > w1  # per-segment (A, B) and entering states
     assert b(1, 4096, 16, 32, n_segments=1) > w1
     assert f(2, 1000, 2, 4) > 0
+    # 64-token chunks keep the 128-row tiles: the same workspace with one segment
+    assert f(1, 4096, 16, 32, chunk=64, n_segments=1) == w1
+    assert f(1, 4096 + 64, 16, 32, chunk=64, n_segments=1) == f(1, 4096 + 64, 16, 32, n_segments=1)
+    assert f(1, 4096, 16, 32, chunk=32) == 0
+    assert b(1, 4096, 16, 32, chunk=64) == 0
 
 
 def test_default_segments(L):
@@ -165,6 +182,8 @@ def test_default_segments(L):
     assert 2 <= s1 <= 2048 // 8
     assert s1 >= gdn.default_segments(1, 262144, 2) >= 2
     assert gdn.default_segments(1, 64 * 128 + 1, 1) == 8  # 65 chunks, 8 per segment
+    assert gdn.default_segments(1, 64 * 64 + 1, 1, 64) == 8  # 65 chunks of 64 tokens
+    assert gdn.default_segments(1, 4096, 32, 64) == 1
 
 
 def test_binding_validates_before_calling():
