@@ -31,10 +31,22 @@ sys.path.insert(0, ROOT)
 
 # per-unit algorithmic work of the path (2 m n k per product, triangular
 # operands at their nonzero size; K K^T and Q K^T once per key head)
-FLOP_PER_CHUNK_KHEAD = 4_194_304          # K K^T + Q K^T (both triangular)
-FLOP_LADDER = 1_398_016                   # sum_b 2 b^2 C for b = 1..64
-FLOP_TRI = 2_113_536                      # lower-triangular 128x128 times 128x128
-FLOP_FULL = 4_194_304                     # 128x128x128
+def chunk_flops(C, D=128):
+    """Per-chunk FLOPs at chunk size C: K K^T + Q K^T (per key head), the
+    ladder (sum over its levels b = 1, 2, .., C/2 of 2 b^2 C), a lower-
+    triangular C x C times C x D product, and a full C x D x D product."""
+    ladder, b = 0, 1
+    while b < C:
+        ladder += 2 * b * b * C
+        b *= 2
+    return dict(khead=2 * C * C * D, ladder=ladder, tri=C * (C + 1) * D, full=2 * C * D * D)
+
+
+_F128 = chunk_flops(128)
+FLOP_PER_CHUNK_KHEAD = _F128["khead"]     # 4,194,304: K K^T + Q K^T (both triangular)
+FLOP_LADDER = _F128["ladder"]             # 1,398,016: sum_b 2 b^2 C for b = 1..64
+FLOP_TRI = _F128["tri"]                   # 2,113,536: lower-triangular 128x128 times 128x128
+FLOP_FULL = _F128["full"]                 # 4,194,304: 128x128x128
 FLOPS = {  # per (chunk, value head), per kernel
     "prep": FLOP_LADDER + 2 * FLOP_TRI,   # + FLOP_PER_CHUNK_KHEAD per (chunk, key head)
     "walk": 3 * FLOP_FULL + FLOP_TRI,     # w h, k_g^T Delta, Q h, P Delta
@@ -69,7 +81,8 @@ def algorithmic(wl):
     fwd_bytes = qk + vv + gb + st + vv + st            # read q k v g beta h0, write o hT
     bwd_bytes = qk + vv + gb + st + vv + st + qk + vv + gb + st  # + dO dhT; dq dk dv dg dbeta dh0
     units, kunits = B * Hv * NC, B * Hk * NC
-    fwd_flops = kunits * FLOP_PER_CHUNK_KHEAD + units * (FLOPS["prep"] + FLOPS["walk"])
+    f = chunk_flops(wl.chunk, dk)  # prep: ladder, w, u; walk: w h, k_g^T Delta, Q h, P Delta
+    fwd_flops = kunits * f["khead"] + units * (f["ladder"] + 3 * f["tri"] + 3 * f["full"])
     # the backward takes w, u, P, T, the states and Delta from the forward: the
     # reverse walk and the chunk gradients
     bwd_flops = units * (FLOPS["walk_bwd"] + FLOPS["grads"])
@@ -643,17 +656,22 @@ def run_sweep(args):
     for spec in args.sweep.split(","):  # "all" stands for every workload as configured
         names += list(WORKLOADS) if spec == "all" else [spec]
     for spec in names:
-        # "name" runs the workload as configured, "name@S" with S segments (0: the library's choice)
-        name, _, segs = spec.partition("@")
+        # "name" runs the workload as configured, "name@S" with S segments (0: the library's
+        # choice); a "/64" suffix runs the forward alone with 64-token chunks
+        base, _, ch = spec.partition("/")
+        name, _, segs = base.partition("@")
         wl = WORKLOADS[name]
         if segs:
             wl = wl.replace(n_segments=int(segs))
+        if ch:
+            wl = wl.replace(chunk=int(ch), backward=wl.backward and int(ch) == 128)
         bwd = wl.backward
-        nseg = wl.n_segments or gdn.default_segments(wl.B, wl.T, wl.Hv)
+        C = wl.chunk
+        nseg = wl.n_segments or gdn.default_segments(wl.B, wl.T, wl.Hv, C)
         big = wl.tokens > (1 << 16)
         steps = 5 if big else 20
         d = make_device(wl, dev)
-        ws_f = torch.empty(gdn.fwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
+        ws_f = torch.empty(gdn.fwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, chunk=C, n_segments=nseg),
                            dtype=torch.uint8, device=dev)
         ws_b = (torch.empty(gdn.bwd_workspace_bytes(wl.B, wl.T, wl.Hk, wl.Hv, n_segments=nseg),
                             dtype=torch.uint8, device=dev) if bwd else None)
@@ -672,7 +690,7 @@ def run_sweep(args):
         bev = [evs(len(bk)) for _ in range(steps)] if bwd else None
 
         def step(i=None):
-            gdn.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, n_segments=nseg, workspace=ws_f,
+            gdn.chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, chunk=C, n_segments=nseg, workspace=ws_f,
                           events=None if i is None else fev[i], saved=sv)
             if bwd:
                 gdn.chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.dO, d.dhT, n_segments=nseg,
@@ -700,7 +718,7 @@ def run_sweep(args):
             t_roof = max(t_hbm, t_tc)
             return {"ms": round(ms, 5), "roof_ms": round(t_roof, 5),
                     "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": round(t_roof / ms, 4)}
-        line = {"workload": spec, "B": wl.B, "T": wl.T, "Hk": wl.Hk, "Hv": wl.Hv,
+        line = {"workload": spec, "B": wl.B, "T": wl.T, "Hk": wl.Hk, "Hv": wl.Hv, "chunk": C,
                 "segments": nseg, "timed_steps": steps, "reported": "median",
                 "fwd": path(alg["fwd_bytes"], alg["fwd_flops"], fwd_ms),
                 "fwd_tokens_per_s": round(wl.tokens / (fwd_ms * 1e-3), 1),

@@ -81,3 +81,25 @@ def test_kernel_table_and_roofline_arithmetic():
     assert roof["achieved"] == pytest.approx(achieved, abs=0.01)
     assert roof["frac"] == pytest.approx(achieved / 1886.0, abs=1e-4)
     assert roof["traffic"] == bench.NCU_TRAFFIC.get("grads")
+
+
+def test_chunk64_flops_by_counting():
+    # 64-token chunks: the same products on 64 rows; the ladder's levels stop at b = 32
+    C64 = 64
+    f = bench.chunk_flops(C64, D)
+    assert f["tri"] == sum(2 * D for r in range(C64) for s in range(r + 1))
+    assert f["full"] == sum(2 * D for r in range(C64) for s in range(D))
+    flops, b = 0, 1
+    while b < C64:
+        flops += (C64 // (2 * b)) * 2 * (2 * b * b * b)
+        b *= 2
+    assert f["ladder"] == flops
+    # K K^T and Q K^T: each a C x C triangle of D-long dot products, counted at half the square
+    assert f["khead"] == 2 * (2 * C64 * C64 * D) // 2
+    assert bench.chunk_flops(C, D) == dict(khead=bench.FLOP_PER_CHUNK_KHEAD, ladder=bench.FLOP_LADDER,
+                                           tri=bench.FLOP_TRI, full=bench.FLOP_FULL)
+    # per token the D x D products are unchanged and the intra-chunk ones halve
+    a128 = bench.algorithmic(WORKLOADS["layer_t4096"])
+    a64 = bench.algorithmic(WORKLOADS["layer_t4096"].replace(chunk=64))
+    assert a64["fwd_bytes"] == a128["fwd_bytes"]
+    assert a64["fwd_flops"] < a128["fwd_flops"]
