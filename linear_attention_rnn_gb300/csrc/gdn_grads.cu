@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
   bool ok = true;
   uint32_t mc = 0;  // completed-commit count of barM seen by this thread
   auto wait_mma = [&]() {
-    ok = ok && tc::mbar_wait(&sm.barM, mc & 1);
+    ok = ok && tc::mbar_wait_sleep(&sm.barM, mc & 1);
     ++mc;
     tc::fence_after();
   };
@@ -339,8 +339,8 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       }
     }
     {  // <dh', h>: elementwise over two tiles of the same layout
-      ok = ok && tc::mbar_wait(&sm.barDH, par);
-      ok = ok && tc::mbar_wait(&sm.barH, par);
+      ok = ok && tc::mbar_wait_sleep(&sm.barDH, par);
+      ok = ok && tc::mbar_wait_sleep(&sm.barH, par);
       float d = 0.f;
 #pragma unroll
       for (int i = 0; i < (int)(TILE / 16) / GT; ++i) {
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     }
 
     // ---- E2: dK (+)= -diag(beta gamma) dV' h^T + diag(ef) Delta dh'^T ---------------------
-    if (jj == 0) ok = ok && tc::mbar_wait(&sm.barKQ, kq_par);  // the unit's K and Q (read from here on)
+    if (jj == 0) ok = ok && tc::mbar_wait_sleep(&sm.barKQ, kq_par);  // the unit's K and Q (read from here on)
     wait_mma();
     {
       float kv[32], x[32], acc[32];

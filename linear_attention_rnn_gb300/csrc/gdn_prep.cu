@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       // raw q and k: the rows' 1/||k|| and 1/||q||, 1 / sqrt(sum x^2 + 1e-6), go to
       // nrm (thread t: row t / 4, 32 columns).  The tiles stay raw, as the walk
       // reads them: K K^T, Q K^T and w = T'' K take the scales in their epilogues.
-      ok = ok && tc::mbar_wait(&sm.barKQ, (uint32_t)(kq_uses & 1));
+      ok = ok && tc::mbar_wait_sleep(&sm.barKQ, (uint32_t)(kq_uses & 1));
       float* nb = a.nrm + ((((long)b * a.Hk + kh) * a.NC + c) << 8);
       auto row_scale = [&](const unsigned char* tile, float* dst) {
         const int rr = tid >> 2, q4 = tid & 3;
@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       // before the barrier below lets anyone rewrite them
       if (tid == 0 && (ug > u_begin || jj > jj0)) tc::bulk_wait_read();
       if (jj == jj0) {  // K K^T, Q K^T complete; K readable
-        ok = ok && tc::mbar_wait(&sm.barKQ, (uint32_t)(kq_uses & 1));
-        ok = ok && tc::mbar_wait(&sm.barM, mphase);
+        ok = ok && tc::mbar_wait_sleep(&sm.barKQ, (uint32_t)(kq_uses & 1));
+        ok = ok && tc::mbar_wait_sleep(&sm.barM, mphase);
         mphase ^= 1;
         tc::fence_after();
       }
@@ -585,7 +585,7 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       if (tid == loader && last) load_kq(xn.b, xn.c, xn.kh, sm.A[vbi[(jj1 - jj0) & 1]]);
       if (needU) (vb ? v_use1 : v_use0) += 1;
       if (needU || needW) {
-        ok = ok && tc::mbar_wait(&sm.barM, mphase);
+        ok = ok && tc::mbar_wait_sleep(&sm.barM, mphase);
         mphase ^= 1;
         tc::fence_after();
       }

@@ -159,6 +159,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// try_wait with a suspend-time hint (ns): the thread sleeps until the phase
+// completes or the hint runs out, instead of spinning.  For waits of many
+// threads (epilogue warps waiting out a product): their spinning would take
+// issue slots from the thread that issues the products.  Bounded as mbar_wait.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                long long limit_cycles = WAIT_LIMIT_CYCLES) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait_hint(a, parity, 20000u)) return true;
+    if (clock64() - t0 > limit_cycles) return false;
+  }
+}
+
 }  // namespace tc
 }  // namespace gdn
 

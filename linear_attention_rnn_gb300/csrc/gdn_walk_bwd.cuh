@@ -359,13 +359,13 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
 
       // ---- Y = diag(ef) K dh' + P^T dO ----------------------------------------------
       float y[32];
-      ok = ok && tc::mbar_wait(&sm.barY, par);
+      ok = ok && tc::mbar_wait_sleep(&sm.barY, par);
       tc::fence_after();
       tc::ld32(tl + C_Y, y);
 #pragma unroll
       for (int q = 0; q < 32; ++q) y[q] *= ef_r;
       if (withO) {
-        ok = ok && tc::mbar_wait(&sm.barP, par);
+        ok = ok && tc::mbar_wait_sleep(&sm.barP, par);
         tc::fence_after();
         float pd[32];
         tc::ld32(tl + C_P, pd);
@@ -389,7 +389,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");
       finish_gates(part, ci + 1);
       if (withO && ci + 1 < n) {  // both dO products of this chunk have read the images
-        ok = ok && tc::mbar_wait(&sm.barQ, par);
+        ok = ok && tc::mbar_wait_sleep(&sm.barQ, par);
         write_do_images();
         tc::fence_proxy_async();
         tc::fence_before();
@@ -398,7 +398,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       }
 
       // ---- dh = gamma_C dh' + Q^T (gamma dO) - w^T Y ---------------------------------
-      ok = ok && tc::mbar_wait(&sm.barH, par);
+      ok = ok && tc::mbar_wait_sleep(&sm.barH, par);
       tc::fence_after();
       float hv[32];
       tc::ld32(tl + c_q(ci), hv);

@@ -446,7 +446,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
       if (!FOLD && a.states) stage_row<SW>(stage + set * 2 * SLICE, r, g32, h);
 
       // ---- Delta = u - X -------------------------------------------------------
-      ok = ok && tc::mbar_wait(&sm.barX, par);
+      ok = ok && tc::mbar_wait_sleep(&sm.barX, par);
       tc::fence_after();
       float x[32];  // (64-token chunks, rows 64-127: Q h, kept for the output)
       tc::ld32(tl + 0, x);
@@ -503,7 +503,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
       load_n(c + 2, nk_next, nq_next);
 
       // ---- h' = gamma_C h + H' ---------------------------------------------------
-      ok = ok && tc::mbar_wait(&sm.barH, par);
+      ok = ok && tc::mbar_wait_sleep(&sm.barH, par);
       tc::fence_after();
       float hh[32];
       tc::ld32(tl + C_H, hh);
@@ -515,7 +515,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
       tc::fence_before();
       arrive(&sm.barHt);
       if (withO && C64) {  // rows 64-127: O = gamma (Q h) + P Delta
-        ok = ok && tc::mbar_wait(&sm.barO2, par);
+        ok = ok && tc::mbar_wait_sleep(&sm.barO2, par);
         tc::fence_after();
         if (!dRow) {
           float o2[32];
@@ -527,7 +527,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
           }
         }
       } else if (withO) {  // output epilogue overlaps the next chunk's first product
-        ok = ok && tc::mbar_wait(&sm.barO2, par);  // covers Q h as well
+        ok = ok && tc::mbar_wait_sleep(&sm.barO2, par);  // covers Q h as well
         tc::fence_after();
         float o1[32], o2[32];
         tc::ld32(tl + o1_col(ci), o1);
