@@ -272,7 +272,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       for (int ci = 0; ci < n; ++ci) {
         const int c = chunk_of(ci);
         const int set = ci % NSTAGE, use = ci / NSTAGE;
-        ok = ok && tc::mbar_wait(&sm.sfull[set], (uint32_t)(use & 1));
+        ok = ok && tc::mbar_wait_sleep(&sm.sfull[set], (uint32_t)(use & 1));
         if (a.dstates) tc::tma_store_2d(&mp.Ds, sbase, (int)((bh * a.NC + c) * HD), sm.stage[set][0]);
         if (a.ddelta) tc::tma_store_2d(&mp.Dd, sbase, (int)((bh * a.NC + c) * CH), sm.stage[set][1]);
         tc::bulk_commit();
@@ -285,7 +285,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     // ========================================================== TMA producer
     if (lane == 0) {
       for (int i = 0; i < ntiles; ++i) {
-        if (i >= NRING) ok = ok && tc::mbar_wait(&sm.empty[i % NRING], (uint32_t)((i / NRING - 1) & 1));
+        if (i >= NRING) ok = ok && tc::mbar_wait_sleep(&sm.empty[i % NRING], (uint32_t)((i / NRING - 1) & 1));
         issue(i);
       }
     }
@@ -297,11 +297,11 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     // chunk's P^T dO the gap while dh is formed.  After each product its tile
     // slot is released to the producer by a commit to the slot's empty barrier.
     if (lane == 0) {
-      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % NRING], (i / NRING) & 1); };
+      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait_sleep(&sm.full[i % NRING], (i / NRING) & 1); };
       auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NRING]); };
       auto release = [&](int i) { tc::commit(&sm.empty[i % NRING]); };
       auto issue_p = [&](int ci) {  // P^T dO of chunk ci (its dO images are written)
-        ok = ok && tc::mbar_wait(&sm.barO, (uint32_t)(ci & 1));
+        ok = ok && tc::mbar_wait_sleep(&sm.barO, (uint32_t)(ci & 1));
         wait_tile(ci * TPC);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + C_P, slot_of(ci * TPC), smem_u32(sm.Ot), SW, false);
@@ -313,7 +313,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
         const uint32_t par = (uint32_t)(ci & 1);
         const int t0 = ci * TPC;
         const int iQ = t0 + 1, iK = t0 + (withO ? 2 : 0), iW = t0 + (withO ? 3 : 1);
-        ok = ok && tc::mbar_wait(&sm.barXt, par);  // dh' image of this chunk
+        ok = ok && tc::mbar_wait_sleep(&sm.barXt, par);  // dh' image of this chunk
         wait_tile(iK);
         tc::fence_after();
         tc::gemm_k128(tmem + C_Y, slot_of(iK), smem_u32(sm.Xt), SW, false);
@@ -326,7 +326,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
           tc::commit(&sm.barQ);
           release(iQ);
         }
-        ok = ok && tc::mbar_wait(&sm.barYt, par);  // (-Y)^T written
+        ok = ok && tc::mbar_wait_sleep(&sm.barYt, par);  // (-Y)^T written
         wait_tile(iW);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iW), smem_u32(sm.Yt), SW, withO);
@@ -352,7 +352,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       const uint32_t par = (uint32_t)(ci & 1);
       // staging set ci % NSTAGE (dh', dDelta) was last read by the stores of chunk ci - NSTAGE
       const int set = ci % NSTAGE, use = ci / NSTAGE;
-      if (!FOLD && use >= 1) ok = ok && tc::mbar_wait(&sm.sempty[set], (uint32_t)((use - 1) & 1));
+      if (!FOLD && use >= 1) ok = ok && tc::mbar_wait_sleep(&sm.sempty[set], (uint32_t)((use - 1) & 1));
       if (!FOLD && a.dstates) stage_row<SW>(sm.stage[set][0], r, g32, x);
       part = scan_part(gnext, ci + 1);  // gates of the next chunk
       gnext = load_g(ci + 2);

@@ -335,7 +335,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
     // P Delta(c) (which covers Q h(c), issued before it from this thread)
     // before they overwrite the images or the output columns these read.
     if (lane == 0) {
-      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % nring], (i / nring) & 1); };
+      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait_sleep(&sm.full[i % nring], (i / nring) & 1); };
       auto slot_of = [&](int i) { return smem_u32(sm.slot[i % nring]); };
       auto release = [&](int i) { tc::commit(&sm.empty[i % nring]); };
       for (int c = cbeg; c < cend; ++c) {
@@ -343,7 +343,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
         const uint32_t par = (uint32_t)(ci & 1);
         if (C64) {  // Q h came with w h; P Delta alone, K = 64
           const int iP = ci * TPC + 2;
-          ok = ok && tc::mbar_wait(&sm.barD, par);  // Delta^T written
+          ok = ok && tc::mbar_wait_sleep(&sm.barD, par);  // Delta^T written
           wait_tile(iP);
           tc::fence_after();
           tc::gemm_k128<4>(tmem + C_O2, slot_of(iP), smem_u32(sm.Dt), SW, false);
@@ -352,13 +352,13 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
           continue;
         }
         const int iQ = ci * TPC + 1, iP = ci * TPC + 3;
-        ok = ok && tc::mbar_wait(&sm.barX, par);  // w h(c) done: h(c) is in Ht[ci & 1]
+        ok = ok && tc::mbar_wait_sleep(&sm.barX, par);  // w h(c) done: h(c) is in Ht[ci & 1]
         wait_tile(iQ);
         tc::fence_after();
         tc::gemm_k128(tmem + o1_col(ci), slot_of(iQ), smem_u32(sm.Ht[ci & 1]), SW, false);
         tc::commit(&sm.barO1);
         release(iQ);
-        ok = ok && tc::mbar_wait(&sm.barD, par);  // Delta^T written
+        ok = ok && tc::mbar_wait_sleep(&sm.barD, par);  // Delta^T written
         wait_tile(iP);
         tc::fence_after();
         tc::gemm_k128(tmem + C_O2, slot_of(iP), smem_u32(sm.Dt), SW, false);
@@ -377,7 +377,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
       for (int c = cbeg; c < cend; ++c) {
         const int ci = c - cbeg;
         const int set = ci % NSTAGE, use = ci / NSTAGE;
-        ok = ok && tc::mbar_wait(&sm.sfull[set], (uint32_t)(use & 1));
+        ok = ok && tc::mbar_wait_sleep(&sm.sfull[set], (uint32_t)(use & 1));
         if (a.states) tc::tma_store_2d(&mp.St, sbase, (int)((bh * a.NC + c) * HD), stage + set * 2 * SLICE);
         if (a.delta) tc::tma_store_2d(&mp.De, sbase, (int)((bh * a.NC + c) * CH), stage + set * 2 * SLICE + SLICE);
         tc::bulk_commit();
@@ -392,7 +392,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
     // i - nring has completed (signalled on that slot's empty barrier).
     if (lane == 0) {
       for (int i = 0; i < ntiles; ++i) {
-        if (i >= nring) ok = ok && tc::mbar_wait(&sm.empty[i % nring], (uint32_t)((i / nring - 1) & 1));
+        if (i >= nring) ok = ok && tc::mbar_wait_sleep(&sm.empty[i % nring], (uint32_t)((i / nring - 1) & 1));
         issue(i);
       }
     }
@@ -404,7 +404,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
     // of issue is the order of execution.  After each product its tile slot is
     // released to the producer by a commit to the slot's empty barrier.
     if (lane == 0) {
-      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait(&sm.full[i % nring], (i / nring) & 1); };
+      auto wait_tile = [&](int i) { ok = ok && tc::mbar_wait_sleep(&sm.full[i % nring], (i / nring) & 1); };
       auto slot_of = [&](int i) { return smem_u32(sm.slot[i % nring]); };
       auto release = [&](int i) { tc::commit(&sm.empty[i % nring]); };
       for (int c = cbeg; c < cend; ++c) {
@@ -413,13 +413,13 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
         const int t0 = ci * TPC;
         const int iW = t0, iQ = t0 + 1, iK = t0 + (C64 ? 1 : tile_of(2)), iP = t0 + 3;
         const uint32_t ht = smem_u32(sm.Ht[ci & 1]);
-        if (ci > 0) ok = ok && tc::mbar_wait(&sm.barHt, par ^ 1);  // state image of chunk c
+        if (ci > 0) ok = ok && tc::mbar_wait_sleep(&sm.barHt, par ^ 1);  // state image of chunk c
         wait_tile(iW);
         tc::fence_after();
         tc::gemm_k128(tmem + 0, slot_of(iW), ht, SW, false);
         tc::commit(&sm.barX);
         release(iW);
-        ok = ok && tc::mbar_wait(&sm.barDg, par);  // (ef Delta)^T written
+        ok = ok && tc::mbar_wait_sleep(&sm.barDg, par);  // (ef Delta)^T written
         wait_tile(iK);
         tc::fence_after();
         if (C64)
@@ -442,7 +442,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
       const uint32_t par = (uint32_t)(ci & 1);
       // staging set ci % NSTAGE (h, Delta) was last read by the stores of chunk ci - NSTAGE
       const int set = ci % NSTAGE, use = ci / NSTAGE;
-      if (staged && use >= 1) ok = ok && tc::mbar_wait(&sm.sempty[set], (uint32_t)((use - 1) & 1));
+      if (staged && use >= 1) ok = ok && tc::mbar_wait_sleep(&sm.sempty[set], (uint32_t)((use - 1) & 1));
       if (!FOLD && a.states) stage_row<SW>(stage + set * 2 * SLICE, r, g32, h);
 
       // ---- Delta = u - X -------------------------------------------------------
