@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       __syncthreads();  // the scales are read by every epilogue thread below
     }
     if (tid == 0) {
-      ok = ok && tc::mbar_wait(&sm.barKQ, (uint32_t)(kq_uses & 1));
+      ok = ok && tc::mbar_wait_sleep(&sm.barKQ, (uint32_t)(kq_uses & 1));
       tc::fence_after();
       tc::gemm_k128(tmem + 0, smem_u32(sm.A[kb]), smem_u32(sm.A[kb]), 128, false);
       if (needP) tc::gemm_k128(tmem + 128, smem_u32(qbuf), smem_u32(sm.A[kb]), 128, false);
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       const bool last = (jj + 1 == jj1) && ug_next < u_end;
       if (tid == 0) {
         if (needU) {
-          ok = ok && tc::mbar_wait(&sm.barV[vb], (vb ? v_use1 : v_use0) & 1u);
+          ok = ok && tc::mbar_wait_sleep(&sm.barV[vb], (vb ? v_use1 : v_use0) & 1u);
           tc::fence_after();
           tc::gemm_bmn_k128(tmem + 384, smem_u32(sm.Tp), smem_u32(sm.A[vbi[vb]]), false);
         }

@@ -160,9 +160,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 }
 
 // try_wait with a suspend-time hint (ns): the thread sleeps until the phase
-// completes or the hint runs out, instead of spinning.  For waits of many
-// threads (epilogue warps waiting out a product): their spinning would take
-// issue slots from the thread that issues the products.  Bounded as mbar_wait.
+// completes or the hint runs out, instead of spinning.  Spinning waiters take
+// issue slots from the threads that issue the products and copies.  Measured
+// per kernel: it pays for every wait of the walks and the preparation and for
+// the gradient kernel's many-thread waits; the gradient kernel's issuing
+// thread, which waits on tiles it requested moments before, keeps spinning.
+// Bounded as mbar_wait.
 __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
   uint32_t done;
   asm volatile(
