@@ -7,12 +7,13 @@ namespace gdn {
 
 namespace {
 
+// (one warp more than the walk's configuration: the dO products' issuer)
 template <bool FOLD, int SW>
-__global__ void __launch_bounds__(walkb::BwdCfg<SW>::NT, 1)
+__global__ void __launch_bounds__(walkb::BwdCfg<SW>::NT + 32, 1)
     k_walk_bwd(WalkBwdArgs a, const __grid_constant__ WalkBwdMaps mp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  walkb::walk<FOLD, SW>(a, mp, base, blockIdx.x, blockIdx.y, blockIdx.z);
+  walkb::walk<FOLD, SW, true>(a, mp, base, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
 template <bool FOLD, int SW>
@@ -22,7 +23,7 @@ cudaError_t launch_one(const WalkBwdArgs& a, const WalkBwdMaps& m, cudaStream_t 
       cudaFuncSetAttribute(k_walk_bwd<FOLD, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   constexpr int NSL = HD / SW;
-  k_walk_bwd<FOLD, SW><<<dim3(FOLD ? 2 * NSL : NSL, a.S, a.B * a.Hv), walkb::BwdCfg<SW>::NT, smem, s>>>(a, m);
+  k_walk_bwd<FOLD, SW><<<dim3(FOLD ? 2 * NSL : NSL, a.S, a.B * a.Hv), walkb::BwdCfg<SW>::NT + 32, smem, s>>>(a, m);
   return cudaGetLastError();
 }
 

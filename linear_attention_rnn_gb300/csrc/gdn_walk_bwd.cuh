@@ -27,8 +27,11 @@
 // dh' -> Y -> dh.  A fifth warp issues the MMAs once their operands are
 // signalled ready; a sixth issues the TMA loads of the chunk tiles (P, Q, K, w
 // in the order consumed) into a ring of 32 KiB slots, refilling each as
-// soon as the MMA that read it completes.  Every wait is bounded; one that gives up
-// sets bit 0 of the status word.
+// soon as the MMA that read it completes.  With SPLIT (the kernels that run
+// this walk alone) an eighth warp issues the two dO products, so that their
+// issue never holds the chain's issuer; the chain's issuer then waits for
+// Q^T (gamma dO) to complete before it accumulates w^T (-Y) onto it.  Every
+// wait is bounded; one that gives up sets bit 0 of the status word.
 //
 // Modes:
 //   WALK (fold = 0): from the cotangent leaving the segment, store for every
@@ -109,7 +112,7 @@ __device__ __forceinline__ void arrive(uint64_t* bar) {
 
 // The walk of CTA (slice, seg, bhi) with BwdCfg<SW>::NT threads; `base` is the
 // 1024-byte-aligned dynamic shared memory (sizeof(WalkBwdSmem<SW>) bytes).
-template <bool FOLD, int SW>
+template <bool FOLD, int SW, bool SPLIT = false>
 __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp, unsigned char* base, int slice,
                                      int seg, int bhi) {
   using Cfg = BwdCfg<SW>;
@@ -263,7 +266,28 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     }
   };
 
-  if (warp == NCW + 2) {
+  if (SPLIT && warp == NCW + 3) {
+    // ===================================================== dO products' issuer
+    // P^T dO and Q^T (gamma dO) of each chunk once its dO images are written
+    // (they were written after both products of the chunk before had read them)
+    if (lane == 0 && withO) {
+      for (int ci = 0; ci < n; ++ci) {
+        const int t0 = ci * TPC;
+        ok = ok && tc::mbar_wait_sleep(&sm.barO, (uint32_t)(ci & 1));
+        ok = ok && tc::mbar_wait_sleep(&sm.full[t0 % NRING], (t0 / NRING) & 1);
+        tc::fence_after();
+        tc::gemm_amn_k128(tmem + C_P, smem_u32(sm.slot[t0 % NRING]), smem_u32(sm.Ot), SW, false);
+        tc::commit(&sm.barP);
+        tc::commit(&sm.empty[t0 % NRING]);
+        const int iQ = t0 + 1;
+        ok = ok && tc::mbar_wait_sleep(&sm.full[iQ % NRING], (iQ / NRING) & 1);
+        tc::fence_after();
+        tc::gemm_amn_k128(tmem + c_q(ci), smem_u32(sm.slot[iQ % NRING]), smem_u32(sm.Ogt), SW, false);
+        tc::commit(&sm.barQ);
+        tc::commit(&sm.empty[iQ % NRING]);
+      }
+    }
+  } else if (warp == NCW + 2) {
     // ============================================================ TMA stores
     // The staged dh' and dDelta slices of each chunk leave by TMA stores once the
     // compute threads have signalled them; when the stores have read the buffers
@@ -308,7 +332,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
         tc::commit(&sm.barP);
         release(ci * TPC);
       };
-      if (withO) issue_p(0);
+      if (withO && !SPLIT) issue_p(0);
       for (int ci = 0; ci < n; ++ci) {
         const uint32_t par = (uint32_t)(ci & 1);
         const int t0 = ci * TPC;
@@ -319,20 +343,22 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
         tc::gemm_k128(tmem + C_Y, slot_of(iK), smem_u32(sm.Xt), SW, false);
         tc::commit(&sm.barY);
         release(iK);
-        if (withO) {
+        if (withO && !SPLIT) {
           wait_tile(iQ);
           tc::fence_after();
           tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iQ), smem_u32(sm.Ogt), SW, false);
           tc::commit(&sm.barQ);
           release(iQ);
         }
+        // (SPLIT: Q^T (gamma dO), issued by the other warp, has completed)
+        if (withO && SPLIT) ok = ok && tc::mbar_wait_sleep(&sm.barQ, par);
         ok = ok && tc::mbar_wait_sleep(&sm.barYt, par);  // (-Y)^T written
         wait_tile(iW);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iW), smem_u32(sm.Yt), SW, withO);
         tc::commit(&sm.barH);
         release(iW);
-        if (withO && ci + 1 < n) issue_p(ci + 1);
+        if (withO && !SPLIT && ci + 1 < n) issue_p(ci + 1);
       }
     }
   } else {
