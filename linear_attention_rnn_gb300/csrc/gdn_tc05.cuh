@@ -57,11 +57,15 @@ template <int NK = 8>
 __device__ __forceinline__ void gemm_k128(uint32_t tmem_d, uint32_t a_smem, uint32_t b_smem,
                                           int N, bool accumulate_first) {
   const uint32_t idesc = (N == 128) ? idesc_bf16(128, 128) : idesc_bf16(128, N);
+  // the descriptors are linear in the address (bits 0-13 hold address / 16, and
+  // every operand lies inside the CTA's shared memory, below 256 KiB): each
+  // step adds its constant offset to the base descriptors
+  const uint64_t da0 = desc_sw128(a_smem), db0 = desc_sw128(b_smem);
 #pragma unroll
   for (int k = 0; k < NK; ++k) {
     const uint32_t koff = (uint32_t)(k & 3) * 32u;
-    const uint64_t da = desc_sw128(a_smem + (uint32_t)(k >> 2) * 128u * 128u + koff);
-    const uint64_t db = desc_sw128(b_smem + (uint32_t)(k >> 2) * (uint32_t)N * 128u + koff);
+    const uint64_t da = da0 + (((uint32_t)(k >> 2) * 128u * 128u + koff) >> 4);
+    const uint64_t db = db0 + (((uint32_t)(k >> 2) * (uint32_t)N * 128u + koff) >> 4);
     mma(tmem_d, da, db, idesc, (k > 0 || accumulate_first) ? 1u : 0u);
   }
 }
@@ -231,11 +235,12 @@ template <int NK = 8>
 __device__ __forceinline__ void gemm_amn_k128(uint32_t tmem_d, uint32_t a_smem, uint32_t b_smem,
                                               int N, bool accumulate_first) {
   const uint32_t idesc = idesc_bf16(128, N) | (1u << 15);  // A is MN-major
+  const uint64_t da0 = desc_sw128_mn(a_smem, 128u * 128u), db0 = desc_sw128(b_smem);  // (as gemm_k128)
 #pragma unroll
   for (int k = 0; k < NK; ++k) {
-    const uint64_t da = desc_sw128_mn(a_smem + (uint32_t)k * 2048u, 128u * 128u);
+    const uint64_t da = da0 + (((uint32_t)k * 2048u) >> 4);
     const uint32_t koff = (uint32_t)(k & 3) * 32u;
-    const uint64_t db = desc_sw128(b_smem + (uint32_t)(k >> 2) * (uint32_t)N * 128u + koff);
+    const uint64_t db = db0 + (((uint32_t)(k >> 2) * (uint32_t)N * 128u + koff) >> 4);
     mma(tmem_d, da, db, idesc, (k > 0 || accumulate_first) ? 1u : 0u);
   }
 }
@@ -247,11 +252,12 @@ __device__ __forceinline__ void gemm_amn_k128(uint32_t tmem_d, uint32_t a_smem, 
 __device__ __forceinline__ void gemm_bmn_k128(uint32_t tmem_d, uint32_t a_smem, uint32_t b_smem,
                                               bool accumulate_first) {
   const uint32_t idesc = idesc_bf16(128, 128) | (1u << 16);  // B is MN-major
+  const uint64_t da0 = desc_sw128(a_smem), db0 = desc_sw128_mn(b_smem, 128u * 128u);  // (as gemm_k128)
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const uint32_t koff = (uint32_t)(k & 3) * 32u;
-    const uint64_t da = desc_sw128(a_smem + (uint32_t)(k >> 2) * 128u * 128u + koff);
-    const uint64_t db = desc_sw128_mn(b_smem + (uint32_t)k * 2048u, 128u * 128u);
+    const uint64_t da = da0 + (((uint32_t)(k >> 2) * 128u * 128u + koff) >> 4);
+    const uint64_t db = db0 + (((uint32_t)k * 2048u) >> 4);
     mma(tmem_d, da, db, idesc, (k > 0 || accumulate_first) ? 1u : 0u);
   }
 }
@@ -283,11 +289,13 @@ __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.
 __device__ __forceinline__ void gemm128(uint32_t tmem_d, uint32_t a_smem, bool a_mn, uint32_t b_smem,
                                         bool b_mn, bool accumulate_first) {
   const uint32_t idesc = idesc_bf16(128, 128) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
+  const uint64_t da0 = a_mn ? desc_sw128_mn(a_smem, 128u * 128u) : desc_sw128(a_smem);  // (as gemm_k128)
+  const uint64_t db0 = b_mn ? desc_sw128_mn(b_smem, 128u * 128u) : desc_sw128(b_smem);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const uint32_t kmaj = (uint32_t)(k >> 2) * 128u * 128u + (uint32_t)(k & 3) * 32u;
-    const uint64_t da = a_mn ? desc_sw128_mn(a_smem + (uint32_t)k * 2048u, 128u * 128u) : desc_sw128(a_smem + kmaj);
-    const uint64_t db = b_mn ? desc_sw128_mn(b_smem + (uint32_t)k * 2048u, 128u * 128u) : desc_sw128(b_smem + kmaj);
+    const uint64_t da = da0 + ((a_mn ? (uint32_t)k * 2048u : kmaj) >> 4);
+    const uint64_t db = db0 + ((b_mn ? (uint32_t)k * 2048u : kmaj) >> 4);
     mma(tmem_d, da, db, idesc, (k > 0 || accumulate_first) ? 1u : 0u);
   }
 }
