@@ -60,14 +60,14 @@ FWD_KERNELS_SEG = ["prep", "fold", "prefix", "walk"]
 # the backward of a step reads the w, u, P and T the forward kept (no preparation)
 BWD_KERNELS = ["walk_bwd", "grads"]
 BWD_KERNELS_SEG = ["fold_bwd", "prefix_bwd", "walk_bwd", "grads"]
-KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 1, 32>", "walks": "k_walk_pair", "grads": "k_grads",
+KERNEL_SYMBOL = {"prep": "k_prep", "walk": "k_walk_fwd<0, 1, 32, 0>", "walks": "k_walk_pair", "grads": "k_grads",
                  "walk_bwd": "k_walk_bwd<0, 32>",
-                 "fold": "k_walk_fwd<1, 0, 32>", "prefix": "k_affine_walk",
+                 "fold": "k_walk_fwd<1, 0, 32, 0>", "prefix": "k_affine_walk",
                  "fold_bwd": "k_walk_bwd<1, 32>", "prefix_bwd": "k_affine_walk"}
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum, bytes)
 # from the committed ncu capture of the same kernel code (profiles/*), keyed by
 # kernel; a kernel changed since its capture has no entry.
-NCU_TRAFFIC = {"grads": 317344000}  # profiles/k_grads_layer_t4096_ncu_full.md: 271.08 MB + 46.27 MB
+NCU_TRAFFIC = {"grads": 317725184}  # profiles/k_grads_layer_t4096_ncu_full.md: 271.00 MB + 46.73 MB
 
 
 def algorithmic(wl):
