@@ -23,6 +23,17 @@ constexpr int SL = 32;         // state-column slice width of the sequential wal
 
 typedef __nv_bfloat16 bf16;
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// serialization attribute may start while the kernel before it in the stream
+// still runs; pdl_wait() returns once that kernel has completed and its
+// memory is visible (at once when the kernel was launched normally).  Every
+// kernel of this library waits before it reads anything the kernel before it
+// may write and before it writes anything, and only then lets its own
+// dependents start (pdl_release), so that when a kernel starts, every kernel
+// before its immediate predecessor has completed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -158,10 +158,18 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     tc::mbar_init(&sm.barDO, 1);
     tc::mbar_init(&sm.barM, 1);
     tc::mbar_fence_init();
+    // the first unit's K, Q (inputs) and T (written by the preparation, which
+    // completed before the kernel just before this one started)
     const GUnit x0 = decode(u_begin);
     load_kq(x0);
-    const long cid0 = cid_of(x0, 0);
-    load2d(sm.W1, &mp.Tb, cid0, &sm.barT);
+    load2d(sm.W1, &mp.Tb, cid_of(x0, 0), &sm.barT);
+  }
+  // dDelta, dh' and (without a saved buffer) the entering states and Delta come
+  // from the kernel just before; every store follows too
+  pdl_wait();
+  pdl_release();
+  if (tid == 0) {
+    const long cid0 = cid_of(decode(u_begin), 0);
     load2d(sm.W2, &mp.ddelta, cid0, &sm.barDD);
     load2d(sm.W3, &mp.states, cid0, &sm.barH);
     load2d(sm.W4, &mp.delta, cid0, &sm.barDl);
@@ -623,8 +631,7 @@ cudaError_t launch_grads(const GradArgs& a, cudaStream_t s) {
   const long units = (long)a.B * a.Hk * a.NC;
   const int ctas = (int)(units < sms ? units : sms);
   if (ctas <= 0) return cudaSuccess;
-  k_grads<<<ctas, GT, smem, s>>>(a, mp);
-  return cudaGetLastError();
+  return launch_pdl(k_grads, dim3(ctas), dim3(GT), smem, s, a, mp);
 }
 
 }  // namespace gdn

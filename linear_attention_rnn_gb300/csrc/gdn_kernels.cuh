@@ -139,6 +139,23 @@ struct GradArgs {
   int B, T, Hk, Hv, NC;
 };
 
+// Launches kernel k with programmatic stream serialization: its CTAs may start
+// (and run up to their pdl_wait) while the previous kernel in the stream ends.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
+
 size_t prep_smem_bytes();
 size_t grad_smem_bytes();
 

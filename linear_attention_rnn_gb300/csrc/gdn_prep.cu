@@ -268,6 +268,8 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
+  pdl_wait();     // the kernel before may still read the tiles this one overwrites
+  pdl_release();
   const uint32_t tmem = sm.tmem;  // columns: K K^T 0, Q K^T 128, w 256, u 384
   const uint32_t tlane = tmem + ((uint32_t)(32 * quarter) << 16);
   bool ok = true;
@@ -657,8 +659,7 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
   const long units = (long)a.B * a.NC * a.Hv;
   const int ctas = (int)(units < sms ? units : sms);
   if (ctas <= 0) return cudaSuccess;
-  k_prep<<<ctas, PT, smem, s>>>(a, mp);
-  return cudaGetLastError();
+  return launch_pdl(k_prep, dim3(ctas), dim3(PT), smem, s, a, mp);
 }
 
 }  // namespace gdn

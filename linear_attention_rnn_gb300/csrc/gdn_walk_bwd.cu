@@ -23,8 +23,8 @@ cudaError_t launch_one(const WalkBwdArgs& a, const WalkBwdMaps& m, cudaStream_t 
       cudaFuncSetAttribute(k_walk_bwd<FOLD, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   constexpr int NSL = HD / SW;
-  k_walk_bwd<FOLD, SW><<<dim3(FOLD ? 2 * NSL : NSL, a.S, a.B * a.Hv), walkb::BwdCfg<SW>::NT + 32, smem, s>>>(a, m);
-  return cudaGetLastError();
+  return launch_pdl(k_walk_bwd<FOLD, SW>, dim3(FOLD ? 2 * NSL : NSL, a.S, a.B * a.Hv),
+                    dim3(walkb::BwdCfg<SW>::NT + 32), smem, s, a, m);
 }
 
 }  // namespace

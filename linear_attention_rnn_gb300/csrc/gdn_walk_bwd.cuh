@@ -158,6 +158,8 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
   }
   if (warp == 0) tc::alloc(&sm.tmem, Cfg::TMEM_COLS);
   bool ok = true;
+  pdl_wait();  // before any load of what earlier kernels wrote, and any store
+  pdl_release();
 
   const int r = 32 * (warp & 3) + lane;  // compute threads: row r of the state slice / of the chunk
   float x[32];

@@ -25,8 +25,8 @@ cudaError_t launch_one(const WalkFwdArgs& a, const WalkFwdMaps& m, cudaStream_t 
   if (e != cudaSuccess) return e;
   constexpr int NSL = HD / SW;
   const int nt = walkf::FwdCfg<SW>::NT + ((STAGED && a.o) ? 32 : 0);
-  k_walk_fwd<FOLD, STAGED, SW, C64><<<dim3(FOLD ? 2 * NSL : NSL, a.S, a.B * a.Hv), nt, smem, s>>>(a, m);
-  return cudaGetLastError();
+  return launch_pdl(k_walk_fwd<FOLD, STAGED, SW, C64>, dim3(FOLD ? 2 * NSL : NSL, a.S, a.B * a.Hv), dim3(nt), smem,
+                    s, a, m);
 }
 
 }  // namespace

@@ -189,6 +189,8 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
   }
   if (warp == 0) tc::alloc(&sm.tmem, Cfg::TMEM_COLS);
   bool ok = true;
+  pdl_wait();  // before any load of what earlier kernels wrote, and any store
+  pdl_release();
 
   // state row r = tid (compute threads), columns col0..col0+31
   const int r = 32 * (warp & 3) + lane;

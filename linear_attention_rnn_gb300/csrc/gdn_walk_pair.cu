@@ -42,8 +42,7 @@ cudaError_t launch_walk_pair(const WalkFwdArgs& fa, const WalkFwdMaps& fm, const
   if (fa.S != ba.S || fa.B != ba.B || fa.Hv != ba.Hv || fa.NC != ba.NC || fa.o) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k_walk_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PAIR_SMEM);
   if (e != cudaSuccess) return e;
-  k_walk_pair<<<dim3(NB + NF, fa.S, fa.B * fa.Hv), PAIR_NT, PAIR_SMEM, s>>>(fa, fm, ba, bm);
-  return cudaGetLastError();
+  return launch_pdl(k_walk_pair, dim3(NB + NF, fa.S, fa.B * fa.Hv), dim3(PAIR_NT), PAIR_SMEM, s, fa, fm, ba, bm);
 }
 
 }  // namespace gdn
