@@ -312,20 +312,27 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     }
     // ---- dv = diag(beta) dV' and dbeta += rowsum(dV' V), while S2/S5 run -----------------
     // Read back from the bf16 dV' tile with 16 threads per row, so that V is
-    // loaded and dv stored in whole 256-byte rows.
-    {
-      constexpr int NI = (CH * 16) / GT;  // 4 chunks of 16 bytes per thread
+    // loaded and dv stored in whole 256-byte rows.  Warp 0 takes no share: its
+    // thread 0 waits for dh' and issues S2/S5 meanwhile, and a share of its own
+    // would put that wait in front of every later barrier.  480 threads, 30
+    // rows' worth of 16-byte chunks per pass (a 16-lane group stays on one row).
+    if (warp > 0) {
+      constexpr int DT = GT - 32;                // 480 threads
+      constexpr int NI = (CH * 16 + DT - 1) / DT;  // 5 passes (the last one for warps 1-4 only)
+      const int t2 = tid - 32;
       uint4 v4[NI];
 #pragma unroll
       for (int i = 0; i < NI; ++i) {  // all loads in flight before any is used
-        const int idx = tid + i * GT;
+        const int idx = t2 + i * DT;
         const int r = idx >> 4, jc = idx & 15;
-        v4[i] = r < L ? *reinterpret_cast<const uint4*>(a.v + (tokv + (long)r * a.Hv) * HD + 8 * jc)
-                      : make_uint4(0u, 0u, 0u, 0u);
+        v4[i] = (idx < CH * 16 && r < L)
+                    ? *reinterpret_cast<const uint4*>(a.v + (tokv + (long)r * a.Hv) * HD + 8 * jc)
+                    : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
-        const int idx = tid + i * GT;
+        const int idx = t2 + i * DT;
+        if (idx >= CH * 16) break;  // warp-uniform: whole warps run out together
         const int r = idx >> 4, jc = idx & 15;
         const uint4 d4 = *reinterpret_cast<const uint4*>(sm.W1 + tc::sw128_chunk(r, jc, CH));
         const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w}, vw[4] = {v4[i].x, v4[i].y, v4[i].z, v4[i].w};
