@@ -48,10 +48,15 @@ struct GradSmem {
   unsigned char W2[TILE];          // dDelta; dh'; dO
   unsigned char W3[TILE];          // h
   unsigned char W4[TILE];          // Delta; dQK
-  float Gl[CH], gam[CH], ef[CH], beta[CH];
-  float etab[CH];  // exp2(Gl[c0] - Gl[s]) for the 16-column block c0 of column s
-  float colX[CH], dbeta[CH], dbg[CH], d_ef[CH], rowX[CH], dgamO[CH];
-  float red[GW];
+  // per value head: its gates and per-row sums, two sets (by the parity of the
+  // CTA's value-head count), so that a value head's gate cotangents can be
+  // formed while the next value head starts
+  struct HeadVec {
+    float Gl[CH], gam[CH], ef[CH], beta[CH];
+    float etab[CH];  // exp2(Gl[c0] - Gl[s]) for the 16-column block c0 of column s
+    float colX[CH], dbeta[CH], dbg[CH], d_ef[CH], rowX[CH], dgamO[CH];
+    float red[GW];
+  } hv[2];
   uint64_t barKQ, barT, barDD, barH, barDl, barDH, barDO, barM;
   uint32_t tmem;
 };
@@ -205,6 +210,58 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
   };
   float g_next = 0.f, b_next = 0.f;
   if (tid < CH) load_gates(decode(u_begin), 0, g_next, b_next);
+  // Gate cotangents of a value head (one warp): dg = reverse cumsum over the chunk
+  // of dG, dbeta; with gate logits the chain rule through the activations.
+  auto gate_cot = [&](const GradSmem::HeadVec& P, long tokv_p, int L_p) {
+    float dgC = 0.f;
+#pragma unroll
+    for (int w = 0; w < GW; ++w) dgC += P.red[w];
+    float sum_def = 0.f;
+    float dG[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = lane * 4 + i;
+      const float de = P.d_ef[r] * P.ef[r];
+      sum_def += de;
+      const float dgam = P.dgamO[r] + P.beta[r] * P.dbg[r];
+      dG[i] = P.gam[r] * dgam + P.rowX[r] - P.colX[r] - de;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum_def += __shfl_xor_sync(0xffffffffu, sum_def, off);
+    if (lane == 31) dG[3] += P.gam[CH - 1] * dgC + sum_def;  // row C-1: gamma_C = gamma[C-1]
+    // reverse inclusive cumsum over the 128 rows: dg_s = sum_{r >= s} dG_r
+    const float tot = dG[0] + dG[1] + dG[2] + dG[3];
+    float incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float o = __shfl_down_sync(0xffffffffu, incl, off);
+      if (lane + off < 32) incl += o;
+    }
+    float run = incl - tot;  // sum over lanes > lane
+    float dg[4];
+#pragma unroll
+    for (int i = 3; i >= 0; --i) {
+      run += dG[i];
+      dg[i] = run;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = lane * 4 + i;
+      if (r < L_p) {
+        const long t = tokv_p + (long)r * a.Hv;
+        float dgv = dg[i], dbv = P.dbeta[r] + P.gam[r] * P.dbg[r];
+        if (a.gate_logits) {  // chain rule through g = -softplus(a) and beta = sigmoid(b)
+          const float sa = act_beta(a.g[t], 1), sb = act_beta(a.beta[t], 1);
+          dgv *= -sa;
+          dbv *= sb * (1.f - sb);
+        }
+        a.dg[t] = dgv;
+        a.dbeta[t] = dbv;
+      }
+    }
+  };
+  long pend_tokv = 0;  // the value head whose gate cotangents are pending
+  int pend_L = 0;
   int hc = 0;  // value heads processed by this CTA: the parity of the tile barriers
 
   for (int u = u_begin; u < u_end; ++u) {
@@ -220,19 +277,25 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     const long cid = cid_of(xu, jj);
     const long tokv = ((long)b * a.T + t0) * a.Hv + j;  // row 0 of the v/dO tile
     const uint32_t par = (uint32_t)(hc & 1);
+    GradSmem::HeadVec& H = sm.hv[hc & 1];
     // the value head after this one: the next of this unit, or the next unit's first
     const bool next_here = jj + 1 < group;
     const bool has_after = next_here || has_next;
     const long cid_after = next_here ? cid_of(xu, jj + 1) : cid_of(xn, 0);
     // ---- gates of value head j; per-row sums cleared ----------------------------
+    // (warp 15 forms the previous value head's gate cotangents meanwhile; the two
+    // barriers of this part are over warps 0-14)
+    if (warp == GW - 1) {
+      if (hc > 0) gate_cot(sm.hv[(hc - 1) & 1], pend_tokv, pend_L);
+    }
     if (tid < CH) {
-      sm.Gl[tid] = g_next;
-      sm.beta[tid] = b_next;
+      H.Gl[tid] = g_next;
+      H.beta[tid] = b_next;
       if (next_here)
         load_gates(xu, jj + 1, g_next, b_next);
       else if (has_next)
         load_gates(xn, 0, g_next, b_next);
-      sm.colX[tid] = sm.dbeta[tid] = sm.dbg[tid] = sm.d_ef[tid] = sm.rowX[tid] = sm.dgamO[tid] = 0.f;
+      H.colX[tid] = H.dbeta[tid] = H.dbg[tid] = H.d_ef[tid] = H.rowX[tid] = H.dgamO[tid] = 0.f;
     }
     if (tid == 0) {  // S1: dV' = T^T dDelta (both tiles read MN-major)
       ok = ok && tc::mbar_wait(&sm.barT, par);
@@ -241,30 +304,30 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       tc::gemm128(tmem + C_A, smem_u32(sm.W1), true, smem_u32(sm.W2), true, false);
       tc::commit(&sm.barM);
     }
-    __syncthreads();
+    if (warp < GW - 1) asm volatile("bar.sync 1, %0;" ::"r"(GT - 32) : "memory");
     if (warp == 0) {
       float v[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = sm.Gl[lane * 4 + i];
+      for (int i = 0; i < 4; ++i) v[i] = H.Gl[lane * 4 + i];
       warp_cumsum128(v, lane);
       const float Glast = __shfl_sync(0xffffffffu, v[3], 31);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = lane * 4 + i;
-        sm.Gl[r] = v[i] * LOG2E;
-        sm.gam[r] = expf(v[i]);
-        sm.ef[r] = expf(Glast - v[i]);
+        H.Gl[r] = v[i] * LOG2E;
+        H.gam[r] = expf(v[i]);
+        H.ef[r] = expf(Glast - v[i]);
       }
       __syncwarp();  // every Gl of the chunk is written (by this warp)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = lane * 4 + i;
-        sm.etab[r] = exp2f(sm.Gl[r & ~15] - sm.Gl[r]);  // >= 1
+        H.etab[r] = exp2f(H.Gl[r & ~15] - H.Gl[r]);  // >= 1
       }
     }
-    __syncthreads();
-    const float Glr = sm.Gl[row], br = sm.beta[row], gr = sm.gam[row], efr = sm.ef[row];
-    const float bgr = br * gr;
+    if (warp < GW - 1) asm volatile("bar.sync 1, %0;" ::"r"(GT - 32) : "memory");
+    // this row's gates, read after E1's barrier (which warp 15 reaches late)
+    float Glr = 0.f, br = 0.f, gr = 0.f, efr = 0.f, bgr = 0.f;
     float p_db = 0.f, p_dbg = 0.f, p_def = 0.f, p_rowx = 0.f, p_dgam = 0.f;
     // Decays exp2(Gl_r - Gl_s) of columns c0..c0+31 of this thread's row, masked to
     // s < r (or s <= r).  G is non-increasing, so in each 16-column block b0 the decay
@@ -274,13 +337,13 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int b0 = c0 + 16 * h;
-        if (sm.Gl[b0] - sm.Gl[b0 + 15] <= 100.f) {  // block-uniform
-          const float fr = exp2f(Glr - sm.Gl[b0]);
+        if (H.Gl[b0] - H.Gl[b0 + 15] <= 100.f) {  // block-uniform
+          const float fr = exp2f(Glr - H.Gl[b0]);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) m[16 * h + i] = fr * sm.etab[b0 + i];
+          for (int i = 0; i < 16; ++i) m[16 * h + i] = fr * H.etab[b0 + i];
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) m[16 * h + i] = exp2f(Glr - sm.Gl[b0 + i]);
+          for (int i = 0; i < 16; ++i) m[16 * h + i] = exp2f(Glr - H.Gl[b0 + i]);
         }
       }
 #pragma unroll
@@ -299,6 +362,11 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       row32_store(sm.W1, row, c0, x);
     }
     sync_operands();
+    Glr = H.Gl[row];
+    br = H.beta[row];
+    gr = H.gam[row];
+    efr = H.ef[row];
+    bgr = br * gr;
 
     // ---- S2: dV' h^T -> A;  S5: Delta dh'^T -> B --------------------------------------
     if (tid == 0) {
@@ -336,7 +404,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
         const int r = idx >> 4, jc = idx & 15;
         const uint4 d4 = *reinterpret_cast<const uint4*>(sm.W1 + tc::sw128_chunk(r, jc, CH));
         const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w}, vw[4] = {v4[i].x, v4[i].y, v4[i].z, v4[i].w};
-        const float bt = sm.beta[r];
+        const float bt = H.beta[r];
         float part = 0.f;
         uint32_t ow[4];
 #pragma unroll
@@ -350,7 +418,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
               make_uint4(ow[0], ow[1], ow[2], ow[3]);
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if ((lane & 15) == 0) atomicAdd(&sm.dbeta[r], part);
+        if ((lane & 15) == 0) atomicAdd(&H.dbeta[r], part);
       }
     }
     {  // <dh', h>: elementwise over two tiles of the same layout
@@ -371,7 +439,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-      if (lane == 0) sm.red[warp] = d;
+      if (lane == 0) H.red[warp] = d;
     }
 
     // ---- E2: dK (+)= -diag(beta gamma) dV' h^T + diag(ef) Delta dh'^T ---------------------
@@ -433,7 +501,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
           p_rowx += ds[i];
         }
         const float cs = colsum32(ds, lane);
-        atomicAdd(&sm.colX[c0 + lane], cs);
+        atomicAdd(&H.colX[c0 + lane], cs);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) out[i] = 0.f;
@@ -470,7 +538,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
           p_rowx += dp[i];
         }
         const float cs = colsum32(dp, lane);
-        atomicAdd(&sm.colX[c0 + lane], cs);
+        atomicAdd(&H.colX[c0 + lane], cs);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) out[i] = 0.f;
@@ -518,64 +586,16 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       tc::gemm128(tmem + C_DQ, smem_u32(sm.W4), false, smem_u32(sm.K), true, true);
       tc::commit(&sm.barM);
     }
-    atomicAdd(&sm.dbeta[row], p_db);
-    atomicAdd(&sm.dbg[row], p_dbg);
-    atomicAdd(&sm.d_ef[row], p_def);
-    atomicAdd(&sm.rowX[row], p_rowx);
-    atomicAdd(&sm.dgamO[row], p_dgam);
+    atomicAdd(&H.dbeta[row], p_db);
+    atomicAdd(&H.dbg[row], p_dbg);
+    atomicAdd(&H.d_ef[row], p_def);
+    atomicAdd(&H.rowX[row], p_rowx);
+    atomicAdd(&H.dgamO[row], p_dgam);
     wait_mma();
     if (tid == 0 && has_after) load2d(sm.W4, &mp.delta, cid_after, &sm.barDl);
-    __syncthreads();
-
-    // ---- gate cotangents of value head j ----------------------------------------------
-    if (warp == 0) {
-      float dgC = 0.f;
-#pragma unroll
-      for (int w = 0; w < GW; ++w) dgC += sm.red[w];
-      float sum_def = 0.f;
-      float dG[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = lane * 4 + i;
-        const float de = sm.d_ef[r] * sm.ef[r];
-        sum_def += de;
-        const float dgam = sm.dgamO[r] + sm.beta[r] * sm.dbg[r];
-        dG[i] = sm.gam[r] * dgam + sm.rowX[r] - sm.colX[r] - de;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum_def += __shfl_xor_sync(0xffffffffu, sum_def, off);
-      if (lane == 31) dG[3] += sm.gam[CH - 1] * dgC + sum_def;  // row C-1: gamma_C = gamma[C-1]
-      // reverse inclusive cumsum over the 128 rows: dg_s = sum_{r >= s} dG_r
-      const float tot = dG[0] + dG[1] + dG[2] + dG[3];
-      float incl = tot;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_down_sync(0xffffffffu, incl, off);
-        if (lane + off < 32) incl += o;
-      }
-      float run = incl - tot;  // sum over lanes > lane
-      float dg[4];
-#pragma unroll
-      for (int i = 3; i >= 0; --i) {
-        run += dG[i];
-        dg[i] = run;
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = lane * 4 + i;
-        if (r < L) {
-          const long t = tokv + (long)r * a.Hv;
-          float dgv = dg[i], dbv = sm.dbeta[r] + sm.gam[r] * sm.dbg[r];
-          if (a.gate_logits) {  // chain rule through g = -softplus(a) and beta = sigmoid(b)
-            const float sa = act_beta(a.g[t], 1), sb = act_beta(a.beta[t], 1);
-            dgv *= -sa;
-            dbv *= sb * (1.f - sb);
-          }
-          a.dg[t] = dgv;
-          a.dbeta[t] = dbv;
-        }
-      }
-    }
+    // (its gate cotangents: warp 15, at the next value head's start)
+    pend_tokv = tokv;
+    pend_L = L;
     __syncthreads();
     ++hc;
   }
@@ -603,6 +623,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     }
   }
   }  // units
+  if (warp == GW - 1 && hc > 0) gate_cot(sm.hv[(hc - 1) & 1], pend_tokv, pend_L);
   if (tid == 0) tc::bulk_wait();  // every store has completed before the block exits
   if (!ok && a.status) atomicOr(a.status, 1);
   tc::fence_before();
