@@ -57,7 +57,7 @@ struct GradSmem {
     float colX[CH], dbeta[CH], dbg[CH], d_ef[CH], rowX[CH], dgamO[CH];
     float red[GW];
   } hv[2];
-  uint64_t barKQ, barT, barDD, barH, barDl, barDH, barDO, barM;
+  uint64_t barKQ, barT, barDD, barH, barDl, barDH, barDO, barM, barS8;
   uint32_t tmem;
 };
 
@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     tc::mbar_init(&sm.barDH, 1);
     tc::mbar_init(&sm.barDO, 1);
     tc::mbar_init(&sm.barM, 1);
+    tc::mbar_init(&sm.barS8, 1);
     tc::mbar_fence_init();
     // the first unit's K, Q (inputs) and T (written by the preparation, which
     // completed before the kernel just before this one started)
@@ -283,10 +284,21 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     const bool has_after = next_here || has_next;
     const long cid_after = next_here ? cid_of(xu, jj + 1) : cid_of(xn, 0);
     // ---- gates of value head j; per-row sums cleared ----------------------------
-    // (warp 15 forms the previous value head's gate cotangents meanwhile; the two
-    // barriers of this part are over warps 0-14)
+    // (meanwhile warp 15 forms the previous value head's gate cotangents, and warp
+    // 14 issues S1 once T and dDelta are in and then requests Delta once the
+    // previous head's S8b has read W4; the two barriers of this part are over warps 0-13)
     if (warp == GW - 1) {
       if (hc > 0) gate_cot(sm.hv[(hc - 1) & 1], pend_tokv, pend_L);
+    } else if (tid == 32 * (GW - 2)) {  // S1: dV' = T^T dDelta (both tiles read MN-major)
+      ok = ok && tc::mbar_wait(&sm.barT, par);
+      ok = ok && tc::mbar_wait(&sm.barDD, par);
+      tc::fence_after();
+      tc::gemm128(tmem + C_A, smem_u32(sm.W1), true, smem_u32(sm.W2), true, false);
+      tc::commit(&sm.barM);
+      if (hc > 0) {  // (the first value head's Delta came with the CTA's first tiles)
+        ok = ok && tc::mbar_wait(&sm.barS8, (uint32_t)((hc - 1) & 1));
+        load2d(sm.W4, &mp.delta, cid, &sm.barDl);
+      }
     }
     if (tid < CH) {
       H.Gl[tid] = g_next;
@@ -297,14 +309,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
         load_gates(xn, 0, g_next, b_next);
       H.colX[tid] = H.dbeta[tid] = H.dbg[tid] = H.d_ef[tid] = H.rowX[tid] = H.dgamO[tid] = 0.f;
     }
-    if (tid == 0) {  // S1: dV' = T^T dDelta (both tiles read MN-major)
-      ok = ok && tc::mbar_wait(&sm.barT, par);
-      ok = ok && tc::mbar_wait(&sm.barDD, par);
-      tc::fence_after();
-      tc::gemm128(tmem + C_A, smem_u32(sm.W1), true, smem_u32(sm.W2), true, false);
-      tc::commit(&sm.barM);
-    }
-    if (warp < GW - 1) asm volatile("bar.sync 1, %0;" ::"r"(GT - 32) : "memory");
+    if (warp < GW - 2) asm volatile("bar.sync 1, %0;" ::"r"(GT - 64) : "memory");
     if (warp == 0) {
       float v[4];
 #pragma unroll
@@ -325,8 +330,8 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
         H.etab[r] = exp2f(H.Gl[r & ~15] - H.Gl[r]);  // >= 1
       }
     }
-    if (warp < GW - 1) asm volatile("bar.sync 1, %0;" ::"r"(GT - 32) : "memory");
-    // this row's gates, read after E1's barrier (which warp 15 reaches late)
+    if (warp < GW - 2) asm volatile("bar.sync 1, %0;" ::"r"(GT - 64) : "memory");
+    // this row's gates, read after E1's barrier (which warps 14 and 15 reach late)
     float Glr = 0.f, br = 0.f, gr = 0.f, efr = 0.f, bgr = 0.f;
     float p_db = 0.f, p_dbg = 0.f, p_def = 0.f, p_rowx = 0.f, p_dgam = 0.f;
     // Decays exp2(Gl_r - Gl_s) of columns c0..c0+31 of this thread's row, masked to
@@ -511,14 +516,15 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     sync_operands();
 
     // ---- S4: dK += dKK K + dKK^T K;  S6: dP = dO Delta^T -> A;  Q K^T -> B -------------
+    // (S6 first and committed alone: E4 needs only it, and S4 runs under E4)
     if (tid == 0) {
-      tc::gemm128(tmem + C_DK, smem_u32(sm.W1), false, smem_u32(sm.K), true, true);
-      tc::gemm128(tmem + C_DK, smem_u32(sm.W1), true, smem_u32(sm.K), true, true);
       ok = ok && tc::mbar_wait(&sm.barDO, par);
       tc::fence_after();
       tc::gemm128(tmem + C_A, smem_u32(sm.W2), false, smem_u32(sm.W4), false, false);
       tc::gemm128(tmem + C_B, smem_u32(sm.Q), false, smem_u32(sm.K), false, false);
       tc::commit(&sm.barM);
+      tc::gemm128(tmem + C_DK, smem_u32(sm.W1), false, smem_u32(sm.K), true, true);
+      tc::gemm128(tmem + C_DK, smem_u32(sm.W1), true, smem_u32(sm.K), true, true);
     }
     // ---- E4: dQK = dP * M (diagonal included) -> W4; rowX, colX --------------------------
     wait_mma();
@@ -548,10 +554,12 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     sync_operands();
 
     // ---- S7: dK += dQK^T Q;  S8: dO h^T -> A -------------------------------------------
+    // (S8 first and committed alone: E5 needs only it, and S7 runs under E5; the
+    // commit also covers S4, issued before it, so W1 may be reloaded at E5)
     if (tid == 0) {
-      tc::gemm128(tmem + C_DK, smem_u32(sm.W4), true, smem_u32(sm.Q), true, true);
       tc::gemm128(tmem + C_A, smem_u32(sm.W2), false, smem_u32(sm.W3), false, false);
       tc::commit(&sm.barM);
+      tc::gemm128(tmem + C_DK, smem_u32(sm.W4), true, smem_u32(sm.Q), true, true);
     }
     // ---- E5: dgamma_O = rowsum(Q * (dO h^T));  dQ (+)= diag(gamma) dO h^T ------------------
     wait_mma();
@@ -582,17 +590,17 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     __syncthreads();
     tc::fence_after();
     // ---- S8b: dQ += dQK K ----------------------------------------------------------------
+    // (committed to barS8, covering S7 too: waited for before W4 is reloaded, by
+    // warp 14 at the next value head's start, and before the unit's dq, dk leave)
     if (tid == 0) {
       tc::gemm128(tmem + C_DQ, smem_u32(sm.W4), false, smem_u32(sm.K), true, true);
-      tc::commit(&sm.barM);
+      tc::commit(&sm.barS8);
     }
     atomicAdd(&H.dbeta[row], p_db);
     atomicAdd(&H.dbg[row], p_dbg);
     atomicAdd(&H.d_ef[row], p_def);
     atomicAdd(&H.rowX[row], p_rowx);
     atomicAdd(&H.dgamO[row], p_dgam);
-    wait_mma();
-    if (tid == 0 && has_after) load2d(sm.W4, &mp.delta, cid_after, &sm.barDl);
     // (its gate cotangents: warp 15, at the next value head's start)
     pend_tokv = tokv;
     pend_L = L;
@@ -600,8 +608,11 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     ++hc;
   }
 
-  // ---- dq, dk of the key head: bf16 staging tiles in the Q and K buffers (the unit's
-  //      last products have read them; W1-W4 already hold the next unit's tiles) -------
+  // ---- dq, dk of the key head: bf16 staging tiles in the Q and K buffers, once the
+  //      unit's last products (S7, S8b) have completed and read them; W1-W3 already
+  //      hold the next unit's first tiles ------------------------------------------------
+  ok = ok && tc::mbar_wait_sleep(&sm.barS8, (uint32_t)((hc - 1) & 1));
+  tc::fence_after();
   {
     float x[32];
     tc::ld32(tl + C_DQ, x);
