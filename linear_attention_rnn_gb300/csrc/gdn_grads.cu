@@ -283,6 +283,19 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     const bool next_here = jj + 1 < group;
     const bool has_after = next_here || has_next;
     const long cid_after = next_here ? cid_of(xu, jj + 1) : cid_of(xn, 0);
+    // this head's V rows for the dv pass (warps 1-15, 16 threads per 256-byte row),
+    // requested now so that their latency passes under the gates, S1 and E1
+    constexpr int DT = GT - 32;                  // 480 threads
+    constexpr int NI = (CH * 16 + DT - 1) / DT;  // 5 passes (the last one for warps 1-4 only)
+    uint4 v4[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int idx = tid - 32 + i * DT;
+      const int r = idx >> 4, jc = idx & 15;
+      v4[i] = (warp > 0 && idx < CH * 16 && r < L)
+                  ? *reinterpret_cast<const uint4*>(a.v + (tokv + (long)r * a.Hv) * HD + 8 * jc)
+                  : make_uint4(0u, 0u, 0u, 0u);
+    }
     // ---- gates of value head j; per-row sums cleared ----------------------------
     // (meanwhile warp 15 forms the previous value head's gate cotangents, and warp
     // 14 issues S1 once T and dDelta are in and then requests Delta once the
@@ -390,18 +403,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     // would put that wait in front of every later barrier.  480 threads, 30
     // rows' worth of 16-byte chunks per pass (a 16-lane group stays on one row).
     if (warp > 0) {
-      constexpr int DT = GT - 32;                // 480 threads
-      constexpr int NI = (CH * 16 + DT - 1) / DT;  // 5 passes (the last one for warps 1-4 only)
       const int t2 = tid - 32;
-      uint4 v4[NI];
-#pragma unroll
-      for (int i = 0; i < NI; ++i) {  // all loads in flight before any is used
-        const int idx = t2 + i * DT;
-        const int r = idx >> 4, jc = idx & 15;
-        v4[i] = (idx < CH * 16 && r < L)
-                    ? *reinterpret_cast<const uint4*>(a.v + (tokv + (long)r * a.Hv) * HD + 8 * jc)
-                    : make_uint4(0u, 0u, 0u, 0u);
-      }
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
         const int idx = t2 + i * DT;
