@@ -275,8 +275,8 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     if (lane == 0 && withO) {
       for (int ci = 0; ci < n; ++ci) {
         const int t0 = ci * TPC;
+        ok = ok && tc::mbar_wait_sleep(&sm.full[t0 % NRING], (t0 / NRING) & 1);  // (tile first)
         ok = ok && tc::mbar_wait_sleep(&sm.barO, (uint32_t)(ci & 1));
-        ok = ok && tc::mbar_wait_sleep(&sm.full[t0 % NRING], (t0 / NRING) & 1);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + C_P, smem_u32(sm.slot[t0 % NRING]), smem_u32(sm.Ot), SW, false);
         tc::commit(&sm.barP);
@@ -327,8 +327,8 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       auto slot_of = [&](int i) { return smem_u32(sm.slot[i % NRING]); };
       auto release = [&](int i) { tc::commit(&sm.empty[i % NRING]); };
       auto issue_p = [&](int ci) {  // P^T dO of chunk ci (its dO images are written)
+        wait_tile(ci * TPC);  // (tile first)
         ok = ok && tc::mbar_wait_sleep(&sm.barO, (uint32_t)(ci & 1));
-        wait_tile(ci * TPC);
         tc::fence_after();
         tc::gemm_amn_k128(tmem + C_P, slot_of(ci * TPC), smem_u32(sm.Ot), SW, false);
         tc::commit(&sm.barP);
@@ -339,8 +339,9 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
         const uint32_t par = (uint32_t)(ci & 1);
         const int t0 = ci * TPC;
         const int iQ = t0 + 1, iK = t0 + (withO ? 2 : 0), iW = t0 + (withO ? 3 : 1);
-        ok = ok && tc::mbar_wait_sleep(&sm.barXt, par);  // dh' image of this chunk
+        // (each tile is waited for before the compute threads' signal, which comes later)
         wait_tile(iK);
+        ok = ok && tc::mbar_wait_sleep(&sm.barXt, par);  // dh' image of this chunk
         tc::fence_after();
         tc::gemm_k128(tmem + C_Y, slot_of(iK), smem_u32(sm.Xt), SW, false);
         tc::commit(&sm.barY);
@@ -354,8 +355,8 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
         }
         // (SPLIT: Q^T (gamma dO), issued by the other warp, has completed)
         if (withO && SPLIT) ok = ok && tc::mbar_wait_sleep(&sm.barQ, par);
-        ok = ok && tc::mbar_wait_sleep(&sm.barYt, par);  // (-Y)^T written
         wait_tile(iW);
+        ok = ok && tc::mbar_wait_sleep(&sm.barYt, par);  // (-Y)^T written
         tc::fence_after();
         tc::gemm_amn_k128(tmem + c_q(ci), slot_of(iW), smem_u32(sm.Yt), SW, withO);
         tc::commit(&sm.barH);

@@ -345,8 +345,8 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
         const uint32_t par = (uint32_t)(ci & 1);
         if (C64) {  // Q h came with w h; P Delta alone, K = 64
           const int iP = ci * TPC + 2;
+          wait_tile(iP);  // (the tile first: it is in long before Delta)
           ok = ok && tc::mbar_wait_sleep(&sm.barD, par);  // Delta^T written
-          wait_tile(iP);
           tc::fence_after();
           tc::gemm_k128<4>(tmem + C_O2, slot_of(iP), smem_u32(sm.Dt), SW, false);
           tc::commit(&sm.barO2);
@@ -354,14 +354,14 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
           continue;
         }
         const int iQ = ci * TPC + 1, iP = ci * TPC + 3;
+        wait_tile(iQ);  // (the tile first: it is in long before w h)
         ok = ok && tc::mbar_wait_sleep(&sm.barX, par);  // w h(c) done: h(c) is in Ht[ci & 1]
-        wait_tile(iQ);
         tc::fence_after();
         tc::gemm_k128(tmem + o1_col(ci), slot_of(iQ), smem_u32(sm.Ht[ci & 1]), SW, false);
         tc::commit(&sm.barO1);
         release(iQ);
-        ok = ok && tc::mbar_wait_sleep(&sm.barD, par);  // Delta^T written
         wait_tile(iP);
+        ok = ok && tc::mbar_wait_sleep(&sm.barD, par);  // Delta^T written
         tc::fence_after();
         tc::gemm_k128(tmem + C_O2, slot_of(iP), smem_u32(sm.Dt), SW, false);
         tc::commit(&sm.barO2);
@@ -415,14 +415,16 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
         const int t0 = ci * TPC;
         const int iW = t0, iQ = t0 + 1, iK = t0 + (C64 ? 1 : tile_of(2)), iP = t0 + 3;
         const uint32_t ht = smem_u32(sm.Ht[ci & 1]);
-        if (ci > 0) ok = ok && tc::mbar_wait_sleep(&sm.barHt, par ^ 1);  // state image of chunk c
+        // (each tile is waited for before the compute threads' signal: the tiles
+        // are in long before it, so the product issues as soon as the signal comes)
         wait_tile(iW);
+        if (ci > 0) ok = ok && tc::mbar_wait_sleep(&sm.barHt, par ^ 1);  // state image of chunk c
         tc::fence_after();
         tc::gemm_k128(tmem + 0, slot_of(iW), ht, SW, false);
         tc::commit(&sm.barX);
         release(iW);
-        ok = ok && tc::mbar_wait_sleep(&sm.barDg, par);  // (ef Delta)^T written
         wait_tile(iK);
+        ok = ok && tc::mbar_wait_sleep(&sm.barDg, par);  // (ef Delta)^T written
         tc::fence_after();
         if (C64)
           tc::gemm_amn_k128<4>(tmem + C_H, slot_of(iK), smem_u32(sm.Dgt), SW, false);
