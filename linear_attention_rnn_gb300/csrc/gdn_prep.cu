@@ -60,6 +60,8 @@ struct PrepSmem {
   bf16 Fh[CH * CH];        // S, overwritten in place by T: high parts (XOR-swizzled rows);
                            // at a group's start, its Q (SW128) until Q K^T has read it
   bf16 Fl[CH * CH];        // low parts
+  // gates of a value head; the next value head's are built while the current one's
+  // products run (its own are last read by the T' / T'' build, before the products)
   float Gl[CH], beta[CH];
   float etab[CH];  // exp2(Gl[c0] - Gl[s]) for the 16-column block c0 of column s
   uint64_t barKQ, barV[2], barM;
@@ -291,6 +293,32 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
   };
   float g_next = 0.f, b_next = 0.f;
   load_gates(u_begin, g_next, b_next);
+  // The gate vectors of the value head that runs next (Gl = log2 of the chunk-local
+  // cumsum, beta, etab); g_next, b_next hold its gates and are then reloaded with
+  // those of unit u_after.  Warps 0-3 (a named barrier between them).
+  auto build_gates = [&](long u_after) {
+    if (tid < CH) {
+      sm.Gl[tid] = g_next;
+      sm.beta[tid] = b_next;
+      load_gates(u_after, g_next, b_next);
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+      if (warp == 0) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = sm.Gl[lane * 4 + i];
+        warp_cumsum128(v, lane, a.c64 != 0);  // 64-token chunks: G restarts at row 64
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sm.Gl[lane * 4 + i] = v[i] * LOG2E;
+        __syncwarp();  // every Gl of the chunk is written (by this warp)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane * 4 + i;
+          sm.etab[r] = exp2f(sm.Gl[r & ~15] - sm.Gl[r]);  // >= 1
+        }
+      }
+    }
+  };
+  build_gates(u_begin + 1);  // the first value head's (read after the head's first barrier)
   unsigned char* const qbuf = reinterpret_cast<unsigned char*>(sm.Fh);
   // K and Q of the key-head group (b, c, kh): K into tile kbuf, Q into the Fh region
   auto load_kq = [&](int bb, int cc, int kk, unsigned char* kdst) {
@@ -381,29 +409,7 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       const long bh = (long)b * a.Hv + j;
       const long chunk_id = bh * a.NC + c;
       const int vb = (jj - jj0) & 1;  // V buffer of this head
-      // ---- gates of value head j --------------------------------------------------
-      if (tid < CH) {
-        sm.Gl[tid] = g_next;
-        sm.beta[tid] = b_next;
-      }
-      load_gates(ug + (jj - jj0) + 1, g_next, b_next);
-      __syncthreads();
-      if (warp == 0) {
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = sm.Gl[lane * 4 + i];
-        warp_cumsum128(v, lane, a.c64 != 0);  // 64-token chunks: G restarts at row 64
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          sm.Gl[lane * 4 + i] = v[i] * LOG2E;
-        }
-        __syncwarp();  // every Gl of the chunk is written (by this warp)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = lane * 4 + i;
-          sm.etab[r] = exp2f(sm.Gl[r & ~15] - sm.Gl[r]);  // >= 1
-        }
-      }
+      // ---- gates of value head j: built while the previous head's products ran
       // the previous head's stores have read their staging tiles (Kg, Tp, F)
       // before the barrier below lets anyone rewrite them
       if (tid == 0 && (ug > u_begin || jj > jj0)) tc::bulk_wait_read();
@@ -585,6 +591,8 @@ __global__ void __launch_bounds__(PT, 1) k_prep(PrepArgs a, const __grid_constan
       // the next group's K into the tile no V of this group needs any more, its Q
       // into the Fh region (the T' / T'' build has read it), while the products run
       if (tid == loader && last) load_kq(xn.b, xn.c, xn.kh, sm.A[vbi[(jj1 - jj0) & 1]]);
+      // the next value head's gates, while the products run (this head's are dead)
+      build_gates(ug + (jj - jj0) + 2);
       if (needU) (vb ? v_use1 : v_use0) += 1;
       if (needU || needW) {
         ok = ok && tc::mbar_wait_sleep(&sm.barM, mphase);
