@@ -180,9 +180,21 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
       : "memory");
   return done != 0;
 }
+// Non-blocking test of the phase: never suspends the thread.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
                                                 long long limit_cycles = WAIT_LIMIT_CYCLES) {
   const uint32_t a = smem_u32(bar);
+  if (mbar_test(a, parity)) return true;  // (a phase already complete costs no suspension)
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait_hint(a, parity, 20000u)) return true;
