@@ -58,6 +58,26 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Predicated read-only global loads straight into the destination registers:
+// with pred false nothing is read and the registers keep their values.  A plain
+// `v = pred ? *p : 0` merges the loaded value into v with an instruction that
+// waits for the load where it is issued; these leave the wait to the first real
+// use of v.  p must point to readable memory whenever pred is true.
+__device__ __forceinline__ void ld_pred_v4(uint4& v, const void* p, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}\n"
+      : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+      : "l"(p), "r"((int)pred));
+}
+__device__ __forceinline__ void ld_pred_f32(float& v, const float* p, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+      "@q ld.global.nc.f32 %0, [%1];\n\t}\n"
+      : "+f"(v)
+      : "l"(p), "r"((int)pred));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -163,31 +163,34 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
 
   const int r = 32 * (warp & 3) + lane;  // compute threads: row r of the state slice / of the chunk
   float x[32];
-  float gnext = 0.f, part = 0.f;
+  float gnext = 0.f, part = 0.f;  // gnext: the raw gate entry of row r of a later chunk
   float gam_r = 0.f, ef_r = 0.f, gC = 0.f;
-  uint4 don[4];  // dO row r of the next chunk's images (this thread's 32 columns)
+  uint4 don[4];  // dO row r of the first chunk's images (this thread's 32 columns)
+  auto has_row = [&](int ci) { return ci < n && r < rows_of(chunk_of(ci)); };
+  // The loads land in their registers untouched (ld_pred_*): the raw gate is
+  // activated, and the dO row unpacked, where they are used, long after the load.
   auto load_g = [&](int ci) {
-    if (ci >= n) return 0.f;
-    const int c = chunk_of(ci);
-    return r < rows_of(c) ? act_g(a.g[((long)b * a.T + (long)c * CH + r) * a.Hv + j], a.gate_logits) : 0.f;
+    float v = 0.f;
+    const bool in = has_row(ci);
+    ld_pred_f32(v, a.g + ((long)b * a.T + (long)chunk_of(in ? ci : 0) * CH + (in ? r : 0)) * a.Hv + j, in);
+    return v;
   };
-  auto load_do = [&](int ci) {
+  auto gate_of = [&](float raw, int ci) { return has_row(ci) ? act_g(raw, a.gate_logits) : 0.f; };
+  auto load_do = [&](int ci, uint4 (&dst)[4]) {
+    const bool in = withO && has_row(ci);
+    const bf16* src = a.dO + (((long)b * a.T + (long)chunk_of(in ? ci : 0) * CH + (in ? r : 0)) * a.Hv + j) * HD + col0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) don[q] = make_uint4(0u, 0u, 0u, 0u);
-    if (!withO || ci >= n) return;
-    const int c = chunk_of(ci);
-    if (r < rows_of(c)) {
-      const bf16* src = a.dO + (((long)b * a.T + (long)c * CH + r) * a.Hv + j) * HD + col0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) don[q] = *reinterpret_cast<const uint4*>(src + 8 * q);
+    for (int q = 0; q < 4; ++q) {
+      dst[q] = make_uint4(0u, 0u, 0u, 0u);
+      ld_pred_v4(dst[q], src + 8 * q, in);
     }
   };
-  // dO^T and (gamma dO)^T images of the chunk whose dO rows are in don
-  auto write_do_images = [&]() {
+  // dO^T and (gamma dO)^T images of the chunk whose dO rows are in dn
+  auto write_do_images = [&](const uint4 (&dn)[4]) {
     float d[32], dg[32];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint32_t w4[4] = {don[q].x, don[q].y, don[q].z, don[q].w};
+      const uint32_t w4[4] = {dn[q].x, dn[q].y, dn[q].z, dn[q].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 f = unpack_bf16(w4[e]);
@@ -239,9 +242,9 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       }
     }
     write_bt_column<SW>(sm.Xt, r, 32 * g32, x);
-    part = scan_part(load_g(0), 0);
+    part = scan_part(gate_of(load_g(0), 0), 0);
     gnext = load_g(1);
-    load_do(0);
+    load_do(0, don);
   }
   tc::fence_proxy_async();
   tc::fence_before();
@@ -368,11 +371,10 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     // ========================================================== compute threads
     finish_gates(part, 0);
     if (withO) {
-      write_do_images();
+      write_do_images(don);
       tc::fence_proxy_async();
       tc::fence_before();
       arrive(&sm.barO);
-      load_do(1);
     }
     arrive(&sm.barXt);  // the first dh' image was written before the block barrier
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32u * g32;  // lanes of this warp, its columns
@@ -381,9 +383,11 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       const uint32_t par = (uint32_t)(ci & 1);
       // staging set ci % NSTAGE (dh', dDelta) was last read by the stores of chunk ci - NSTAGE
       const int set = ci % NSTAGE, use = ci / NSTAGE;
+      uint4 dn[4];  // dO rows of chunk ci + 1: their images are written in this iteration
+      load_do(ci + 1, dn);
       if (!FOLD && use >= 1) ok = ok && tc::mbar_wait_sleep(&sm.sempty[set], (uint32_t)((use - 1) & 1));
       if (!FOLD && a.dstates) stage_row<SW>(sm.stage[set][0], r, g32, x);
-      part = scan_part(gnext, ci + 1);  // gates of the next chunk
+      part = scan_part(gate_of(gnext, ci + 1), ci + 1);  // gates of the next chunk
       gnext = load_g(ci + 2);
 
       // ---- Y = diag(ef) K dh' + P^T dO ----------------------------------------------
@@ -419,11 +423,10 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       finish_gates(part, ci + 1);
       if (withO && ci + 1 < n) {  // both dO products of this chunk have read the images
         ok = ok && tc::mbar_wait_sleep(&sm.barQ, par);
-        write_do_images();
+        write_do_images(dn);
         tc::fence_proxy_async();
         tc::fence_before();
         arrive(&sm.barO);
-        load_do(ci + 2);
       }
 
       // ---- dh = gamma_C dh' + Q^T (gamma dO) - w^T Y ---------------------------------
