@@ -200,14 +200,14 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     __syncthreads();
     tc::fence_after();
   };
-  // g and beta of row tid for value head jj of unit x (loaded a head ahead)
+  // raw g and beta of row tid for value head jj of unit x (loaded a head ahead,
+  // straight into their registers: activated where they are used, a head later)
   auto load_gates = [&](const GUnit& x, int jj, float& gv, float& bv) {
     gv = bv = 0.f;
-    if (tid < min(CH, a.T - x.c * CH)) {
-      const long idx = ((long)x.b * a.T + x.c * CH + tid) * a.Hv + x.kh * group + jj;
-      gv = act_g(a.g[idx], a.gate_logits);
-      bv = act_beta(a.beta[idx], a.gate_logits);
-    }
+    const bool in = tid < min(CH, a.T - x.c * CH);
+    const long idx = ((long)x.b * a.T + x.c * CH + (in ? tid : 0)) * a.Hv + x.kh * group + jj;
+    ld_pred_f32(gv, a.g + idx, in);
+    ld_pred_f32(bv, a.beta + idx, in);
   };
   float g_next = 0.f, b_next = 0.f;
   if (tid < CH) load_gates(decode(u_begin), 0, g_next, b_next);
@@ -292,9 +292,9 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     for (int i = 0; i < NI; ++i) {
       const int idx = tid - 32 + i * DT;
       const int r = idx >> 4, jc = idx & 15;
-      v4[i] = (warp > 0 && idx < CH * 16 && r < L)
-                  ? *reinterpret_cast<const uint4*>(a.v + (tokv + (long)r * a.Hv) * HD + 8 * jc)
-                  : make_uint4(0u, 0u, 0u, 0u);
+      const bool in = warp > 0 && idx < CH * 16 && r < L;
+      v4[i] = make_uint4(0u, 0u, 0u, 0u);
+      ld_pred_v4(v4[i], a.v + (tokv + (long)(in ? r : 0) * a.Hv) * HD + 8 * (in ? jc : 0), in);
     }
     // ---- gates of value head j; per-row sums cleared ----------------------------
     // (meanwhile warp 15 forms the previous value head's gate cotangents, and warp
@@ -314,8 +314,8 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       }
     }
     if (tid < CH) {
-      H.Gl[tid] = g_next;
-      H.beta[tid] = b_next;
+      H.Gl[tid] = tid < L ? act_g(g_next, a.gate_logits) : 0.f;
+      H.beta[tid] = tid < L ? act_beta(b_next, a.gate_logits) : 0.f;
       if (next_here)
         load_gates(xu, jj + 1, g_next, b_next);
       else if (has_next)
