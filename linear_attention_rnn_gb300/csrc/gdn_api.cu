@@ -457,7 +457,8 @@ static int bwd_impl(const void* q, const void* k, const void* v, const float* g,
         !tmap_2d(&bm.W, w.W, HD, wrows, HD * sizeof(bf16), 64, CH, true) ||
         !tmap_2d(&bm.P, w.P, CH, wrows, CH * sizeof(bf16), 64, CH, true) ||
         !tmap_2d_sw(&bm.Ds, w.dstates, HD, wrows, HD * sizeof(bf16), bsw, CH, slice_swizzle(bsw)) ||
-        !tmap_2d_sw(&bm.Dd, w.ddelta, HD, wrows, HD * sizeof(bf16), bsw, CH, slice_swizzle(bsw)))
+        !tmap_2d_sw(&bm.Dd, w.ddelta, HD, wrows, HD * sizeof(bf16), bsw, CH, slice_swizzle(bsw)) ||
+        !tmap_heads_box(&bm.dO, dO, d.B, d.T, d.Hv, HD, 32, CH, CU_TENSOR_MAP_SWIZZLE_64B))
       return GDN_ERR_CUDA;
   }
   if (d.S == 1) {

@@ -101,6 +101,7 @@ constexpr int WALK_BWD_SW = 64;
 struct WalkBwdMaps {
   CUtensorMap k, q, W, P;
   CUtensorMap Ds, Dd;  // stores: leaving-state cotangents and dDelta (WALK_BWD_SW-column slices)
+  CUtensorMap dO;      // loads: 32-column slices of dO over 128 tokens (64-byte swizzle)
 };
 
 // Sequential affine walk X <- A_i X (+ B_i) over i (segment prefix / compose).

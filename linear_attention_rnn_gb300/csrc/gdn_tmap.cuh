@@ -69,4 +69,19 @@ inline bool tmap_heads(CUtensorMap* m, const void* base, int B, int T, int H, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 activations [B][T][H][D]; box = box_cols columns of one head over
+// box_tokens tokens with the given swizzle, tokens past T read as zero.
+inline bool tmap_heads_box(CUtensorMap* m, const void* base, int B, int T, int H, int D, uint32_t box_cols,
+                           uint32_t box_tokens, CUtensorMapSwizzle sw) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)T * H * D * 2};
+  cuuint32_t box[4] = {box_cols, 1, box_tokens, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gdn

@@ -57,7 +57,11 @@ struct BwdCfg {
   static constexpr int NCW = NCT / 32;             // compute warps
   static constexpr int NT = NCT + 96;              // + MMA issuer, TMA producer and TMA store warps
   static constexpr int NRING = SW == 32 ? 5 : 4;   // tile ring
-  static constexpr int NSTAGE = SW == 32 ? 2 : 1;  // staging sets of the stored dh' and dDelta slices
+  static constexpr int NSTAGE = 1;                 // staging sets of the stored dh' and dDelta slices
+  // SW 32: each chunk's dO slice arrives by TMA into shared memory (dOt), so
+  // the compute threads issue no global loads: their every arrive (a release)
+  // would wait for those loads to return.
+  static constexpr bool DOTMA = SW == 32;
   static constexpr uint32_t BT = SW * HD * 2;      // a [SW x 128] B-operand image
   static constexpr uint32_t SLICE = CH * SW * 2;   // a [128 x SW] staged slice
   static constexpr uint32_t TMEM_COLS = 4 * SW;    // K dh', P^T dO, Q^T (gamma dO) - w^T Y twice
@@ -72,10 +76,12 @@ struct WalkBwdSmem {
   unsigned char Yt[C::BT];   // (-Y)^T
   unsigned char Ot[C::BT];   // dO^T (this slice)
   unsigned char Ogt[C::BT];  // (diag(gamma) dO)^T
+  unsigned char dOt[C::DOTMA ? C::SLICE : 16];  // DOTMA: dO slice [128 x 32] of the next chunk, 64-byte swizzle
   float gsum[2][4];
   uint64_t full[C::NRING], empty[C::NRING];
   uint64_t barO, barXt, barYt, barP, barQ, barY, barH;
   uint64_t sfull[C::NSTAGE], sempty[C::NSTAGE];  // staging set: written by the compute threads / read by its stores
+  uint64_t barDO;  // DOTMA: dOt loaded
   uint32_t tmem;
 };
 
@@ -117,6 +123,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
                                      int seg, int bhi) {
   using Cfg = BwdCfg<SW>;
   constexpr int NCT = Cfg::NCT, NCW = Cfg::NCW, NRING = Cfg::NRING, NSTAGE = Cfg::NSTAGE;
+  constexpr bool DOTMA = Cfg::DOTMA;
   constexpr int NSL = HD / SW;  // slices per state
   // TMEM columns: K dh' at 0, P^T dO at SW; Q^T (gamma dO) - w^T Y alternates 2 SW / 3 SW
   constexpr uint32_t C_Y = 0, C_P = SW;
@@ -150,6 +157,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     tc::mbar_init(&sm.barQ, 1);
     tc::mbar_init(&sm.barY, 1);
     tc::mbar_init(&sm.barH, 1);
+    tc::mbar_init(&sm.barDO, 1);
     for (int k = 0; k < NSTAGE; ++k) {
       tc::mbar_init(&sm.sfull[k], NCT);
       tc::mbar_init(&sm.sempty[k], 1);
@@ -296,19 +304,42 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     // ============================================================ TMA stores
     // The staged dh' and dDelta slices of each chunk leave by TMA stores once the
     // compute threads have signalled them; when the stores have read the buffers
-    // they are handed back.  A store request can block its thread.
-    if (!FOLD && lane == 0 && (a.dstates || a.ddelta)) {
-      for (int ci = 0; ci < n; ++ci) {
-        const int c = chunk_of(ci);
-        const int set = ci % NSTAGE, use = ci / NSTAGE;
-        ok = ok && tc::mbar_wait_sleep(&sm.sfull[set], (uint32_t)(use & 1));
-        if (a.dstates) tc::tma_store_2d(&mp.Ds, sbase, (int)((bh * a.NC + c) * HD), sm.stage[set][0]);
-        if (a.ddelta) tc::tma_store_2d(&mp.Dd, sbase, (int)((bh * a.NC + c) * CH), sm.stage[set][1]);
-        tc::bulk_commit();
-        tc::bulk_wait_read();
-        arrive(&sm.sempty[set]);
+    // they are handed back.  A store request can block its thread.  DOTMA: this
+    // thread also loads each chunk's dO slice into dOt, once the compute
+    // threads have written the images of the chunk before from it (barO).
+    const bool stores = !FOLD && (a.dstates || a.ddelta);
+    const bool dol = DOTMA && withO;
+    auto load_slice = [&](int ci) {  // dO slice of chunk index ci (rows past T read as zero)
+      tc::arrive_expect_tx(&sm.barDO, Cfg::SLICE);
+      tc::tma_load_4d(sm.dOt, &mp.dO, col0, j, chunk_of(ci) * CH, b, &sm.barDO);
+    };
+    if (lane == 0 && (stores || dol)) {
+      // barO's phases are waited for in order, from phase 0 (the images of chunk
+      // index 0, from plain loads), each while barO is in it or just past it: a
+      // parity wait for the phase after the current one would pass at once, one
+      // for a phase two back would not pass.  Its phase ci + 1 needs the slice
+      // of chunk index ci + 1, loaded only after the wait for phase ci.
+      if (dol && n > 1) {
+        ok = ok && tc::mbar_wait_sleep(&sm.barO, 0u);
+        load_slice(1);
       }
-      tc::bulk_wait();  // every store has completed before the block exits
+      for (int ci = 0; ci < n; ++ci) {
+        if (stores) {
+          const int c = chunk_of(ci);
+          const int set = ci % NSTAGE, use = ci / NSTAGE;
+          ok = ok && tc::mbar_wait_sleep(&sm.sfull[set], (uint32_t)(use & 1));
+          if (a.dstates) tc::tma_store_2d(&mp.Ds, sbase, (int)((bh * a.NC + c) * HD), sm.stage[set][0]);
+          if (a.ddelta) tc::tma_store_2d(&mp.Dd, sbase, (int)((bh * a.NC + c) * CH), sm.stage[set][1]);
+          tc::bulk_commit();
+          tc::bulk_wait_read();
+          arrive(&sm.sempty[set]);
+        }
+        if (dol && ci + 2 < n) {  // the images of chunk index ci + 1 are written
+          ok = ok && tc::mbar_wait_sleep(&sm.barO, (uint32_t)((ci + 1) & 1));
+          load_slice(ci + 2);
+        }
+      }
+      if (stores) tc::bulk_wait();  // every store has completed before the block exits
     }
   } else if (warp == NCW + 1) {
     // ========================================================== TMA producer
@@ -384,7 +415,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       // staging set ci % NSTAGE (dh', dDelta) was last read by the stores of chunk ci - NSTAGE
       const int set = ci % NSTAGE, use = ci / NSTAGE;
       uint4 dn[4];  // dO rows of chunk ci + 1: their images are written in this iteration
-      load_do(ci + 1, dn);
+      if (!DOTMA) load_do(ci + 1, dn);
       if (!FOLD && use >= 1) ok = ok && tc::mbar_wait_sleep(&sm.sempty[set], (uint32_t)((use - 1) & 1));
       if (!FOLD && a.dstates) stage_row<SW>(sm.stage[set][0], r, g32, x);
       part = scan_part(gate_of(gnext, ci + 1), ci + 1);  // gates of the next chunk
@@ -423,6 +454,11 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       finish_gates(part, ci + 1);
       if (withO && ci + 1 < n) {  // both dO products of this chunk have read the images
         ok = ok && tc::mbar_wait_sleep(&sm.barQ, par);
+        if (DOTMA) {  // the slice of chunk index ci + 1 (load number ci of dOt)
+          ok = ok && tc::mbar_wait_sleep(&sm.barDO, par);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dn[q] = *reinterpret_cast<const uint4*>(sm.dOt + tc::sw64_chunk(r, q));
+        }
         write_do_images(dn);
         tc::fence_proxy_async();
         tc::fence_before();
