@@ -436,17 +436,21 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
 #pragma unroll
         for (int q = 0; q < 32; ++q) y[q] += pd[q];
       }
-      if (!FOLD && a.ddelta) stage_row<SW>(sm.stage[set][1], r, g32, y);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) y[q] = -y[q];
+      write_bt_column<SW>(sm.Yt, r, 32 * g32, y);  // the chain's operand first
+      tc::fence_proxy_async();
+      tc::fence_before();
+      arrive(&sm.barYt);
+      if (!FOLD && a.ddelta) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) y[q] = -y[q];
+        stage_row<SW>(sm.stage[set][1], r, g32, y);
+      }
       if (!FOLD) {  // dh' and dDelta of this chunk are staged
         tc::fence_proxy_async();
         arrive(&sm.sfull[set]);
       }
-#pragma unroll
-      for (int q = 0; q < 32; ++q) y[q] = -y[q];
-      write_bt_column<SW>(sm.Yt, r, 32 * g32, y);
-      tc::fence_proxy_async();
-      tc::fence_before();
-      arrive(&sm.barYt);
 
       // ---- gates and dO images of the next chunk -------------------------------------
       const float gC_cur = gC;
