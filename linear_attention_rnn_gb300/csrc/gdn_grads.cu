@@ -57,6 +57,7 @@ struct GradSmem {
     float colX[CH], dbeta[CH], dbg[CH], d_ef[CH], rowX[CH], dgamO[CH];
     float red[GW];
   } hv[2];
+  float gcot[2][CH];  // a value head's dg and dbeta, formed by warp 15, stored later by it
   uint64_t barKQ, barT, barDD, barH, barDl, barDH, barDO, barM, barS8;
   uint32_t tmem;
 };
@@ -212,8 +213,11 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
   float g_next = 0.f, b_next = 0.f;
   if (tid < CH) load_gates(decode(u_begin), 0, g_next, b_next);
   // Gate cotangents of a value head (one warp): dg = reverse cumsum over the chunk
-  // of dG, dbeta; with gate logits the chain rule through the activations.
-  auto gate_cot = [&](const GradSmem::HeadVec& P, long tokv_p, int L_p) {
+  // of dG, dbeta; with gate logits the chain rule through the activations.  They
+  // are formed into sm.gcot (gate_cot) and written out by gate_cot_store, later:
+  // at a value head's start the memory pipe is full of that head's V-row loads,
+  // and stores issued then wait behind them.
+  auto gate_cot = [&](const GradSmem::HeadVec& P, int L_p) {
     float dgC = 0.f;
 #pragma unroll
     for (int w = 0; w < GW; ++w) dgC += P.red[w];
@@ -248,9 +252,19 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = lane * 4 + i;
+      sm.gcot[0][r] = dg[i];
+      sm.gcot[1][r] = P.dbeta[r] + P.gam[r] * P.dbg[r];
+    }
+    __syncwarp();
+    (void)L_p;
+  };
+  auto gate_cot_store = [&](long tokv_p, int L_p) {  // the same warp, after gate_cot
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = lane + 32 * i;
       if (r < L_p) {
         const long t = tokv_p + (long)r * a.Hv;
-        float dgv = dg[i], dbv = P.dbeta[r] + P.gam[r] * P.dbg[r];
+        float dgv = sm.gcot[0][r], dbv = sm.gcot[1][r];
         if (a.gate_logits) {  // chain rule through g = -softplus(a) and beta = sigmoid(b)
           const float sa = act_beta(a.g[t], 1), sb = act_beta(a.beta[t], 1);
           dgv *= -sa;
@@ -301,7 +315,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     // 14 issues S1 once T and dDelta are in and then requests Delta once the
     // previous head's S8b has read W4; the two barriers of this part are over warps 0-13)
     if (warp == GW - 1) {
-      if (hc > 0) gate_cot(sm.hv[(hc - 1) & 1], pend_tokv, pend_L);
+      if (hc > 0) gate_cot(sm.hv[(hc - 1) & 1], pend_L);
     } else if (tid == 32 * (GW - 2)) {  // S1: dV' = T^T dDelta (both tiles read MN-major)
       ok = ok && tc::mbar_wait(&sm.barT, par);
       ok = ok && tc::mbar_wait(&sm.barDD, par);
@@ -489,6 +503,8 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       tc::commit(&sm.barM);
     }
     // ---- E3: dKK = -(ds * M) diag-row(beta), strictly lower -> W1; dbeta, rowX, colX -----
+    // (warp 15: the previous value head's gate cotangents leave while S3 runs)
+    if (warp == GW - 1 && hc > 0) gate_cot_store(pend_tokv, pend_L);
     wait_mma();
     {
       float out[32];
@@ -636,7 +652,10 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     }
   }
   }  // units
-  if (warp == GW - 1 && hc > 0) gate_cot(sm.hv[(hc - 1) & 1], pend_tokv, pend_L);
+  if (warp == GW - 1 && hc > 0) {
+    gate_cot(sm.hv[(hc - 1) & 1], pend_L);
+    gate_cot_store(pend_tokv, pend_L);
+  }
   if (tid == 0) tc::bulk_wait();  // every store has completed before the block exits
   if (!ok && a.status) atomicOr(a.status, 1);
   tc::fence_before();
