@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       sm.gcot[0][r] = dg[i];
       sm.gcot[1][r] = P.dbeta[r] + P.gam[r] * P.dbg[r];
     }
-    __syncwarp();
+    // (no warp barrier: the warp reads sm.gcot back only after several CTA barriers,
+    // and one here would wait for its outstanding V-row loads)
     (void)L_p;
   };
   auto gate_cot_store = [&](long tokv_p, int L_p) {  // the same warp, after gate_cot
@@ -297,23 +298,27 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     const bool next_here = jj + 1 < group;
     const bool has_after = next_here || has_next;
     const long cid_after = next_here ? cid_of(xu, jj + 1) : cid_of(xn, 0);
-    // this head's V rows for the dv pass (warps 1-15, 16 threads per 256-byte row),
-    // requested now so that their latency passes under the gates, S1 and E1
-    constexpr int DT = GT - 32;                  // 480 threads
-    constexpr int NI = (CH * 16 + DT - 1) / DT;  // 5 passes (the last one for warps 1-4 only)
+    // this head's V rows for the dv pass (warps 4-15, 16 threads per 256-byte row),
+    // requested now so that their latency passes under S1 and E1.  Warps 0-3 build
+    // the gates behind two barriers, and a barrier waits for the loads its threads
+    // have outstanding: they load none.
+    constexpr int DW0 = 4;                       // first warp of the dv pass
+    constexpr int DT = GT - 32 * DW0;            // 384 threads
+    constexpr int NI = (CH * 16 + DT - 1) / DT;  // 6 passes (the last one for warps 4-7 only)
     uint4 v4[NI];
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-      const int idx = tid - 32 + i * DT;
+      const int idx = tid - 32 * DW0 + i * DT;
       const int r = idx >> 4, jc = idx & 15;
-      const bool in = warp > 0 && idx < CH * 16 && r < L;
+      const bool in = warp >= DW0 && idx < CH * 16 && r < L;
       v4[i] = make_uint4(0u, 0u, 0u, 0u);
       ld_pred_v4(v4[i], a.v + (tokv + (long)(in ? r : 0) * a.Hv) * HD + 8 * (in ? jc : 0), in);
     }
     // ---- gates of value head j; per-row sums cleared ----------------------------
     // (meanwhile warp 15 forms the previous value head's gate cotangents, and warp
     // 14 issues S1 once T and dDelta are in and then requests Delta once the
-    // previous head's S8b has read W4; the two barriers of this part are over warps 0-13)
+    // previous head's S8b has read W4; the two barriers of this part are over warps
+    // 0-3, which write and scan the gates; the other warps read them after E1's barrier)
     if (warp == GW - 1) {
       if (hc > 0) gate_cot(sm.hv[(hc - 1) & 1], pend_L);
     } else if (tid == 32 * (GW - 2)) {  // S1: dV' = T^T dDelta (both tiles read MN-major)
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
         load_gates(xn, 0, g_next, b_next);
       H.colX[tid] = H.dbeta[tid] = H.dbg[tid] = H.d_ef[tid] = H.rowX[tid] = H.dgamO[tid] = 0.f;
     }
-    if (warp < GW - 2) asm volatile("bar.sync 1, %0;" ::"r"(GT - 64) : "memory");
+    if (warp < 4) asm volatile("bar.sync 1, 128;" ::: "memory");
     if (warp == 0) {
       float v[4];
 #pragma unroll
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
         H.etab[r] = exp2f(H.Gl[r & ~15] - H.Gl[r]);  // >= 1
       }
     }
-    if (warp < GW - 2) asm volatile("bar.sync 1, %0;" ::"r"(GT - 64) : "memory");
+    if (warp < 4) asm volatile("bar.sync 1, 128;" ::: "memory");
     // this row's gates, read after E1's barrier (which warps 14 and 15 reach late)
     float Glr = 0.f, br = 0.f, gr = 0.f, efr = 0.f, bgr = 0.f;
     float p_db = 0.f, p_dbg = 0.f, p_def = 0.f, p_rowx = 0.f, p_dgam = 0.f;
@@ -412,12 +417,13 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     }
     // ---- dv = diag(beta) dV' and dbeta += rowsum(dV' V), while S2/S5 run -----------------
     // Read back from the bf16 dV' tile with 16 threads per row, so that V is
-    // loaded and dv stored in whole 256-byte rows.  Warp 0 takes no share: its
-    // thread 0 waits for dh' and issues S2/S5 meanwhile, and a share of its own
-    // would put that wait in front of every later barrier.  480 threads, 30
-    // rows' worth of 16-byte chunks per pass (a 16-lane group stays on one row).
-    if (warp > 0) {
-      const int t2 = tid - 32;
+    // loaded and dv stored in whole 256-byte rows.  Warps 0-3 take no share: warp
+    // 0's thread 0 waits for dh' and issues S2/S5 meanwhile (a share of its own
+    // would put that wait in front of every later barrier), and warps 0-3 hold no
+    // V loads at the gates' barriers.  384 threads, 24 rows' worth of 16-byte
+    // chunks per pass (a 16-lane group stays on one row).
+    if (warp >= DW0) {
+      const int t2 = tid - 32 * DW0;
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
         const int idx = t2 + i * DT;
