@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       }
     }
   };
+  bool kq_pending = false;  // thread 0: the unit's K and Q are still to be requested
   long pend_tokv = 0;  // the value head whose gate cotangents are pending
   int pend_L = 0;
   int hc = 0;  // value heads processed by this CTA: the parity of the tile barriers
@@ -363,6 +364,11 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
       }
     }
     if (warp < 4) asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (tid == 0 && kq_pending) {  // the last unit's dq, dk stores have read the K, Q tiles
+      tc::bulk_wait_read();
+      load_kq(xu);
+      kq_pending = false;
+    }
     // this row's gates, read after E1's barrier (which warps 14 and 15 reach late)
     float Glr = 0.f, br = 0.f, gr = 0.f, efr = 0.f, bgr = 0.f;
     float p_db = 0.f, p_dbg = 0.f, p_def = 0.f, p_rowx = 0.f, p_dgam = 0.f;
@@ -652,10 +658,10 @@ __global__ void __launch_bounds__(GT, 1) k_grads(GradArgs a, const __grid_consta
     tc::tma_store_4d(&mp.dk, 0, kh, t0, b, sm.K);
     tc::tma_store_4d(&mp.dk, 64, kh, t0, b, sm.K + TILE / 2);
     tc::bulk_commit();
-    if (has_next) {  // the stores have read the staging tiles: the next unit's K and Q
-      tc::bulk_wait_read();
-      load_kq(xn);
-    }
+    // (the next unit's K and Q are requested once these stores have read the staging
+    // tiles: at the next value head's start, after its gates, where thread 0 waits
+    // for S1 anyway; waiting here held warp 0, and with it the next head's start)
+    kq_pending = has_next;
   }
   }  // units
   if (warp == GW - 1 && hc > 0) {
