@@ -120,13 +120,17 @@ def test_batched_workload_bwd(gdn_lib):
 
 # ------------------------------------------- forward keeps w, u, P, T for the backward
 @pytest.mark.parametrize("name,T,S", [("layer_t4096", 4096, 1), ("tiny_t1024", 300, 1),
-                                      ("tiny_t1024", 1024 + 50, 3)])
+                                      ("tiny_t1024", 1024 + 50, 3), ("tiny_t1024", 128, 1),
+                                      ("tiny_t1024", 129, 1), ("tiny_t1024", 256 + 7, 2),
+                                      ("tiny_t1024", 1024 + 50, 9)])
 def test_saved_chunk_quantities(gdn_lib, name, T, S):
     """The forward that keeps w, u, P, T, the entering states and Delta
     (gdn_chunk_fwd_ex with a saved buffer) gives the plain forward's o and hT
     bit for bit; the backward that reads them (gdn_chunk_bwd_ex: the reverse
     walk alone, no preparation, no recompute) matches the per-token adjoint on
-    every head, as the plain backward does."""
+    every head, as the plain backward does.  The segment lengths cover walks
+    of one, two and three or more chunks (the reverse walk requests each
+    chunk's dO slice from the second chunk on), with a last chunk of one row."""
     wl = WORKLOADS[name].replace(T=T, backward=True, h0_std=0.2, gate_shift=-2.0 if S > 1 else 0.0,
                                  seed=70 + S)
     inp = make_host(wl)
