@@ -30,8 +30,12 @@
 // soon as the MMA that read it completes.  With SPLIT (the kernels that run
 // this walk alone) an eighth warp issues the two dO products, so that their
 // issue never holds the chain's issuer; the chain's issuer then waits for
-// Q^T (gamma dO) to complete before it accumulates w^T (-Y) onto it.  Every
-// wait is bounded; one that gives up sets bit 0 of the status word.
+// Q^T (gamma dO) to complete before it accumulates w^T (-Y) onto it.  The
+// compute threads form the dO images from each chunk's dO rows.  On 32-column
+// slices those rows arrive by TMA (the store warp requests each chunk's slice
+// once the images of the chunk before are written), so the compute threads
+// issue no global loads: an mbarrier arrive, a release, would wait for them.
+// Every wait is bounded; one that gives up sets bit 0 of the status word.
 //
 // Modes:
 //   WALK (fold = 0): from the cotangent leaving the segment, store for every
