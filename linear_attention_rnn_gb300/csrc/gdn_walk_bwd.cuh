@@ -325,7 +325,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       // of chunk index ci + 1, loaded only after the wait for phase ci.
       if (dol && n > 1) {
         ok = ok && tc::mbar_wait_sleep(&sm.barO, 0u);
-        load_slice(1);
+        if (ok) load_slice(1);
       }
       for (int ci = 0; ci < n; ++ci) {
         if (stores) {
@@ -340,7 +340,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
         }
         if (dol && ci + 2 < n) {  // the images of chunk index ci + 1 are written
           ok = ok && tc::mbar_wait_sleep(&sm.barO, (uint32_t)((ci + 1) & 1));
-          load_slice(ci + 2);
+          if (ok) load_slice(ci + 2);
         }
       }
       if (stores) tc::bulk_wait();  // every store has completed before the block exits
@@ -350,6 +350,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     if (lane == 0) {
       for (int i = 0; i < ntiles; ++i) {
         if (i >= NRING) ok = ok && tc::mbar_wait_sleep(&sm.empty[i % NRING], (uint32_t)((i / NRING - 1) & 1));
+        if (!ok) break;  // a wait gave up: request nothing more (the CTA ends soon)
         issue(i);
       }
     }

@@ -395,6 +395,7 @@ __device__ __forceinline__ void walk(const WalkFwdArgs& a, const WalkFwdMaps& mp
     if (lane == 0) {
       for (int i = 0; i < ntiles; ++i) {
         if (i >= nring) ok = ok && tc::mbar_wait_sleep(&sm.empty[i % nring], (uint32_t)((i / nring - 1) & 1));
+        if (!ok) break;  // a wait gave up: request nothing more (the CTA ends soon)
         issue(i);
       }
     }
