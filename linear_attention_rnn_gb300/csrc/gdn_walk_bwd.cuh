@@ -83,7 +83,7 @@ struct WalkBwdSmem {
   unsigned char dOt[C::DOTMA ? C::SLICE : 16];  // DOTMA: dO slice [128 x 32] of the next chunk, 64-byte swizzle
   float gsum[2][4];
   uint64_t full[C::NRING], empty[C::NRING];
-  uint64_t barO, barXt, barYt, barP, barQ, barY, barH;
+  uint64_t barO, barXt, barYt, barQ, barY, barH;  // barY: K dh' and P^T dO complete
   uint64_t sfull[C::NSTAGE], sempty[C::NSTAGE];  // staging set: written by the compute threads / read by its stores
   uint64_t barDO;  // DOTMA: dOt loaded
   uint32_t tmem;
@@ -157,9 +157,10 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     tc::mbar_init(&sm.barO, NCT);
     tc::mbar_init(&sm.barXt, NCT);
     tc::mbar_init(&sm.barYt, NCT);
-    tc::mbar_init(&sm.barP, 1);
     tc::mbar_init(&sm.barQ, 1);
-    tc::mbar_init(&sm.barY, 1);
+    // SPLIT: the chain's issuer (K dh') and the dO products' issuer (P^T dO) both
+    // commit to barY; otherwise the chain's issuer issues P^T dO before K dh'
+    tc::mbar_init(&sm.barY, (SPLIT && withO) ? 2 : 1);
     tc::mbar_init(&sm.barH, 1);
     tc::mbar_init(&sm.barDO, 1);
     for (int k = 0; k < NSTAGE; ++k) {
@@ -294,7 +295,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
         ok = ok && tc::mbar_wait_sleep(&sm.barO, (uint32_t)(ci & 1));
         tc::fence_after();
         tc::gemm_amn_k128(tmem + C_P, smem_u32(sm.slot[t0 % NRING]), smem_u32(sm.Ot), SW, false);
-        tc::commit(&sm.barP);
+        tc::commit(&sm.barY);  // (barY's second arrival of the chunk)
         tc::commit(&sm.empty[t0 % NRING]);
         const int iQ = t0 + 1;
         ok = ok && tc::mbar_wait_sleep(&sm.full[iQ % NRING], (iQ / NRING) & 1);
@@ -370,8 +371,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
         ok = ok && tc::mbar_wait_sleep(&sm.barO, (uint32_t)(ci & 1));
         tc::fence_after();
         tc::gemm_amn_k128(tmem + C_P, slot_of(ci * TPC), smem_u32(sm.Ot), SW, false);
-        tc::commit(&sm.barP);
-        release(ci * TPC);
+        release(ci * TPC);  // (the commit after the chunk's K dh' covers it)
       };
       if (withO && !SPLIT) issue_p(0);
       for (int ci = 0; ci < n; ++ci) {
@@ -426,16 +426,14 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       part = scan_part(gate_of(gnext, ci + 1), ci + 1);  // gates of the next chunk
       gnext = load_g(ci + 2);
 
-      // ---- Y = diag(ef) K dh' + P^T dO ----------------------------------------------
+      // ---- Y = diag(ef) K dh' + P^T dO (both complete on barY) ------------------------
       float y[32];
       ok = ok && tc::mbar_wait_sleep(&sm.barY, par);
       tc::fence_after();
       tc::ld32(tl + C_Y, y);
 #pragma unroll
       for (int q = 0; q < 32; ++q) y[q] *= ef_r;
-      if (withO) {
-        ok = ok && tc::mbar_wait_sleep(&sm.barP, par);
-        tc::fence_after();
+      if (withO) {  // (P^T dO has completed too: barY)
         float pd[32];
         tc::ld32(tl + C_P, pd);
 #pragma unroll
