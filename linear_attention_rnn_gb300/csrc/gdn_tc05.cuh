@@ -257,6 +257,28 @@ __device__ __forceinline__ void gemm_amn_k128(uint32_t tmem_d, uint32_t a_smem, 
   }
 }
 
+// descriptor of a [K rows x 32] bf16 tile stored MN-major with 64-byte rows in the
+// 64-byte swizzle (a tiled TMA load of 32 columns lands it): one 32-element
+// atom along MN, 8-row groups of 512 bytes along K
+__device__ __forceinline__ uint64_t desc_sw64_mn(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(512 >> 4) << 16;  // LBO (a single MN atom at N = 32)
+  d |= (uint64_t)(512 >> 4) << 32;  // SBO: 8 K-rows of 64 bytes
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;           // 64-byte swizzle
+  return d;
+}
+// D[128 x 32] = A * B where A (M = 128, K = 128) is stored MN-major as
+// gemm_amn_k128 reads it and B (K = 128 rows, N = 32 columns) is the
+// 64-byte-swizzled MN-major tile of desc_sw64_mn
+__device__ __forceinline__ void gemm_amn_bmn64_k128(uint32_t tmem_d, uint32_t a_smem, uint32_t b_smem) {
+  const uint32_t idesc = idesc_bf16(128, 32) | (1u << 15) | (1u << 16);  // A and B MN-major
+  const uint64_t da0 = desc_sw128_mn(a_smem, 128u * 128u), db0 = desc_sw64_mn(b_smem);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    mma(tmem_d, da0 + (((uint32_t)k * 2048u) >> 4), db0 + (((uint32_t)k * 1024u) >> 4), idesc, k > 0 ? 1u : 0u);
+}
+
 // D[128 x 128] (+)= A * B where A is a K-major [128 x 128] SW128 tile and B
 // (K = 128 rows, N = 128 columns) is stored MN-major: the [K rows x N] SW128
 // tile as a tiled load of a row-major [K][N] matrix lands it (two 64-column

@@ -78,9 +78,9 @@ struct WalkBwdSmem {
   unsigned char stage[C::NSTAGE][2][C::SLICE];  // [set][dh', dDelta]; SW 32: 64-byte, SW 64: 128-byte swizzle
   unsigned char Xt[C::BT];   // dh'^T
   unsigned char Yt[C::BT];   // (-Y)^T
-  unsigned char Ot[C::BT];   // dO^T (this slice)
+  unsigned char Ot[C::BT];   // dO^T (this slice); DOTMA: the second dO-slice buffer
   unsigned char Ogt[C::BT];  // (diag(gamma) dO)^T
-  unsigned char dOt[C::DOTMA ? C::SLICE : 16];  // DOTMA: dO slice [128 x 32] of the next chunk, 64-byte swizzle
+  unsigned char dOt[C::DOTMA ? C::SLICE : 16];  // DOTMA: dO slice [128 x 32] of even chunk indices, 64-byte swizzle
   float gsum[2][4];
   uint64_t full[C::NRING], empty[C::NRING];
   uint64_t barO, barXt, barYt, barQ, barY, barH;  // barY: K dh' and P^T dO complete
@@ -198,7 +198,11 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
       ld_pred_v4(dst[q], src + 8 * q, in);
     }
   };
-  // dO^T and (gamma dO)^T images of the chunk whose dO rows are in dn
+  // DOTMA: the dO slice of chunk index i lies in dO_slice(i), where P^T dO reads it
+  // directly (MN-major); only (gamma dO)^T is written as an image
+  static_assert(!DOTMA || (SPLIT && Cfg::SLICE == Cfg::BT), "the slice buffers take the dO^T image's place");
+  auto dO_slice = [&](int i) { return (i & 1) ? sm.Ot : sm.dOt; };
+  // dO^T (unless DOTMA) and (gamma dO)^T images of the chunk whose dO rows are in dn
   auto write_do_images = [&](const uint4 (&dn)[4]) {
     float d[32], dg[32];
 #pragma unroll
@@ -213,7 +217,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i) dg[i] = gam_r * d[i];
-    write_bt_column<SW>(sm.Ot, r, 32 * g32, d);
+    if (!DOTMA) write_bt_column<SW>(sm.Ot, r, 32 * g32, d);
     write_bt_column<SW>(sm.Ogt, r, 32 * g32, dg);
   };
   auto scan_part = [&](float gv, int i) {  // warp-inclusive scan; warp totals to gsum[i & 1]
@@ -294,7 +298,10 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
         ok = ok && tc::mbar_wait_sleep(&sm.full[t0 % NRING], (t0 / NRING) & 1);  // (tile first)
         ok = ok && tc::mbar_wait_sleep(&sm.barO, (uint32_t)(ci & 1));
         tc::fence_after();
-        tc::gemm_amn_k128(tmem + C_P, smem_u32(sm.slot[t0 % NRING]), smem_u32(sm.Ot), SW, false);
+        if (DOTMA)
+          tc::gemm_amn_bmn64_k128(tmem + C_P, smem_u32(sm.slot[t0 % NRING]), smem_u32(dO_slice(ci)));
+        else
+          tc::gemm_amn_k128(tmem + C_P, smem_u32(sm.slot[t0 % NRING]), smem_u32(sm.Ot), SW, false);
         tc::commit(&sm.barY);  // (barY's second arrival of the chunk)
         tc::commit(&sm.empty[t0 % NRING]);
         const int iQ = t0 + 1;
@@ -316,7 +323,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     const bool dol = DOTMA && withO;
     auto load_slice = [&](int ci) {  // dO slice of chunk index ci (rows past T read as zero)
       tc::arrive_expect_tx(&sm.barDO, Cfg::SLICE);
-      tc::tma_load_4d(sm.dOt, &mp.dO, col0, j, chunk_of(ci) * CH, b, &sm.barDO);
+      tc::tma_load_4d(dO_slice(ci), &mp.dO, col0, j, chunk_of(ci) * CH, b, &sm.barDO);
     };
     if (lane == 0 && (stores || dol)) {
       // barO's phases are waited for in order, from phase 0 (the images of chunk
@@ -407,6 +414,10 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
     // ========================================================== compute threads
     finish_gates(part, 0);
     if (withO) {
+      if (DOTMA) {  // chunk index 0's rows (plain loads) into its slice buffer, for P^T dO
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(dO_slice(0) + tc::sw64_chunk(r, q)) = don[q];
+      }
       write_do_images(don);
       tc::fence_proxy_async();
       tc::fence_before();
@@ -464,7 +475,7 @@ __device__ __forceinline__ void walk(const WalkBwdArgs& a, const WalkBwdMaps& mp
         if (DOTMA) {  // the slice of chunk index ci + 1 (load number ci of dOt)
           ok = ok && tc::mbar_wait_sleep(&sm.barDO, par);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) dn[q] = *reinterpret_cast<const uint4*>(sm.dOt + tc::sw64_chunk(r, q));
+          for (int q = 0; q < 4; ++q) dn[q] = *reinterpret_cast<const uint4*>(dO_slice(ci + 1) + tc::sw64_chunk(r, q));
         }
         write_do_images(dn);
         tc::fence_proxy_async();
