@@ -22,7 +22,8 @@
 //     Q^T (gamma dO)   (A = the Q tile read MN-major), then += w^T (-Y) on top
 //                      (A = the w tile read MN-major)
 // take B operands written column by column by the compute threads (dh'^T,
-// dO^T, (gamma dO)^T, (-Y)^T, SW x 128 bf16, 128-byte-swizzled K-major).  The
+// dO^T, (gamma dO)^T, (-Y)^T, SW x 128 bf16, 128-byte-swizzled K-major); on
+// 32-column slices P^T dO reads the chunk's dO slice instead, as TMA stored it.  The
 // two dO products do not depend on dh', so they run ahead of the chain
 // dh' -> Y -> dh.  A fifth warp issues the MMAs once their operands are
 // signalled ready; a sixth issues the TMA loads of the chunk tiles (P, Q, K, w
@@ -32,9 +33,11 @@
 // issue never holds the chain's issuer; the chain's issuer then waits for
 // Q^T (gamma dO) to complete before it accumulates w^T (-Y) onto it.  The
 // compute threads form the dO images from each chunk's dO rows.  On 32-column
-// slices those rows arrive by TMA (the store warp requests each chunk's slice
-// once the images of the chunk before are written), so the compute threads
-// issue no global loads: an mbarrier arrive, a release, would wait for them.
+// slices those rows arrive by TMA into one of two slice buffers (the store warp
+// requests each chunk's slice once the images of the chunk before are written),
+// so the compute threads issue no global loads: an mbarrier arrive, a release,
+// would wait for them.  There P^T dO reads the slice directly (MN-major, 64-byte
+// swizzle) and only (gamma dO)^T is written as an image.
 // Every wait is bounded; one that gives up sets bit 0 of the status word.
 //
 // Modes:
